@@ -1,0 +1,239 @@
+/*
+ * soup.h — C ABI of libsoup: one LoRA fine-tuning step over a frozen decoder stack that is
+ * streamed layer by layer from a pinned host store through a small pool of device slots.
+ *
+ * Sources (page title, section):
+ *   "About Soup"                                   — the frozen base is never loaded whole;
+ *       one shard per layer, copied into a small pool of pre-allocated buffers on a
+ *       dedicated stream so the next layer's load overlaps the current layer's compute;
+ *       NF4 shrinks the store about fourfold.
+ *   "Layer streaming: fine-tune a model that does not fit in your card" (the docs page),
+ *       "Turn it on"     — quantization none (bf16) or 4bit (NF4); stream_buffers in [2, 8].
+ *       "How it works"   — resident embeddings, final norm, untied head, LoRA adapters and
+ *                          their gradients; page-locked store; each layer read twice per
+ *                          step because the backward needs W^T dL/dy.
+ *       "Read this first" / "Bit-exact is two claims, not one" — the streamed run must equal
+ *                          the resident run bit for bit, forward and every LoRA gradient,
+ *                          including layers above ~165 MiB.
+ *       "Measured numbers" — pinned copies overlap compute, pageable ones do not.
+ *
+ * Conventions for every entry point:
+ *   - Return value: SOUP_OK (0) or a negative SOUP_E* code; soup_last_error() then holds a
+ *     one-line message (thread-local, valid until the next call on the same thread).
+ *     SOUP_EPAGEABLE is a warning: the object was created and is usable.
+ *   - "dev" pointers are CUDA device pointers owned by the caller; "host" pointers are
+ *     ordinary host memory owned by the caller.  The library never frees caller memory.
+ *   - Streams are raw cudaStream_t values passed as uintptr_t (0 = legacy default stream).
+ *     Work is enqueued asynchronously; the host returns before the GPU finishes.
+ *   - bf16 values travel as uint16_t bit patterns; float is IEEE binary32.
+ *   - Matrices are row-major and densely packed unless a leading dimension is given.
+ *   - Nothing in a step allocates device memory: the caller passes one workspace sized by
+ *     soup_workspace_bytes().
+ */
+#ifndef SOUP_H
+#define SOUP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  SOUP_OK = 0,
+  SOUP_EINVAL = -1,     /* bad argument or unsupported shape; nothing was enqueued      */
+  SOUP_ENOMEM = -2,     /* a host allocation failed, or the workspace is too small      */
+  SOUP_ECUDA = -3,      /* a CUDA runtime call failed (message names it)                */
+  SOUP_ESTATE = -4,     /* call out of order (e.g. backward without a forward)          */
+  SOUP_ETIMEDOUT = -5,  /* soup_sync gave up, or a kernel's bounded wait ran out        */
+  SOUP_EPAGEABLE = -6   /* warning: page-locking failed, the store is pageable          */
+};
+
+enum { SOUP_FMT_BF16 = 0, SOUP_FMT_NF4 = 1 };
+
+/* Projection order used by every per-projection array: index p in [0, 7). */
+enum { SOUP_Q = 0, SOUP_K, SOUP_V, SOUP_O, SOUP_GATE, SOUP_UP, SOUP_DOWN, SOUP_NPROJ };
+/* The four GEMM groups of a layer: projections that share an input are fused along N. */
+enum { SOUP_G_QKV = 0, SOUP_G_O, SOUP_G_GU, SOUP_G_DOWN, SOUP_NGROUP };
+
+/* Shape of a Llama-shaped decoder stack. */
+typedef struct soup_cfg {
+  int32_t n_layers, hidden, inter, n_heads, n_kv_heads, head_dim, vocab;
+  int32_t tied;          /* 1: the output head is the embedding matrix                  */
+  float rope_theta, rms_eps;
+  int32_t base_fmt;      /* SOUP_FMT_BF16 or SOUP_FMT_NF4 for the streamed projections   */
+  int32_t lora_r;        /* LoRA rank r, 1..64                                           */
+  float lora_alpha;      /* LoRA scale s = lora_alpha / lora_r                            */
+} soup_cfg;
+
+/* Byte layout of one layer shard.  All offsets are multiples of 1024 and relative to the
+ * shard's start; shards sit at multiples of `stride` in the store, in a slot and in the
+ * resident array alike, so kernels see identical alignment in every mode.
+ * Group g's weight section holds the group's projections stacked along the output
+ * dimension (q,k,v / o / gate,up / down):
+ *   NF4:  codes  uint8 [n_out[g] * n_in[g] / 2], byte j = code[2j] << 4 | code[2j+1],
+ *         absmax float [n_out[g] * n_in[g] / 64], blocks of 64 over the flattened
+ *         row-major [n_out, n_in] matrix (stacking keeps each projection's own blocks
+ *         because every projection's element count is a multiple of 64);
+ *   bf16: weights uint16 [n_out[g], n_in[g]] and no absmax section (a_bytes = 0).
+ * ln1/ln2: the two RMSNorm weight vectors, bf16 [hidden]. */
+typedef struct soup_shard_layout {
+  uint64_t stride, payload;
+  uint64_t w_off[SOUP_NGROUP], w_bytes[SOUP_NGROUP];
+  uint64_t a_off[SOUP_NGROUP], a_bytes[SOUP_NGROUP];
+  uint64_t ln1_off, ln2_off;
+  int32_t n_out[SOUP_NGROUP], n_in[SOUP_NGROUP];
+} soup_shard_layout;
+
+typedef struct soup_store soup_store;
+typedef struct soup_stream soup_stream;
+
+/* Per-handle counters since soup_stream_init (or the last reset). Times in ms, from CUDA
+ * events on the stream that ran the work; a field is 0 when its events were not enabled. */
+typedef struct soup_stats {
+  uint64_t steps_fwd, steps_bwd;
+  uint64_t copies, copy_bytes;    /* shard copies host -> slot                              */
+  double copy_ms;                 /* sum of per-copy durations on the copy stream           */
+  uint64_t gemm_launches;         /* NF4/bf16 base-weight GEMM launches (profiling on)       */
+  double gemm_ms;                 /* their summed durations                                 */
+  double gemm_flops, gemm_bytes;  /* their algorithmic flops and bytes                      */
+} soup_stats;
+
+/* ------------------------------------------------------------------ diagnostics */
+
+/* Message of the last failing call on this thread ("" if none). Never NULL. */
+const char *soup_last_error(void);
+/* Library version string. */
+const char *soup_version(void);
+
+/* The 16 NF4 code values, ascending, as this library derives them (float64 construction
+ * from normal quantiles, rounded once to float): "Turn it on" names NF4 without printing
+ * it, so the construction follows the NormalFloat definition.  out: host float[16]. */
+int soup_nf4_codebook(float *out);
+
+/* ------------------------------------------------------------------ store (host) */
+
+/* Fill `out` with the shard layout for cfg.  Returns SOUP_EINVAL for an invalid cfg. */
+int soup_shard_layout_of(const soup_cfg *cfg, soup_shard_layout *out);
+
+/* Quantise one tensor on the host ("How it works": the checkpoint is rewritten once into
+ * one shard per layer, quantising as it goes).
+ *   src:    host uint16 [n] bf16 source values (row-major flattened)
+ *   codes:  host uint8  [(n + 1) / 2] out; absmax: host float [(n + 63) / 64] out.
+ *   n_threads <= 0 uses all host cores.  Bit-exact with the plain definition: IEEE float
+ *   divide, code = number of midpoints strictly below x / absmax, zero blocks -> code 7. */
+int soup_nf4_quantize_host(const uint16_t *src, int64_t n, uint8_t *codes, float *absmax,
+                           int n_threads);
+
+/* Create an empty store of cfg.n_layers shards in ONE page-locked host arena (exact size,
+ * no power-of-two rounding: the pages report rounding cost 1.73x at 14B).  If page-locking
+ * fails and allow_pageable != 0, a pageable arena is used and SOUP_EPAGEABLE is returned
+ * ("Measured numbers": pageable copies are synchronous and lose the overlap). */
+int soup_store_create(const soup_cfg *cfg, int allow_pageable, soup_store **out);
+/* Quantise (NF4) or copy (bf16) one layer into its shard.  src: host pointers to the nine
+ * bf16 tensors of the layer in order q,k,v,o,gate,up,down ([out,in] each), ln1, ln2 [hidden].
+ * May be called from several host threads for different layers. */
+int soup_store_put_layer(soup_store *st, int layer, const uint16_t *const *src, int n_threads);
+/* soup_store_create + put_layer for every layer: src is [n_layers * 9] host pointers. */
+int soup_store_build(const soup_cfg *cfg, const uint16_t *const *src, int allow_pageable,
+                     soup_store **out);
+/* Arena base (host pointer), total bytes, and whether it is page-locked. */
+int soup_store_info(const soup_store *st, void **base, uint64_t *bytes, int *pinned);
+void soup_store_free(soup_store *st);
+
+/* ------------------------------------------------------------------ memory plan */
+
+/* Device bytes of the workspace a stream handle needs for batches up to max_batch x max_seq:
+ * n_slots shard slots (or every layer when resident != 0), saved activations, per-layer
+ * scratch, LoRA operand packs and the vocabulary chunk of the loss. Writes *ws_bytes. */
+int soup_workspace_bytes(const soup_cfg *cfg, int max_batch, int max_seq, int n_slots,
+                         int resident, uint64_t *ws_bytes);
+/* Device bytes of a whole run: workspace + caller-side resident tensors (embedding, untied
+ * head, final norm, LoRA A/B and their gradients).  The pages bound peak VRAM by a single
+ * layer plus the resident parts ("About Soup"); this is that bound made exact.
+ * Returns 0 for an invalid cfg. workspace_bytes (optional) receives the workspace part. */
+uint64_t soup_peak_bytes(const soup_cfg *cfg, int batch, int seq, int n_slots, int resident,
+                         uint64_t *workspace_bytes);
+
+/* ------------------------------------------------------------------ streamed step */
+
+/* Bind a store to a device workspace.
+ *   dev_ws / ws_bytes: caller device buffer, >= soup_workspace_bytes(), 256-B aligned.
+ *   embed: dev bf16 [vocab, hidden]; lm_head: dev bf16 [vocab, hidden] or NULL when tied;
+ *   final_norm: dev bf16 [hidden].
+ *   compute_stream / copy_stream: distinct streams ("How it works": a dedicated copy stream).
+ *   n_slots in [2, 8] ("Turn it on": stream_buffers).  resident != 0 copies every shard to
+ *   the workspace once here (synchronously) and then runs the same kernels with no copies —
+ *   the reference the streamed run must match bit for bit. */
+int soup_stream_init(soup_store *st, const soup_cfg *cfg, int max_batch, int max_seq,
+                     void *dev_ws, uint64_t ws_bytes, const void *embed, const void *lm_head,
+                     const void *final_norm, uintptr_t compute_stream, uintptr_t copy_stream,
+                     int n_slots, int resident, soup_stream **out);
+
+/* Forward over all layers plus the vocabulary-chunked loss.
+ *   tokens_dev: dev int32 [B, S], ids in [0, vocab) (ids out of range are clamped).
+ *   lora_A: host array [n_layers * 7] of dev float [r, in_p]; lora_B: [n_layers * 7] of dev
+ *   float [out_p, r]; p in SOUP_Q..SOUP_DOWN order.  They must stay valid until the matching
+ *   soup_step_bwd has been enqueued.
+ *   loss_dev: dev float [1], mean next-token cross-entropy over B*(S-1) positions.
+ *   logits_dev (optional, NULL in timed runs): dev float [B*S, vocab].
+ *   layer_out_dev (optional): dev float [(n_layers + 1), B*S, hidden] — the residual stream
+ *   entering each layer and leaving the last.
+ * B*S must be <= max_batch*max_seq, S <= max_seq, S >= 2. */
+int soup_step_fwd(soup_stream *h, const int32_t *tokens_dev, int B, int S,
+                  const float *const *lora_A, const float *const *lora_B, float *loss_dev,
+                  float *logits_dev, float *layer_out_dev);
+
+/* Backward of the last forward: re-streams the layers in reverse, recomputes each layer's
+ * forward, and writes every LoRA gradient (overwritten, not accumulated).
+ *   dA: host array [n_layers * 7] of dev float [r, in_p]; dB: [n_layers * 7] of dev float
+ *   [out_p, r].  dh_out_dev (optional): dev float [(n_layers + 1), B*S, hidden], dL/dh of the
+ *   residual stream at each layer boundary.  SOUP_ESTATE without a preceding forward. */
+int soup_step_bwd(soup_stream *h, float *const *dA, float *const *dB, float *dh_out_dev);
+
+/* Host-side bounded wait for all work enqueued on the handle: polls, never spins on the
+ * device.  Returns SOUP_ETIMEDOUT after timeout_ms, or the error a kernel reported. */
+int soup_sync(soup_stream *h, int timeout_ms);
+int soup_stream_stats(soup_stream *h, soup_stats *out, int reset);
+/* Debug switches: what = SOUP_DBG_PROFILE (time every base GEMM with events),
+ * SOUP_DBG_STALE_SLOT (backward reads the slot of a neighbouring layer: a deliberately
+ * broken control that the exactness tests must catch; reads valid memory only). */
+enum { SOUP_DBG_PROFILE = 1, SOUP_DBG_STALE_SLOT = 2 };
+int soup_stream_debug(soup_stream *h, int what, int value);
+void soup_stream_free(soup_stream *h);
+
+/* ------------------------------------------------------------------ single projection */
+
+/* One projection of the step, for the microbench and the kernel tests.  W is a weight
+ * [N, K] (out x in) given as NF4 (codes dev uint8 [N*K/2] + absmax dev float [N*K/64]) or
+ * bf16 (w_bf16 dev uint16 [N, K]; codes/absmax NULL).  LoRA: A dev float [r, K],
+ * B dev float [N, r], s = alpha / r.  scratch: dev buffer of soup_proj_scratch_bytes().
+ * Shapes: any M >= 1; the tensor-core path needs K % 256 == 0 and N % 16 == 0 for the
+ * forward, N % 64 == 0 and K % 256 == 0 for dX; other shapes use a plain tiled kernel. */
+int soup_proj_scratch_bytes(int M, int N, int K, int r, uint64_t *bytes);
+
+/* y[M, N] (bf16 out, dev uint16) = x W^T + s (x A^T) B^T,  x: dev bf16 [M, K]. */
+int soup_proj_fwd(const uint16_t *x, int M, int N, int K, const uint8_t *codes,
+                  const float *absmax, const uint16_t *w_bf16, const float *A, const float *B,
+                  int r, float s, uint16_t *y, void *scratch, uint64_t scratch_bytes,
+                  uintptr_t stream);
+/* dx[M, K] (float out) = dY W + s (dY B) A,  dY: dev bf16 [M, N]. */
+int soup_proj_dx(const uint16_t *dy, int M, int N, int K, const uint8_t *codes,
+                 const float *absmax, const uint16_t *w_bf16, const float *A, const float *B,
+                 int r, float s, float *dx, void *scratch, uint64_t scratch_bytes,
+                 uintptr_t stream);
+/* dA[r, K] = s (dY B)^T x,  dB[N, r] = s dY^T (x A^T); float outputs, fixed summation order. */
+int soup_proj_lora_grad(const uint16_t *x, const uint16_t *dy, int M, int N, int K,
+                        const float *A, const float *B, int r, float s, float *dA, float *dB,
+                        void *scratch, uint64_t scratch_bytes, uintptr_t stream);
+
+/* Dequantise n NF4 weights on the device: out_f32[i] = float(c[code_i] * absmax[i / 64])
+ * and out_bf16[i] = that value rounded to nearest-even bf16 (either output may be NULL). */
+int soup_nf4_dequant(const uint8_t *codes, const float *absmax, int64_t n, float *out_f32,
+                     uint16_t *out_bf16, uintptr_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SOUP_H */

@@ -1,0 +1,310 @@
+"""ctypes binding of the C ABI in include/soup.h, with the same names.
+
+PyTorch supplies device memory and streams; tensors are passed as raw pointers.  Every call
+checks the status code and raises :class:`SoupError` with the library's message.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsoup.so")
+
+OK, EINVAL, ENOMEM, ECUDA, ESTATE, ETIMEDOUT, EPAGEABLE = 0, -1, -2, -3, -4, -5, -6
+FMT_BF16, FMT_NF4 = 0, 1
+DBG_PROFILE, DBG_STALE_SLOT = 1, 2
+PROJ = ("q", "k", "v", "o", "gate", "up", "down")
+
+
+class SoupError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"soup error {code}: {msg}")
+        self.code = code
+
+
+class soup_cfg(C.Structure):
+    _fields_ = [("n_layers", C.c_int32), ("hidden", C.c_int32), ("inter", C.c_int32),
+                ("n_heads", C.c_int32), ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32),
+                ("vocab", C.c_int32), ("tied", C.c_int32), ("rope_theta", C.c_float),
+                ("rms_eps", C.c_float), ("base_fmt", C.c_int32), ("lora_r", C.c_int32),
+                ("lora_alpha", C.c_float)]
+
+
+class soup_shard_layout(C.Structure):
+    _fields_ = [("stride", C.c_uint64), ("payload", C.c_uint64),
+                ("w_off", C.c_uint64 * 4), ("w_bytes", C.c_uint64 * 4),
+                ("a_off", C.c_uint64 * 4), ("a_bytes", C.c_uint64 * 4),
+                ("ln1_off", C.c_uint64), ("ln2_off", C.c_uint64),
+                ("n_out", C.c_int32 * 4), ("n_in", C.c_int32 * 4)]
+
+
+class soup_stats(C.Structure):
+    _fields_ = [("steps_fwd", C.c_uint64), ("steps_bwd", C.c_uint64), ("copies", C.c_uint64),
+                ("copy_bytes", C.c_uint64), ("copy_ms", C.c_double),
+                ("gemm_launches", C.c_uint64), ("gemm_ms", C.c_double),
+                ("gemm_flops", C.c_double), ("gemm_bytes", C.c_double)]
+
+    def as_dict(self) -> dict:
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+def _load() -> C.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built; run python -m nf4_dequant_gemm_blockwise_b300.build")
+    lib = C.CDLL(LIB_PATH)
+    P, U64, I32, F32, VP = C.c_void_p, C.c_uint64, C.c_int, C.c_float, C.c_void_p
+    sig = {
+        "soup_last_error": (C.c_char_p, []),
+        "soup_version": (C.c_char_p, []),
+        "soup_nf4_codebook": (I32, [P]),
+        "soup_shard_layout_of": (I32, [C.POINTER(soup_cfg), C.POINTER(soup_shard_layout)]),
+        "soup_nf4_quantize_host": (I32, [P, C.c_int64, P, P, I32]),
+        "soup_store_create": (I32, [C.POINTER(soup_cfg), I32, C.POINTER(VP)]),
+        "soup_store_put_layer": (I32, [VP, I32, C.POINTER(P), I32]),
+        "soup_store_build": (I32, [C.POINTER(soup_cfg), C.POINTER(P), I32, C.POINTER(VP)]),
+        "soup_store_info": (I32, [VP, C.POINTER(P), C.POINTER(U64), C.POINTER(I32)]),
+        "soup_store_free": (None, [VP]),
+        "soup_workspace_bytes": (I32, [C.POINTER(soup_cfg), I32, I32, I32, I32, C.POINTER(U64)]),
+        "soup_peak_bytes": (U64, [C.POINTER(soup_cfg), I32, I32, I32, I32, C.POINTER(U64)]),
+        "soup_stream_init": (I32, [VP, C.POINTER(soup_cfg), I32, I32, P, U64, P, P, P, C.c_size_t,
+                                   C.c_size_t, I32, I32, C.POINTER(VP)]),
+        "soup_step_fwd": (I32, [VP, P, I32, I32, C.POINTER(P), C.POINTER(P), P, P, P]),
+        "soup_step_bwd": (I32, [VP, C.POINTER(P), C.POINTER(P), P]),
+        "soup_sync": (I32, [VP, I32]),
+        "soup_stream_stats": (I32, [VP, C.POINTER(soup_stats), I32]),
+        "soup_stream_debug": (I32, [VP, I32, I32]),
+        "soup_stream_free": (None, [VP]),
+        "soup_proj_scratch_bytes": (I32, [I32, I32, I32, I32, C.POINTER(U64)]),
+        "soup_proj_fwd": (I32, [P, I32, I32, I32, P, P, P, P, P, I32, F32, P, P, U64, C.c_size_t]),
+        "soup_proj_dx": (I32, [P, I32, I32, I32, P, P, P, P, P, I32, F32, P, P, U64, C.c_size_t]),
+        "soup_proj_lora_grad": (I32, [P, P, I32, I32, I32, P, P, I32, F32, P, P, P, U64, C.c_size_t]),
+        "soup_nf4_dequant": (I32, [P, P, C.c_int64, P, P, C.c_size_t]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+
+# every entry point include/soup.h declares (the CPU tests check the exports against it)
+EXPORTS = tuple(sorted(n for n in dir(lib) if n.startswith("soup_")))
+
+
+def _check(rc: int, allow=()) -> int:
+    if rc != OK and rc not in allow:
+        raise SoupError(rc, lib.soup_last_error().decode())
+    return rc
+
+
+def last_error() -> str:
+    return lib.soup_last_error().decode()
+
+
+def version() -> str:
+    return lib.soup_version().decode()
+
+
+def _ptr(x) -> int | None:
+    """Device or host address of a torch tensor / numpy array / int (None -> NULL)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if isinstance(x, np.ndarray):
+        return x.ctypes.data
+    return x.data_ptr()
+
+
+def make_cfg(cfg) -> soup_cfg:
+    """soup_cfg from any object with the stack's fields (n_layers, hidden, ..., base_fmt
+    'nf4'|'bf16', lora_r, lora_alpha)."""
+    fmt = cfg.base_fmt
+    if isinstance(fmt, str):
+        fmt = FMT_NF4 if fmt == "nf4" else FMT_BF16
+    return soup_cfg(cfg.n_layers, cfg.hidden, cfg.inter, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim,
+                    cfg.vocab, int(bool(cfg.tied)), float(cfg.rope_theta), float(cfg.rms_eps), fmt,
+                    cfg.lora_r, float(cfg.lora_alpha))
+
+
+def nf4_codebook() -> np.ndarray:
+    out = np.zeros(16, np.float32)
+    _check(lib.soup_nf4_codebook(out.ctypes.data))
+    return out
+
+
+def shard_layout_of(cfg) -> soup_shard_layout:
+    c = make_cfg(cfg)
+    out = soup_shard_layout()
+    _check(lib.soup_shard_layout_of(C.byref(c), C.byref(out)))
+    return out
+
+
+def nf4_quantize_host(src_bf16_bits: np.ndarray, n_threads: int = 0):
+    """Host packer: bf16 bit patterns -> (packed codes uint8, absmax float32)."""
+    src = np.ascontiguousarray(src_bf16_bits, np.uint16).reshape(-1)
+    n = src.size
+    codes = np.empty((n + 1) // 2, np.uint8)
+    absmax = np.empty((n + 63) // 64, np.float32)
+    _check(lib.soup_nf4_quantize_host(src.ctypes.data, n, codes.ctypes.data, absmax.ctypes.data,
+                                      n_threads))
+    return codes, absmax
+
+
+def workspace_bytes(cfg, max_batch, max_seq, n_slots=2, resident=False) -> int:
+    c = make_cfg(cfg)
+    out = C.c_uint64()
+    _check(lib.soup_workspace_bytes(C.byref(c), max_batch, max_seq, n_slots, int(resident), C.byref(out)))
+    return out.value
+
+
+def peak_bytes(cfg, batch, seq, n_slots=2, resident=False):
+    """(total device bytes of a run, workspace part)."""
+    c = make_cfg(cfg)
+    ws = C.c_uint64()
+    tot = lib.soup_peak_bytes(C.byref(c), batch, seq, n_slots, int(resident), C.byref(ws))
+    if tot == 0:
+        raise SoupError(EINVAL, last_error())
+    return tot, ws.value
+
+
+class Store:
+    """One page-locked host arena holding every layer's shard (soup_store_*)."""
+
+    def __init__(self, cfg, allow_pageable: bool = True):
+        self.cfg = make_cfg(cfg)
+        h = C.c_void_p()
+        rc = lib.soup_store_create(C.byref(self.cfg), int(allow_pageable), C.byref(h))
+        self.pageable_warning = rc == EPAGEABLE
+        _check(rc, allow=(EPAGEABLE,))
+        self.handle = h
+
+    def put_layer(self, layer: int, tensors, n_threads: int = 0):
+        """tensors: nine bf16-bit arrays q,k,v,o,gate,up,down ([out,in]) and ln1, ln2."""
+        arrs = [np.ascontiguousarray(t, np.uint16) for t in tensors]
+        ptrs = (C.c_void_p * 9)(*[a.ctypes.data for a in arrs])
+        _check(lib.soup_store_put_layer(self.handle, layer, ptrs, n_threads))
+
+    def info(self):
+        base, nb, pinned = C.c_void_p(), C.c_uint64(), C.c_int()
+        _check(lib.soup_store_info(self.handle, C.byref(base), C.byref(nb), C.byref(pinned)))
+        return base.value, nb.value, bool(pinned.value)
+
+    def shard_bytes(self, layer: int) -> np.ndarray:
+        """A numpy view of one shard in the arena (host memory)."""
+        base, _, _ = self.info()
+        lay = shard_layout_of_cfg(self.cfg)
+        buf = (C.c_uint8 * lay.stride).from_address(base + layer * lay.stride)
+        return np.frombuffer(buf, np.uint8)
+
+    def free(self):
+        if self.handle:
+            lib.soup_store_free(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+def shard_layout_of_cfg(c: soup_cfg) -> soup_shard_layout:
+    out = soup_shard_layout()
+    _check(lib.soup_shard_layout_of(C.byref(c), C.byref(out)))
+    return out
+
+
+class Stream:
+    """A stream handle: a store bound to a device workspace and two CUDA streams."""
+
+    def __init__(self, store: Store, max_batch, max_seq, workspace, embed, lm_head, final_norm,
+                 compute_stream, copy_stream, n_slots=2, resident=False):
+        self.store = store
+        self.cfg = store.cfg
+        ws_need = C.c_uint64()
+        _check(lib.soup_workspace_bytes(C.byref(self.cfg), max_batch, max_seq, n_slots, int(resident),
+                                        C.byref(ws_need)))
+        self.keep = (workspace, embed, lm_head, final_norm)
+        h = C.c_void_p()
+        _check(lib.soup_stream_init(store.handle, C.byref(self.cfg), max_batch, max_seq, _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _ptr(embed),
+                                    _ptr(lm_head), _ptr(final_norm), compute_stream.cuda_stream,
+                                    copy_stream.cuda_stream, n_slots, int(resident), C.byref(h)))
+        self.handle = h
+
+    def fwd(self, tokens, B, S, lora_A, lora_B, loss, logits=None, layer_out=None):
+        n = len(lora_A)
+        a = (C.c_void_p * n)(*[_ptr(t) for t in lora_A])
+        b = (C.c_void_p * n)(*[_ptr(t) for t in lora_B])
+        self._lora = (a, b, lora_A, lora_B)
+        _check(lib.soup_step_fwd(self.handle, _ptr(tokens), B, S, a, b, _ptr(loss), _ptr(logits),
+                                 _ptr(layer_out)))
+
+    def bwd(self, dA, dB, dh_out=None):
+        n = len(dA)
+        a = (C.c_void_p * n)(*[_ptr(t) for t in dA])
+        b = (C.c_void_p * n)(*[_ptr(t) for t in dB])
+        _check(lib.soup_step_bwd(self.handle, a, b, _ptr(dh_out)))
+
+    def sync(self, timeout_ms: int = 60000):
+        _check(lib.soup_sync(self.handle, timeout_ms))
+
+    def stats(self, reset: bool = False) -> dict:
+        s = soup_stats()
+        _check(lib.soup_stream_stats(self.handle, C.byref(s), int(reset)))
+        return s.as_dict()
+
+    def debug(self, what: int, value: int):
+        _check(lib.soup_stream_debug(self.handle, what, value))
+
+    def free(self):
+        if getattr(self, "handle", None):
+            lib.soup_stream_free(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+def proj_scratch_bytes(M, N, K, r) -> int:
+    out = C.c_uint64()
+    _check(lib.soup_proj_scratch_bytes(M, N, K, r, C.byref(out)))
+    return out.value
+
+
+def proj_fwd(x, M, N, K, codes, absmax, w_bf16, A, B, r, s, y, scratch, stream=0):
+    _check(lib.soup_proj_fwd(_ptr(x), M, N, K, _ptr(codes), _ptr(absmax), _ptr(w_bf16), _ptr(A),
+                             _ptr(B), r, s, _ptr(y), _ptr(scratch),
+                             scratch.numel() * scratch.element_size(), _stream(stream)))
+
+
+def proj_dx(dy, M, N, K, codes, absmax, w_bf16, A, B, r, s, dx, scratch, stream=0):
+    _check(lib.soup_proj_dx(_ptr(dy), M, N, K, _ptr(codes), _ptr(absmax), _ptr(w_bf16), _ptr(A),
+                            _ptr(B), r, s, _ptr(dx), _ptr(scratch),
+                            scratch.numel() * scratch.element_size(), _stream(stream)))
+
+
+def proj_lora_grad(x, dy, M, N, K, A, B, r, s, dA, dB, scratch, stream=0):
+    _check(lib.soup_proj_lora_grad(_ptr(x), _ptr(dy), M, N, K, _ptr(A), _ptr(B), r, s, _ptr(dA),
+                                   _ptr(dB), _ptr(scratch), scratch.numel() * scratch.element_size(),
+                                   _stream(stream)))
+
+
+def nf4_dequant(codes, absmax, n, out_f32=None, out_bf16=None, stream=0):
+    _check(lib.soup_nf4_dequant(_ptr(codes), _ptr(absmax), n, _ptr(out_f32), _ptr(out_bf16),
+                                _stream(stream)))
+
+
+def _stream(s) -> int:
+    if s is None or isinstance(s, int):
+        return s or 0
+    return s.cuda_stream

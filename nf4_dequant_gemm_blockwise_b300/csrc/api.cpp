@@ -1,0 +1,282 @@
+// The C ABI declared in include/soup.h: argument checks, error strings, and thin wrappers
+// over the store, the step orchestrator and the single-projection kernels.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "gemm.h"
+#include "kernels.h"
+#include "soup.h"
+#include "step.h"
+#include "store.h"
+#include "util.h"
+
+namespace soup {
+namespace {
+thread_local std::string g_err;
+}
+int set_error(int code, const char *fmt, ...) {
+  char buf[1024];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+void clear_error() { g_err.clear(); }
+}  // namespace soup
+
+using namespace soup;
+
+extern "C" {
+
+const char *soup_last_error(void) { return g_err.c_str(); }
+const char *soup_version(void) { return "soup-b300 0.1 (sm_103a)"; }
+
+int soup_nf4_codebook(float *out) {
+  if (!out) return set_error(SOUP_EINVAL, "out is NULL");
+  std::memcpy(out, nf4_codebook_param().v, 16 * sizeof(float));
+  return 0;
+}
+
+int soup_shard_layout_of(const soup_cfg *cfg, soup_shard_layout *out) {
+  if (!out) return set_error(SOUP_EINVAL, "out is NULL");
+  return shard_layout(cfg, out);
+}
+
+int soup_nf4_quantize_host(const uint16_t *src, int64_t n, uint8_t *codes, float *absmax,
+                           int n_threads) {
+  if (n < 0 || (n > 0 && (!src || !codes || !absmax))) return set_error(SOUP_EINVAL, "NULL argument");
+  nf4_quantize_host(src, n, codes, absmax, n_threads);
+  return 0;
+}
+
+int soup_store_create(const soup_cfg *cfg, int allow_pageable, soup_store **out) {
+  return store_create(cfg, allow_pageable, out);
+}
+int soup_store_put_layer(soup_store *st, int layer, const uint16_t *const *src, int n_threads) {
+  return store_put_layer(st, layer, src, n_threads);
+}
+int soup_store_build(const soup_cfg *cfg, const uint16_t *const *src, int allow_pageable,
+                     soup_store **out) {
+  if (!src) return set_error(SOUP_EINVAL, "src is NULL");
+  int rc = store_create(cfg, allow_pageable, out);
+  if (rc < 0 && rc != SOUP_EPAGEABLE) return rc;
+  for (int l = 0; l < cfg->n_layers; ++l) {
+    int r2 = store_put_layer(*out, l, src + (size_t)l * 9, 0);
+    if (r2 < 0) {
+      store_free(*out);
+      *out = nullptr;
+      return r2;
+    }
+  }
+  return rc;
+}
+int soup_store_info(const soup_store *st, void **base, uint64_t *bytes, int *pinned) {
+  if (!st) return set_error(SOUP_EINVAL, "store is NULL");
+  if (base) *base = st->base;
+  if (bytes) *bytes = st->bytes;
+  if (pinned) *pinned = st->pinned;
+  return 0;
+}
+void soup_store_free(soup_store *st) { store_free(st); }
+
+int soup_workspace_bytes(const soup_cfg *cfg, int max_batch, int max_seq, int n_slots, int resident,
+                         uint64_t *ws_bytes) {
+  if (!ws_bytes) return set_error(SOUP_EINVAL, "ws_bytes is NULL");
+  Plan P;
+  SOUP_TRY(make_plan(cfg, max_batch, max_seq, n_slots, resident, &P));
+  *ws_bytes = P.total;
+  return 0;
+}
+
+uint64_t soup_peak_bytes(const soup_cfg *cfg, int batch, int seq, int n_slots, int resident,
+                         uint64_t *workspace_bytes) {
+  Plan P;
+  if (make_plan(cfg, batch, seq, n_slots, resident, &P) < 0) return 0;
+  if (workspace_bytes) *workspace_bytes = P.total;
+  const uint64_t V = cfg->vocab, H = cfg->hidden, r = cfg->lora_r;
+  uint64_t lora = 0;
+  int n_out[4], n_in[4];
+  group_shapes(cfg, n_out, n_in);
+  const int qd = cfg->n_heads * cfg->head_dim, kvd = cfg->n_kv_heads * cfg->head_dim;
+  const uint64_t outs[7] = {(uint64_t)qd, (uint64_t)kvd, (uint64_t)kvd, H, (uint64_t)cfg->inter,
+                            (uint64_t)cfg->inter, H};
+  const uint64_t ins[7] = {H, H, H, (uint64_t)qd, H, H, (uint64_t)cfg->inter};
+  for (int p = 0; p < 7; ++p) lora += r * (outs[p] + ins[p]);
+  lora *= (uint64_t)cfg->n_layers;
+  const uint64_t resident_t = 2 * V * H + (cfg->tied ? 0 : 2 * V * H) + 2 * H + 2 * 4 * lora;
+  return P.total + resident_t;
+}
+
+int soup_stream_init(soup_store *st, const soup_cfg *cfg, int max_batch, int max_seq, void *dev_ws,
+                     uint64_t ws_bytes, const void *embed, const void *lm_head, const void *final_norm,
+                     uintptr_t compute_stream, uintptr_t copy_stream, int n_slots, int resident,
+                     soup_stream **out) {
+  return stream_init(st, cfg, max_batch, max_seq, dev_ws, ws_bytes, embed, lm_head, final_norm,
+                     compute_stream, copy_stream, n_slots, resident, out);
+}
+int soup_step_fwd(soup_stream *h, const int32_t *tokens_dev, int B, int S, const float *const *lora_A,
+                  const float *const *lora_B, float *loss_dev, float *logits_dev, float *layer_out_dev) {
+  return step_fwd(h, tokens_dev, B, S, lora_A, lora_B, loss_dev, logits_dev, layer_out_dev);
+}
+int soup_step_bwd(soup_stream *h, float *const *dA, float *const *dB, float *dh_out_dev) {
+  return step_bwd(h, dA, dB, dh_out_dev);
+}
+int soup_sync(soup_stream *h, int timeout_ms) { return stream_sync(h, timeout_ms); }
+int soup_stream_stats(soup_stream *h, soup_stats *out, int reset) { return stream_stats(h, out, reset); }
+int soup_stream_debug(soup_stream *h, int what, int value) {
+  if (!h) return set_error(SOUP_EINVAL, "handle is NULL");
+  if (what == SOUP_DBG_PROFILE) h->dbg_profile = value;
+  else if (what == SOUP_DBG_STALE_SLOT) h->dbg_stale = value;
+  else return set_error(SOUP_EINVAL, "unknown debug switch %d", what);
+  return 0;
+}
+void soup_stream_free(soup_stream *h) { soup_stream_free_impl(h); }
+
+// ------------------------------------------------------------------ single projection
+namespace {
+struct ProjScratch {
+  uint64_t u_f32, ul, vl, ac, du_f32, dul, err, total;
+};
+ProjScratch proj_plan(int M, int N, int K) {
+  ProjScratch s;
+  uint64_t off = 0;
+  auto take = [&](uint64_t b) {
+    const uint64_t o = off;
+    off = (off + b + 1023) / 1024 * 1024;
+    return o;
+  };
+  s.u_f32 = take(4ull * M * 64);
+  s.ul = take(2ull * M * 64);
+  s.vl = take(2ull * N * 64);
+  s.ac = take(2ull * 64 * K);
+  s.du_f32 = take(4ull * M * 64);
+  s.dul = take(2ull * M * 64);
+  s.err = take(64);
+  s.total = off;
+  return s;
+}
+int proj_check(int M, int N, int K, const uint8_t *codes, const float *absmax, const uint16_t *w,
+               const float *A, const float *B, int r, void *scratch, uint64_t bytes) {
+  if (M < 0 || N < 1 || K < 1 || r < 1 || r > 64)
+    return set_error(SOUP_EINVAL, "bad shape M=%d N=%d K=%d r=%d", M, N, K, r);
+  if (!A || !B || !scratch) return set_error(SOUP_EINVAL, "NULL LoRA or scratch pointer");
+  if (!(codes && absmax) && !w) return set_error(SOUP_EINVAL, "no weight given");
+  if ((int64_t)N * K % 64 && codes) return set_error(SOUP_EINVAL, "N*K must be a multiple of 64");
+  if (bytes < proj_plan(M, N, K).total) return set_error(SOUP_ENOMEM, "scratch too small");
+  if (reinterpret_cast<uintptr_t>(scratch) % 256) return set_error(SOUP_EINVAL, "scratch must be 256-byte aligned");
+  return 0;
+}
+LoraSeg one_seg(int N, const float *A, const float *B, int r, float s, float *dA, float *dB) {
+  LoraSeg L;
+  L.nseg = 1;
+  L.r = r;
+  L.s = s;
+  L.off[0] = 0;
+  L.n[0] = N;
+  L.A[0] = A;
+  L.B[0] = B;
+  L.dA[0] = dA;
+  L.dB[0] = dB;
+  return L;
+}
+GemmArgs proj_weight(int mode, int N, int K, const uint8_t *codes, const float *absmax, const uint16_t *w) {
+  GemmArgs g;
+  g.mode = mode;
+  g.Nw = N;
+  g.Kw = K;
+  if (codes) {
+    g.wfmt = W_NF4;
+    g.codes = codes;
+    g.absmax = absmax;
+  } else {
+    g.wfmt = W_BF16;
+    g.w = w;
+  }
+  return g;
+}
+}  // namespace
+
+int soup_proj_scratch_bytes(int M, int N, int K, int r, uint64_t *bytes) {
+  if (!bytes || M < 0 || N < 1 || K < 1 || r < 1 || r > 64) return set_error(SOUP_EINVAL, "bad argument");
+  *bytes = proj_plan(M, N, K).total;
+  return 0;
+}
+
+int soup_proj_fwd(const uint16_t *x, int M, int N, int K, const uint8_t *codes, const float *absmax,
+                  const uint16_t *w_bf16, const float *A, const float *B, int r, float s, uint16_t *y,
+                  void *scratch, uint64_t scratch_bytes, uintptr_t stream) {
+  SOUP_TRY(proj_check(M, N, K, codes, absmax, w_bf16, A, B, r, scratch, scratch_bytes));
+  if (M == 0) return 0;
+  if (!x || !y) return set_error(SOUP_EINVAL, "NULL x or y");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const ProjScratch P = proj_plan(M, N, K);
+  uint8_t *base = static_cast<uint8_t *>(scratch);
+  LoraSeg L = one_seg(N, A, B, r, s, nullptr, nullptr);
+  k_lora_down(x, K, M, K, L, reinterpret_cast<float *>(base + P.u_f32),
+              reinterpret_cast<uint16_t *>(base + P.ul), st);
+  k_pack_fwd(L, N, reinterpret_cast<uint16_t *>(base + P.vl), st);
+  GemmArgs g = proj_weight(GEMM_FWD, N, K, codes, absmax, w_bf16);
+  g.M = M; g.a = x; g.lda = K;
+  g.ul = reinterpret_cast<uint16_t *>(base + P.ul); g.vl = reinterpret_cast<uint16_t *>(base + P.vl);
+  g.R = L.Rpad(); g.epi = EPI_BF16; g.out = y; g.ldo = N;
+  g.err = reinterpret_cast<int *>(base + P.err);
+  return gemm_launch(g, st);
+}
+
+int soup_proj_dx(const uint16_t *dy, int M, int N, int K, const uint8_t *codes, const float *absmax,
+                 const uint16_t *w_bf16, const float *A, const float *B, int r, float s, float *dx,
+                 void *scratch, uint64_t scratch_bytes, uintptr_t stream) {
+  SOUP_TRY(proj_check(M, N, K, codes, absmax, w_bf16, A, B, r, scratch, scratch_bytes));
+  if (M == 0) return 0;
+  if (!dy || !dx) return set_error(SOUP_EINVAL, "NULL dy or dx");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const ProjScratch P = proj_plan(M, N, K);
+  uint8_t *base = static_cast<uint8_t *>(scratch);
+  LoraSeg L = one_seg(N, A, B, r, s, nullptr, nullptr);
+  k_lora_du(dy, N, M, L, reinterpret_cast<float *>(base + P.du_f32),
+            reinterpret_cast<uint16_t *>(base + P.dul), st);
+  k_pack_bwd(L, K, reinterpret_cast<uint16_t *>(base + P.ac), st);
+  GemmArgs g = proj_weight(GEMM_DX, N, K, codes, absmax, w_bf16);
+  g.M = M; g.a = dy; g.lda = N;
+  g.ul = reinterpret_cast<uint16_t *>(base + P.dul); g.vl = reinterpret_cast<uint16_t *>(base + P.ac);
+  g.R = L.Rpad(); g.epi = EPI_F32; g.out = dx; g.ldo = K;
+  g.err = reinterpret_cast<int *>(base + P.err);
+  return gemm_launch(g, st);
+}
+
+int soup_proj_lora_grad(const uint16_t *x, const uint16_t *dy, int M, int N, int K, const float *A,
+                        const float *B, int r, float s, float *dA, float *dB, void *scratch,
+                        uint64_t scratch_bytes, uintptr_t stream) {
+  if (!dA || !dB || !x || !dy) return set_error(SOUP_EINVAL, "NULL argument");
+  if (M < 1 || N < 1 || K < 1 || r < 1 || r > 64 || !A || !B || !scratch)
+    return set_error(SOUP_EINVAL, "bad argument");
+  if (scratch_bytes < proj_plan(M, N, K).total) return set_error(SOUP_ENOMEM, "scratch too small");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const ProjScratch P = proj_plan(M, N, K);
+  uint8_t *base = static_cast<uint8_t *>(scratch);
+  LoraSeg L = one_seg(N, A, B, r, s, dA, dB);
+  k_lora_down(x, K, M, K, L, reinterpret_cast<float *>(base + P.u_f32),
+              reinterpret_cast<uint16_t *>(base + P.ul), st);
+  k_lora_du(dy, N, M, L, reinterpret_cast<float *>(base + P.du_f32),
+            reinterpret_cast<uint16_t *>(base + P.dul), st);
+  k_lora_dB(dy, N, M, reinterpret_cast<float *>(base + P.u_f32), L, st);
+  k_lora_dA(reinterpret_cast<float *>(base + P.du_f32), x, K, M, K, L, st);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(SOUP_ECUDA, "lora grad launch: %s", cudaGetErrorString(e));
+  return 0;
+}
+
+int soup_nf4_dequant(const uint8_t *codes, const float *absmax, int64_t n, float *out_f32,
+                     uint16_t *out_bf16, uintptr_t stream) {
+  if (n < 0 || (n > 0 && (!codes || !absmax))) return set_error(SOUP_EINVAL, "NULL argument");
+  k_nf4_dequant(codes, absmax, n, out_f32, out_bf16, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(SOUP_ECUDA, "dequant launch: %s", cudaGetErrorString(e));
+  return 0;
+}
+
+}  // extern "C"

@@ -1,0 +1,59 @@
+// Internal interface of the base-weight GEMMs (NF4-dequant or bf16 weights, with the rank-r
+// LoRA term folded in as extra reduction tiles).  Not part of the C ABI.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace soup {
+
+enum GemmMode { GEMM_FWD = 0, GEMM_DX = 1 };   // FWD: y = a W^T ; DX: y = a W
+enum WFmt { W_BF16 = 0, W_NF4 = 1 };
+enum Epi {
+  EPI_BF16 = 0,     // out bf16 = acc
+  EPI_F32 = 1,      // out f32 = acc
+  EPI_F32_ADD = 2,  // out f32 = add_src + acc   (residual; add_src may alias out)
+  EPI_F32_ACC = 3   // out f32 += acc
+};
+
+struct GemmArgs {
+  int mode = GEMM_FWD;
+  int M = 0;
+  const uint16_t *a = nullptr;  // bf16 [M, Kg], row stride lda elements
+  int lda = 0;
+  // base weight W [Nw, Kw] (out x in)
+  int wfmt = W_NF4;
+  const uint8_t *codes = nullptr;   // NF4: [Nw*Kw/2]
+  const float *absmax = nullptr;    // NF4: [Nw*Kw/64]
+  const uint16_t *w = nullptr;      // bf16: [Nw, Kw], row stride ldw (0 = Kw)
+  int ldw = 0;
+  int Nw = 0, Kw = 0;
+  // LoRA extension: y += ul[M, R] . vl, R a multiple of 64 (0 = none).
+  // FWD: vl is [Ng, R] (row n holds the LoRA "B" row of output n, zero-padded);
+  // DX:  vl is [R, Ng] (row j holds A's row j).
+  const uint16_t *ul = nullptr;
+  const uint16_t *vl = nullptr;
+  int R = 0;
+  int epi = EPI_BF16;
+  void *out = nullptr;
+  int ldo = 0;
+  const float *add_src = nullptr;
+  int ld_add = 0;
+  int *err = nullptr;              // device int: kernels OR error bits into it
+  // derived: Ng = output columns, Kg = reduction length
+  int Ng() const { return mode == GEMM_FWD ? Nw : Kw; }
+  int Kg() const { return mode == GEMM_FWD ? Kw : Nw; }
+};
+
+// Algorithmic work of one call (for the roofline): flops and compulsory bytes.
+double gemm_flops(const GemmArgs &g);
+double gemm_bytes(const GemmArgs &g);
+
+// Enqueue one GEMM on `stream`.  Chooses the tcgen05 kernel when the shape allows it and the
+// tiled fallback otherwise.  Returns 0 or a negative SOUP_E* code (message set).
+int gemm_launch(const GemmArgs &g, cudaStream_t stream);
+// 1 if gemm_launch would take the tensor-core path for this shape.
+int gemm_uses_tc(const GemmArgs &g);
+// Force the fallback path (tests compare the two).
+void gemm_force_fallback(int on);
+
+}  // namespace soup

@@ -1,0 +1,87 @@
+// Launchers of the memory-bound kernels of the step (row norms, RoPE, SwiGLU, LoRA
+// projections and gradients, loss) and of attention.  All reductions run in a fixed order:
+// no floating-point atomics, so every launch is bit-reproducible.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace soup {
+
+constexpr int MAX_SEG = 3;  // projections fused in one GEMM group (q,k,v)
+
+// The 16 NF4 values, passed to kernels by value (they live in the parameter bank).
+struct Codebook {
+  float v[16];
+};
+// The library's codebook (derived once on the host).
+const Codebook &nf4_codebook_param();
+
+// A group of LoRA segments that share one input x: segment p covers output columns
+// [off[p], off[p] + n[p]) of the fused GEMM, with A_p [r, K] and B_p [n[p], r].
+struct LoraSeg {
+  int nseg = 0, r = 0;
+  int off[MAX_SEG] = {0, 0, 0}, n[MAX_SEG] = {0, 0, 0};
+  const float *A[MAX_SEG] = {nullptr, nullptr, nullptr};
+  const float *B[MAX_SEG] = {nullptr, nullptr, nullptr};
+  float *dA[MAX_SEG] = {nullptr, nullptr, nullptr};
+  float *dB[MAX_SEG] = {nullptr, nullptr, nullptr};
+  float s = 1.f;
+  __host__ __device__ int Rpad() const { return ((nseg * r + 63) / 64) * 64; }
+};
+
+void k_embed(const int32_t *tok, const uint16_t *E, int V, int H, int M, float *out, cudaStream_t st);
+void k_rmsnorm_fwd(const float *h, const uint16_t *w, float eps, int M, int H, uint16_t *out,
+                   cudaStream_t st);
+// out = dres + rmsnorm_backward(dy); dres may be null (treated as 0) or alias out.
+void k_rmsnorm_bwd(const float *dy, const float *h, const uint16_t *w, float eps, int M, int H,
+                   const float *dres, float *out, uint16_t *out_bf16, cudaStream_t st);
+void k_rope_fwd(uint16_t *qkv, int ld, const float *cos, const float *sin, int M, int S, int nh,
+                int nkv, int d, cudaStream_t st);
+// in: dqkv float [M, ld]; out bf16 [M, ld]: q/k heads rotated back, v heads cast.
+void k_rope_bwd(const float *dqkv, uint16_t *out, int ld, const float *cos, const float *sin,
+                int M, int S, int nh, int nkv, int d, cudaStream_t st);
+void k_swiglu_fwd(const uint16_t *gu, int M, int I, uint16_t *act, cudaStream_t st);
+void k_swiglu_bwd(const float *dact, const uint16_t *gu, int M, int I, uint16_t *dgu, cudaStream_t st);
+
+// u = x A^T per segment -> u_f32 [M, nseg*r]; ul = bf16(s * u) [M, Rpad] (zero padded)
+void k_lora_down(const uint16_t *x, int lda, int M, int K, const LoraSeg &L, float *u_f32,
+                 uint16_t *ul, cudaStream_t st);
+// du_p = s dY_p B_p -> du_f32 [M, nseg*r]; dul = bf16(du) [M, Rpad]
+void k_lora_du(const uint16_t *dy, int ldy, int M, const LoraSeg &L, float *du_f32, uint16_t *dul,
+               cudaStream_t st);
+// dB_p = s dY_p^T u_p   (written into L.dB)
+void k_lora_dB(const uint16_t *dy, int ldy, int M, const float *u_f32, const LoraSeg &L, cudaStream_t st);
+// dA_p = du_p^T x       (written into L.dA)
+void k_lora_dA(const float *du_f32, const uint16_t *x, int lda, int M, int K, const LoraSeg &L,
+               cudaStream_t st);
+// Vl [Ng, Rpad]: row n of segment p holds bf16(B_p[n - off_p, :]) at columns p*r .. p*r+r-1
+void k_pack_fwd(const LoraSeg &L, int Ng, uint16_t *vl, cudaStream_t st);
+// Acat [Rpad, K]: row p*r + j holds bf16(A_p[j, :]); rows past nseg*r are zero
+void k_pack_bwd(const LoraSeg &L, int K, uint16_t *acat, cudaStream_t st);
+
+// Vocabulary-chunked cross-entropy.  Rows are tokens b*S + t; row t has label tok[b*S+t+1]
+// for t < S-1 and none for t = S-1.
+void k_ce_chunk_fwd(const float *z, int ldz, int v0, int vc, const int32_t *tok, int M, int S,
+                    int first, float *rmax, float *rsum, float *zlab, cudaStream_t st);
+void k_ce_finalize(const float *rmax, const float *rsum, const float *zlab, int M, int S,
+                   float *lse, float *loss, cudaStream_t st);
+void k_ce_chunk_bwd(const float *z, int ldz, int v0, int vc, const float *lse, const int32_t *tok,
+                    int M, int S, float inv_n, uint16_t *dz, cudaStream_t st);
+
+void k_cast_bf16(const float *in, uint16_t *out, int64_t n, cudaStream_t st);
+void k_nf4_dequant(const uint8_t *codes, const float *absmax, int64_t n, float *out_f32,
+                   uint16_t *out_bf16, cudaStream_t st);
+
+// Causal GQA attention on the fused qkv buffer [M, ld] (q heads, then k heads, then v heads,
+// each head_dim wide), rows b*S + t.  o: bf16 [M, nh*d]; lse: float [B*nh*S] (base-2 log-sum
+// of exp2(scale*log2e*score)).  head_dim 64 or 128.
+int k_attn_fwd(const uint16_t *qkv, int ld, int B, int S, int nh, int nkv, int d, uint16_t *o,
+               float *lse, cudaStream_t st);
+// dO: bf16 [M, nh*d]; dqkv: float [M, ld] written completely (dq, dk, dv);
+// scratch: float [attn_bwd_scratch_floats()].
+size_t attn_bwd_scratch_floats(int B, int S, int nh, int d);
+int k_attn_bwd(const uint16_t *qkv, int ld, const uint16_t *o, const uint16_t *dO,
+               const float *lse, int B, int S, int nh, int nkv, int d, float *scratch, float *dqkv,
+               cudaStream_t st);
+
+}  // namespace soup

@@ -1,0 +1,646 @@
+// The streamed LoRA step: workspace plan, slot scheduling on a dedicated copy stream, and
+// the per-layer forward / recompute / backward built from the library's kernels.
+//
+// "About Soup" and "Layer streaming: fine-tune a model that does not fit in your card",
+// "How it works": each decoder layer is copied into one of N pre-allocated device buffers
+// on a dedicated stream so the load of the next layer overlaps the compute of the current
+// one; the same kernels run on the same weight bytes as a resident run; each layer is read
+// twice per step because the backward recomputes the layer and needs W^T dL/dy.
+// "Read this first": above ~165 MiB per layer the pages' stack read a buffer that had
+// already been refilled with another layer.  Here every use of a slot is ordered by two
+// events: `ready` (copy -> compute, recorded after the copy) and `freed` (compute -> copy,
+// recorded after the last kernel that reads the slot); a copy into a slot waits on that
+// slot's `freed`, and no kernel keeps a weight pointer beyond its own launch.
+#include "step.h"
+
+#include <algorithm>
+#include <chrono>
+#include <cmath>
+#include <cstring>
+#include <thread>
+
+#include "gemm.h"
+#include "kernels.h"
+#include "store.h"
+#include "util.h"
+
+namespace soup {
+
+static uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
+
+int ce_chunk_cols(int M, int V) {
+  int vc = (int)((1ull << 24) / (uint64_t)std::max(M, 1) / 256ull) * 256;
+  vc = std::max(256, std::min(vc, 32768));
+  if (vc >= V) vc = (int)align_up((uint64_t)(V + 1) / 2, 256);  // at least two chunks
+  return std::max(vc, 256);
+}
+
+int make_plan(const soup_cfg *c, int maxB, int maxS, int n_slots, int resident, Plan *P) {
+  SOUP_TRY(validate_cfg(c));
+  if (maxB < 1 || maxS < 2) return set_error(SOUP_EINVAL, "max_batch >= 1 and max_seq >= 2 required");
+  if (!resident && (n_slots < 2 || n_slots > 8)) return set_error(SOUP_EINVAL, "n_slots must be in [2, 8]");
+  soup_shard_layout L;
+  SOUP_TRY(shard_layout(c, &L));
+  *P = Plan();
+  const uint64_t M = (uint64_t)maxB * maxS, H = c->hidden, I = c->inter;
+  const uint64_t qd = (uint64_t)c->n_heads * c->head_dim, kvd = (uint64_t)c->n_kv_heads * c->head_dim;
+  const uint64_t nqkv = qd + 2 * kvd;
+  uint64_t off = 0;
+  auto take = [&](uint64_t bytes) {
+    const uint64_t o = off;
+    off = align_up(off + std::max<uint64_t>(bytes, 1), 1024);
+    return o;
+  };
+  P->n_slots = resident ? c->n_layers : n_slots;
+  P->slots = take(L.stride * (uint64_t)P->n_slots);
+  P->h_all = take(4 * (c->n_layers + 1ull) * M * H);
+  P->hm = take(4 * M * H);
+  P->x1 = take(2 * M * H);
+  P->x2 = take(2 * M * H);
+  P->qkv = take(2 * M * nqkv);
+  P->att = take(2 * M * qd);
+  P->lse = take(4 * M * c->n_heads);
+  P->gu = take(4 * M * I);
+  P->act = take(2 * M * I);
+  for (int g = 0; g < 4; ++g) {
+    P->u_f32[g] = take(4 * M * 64);
+    P->u_b[g] = take(2 * M * 64);
+  }
+  P->dh = take(4 * M * H);
+  P->dhm = take(4 * M * H);
+  P->dh_b = take(2 * M * H);
+  P->dhm_b = take(2 * M * H);
+  P->dact = take(4 * M * I);
+  P->dgu = take(4 * M * I);
+  P->dx = take(4 * M * H);
+  P->datt = take(4 * M * qd);
+  P->datt_b = take(2 * M * qd);
+  P->dqkv = take(4 * M * nqkv);
+  P->dqkv_b = take(2 * M * nqkv);
+  P->attn_scratch = take(4 * attn_bwd_scratch_floats(maxB, maxS, c->n_heads, c->head_dim));
+  P->du_f32 = take(4 * M * 64);
+  P->du_b = take(2 * M * 64);
+  P->hn = take(2 * M * H);
+  P->vc = ce_chunk_cols((int)M, c->vocab);
+  P->z = take(4 * M * (uint64_t)P->vc);
+  P->dz = take(2 * M * (uint64_t)P->vc);
+  P->dhn = take(4 * M * H);
+  P->ce_max = take(4 * M);
+  P->ce_sum = take(4 * M);
+  P->ce_lab = take(4 * M);
+  P->ce_lse = take(4 * M);
+  const int r = c->lora_r;
+  const int nseg[4] = {3, 1, 2, 1};
+  P->vl.resize((size_t)c->n_layers * 4);
+  P->ac.resize((size_t)c->n_layers * 4);
+  for (int l = 0; l < c->n_layers; ++l)
+    for (int g = 0; g < 4; ++g) {
+      const uint64_t rp = align_up((uint64_t)nseg[g] * r, 64);
+      P->vl[(size_t)l * 4 + g] = take(2 * (uint64_t)L.n_out[g] * rp);
+      P->ac[(size_t)l * 4 + g] = take(2 * rp * (uint64_t)L.n_in[g]);
+    }
+  P->rope_cos = take(4ull * maxS * (c->head_dim / 2));
+  P->rope_sin = take(4ull * maxS * (c->head_dim / 2));
+  P->err = take(64);
+  P->total = off;
+  return 0;
+}
+
+// ------------------------------------------------------------------------------------------
+namespace {
+
+inline float *F(soup_stream *h, uint64_t off) { return reinterpret_cast<float *>(h->ws + off); }
+inline uint16_t *B16(soup_stream *h, uint64_t off) { return reinterpret_cast<uint16_t *>(h->ws + off); }
+
+int check_cuda(const char *what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(SOUP_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+  return 0;
+}
+
+void harvest(soup_stream *h, bool block) {
+  auto run = [&](std::vector<TimedEv> &v, double &ms_sum, uint64_t *count, double *flops,
+                 double *bytes) {
+    size_t keep = 0;
+    for (size_t i = 0; i < v.size(); ++i) {
+      TimedEv &e = v[i];
+      cudaError_t q = block ? cudaEventSynchronize(e.end) : cudaEventQuery(e.end);
+      if (q == cudaSuccess) {
+        float ms = 0.f;
+        cudaEventElapsedTime(&ms, e.start, e.end);
+        ms_sum += ms;
+        if (count) ++*count;
+        if (flops) *flops += e.flops;
+        if (bytes) *bytes += e.bytes;
+        cudaEventDestroy(e.start);
+        cudaEventDestroy(e.end);
+      } else {
+        if (q != cudaErrorNotReady) (void)cudaGetLastError();
+        v[keep++] = e;
+      }
+    }
+    v.resize(keep);
+  };
+  run(h->copy_ev, h->stats.copy_ms, nullptr, nullptr, nullptr);
+  run(h->gemm_ev, h->stats.gemm_ms, &h->stats.gemm_launches, &h->stats.gemm_flops,
+      &h->stats.gemm_bytes);
+}
+
+int timed_gemm(soup_stream *h, GemmArgs &g) {
+  g.err = h->err_dev;
+  if (!h->dbg_profile) return gemm_launch(g, h->cs);
+  TimedEv e;
+  e.flops = gemm_flops(g);
+  e.bytes = gemm_bytes(g);
+  SOUP_CUDA_TRY(cudaEventCreate(&e.start));
+  SOUP_CUDA_TRY(cudaEventCreate(&e.end));
+  SOUP_CUDA_TRY(cudaEventRecord(e.start, h->cs));
+  int rc = gemm_launch(g, h->cs);
+  SOUP_CUDA_TRY(cudaEventRecord(e.end, h->cs));
+  h->gemm_ev.push_back(e);
+  return rc;
+}
+
+// Weight operand of group g inside a shard (slot, resident array, or any device copy).
+GemmArgs weight_args(soup_stream *h, const uint8_t *shard, int g, int mode) {
+  GemmArgs a;
+  a.mode = mode;
+  const soup_shard_layout &L = h->lay;
+  a.Nw = L.n_out[g];
+  a.Kw = L.n_in[g];
+  if (h->cfg.base_fmt == SOUP_FMT_NF4) {
+    a.wfmt = W_NF4;
+    a.codes = shard + L.w_off[g];
+    a.absmax = reinterpret_cast<const float *>(shard + L.a_off[g]);
+  } else {
+    a.wfmt = W_BF16;
+    a.w = reinterpret_cast<const uint16_t *>(shard + L.w_off[g]);
+  }
+  return a;
+}
+
+LoraSeg make_seg(soup_stream *h, int layer, int g, bool grads) {
+  const soup_cfg &c = h->cfg;
+  LoraSeg L;
+  L.r = c.lora_r;
+  L.s = c.lora_alpha / (float)c.lora_r;
+  static const int first[4] = {SOUP_Q, SOUP_O, SOUP_GATE, SOUP_DOWN};
+  static const int nseg[4] = {3, 1, 2, 1};
+  L.nseg = nseg[g];
+  const int qd = c.n_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim;
+  int sizes[7] = {qd, kvd, kvd, c.hidden, c.inter, c.inter, c.hidden};
+  int off = 0;
+  for (int p = 0; p < L.nseg; ++p) {
+    const int proj = first[g] + p;
+    const size_t idx = (size_t)layer * 7 + proj;
+    L.off[p] = off;
+    L.n[p] = sizes[proj];
+    off += sizes[proj];
+    L.A[p] = h->lora_A[idx];
+    L.B[p] = h->lora_B[idx];
+    if (grads) {
+      L.dA[p] = h->grad_A[idx];
+      L.dB[p] = h->grad_B[idx];
+    }
+  }
+  return L;
+}
+
+// ---------------------------------------------------------------- slot scheduling
+// Next position >= from at which `layer` is used in seq (INT32_MAX if never).
+int next_use(const std::vector<int> &seq, size_t from, int layer) {
+  for (size_t j = from; j < seq.size(); ++j)
+    if (seq[j] == layer) return (int)j;
+  return INT32_MAX;
+}
+
+int issue_copy(soup_stream *h, int slot, int layer) {
+  Slot &s = h->slot[slot];
+  SOUP_CUDA_TRY(cudaStreamWaitEvent(h->xs, s.freed, 0));  // WAR: last reader of the slot done
+  TimedEv e;
+  e.bytes = (double)h->lay.stride;
+  SOUP_CUDA_TRY(cudaEventCreate(&e.start));
+  SOUP_CUDA_TRY(cudaEventCreate(&e.end));
+  SOUP_CUDA_TRY(cudaEventRecord(e.start, h->xs));
+  SOUP_CUDA_TRY(cudaMemcpyAsync(s.dev, h->store->base + (uint64_t)layer * h->lay.stride, h->lay.stride,
+                                cudaMemcpyHostToDevice, h->xs));
+  SOUP_CUDA_TRY(cudaEventRecord(e.end, h->xs));
+  SOUP_CUDA_TRY(cudaEventRecord(s.ready, h->xs));         // RAW: the copy landed
+  h->copy_ev.push_back(e);
+  s.layer = layer;
+  s.pending = 1;
+  h->stats.copies += 1;
+  h->stats.copy_bytes += h->lay.stride;
+  return 0;
+}
+
+// Make sure seq[pos..pos+look] are resident or in flight; Belady choice of the victim among
+// slots: evict the one whose content is needed furthest in the future (never one needed
+// before the layer being fetched).
+int prefetch(soup_stream *h, const std::vector<int> &seq, size_t pos, int look) {
+  for (size_t j = pos; j < seq.size() && j <= pos + (size_t)look; ++j) {
+    const int layer = seq[j];
+    bool have = false;
+    for (auto &s : h->slot) have |= (s.layer == layer);
+    if (have) continue;
+    int victim = -1, far = -1;
+    uint64_t oldest = UINT64_MAX;
+    for (int k = 0; k < (int)h->slot.size(); ++k) {
+      const int nu = h->slot[k].layer < 0 ? INT32_MAX : next_use(seq, pos, h->slot[k].layer);
+      const uint64_t t = h->slot[k].layer < 0 ? 0 : h->slot[k].tick;
+      if (nu > far || (nu == far && t < oldest)) {  // ties: least recently released
+        far = nu;
+        oldest = t;
+        victim = k;
+      }
+    }
+    if (victim < 0 || far <= (int)j) break;  // every slot is needed before this layer
+    SOUP_TRY(issue_copy(h, victim, layer));
+  }
+  return 0;
+}
+
+// Device pointer of `layer`'s shard for the use at position pos; waits for its copy.
+int acquire(soup_stream *h, const std::vector<int> &seq, size_t pos, const uint8_t **shard,
+            int *slot_out) {
+  const int layer = seq[pos];
+  if (h->resident) {
+    *shard = h->ws + h->plan.slots + (uint64_t)layer * h->lay.stride;
+    *slot_out = -1;
+    return 0;
+  }
+  SOUP_TRY(prefetch(h, seq, pos, 0));
+  int s = -1;
+  for (int k = 0; k < (int)h->slot.size(); ++k)
+    if (h->slot[k].layer == layer) s = k;
+  if (s < 0) return set_error(SOUP_ESTATE, "internal: layer %d has no slot", layer);
+  if (h->slot[s].pending) {
+    SOUP_CUDA_TRY(cudaStreamWaitEvent(h->cs, h->slot[s].ready, 0));
+    h->slot[s].pending = 0;
+  }
+  int use = s;
+  if (h->dbg_stale && h->in_bwd) use = (s + 1) % (int)h->slot.size();  // deliberately wrong
+  *shard = h->slot[use].dev;
+  *slot_out = s;
+  return 0;
+}
+
+int release(soup_stream *h, int slot) {
+  if (slot < 0) return 0;
+  SOUP_CUDA_TRY(cudaEventRecord(h->slot[slot].freed, h->cs));
+  h->slot[slot].tick = ++h->tick;
+  return 0;
+}
+
+// ---------------------------------------------------------------- layer maths
+int layer_forward(soup_stream *h, int li, const uint8_t *shard, bool recompute) {
+  const soup_cfg &c = h->cfg;
+  const Plan &P = h->plan;
+  const soup_shard_layout &SL = h->lay;
+  cudaStream_t st = h->cs;
+  const int B = h->B, S = h->S, M = B * S, H = c.hidden, I = c.inter;
+  const int qd = c.n_heads * c.head_dim, nqkv = SL.n_out[SOUP_G_QKV];
+  const float *hin = F(h, P.h_all) + (size_t)li * M * H;
+  const uint16_t *ln1 = reinterpret_cast<const uint16_t *>(shard + SL.ln1_off);
+  const uint16_t *ln2 = reinterpret_cast<const uint16_t *>(shard + SL.ln2_off);
+  LoraSeg Lq = make_seg(h, li, SOUP_G_QKV, false), Lo = make_seg(h, li, SOUP_G_O, false),
+          Lg = make_seg(h, li, SOUP_G_GU, false), Ld = make_seg(h, li, SOUP_G_DOWN, false);
+
+  k_rmsnorm_fwd(hin, ln1, c.rms_eps, M, H, B16(h, P.x1), st);
+  k_lora_down(B16(h, P.x1), H, M, H, Lq, F(h, P.u_f32[0]), B16(h, P.u_b[0]), st);
+  {
+    GemmArgs g = weight_args(h, shard, SOUP_G_QKV, GEMM_FWD);
+    g.M = M; g.a = B16(h, P.x1); g.lda = H;
+    g.ul = B16(h, P.u_b[0]); g.vl = B16(h, P.vl[(size_t)li * 4 + 0]); g.R = Lq.Rpad();
+    g.epi = EPI_BF16; g.out = B16(h, P.qkv); g.ldo = nqkv;
+    SOUP_TRY(timed_gemm(h, g));
+  }
+  k_rope_fwd(B16(h, P.qkv), nqkv, F(h, P.rope_cos), F(h, P.rope_sin), M, S, c.n_heads,
+             c.n_kv_heads, c.head_dim, st);
+  SOUP_TRY(k_attn_fwd(B16(h, P.qkv), nqkv, B, S, c.n_heads, c.n_kv_heads, c.head_dim,
+                      B16(h, P.att), F(h, P.lse), st));
+  k_lora_down(B16(h, P.att), qd, M, qd, Lo, F(h, P.u_f32[1]), B16(h, P.u_b[1]), st);
+  {
+    GemmArgs g = weight_args(h, shard, SOUP_G_O, GEMM_FWD);
+    g.M = M; g.a = B16(h, P.att); g.lda = qd;
+    g.ul = B16(h, P.u_b[1]); g.vl = B16(h, P.vl[(size_t)li * 4 + 1]); g.R = Lo.Rpad();
+    g.epi = EPI_F32_ADD; g.add_src = hin; g.ld_add = H; g.out = F(h, P.hm); g.ldo = H;
+    SOUP_TRY(timed_gemm(h, g));
+  }
+  k_rmsnorm_fwd(F(h, P.hm), ln2, c.rms_eps, M, H, B16(h, P.x2), st);
+  k_lora_down(B16(h, P.x2), H, M, H, Lg, F(h, P.u_f32[2]), B16(h, P.u_b[2]), st);
+  {
+    GemmArgs g = weight_args(h, shard, SOUP_G_GU, GEMM_FWD);
+    g.M = M; g.a = B16(h, P.x2); g.lda = H;
+    g.ul = B16(h, P.u_b[2]); g.vl = B16(h, P.vl[(size_t)li * 4 + 2]); g.R = Lg.Rpad();
+    g.epi = EPI_BF16; g.out = B16(h, P.gu); g.ldo = 2 * I;
+    SOUP_TRY(timed_gemm(h, g));
+  }
+  k_swiglu_fwd(B16(h, P.gu), M, I, B16(h, P.act), st);
+  k_lora_down(B16(h, P.act), I, M, I, Ld, F(h, P.u_f32[3]), B16(h, P.u_b[3]), st);
+  if (!recompute) {
+    GemmArgs g = weight_args(h, shard, SOUP_G_DOWN, GEMM_FWD);
+    g.M = M; g.a = B16(h, P.act); g.lda = I;
+    g.ul = B16(h, P.u_b[3]); g.vl = B16(h, P.vl[(size_t)li * 4 + 3]); g.R = Ld.Rpad();
+    g.epi = EPI_F32_ADD; g.add_src = F(h, P.hm); g.ld_add = H;
+    g.out = F(h, P.h_all) + (size_t)(li + 1) * M * H; g.ldo = H;
+    SOUP_TRY(timed_gemm(h, g));
+  }
+  return check_cuda("layer forward");
+}
+
+// Backward of one projection group: LoRA gradients and dX (= dY W + s (dY B) A, float out).
+int group_backward(soup_stream *h, int li, const uint8_t *shard, int grp, const uint16_t *dy,
+                   int ldy, const uint16_t *x, int ldx, float *dx_out) {
+  const Plan &P = h->plan;
+  cudaStream_t st = h->cs;
+  const int M = h->B * h->S;
+  LoraSeg L = make_seg(h, li, grp, true);
+  const int K = h->lay.n_in[grp];
+  k_lora_du(dy, ldy, M, L, F(h, P.du_f32), B16(h, P.du_b), st);
+  k_lora_dB(dy, ldy, M, F(h, P.u_f32[grp]), L, st);
+  k_lora_dA(F(h, P.du_f32), x, ldx, M, K, L, st);
+  GemmArgs g = weight_args(h, shard, grp, GEMM_DX);
+  g.M = M; g.a = dy; g.lda = ldy;
+  g.ul = B16(h, P.du_b); g.vl = B16(h, P.ac[(size_t)li * 4 + grp]); g.R = L.Rpad();
+  g.epi = EPI_F32; g.out = dx_out; g.ldo = K;
+  return timed_gemm(h, g);
+}
+
+int layer_backward(soup_stream *h, int li, const uint8_t *shard) {
+  const soup_cfg &c = h->cfg;
+  const Plan &P = h->plan;
+  const soup_shard_layout &SL = h->lay;
+  cudaStream_t st = h->cs;
+  const int B = h->B, S = h->S, M = B * S, H = c.hidden, I = c.inter;
+  const int qd = c.n_heads * c.head_dim, nqkv = SL.n_out[SOUP_G_QKV];
+  const float *hin = F(h, P.h_all) + (size_t)li * M * H;
+  const uint16_t *ln1 = reinterpret_cast<const uint16_t *>(shard + SL.ln1_off);
+  const uint16_t *ln2 = reinterpret_cast<const uint16_t *>(shard + SL.ln2_off);
+
+  // dh / dh_b hold dL/dh_{li+1}
+  SOUP_TRY(group_backward(h, li, shard, SOUP_G_DOWN, B16(h, P.dh_b), H, B16(h, P.act), I, F(h, P.dact)));
+  k_swiglu_bwd(F(h, P.dact), B16(h, P.gu), M, I, B16(h, P.dgu), st);
+  SOUP_TRY(group_backward(h, li, shard, SOUP_G_GU, B16(h, P.dgu), 2 * I, B16(h, P.x2), H, F(h, P.dx)));
+  k_rmsnorm_bwd(F(h, P.dx), F(h, P.hm), ln2, c.rms_eps, M, H, F(h, P.dh), F(h, P.dhm), B16(h, P.dhm_b), st);
+  SOUP_TRY(group_backward(h, li, shard, SOUP_G_O, B16(h, P.dhm_b), H, B16(h, P.att), qd, F(h, P.datt)));
+  k_cast_bf16(F(h, P.datt), B16(h, P.datt_b), (int64_t)M * qd, st);
+  SOUP_TRY(k_attn_bwd(B16(h, P.qkv), nqkv, B16(h, P.att), B16(h, P.datt_b), F(h, P.lse), B, S,
+                      c.n_heads, c.n_kv_heads, c.head_dim, F(h, P.attn_scratch), F(h, P.dqkv), st));
+  k_rope_bwd(F(h, P.dqkv), B16(h, P.dqkv_b), nqkv, F(h, P.rope_cos), F(h, P.rope_sin), M, S,
+             c.n_heads, c.n_kv_heads, c.head_dim, st);
+  SOUP_TRY(group_backward(h, li, shard, SOUP_G_QKV, B16(h, P.dqkv_b), nqkv, B16(h, P.x1), H, F(h, P.dx)));
+  k_rmsnorm_bwd(F(h, P.dx), hin, ln1, c.rms_eps, M, H, F(h, P.dhm), F(h, P.dh), B16(h, P.dh_b), st);
+  return check_cuda("layer backward");
+}
+
+const uint16_t *lm_weight(soup_stream *h) { return h->lm_head ? h->lm_head : h->embed; }
+
+}  // namespace
+
+// ------------------------------------------------------------------------------------------
+int stream_init(soup_store *st, const soup_cfg *c, int maxB, int maxS, void *ws, uint64_t ws_bytes,
+                const void *embed, const void *lm_head, const void *final_norm, uintptr_t cs,
+                uintptr_t xs, int n_slots, int resident, soup_stream **out) {
+  if (!out) return set_error(SOUP_EINVAL, "out is NULL");
+  *out = nullptr;
+  if (!st || !c || !ws || !embed || !final_norm)
+    return set_error(SOUP_EINVAL, "stream_init: NULL argument");
+  if (!c->tied && !lm_head) return set_error(SOUP_EINVAL, "untied config needs lm_head");
+  if (std::memcmp(&st->cfg, c, sizeof(soup_cfg)) != 0)
+    return set_error(SOUP_EINVAL, "stream_init: cfg differs from the store's");
+  for (int l = 0; l < c->n_layers; ++l)
+    if (!st->filled[l]) return set_error(SOUP_ESTATE, "store layer %d was never filled", l);
+  if (cs == xs && !resident) return set_error(SOUP_EINVAL, "compute and copy streams must differ");
+  if (reinterpret_cast<uintptr_t>(ws) % 256) return set_error(SOUP_EINVAL, "workspace must be 256-byte aligned");
+  Plan P;
+  SOUP_TRY(make_plan(c, maxB, maxS, n_slots, resident, &P));
+  if (ws_bytes < P.total)
+    return set_error(SOUP_ENOMEM, "workspace %llu bytes < required %llu",
+                     (unsigned long long)ws_bytes, (unsigned long long)P.total);
+  soup_stream *h = new (std::nothrow) soup_stream();
+  if (!h) return set_error(SOUP_ENOMEM, "host allocation failed");
+  h->cfg = *c;
+  h->store = st;
+  h->plan = P;
+  h->lay = st->lay;
+  h->maxB = maxB;
+  h->maxS = maxS;
+  h->resident = resident ? 1 : 0;
+  h->cs = reinterpret_cast<cudaStream_t>(cs);
+  h->xs = reinterpret_cast<cudaStream_t>(xs);
+  h->ws = static_cast<uint8_t *>(ws);
+  h->embed = static_cast<const uint16_t *>(embed);
+  h->lm_head = c->tied ? nullptr : static_cast<const uint16_t *>(lm_head);
+  h->final_norm = static_cast<const uint16_t *>(final_norm);
+  h->err_dev = reinterpret_cast<int *>(h->ws + P.err);
+  auto fail = [&](int rc) {
+    soup_stream_free_impl(h);
+    return rc;
+  };
+  if (cudaMemsetAsync(h->err_dev, 0, 64, h->cs) != cudaSuccess)
+    return fail(set_error(SOUP_ECUDA, "workspace memset failed"));
+  // RoPE tables: angle pos * theta^(-2i/d) formed in double, cos/sin rounded to float.
+  {
+    const int half = c->head_dim / 2;
+    std::vector<float> cs_h((size_t)maxS * half), sn_h((size_t)maxS * half);
+    for (int p = 0; p < maxS; ++p)
+      for (int i = 0; i < half; ++i) {
+        const double inv = std::pow((double)c->rope_theta, -(2.0 * i) / c->head_dim);
+        const double a = p * inv;
+        cs_h[(size_t)p * half + i] = (float)std::cos(a);
+        sn_h[(size_t)p * half + i] = (float)std::sin(a);
+      }
+    if (cudaMemcpy(h->ws + P.rope_cos, cs_h.data(), cs_h.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemcpy(h->ws + P.rope_sin, sn_h.data(), sn_h.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess)
+      return fail(set_error(SOUP_ECUDA, "rope table upload failed"));
+  }
+  if (h->resident) {
+    for (int l = 0; l < c->n_layers; ++l) {
+      if (cudaMemcpy(h->ws + P.slots + (uint64_t)l * h->lay.stride, st->base + (uint64_t)l * h->lay.stride,
+                     h->lay.stride, cudaMemcpyHostToDevice) != cudaSuccess)
+        return fail(set_error(SOUP_ECUDA, "resident upload of layer %d failed", l));
+    }
+  } else {
+    h->slot.resize(n_slots);
+    for (int k = 0; k < n_slots; ++k) {
+      Slot &s = h->slot[k];
+      s.dev = h->ws + P.slots + (uint64_t)k * h->lay.stride;
+      if (cudaEventCreateWithFlags(&s.ready, cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&s.freed, cudaEventDisableTiming) != cudaSuccess)
+        return fail(set_error(SOUP_ECUDA, "event creation failed"));
+      s.has_events = 1;
+      // an unrecorded event counts as complete for cudaStreamWaitEvent
+    }
+  }
+  if (cudaEventCreateWithFlags(&h->done, cudaEventDisableTiming) != cudaSuccess)
+    return fail(set_error(SOUP_ECUDA, "event creation failed"));
+  SOUP_TRY(check_cuda("stream_init"));
+  *out = h;
+  return 0;
+}
+
+int step_fwd(soup_stream *h, const int32_t *tokens, int B, int S, const float *const *lA,
+             const float *const *lB, float *loss, float *logits, float *layer_out) {
+  if (!h || !tokens || !lA || !lB || !loss) return set_error(SOUP_EINVAL, "step_fwd: NULL argument");
+  const soup_cfg &c = h->cfg;
+  if (B < 1 || S < 2 || S > h->maxS || (int64_t)B * S > (int64_t)h->maxB * h->maxS)
+    return set_error(SOUP_EINVAL, "step_fwd: B=%d S=%d outside the workspace (max %d x %d)", B, S,
+                     h->maxB, h->maxS);
+  const int L = c.n_layers;
+  for (int i = 0; i < L * 7; ++i)
+    if (!lA[i] || !lB[i]) return set_error(SOUP_EINVAL, "step_fwd: LoRA pointer %d is NULL", i);
+  h->B = B;
+  h->S = S;
+  h->tokens = tokens;
+  h->lora_A.assign(lA, lA + (size_t)L * 7);
+  h->lora_B.assign(lB, lB + (size_t)L * 7);
+  h->in_bwd = 0;
+  harvest(h, false);
+  const Plan &P = h->plan;
+  cudaStream_t st = h->cs;
+  const int M = B * S, H = c.hidden;
+  // bf16 LoRA operands for the tensor-core GEMMs of every layer
+  for (int l = 0; l < L; ++l)
+    for (int g = 0; g < 4; ++g) {
+      LoraSeg Lg = make_seg(h, l, g, false);
+      k_pack_fwd(Lg, h->lay.n_out[g], B16(h, P.vl[(size_t)l * 4 + g]), st);
+      k_pack_bwd(Lg, h->lay.n_in[g], B16(h, P.ac[(size_t)l * 4 + g]), st);
+    }
+  k_embed(tokens, h->embed, c.vocab, H, M, F(h, P.h_all), st);
+  std::vector<int> seq(L);
+  for (int i = 0; i < L; ++i) seq[i] = i;
+  const int look = std::max(0, (int)h->slot.size() - 1);
+  for (int i = 0; i < L; ++i) {
+    const uint8_t *shard;
+    int s;
+    SOUP_TRY(acquire(h, seq, (size_t)i, &shard, &s));
+    SOUP_TRY(layer_forward(h, i, shard, false));
+    SOUP_TRY(release(h, s));
+    if (!h->resident) SOUP_TRY(prefetch(h, seq, (size_t)i + 1, look - 1));
+  }
+  // final norm + vocabulary-chunked loss
+  k_rmsnorm_fwd(F(h, P.h_all) + (size_t)L * M * H, h->final_norm, c.rms_eps, M, H, B16(h, P.hn), st);
+  const int vc = P.vc;
+  for (int v0 = 0, ci = 0; v0 < c.vocab; v0 += vc, ++ci) {
+    const int n = std::min(vc, c.vocab - v0);
+    GemmArgs g;
+    g.mode = GEMM_FWD; g.wfmt = W_BF16; g.w = lm_weight(h) + (size_t)v0 * H; g.Nw = n; g.Kw = H;
+    g.M = M; g.a = B16(h, P.hn); g.lda = H; g.epi = EPI_F32;
+    float *z = logits ? logits + v0 : F(h, P.z);
+    const int ldz = logits ? c.vocab : vc;
+    g.out = z; g.ldo = ldz; g.err = h->err_dev;
+    SOUP_TRY(gemm_launch(g, st));
+    k_ce_chunk_fwd(z, ldz, v0, n, tokens, M, S, ci == 0, F(h, P.ce_max), F(h, P.ce_sum), F(h, P.ce_lab), st);
+  }
+  k_ce_finalize(F(h, P.ce_max), F(h, P.ce_sum), F(h, P.ce_lab), M, S, F(h, P.ce_lse), loss, st);
+  if (layer_out)
+    SOUP_CUDA_TRY(cudaMemcpyAsync(layer_out, F(h, P.h_all), 4ull * (L + 1) * M * H,
+                                  cudaMemcpyDeviceToDevice, st));
+  SOUP_CUDA_TRY(cudaEventRecord(h->done, st));
+  h->fwd_ready = 1;
+  h->stats.steps_fwd += 1;
+  return check_cuda("step_fwd");
+}
+
+int step_bwd(soup_stream *h, float *const *dA, float *const *dB, float *dh_out) {
+  if (!h || !dA || !dB) return set_error(SOUP_EINVAL, "step_bwd: NULL argument");
+  if (!h->fwd_ready) return set_error(SOUP_ESTATE, "step_bwd without a preceding step_fwd");
+  const soup_cfg &c = h->cfg;
+  const int L = c.n_layers;
+  for (int i = 0; i < L * 7; ++i)
+    if (!dA[i] || !dB[i]) return set_error(SOUP_EINVAL, "step_bwd: gradient pointer %d is NULL", i);
+  h->grad_A.assign(dA, dA + (size_t)L * 7);
+  h->grad_B.assign(dB, dB + (size_t)L * 7);
+  h->in_bwd = 1;
+  harvest(h, false);
+  const Plan &P = h->plan;
+  cudaStream_t st = h->cs;
+  const int B = h->B, S = h->S, M = B * S, H = c.hidden;
+  // loss backward, chunk by chunk: recompute logits, dz = (softmax - onehot) / N, dhn += dz W
+  const int vc = P.vc;
+  const float inv_n = 1.0f / (float)((int64_t)B * (S - 1));
+  for (int v0 = 0, ci = 0; v0 < c.vocab; v0 += vc, ++ci) {
+    const int n = std::min(vc, c.vocab - v0);
+    const uint16_t *w = lm_weight(h) + (size_t)v0 * H;
+    GemmArgs g;
+    g.mode = GEMM_FWD; g.wfmt = W_BF16; g.w = w; g.Nw = n; g.Kw = H;
+    g.M = M; g.a = B16(h, P.hn); g.lda = H; g.epi = EPI_F32; g.out = F(h, P.z); g.ldo = vc;
+    g.err = h->err_dev;
+    SOUP_TRY(gemm_launch(g, st));
+    k_ce_chunk_bwd(F(h, P.z), vc, v0, n, F(h, P.ce_lse), h->tokens, M, S, inv_n, B16(h, P.dz), st);
+    GemmArgs d;
+    d.mode = GEMM_DX; d.wfmt = W_BF16; d.w = w; d.Nw = n; d.Kw = H;
+    d.M = M; d.a = B16(h, P.dz); d.lda = vc; d.epi = ci == 0 ? EPI_F32 : EPI_F32_ACC;
+    d.out = F(h, P.dhn); d.ldo = H; d.err = h->err_dev;
+    SOUP_TRY(gemm_launch(d, st));
+  }
+  k_rmsnorm_bwd(F(h, P.dhn), F(h, P.h_all) + (size_t)L * M * H, h->final_norm, c.rms_eps, M, H,
+                nullptr, F(h, P.dh), B16(h, P.dh_b), st);
+  if (dh_out)
+    SOUP_CUDA_TRY(cudaMemcpyAsync(dh_out + (size_t)L * M * H, F(h, P.dh), 4ull * M * H,
+                                  cudaMemcpyDeviceToDevice, st));
+  std::vector<int> seq(L);
+  for (int i = 0; i < L; ++i) seq[i] = L - 1 - i;
+  const int look = std::max(0, (int)h->slot.size() - 1);
+  for (int j = 0; j < L; ++j) {
+    const int li = seq[j];
+    const uint8_t *shard;
+    int s;
+    SOUP_TRY(acquire(h, seq, (size_t)j, &shard, &s));
+    SOUP_TRY(layer_forward(h, li, shard, true));
+    SOUP_TRY(layer_backward(h, li, shard));
+    SOUP_TRY(release(h, s));
+    if (!h->resident) SOUP_TRY(prefetch(h, seq, (size_t)j + 1, look - 1));
+    if (dh_out)
+      SOUP_CUDA_TRY(cudaMemcpyAsync(dh_out + (size_t)li * M * H, F(h, P.dh), 4ull * M * H,
+                                    cudaMemcpyDeviceToDevice, st));
+  }
+  SOUP_CUDA_TRY(cudaEventRecord(h->done, st));
+  h->in_bwd = 0;
+  h->stats.steps_bwd += 1;
+  return check_cuda("step_bwd");
+}
+
+int stream_sync(soup_stream *h, int timeout_ms) {
+  if (!h) return set_error(SOUP_EINVAL, "handle is NULL");
+  const auto t0 = std::chrono::steady_clock::now();
+  for (;;) {
+    cudaError_t q = cudaEventQuery(h->done);
+    if (q == cudaSuccess) break;
+    if (q != cudaErrorNotReady) return set_error(SOUP_ECUDA, "step failed: %s", cudaGetErrorString(q));
+    const auto dt = std::chrono::duration_cast<std::chrono::milliseconds>(std::chrono::steady_clock::now() - t0);
+    if (timeout_ms >= 0 && dt.count() > timeout_ms)
+      return set_error(SOUP_ETIMEDOUT, "soup_sync: not done after %d ms", timeout_ms);
+    std::this_thread::sleep_for(std::chrono::microseconds(100));
+  }
+  int err = 0;
+  SOUP_CUDA_TRY(cudaMemcpy(&err, h->err_dev, sizeof(int), cudaMemcpyDeviceToHost));
+  if (err) return set_error(SOUP_ETIMEDOUT, "a kernel's bounded wait gave up (flags 0x%x)", err);
+  harvest(h, false);
+  return 0;
+}
+
+int stream_stats(soup_stream *h, soup_stats *out, int reset) {
+  if (!h || !out) return set_error(SOUP_EINVAL, "NULL argument");
+  harvest(h, true);
+  *out = h->stats;
+  if (reset) h->stats = soup_stats();
+  return 0;
+}
+
+void soup_stream_free_impl(soup_stream *h) {
+  if (!h) return;
+  cudaStreamSynchronize(h->cs);
+  if (h->xs) cudaStreamSynchronize(h->xs);
+  harvest(h, true);
+  for (auto &s : h->slot)
+    if (s.has_events) {
+      cudaEventDestroy(s.ready);
+      cudaEventDestroy(s.freed);
+    }
+  if (h->done) cudaEventDestroy(h->done);
+  delete h;
+}
+
+}  // namespace soup

@@ -1,0 +1,78 @@
+// Internal state of a stream handle and the workspace plan (opaque to C callers).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "soup.h"
+
+namespace soup {
+
+// Byte offsets of every buffer inside the caller's device workspace.
+struct Plan {
+  uint64_t total = 0;
+  int n_slots = 0, vc = 0;
+  uint64_t slots = 0, h_all = 0, hm = 0, x1 = 0, x2 = 0, qkv = 0, att = 0, lse = 0, gu = 0, act = 0;
+  uint64_t u_f32[4] = {0, 0, 0, 0}, u_b[4] = {0, 0, 0, 0};
+  uint64_t dh = 0, dhm = 0, dh_b = 0, dhm_b = 0, dact = 0, dgu = 0, dx = 0, datt = 0, datt_b = 0;
+  uint64_t dqkv = 0, dqkv_b = 0, attn_scratch = 0, du_f32 = 0, du_b = 0;
+  uint64_t hn = 0, z = 0, dz = 0, dhn = 0, ce_max = 0, ce_sum = 0, ce_lab = 0, ce_lse = 0;
+  std::vector<uint64_t> vl, ac;  // per (layer, group) LoRA operand packs
+  uint64_t rope_cos = 0, rope_sin = 0, err = 0;
+};
+
+struct Slot {
+  uint8_t *dev = nullptr;
+  int layer = -1;       // layer held (or being copied in); -1 = empty
+  int pending = 0;      // a copy was issued and compute has not waited on it yet
+  uint64_t tick = 0;    // release order, for least-recently-used tie breaks
+  int has_events = 0;
+  cudaEvent_t ready = nullptr, freed = nullptr;
+};
+
+struct TimedEv {
+  cudaEvent_t start = nullptr, end = nullptr;
+  double flops = 0, bytes = 0;
+};
+
+int make_plan(const soup_cfg *c, int maxB, int maxS, int n_slots, int resident, Plan *P);
+int ce_chunk_cols(int M, int V);
+
+}  // namespace soup
+
+struct soup_stream {
+  soup_cfg cfg;
+  soup_shard_layout lay;
+  soup_store *store = nullptr;
+  soup::Plan plan;
+  int maxB = 0, maxS = 0, resident = 0;
+  cudaStream_t cs = nullptr, xs = nullptr;
+  uint8_t *ws = nullptr;
+  const uint16_t *embed = nullptr, *lm_head = nullptr, *final_norm = nullptr;
+  int *err_dev = nullptr;
+  std::vector<soup::Slot> slot;
+  uint64_t tick = 0;
+  cudaEvent_t done = nullptr;
+  // per-step state
+  int B = 0, S = 0, fwd_ready = 0, in_bwd = 0;
+  const int32_t *tokens = nullptr;
+  std::vector<const float *> lora_A, lora_B;
+  std::vector<float *> grad_A, grad_B;
+  // measurement
+  soup_stats stats{};
+  std::vector<soup::TimedEv> copy_ev, gemm_ev;
+  int dbg_profile = 0, dbg_stale = 0;
+};
+
+namespace soup {
+int stream_init(soup_store *st, const soup_cfg *c, int maxB, int maxS, void *ws, uint64_t ws_bytes,
+                const void *embed, const void *lm_head, const void *final_norm, uintptr_t cs,
+                uintptr_t xs, int n_slots, int resident, soup_stream **out);
+int step_fwd(soup_stream *h, const int32_t *tokens, int B, int S, const float *const *lA,
+             const float *const *lB, float *loss, float *logits, float *layer_out);
+int step_bwd(soup_stream *h, float *const *dA, float *const *dB, float *dh_out);
+int stream_sync(soup_stream *h, int timeout_ms);
+int stream_stats(soup_stream *h, soup_stats *out, int reset);
+void soup_stream_free_impl(soup_stream *h);
+}  // namespace soup

@@ -1,0 +1,81 @@
+"""A streamed LoRA training step as a user drives it: build the host store once, keep the
+resident tensors (embedding, head, final norm, LoRA A/B and their gradients) in device
+memory, and run forward + backward through the C ABI.
+
+"About Soup": only the adapters (plus embeddings, final norm and an untied head, per
+"Layer streaming: fine-tune a model that does not fit in your card", "How it works") live
+on the device; the frozen decoder layers stream from a page-locked host store.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import api
+
+LAYER_TENSORS = ("q", "k", "v", "o", "gate", "up", "down", "ln1", "ln2")
+
+
+def _bits_to_dev(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits, np.uint16).view(np.int16)).cuda()
+
+
+class StreamedLoRA:
+    """cfg: any object with the stack's fields (see api.make_cfg).
+    layer_source(i) -> dict of the nine bf16-bit host arrays of layer i.
+    lora: list over layers of 7 (A [r, in], B [out, r]) float32 host arrays."""
+
+    def __init__(self, cfg, layer_source, embed_bits, lm_head_bits, final_bits, lora, max_batch,
+                 max_seq, n_slots=2, resident=False, store=None, threads=0):
+        self.cfg = cfg
+        self.own_store = store is None
+        if store is None:
+            store = api.Store(cfg, allow_pageable=True)
+            for i in range(cfg.n_layers):
+                src = layer_source(i)
+                store.put_layer(i, [src[t] for t in LAYER_TENSORS], n_threads=threads)
+        self.store = store
+        self.embed = _bits_to_dev(embed_bits)
+        self.lm_head = None if cfg.tied else _bits_to_dev(lm_head_bits)
+        self.final = _bits_to_dev(final_bits)
+        self.lora_A = [torch.from_numpy(np.ascontiguousarray(a)).cuda() for layer in lora for a, _ in layer]
+        self.lora_B = [torch.from_numpy(np.ascontiguousarray(b)).cuda() for layer in lora for _, b in layer]
+        self.dA = [torch.zeros_like(a) for a in self.lora_A]
+        self.dB = [torch.zeros_like(b) for b in self.lora_B]
+        nbytes = api.workspace_bytes(cfg, max_batch, max_seq, n_slots, resident)
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        self.compute = torch.cuda.Stream()
+        self.copy = torch.cuda.Stream()
+        self.loss = torch.zeros(1, dtype=torch.float32, device="cuda")
+        self.stream = api.Stream(store, max_batch, max_seq, self.workspace, self.embed, self.lm_head,
+                                 self.final, self.compute, self.copy, n_slots=n_slots,
+                                 resident=resident)
+        torch.cuda.synchronize()
+
+    def fwd(self, tokens: torch.Tensor, logits=None, layer_out=None):
+        B, S = tokens.shape
+        self.compute.wait_stream(torch.cuda.current_stream())
+        self.stream.fwd(tokens, B, S, self.lora_A, self.lora_B, self.loss, logits, layer_out)
+
+    def bwd(self, dh_out=None):
+        self.stream.bwd(self.dA, self.dB, dh_out)
+
+    def step(self, tokens: torch.Tensor, logits=None, layer_out=None, dh_out=None):
+        self.fwd(tokens, logits, layer_out)
+        self.bwd(dh_out)
+
+    def sync(self, timeout_ms: int = 600000):
+        self.stream.sync(timeout_ms)
+        torch.cuda.current_stream().wait_stream(self.compute)
+
+    def grads(self):
+        """Host copies: list over layers of 7 (dA, dB)."""
+        L = self.cfg.n_layers
+        dA = [t.cpu().numpy() for t in self.dA]
+        dB = [t.cpu().numpy() for t in self.dB]
+        return [[(dA[i * 7 + p], dB[i * 7 + p]) for p in range(7)] for i in range(L)]
+
+    def close(self):
+        self.stream.free()
+        if self.own_store:
+            self.store.free()

@@ -1,0 +1,155 @@
+"""GPU parity of the single-projection kernels against the oracle (all calls go through the
+C ABI).  Operands are the oracle's: NF4 codes and absmax from oracle.nf4, dequantised values
+from oracle.nf4.dequantize.  Two references are used:
+
+* the exact-operand reference: the same bf16 operands the kernel is defined on (bf16 x,
+  bf16-rounded dequantised W) multiplied in float64 — the tensor-core result must match it
+  to float32-accumulation accuracy plus the final output rounding;
+* the oracle's float32 layer maths (unrounded W) — relative L2 <= 1e-2, the step's bar.
+"""
+import numpy as np
+import pytest
+
+import synth
+from oracle import nf4
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def api():
+    from nf4_dequant_gemm_blockwise_b300 import api as a
+    return a
+
+
+def _dev(a, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.view(dtype)
+    return t.cuda()
+
+
+def _weights(N, K, seed=0):
+    w_bits = synth.micro_weight(N, K, seed) if (N, K) in synth.MICRO_SHAPES else \
+        synth.normal_bf16(seed, "layer", (7000 + N, K), (N, K), 0.02)
+    packed, absmax = nf4.quantize_tensor(w_bits)
+    wdq = nf4.dequantize_tensor(packed, absmax, (N, K))          # float32, the oracle's W
+    return w_bits, packed, absmax, wdq
+
+
+def _rel_l2(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def test_dequant_bit_exact(api):
+    N, K = 300, 688                                   # blocks straddle rows
+    _, packed, absmax, wdq = _weights(N, K)
+    n = N * K
+    f = torch.empty(n, dtype=torch.float32, device="cuda")
+    b = torch.empty(n, dtype=torch.int16, device="cuda")
+    api.nf4_dequant(_dev(packed), _dev(absmax), n, f, b)
+    torch.cuda.synchronize()
+    assert np.array_equal(f.cpu().numpy().view(np.uint32), wdq.reshape(-1).view(np.uint32))
+    want_b = synth.to_bf16_bits(wdq.reshape(-1))
+    assert np.array_equal(b.cpu().numpy().view(np.uint16), want_b)
+
+
+SHAPES = [  # (M, N, K): tiles, ragged M / N, the fallback (K % 256 != 0), microbench shapes
+    (128, 256, 256), (200, 512, 512), (64, 1376, 256), (64, 256, 688), (1, 256, 256),
+    (130, 4096, 14336), (128, 14336, 4096), (16, 14336, 4096),
+]
+
+
+def _lora(N, K, r=16):
+    return synth.micro_lora(N, K, r)
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_proj_fwd(api, M, N, K):
+    r, s = 16, 2.0
+    w_bits, packed, absmax, wdq = _weights(N, K)
+    x_bits = synth.activations_bf16(M, K, key=1)
+    A, B = _lora(N, K, r)
+    y = torch.empty((M, N), dtype=torch.int16, device="cuda")
+    scratch = torch.empty(api.proj_scratch_bytes(M, N, K, r), dtype=torch.uint8, device="cuda")
+    api.proj_fwd(_dev(x_bits), M, N, K, _dev(packed), _dev(absmax), None, _dev(A), _dev(B), r, s, y, scratch)
+    torch.cuda.synchronize()
+    got = synth.bf16_bits_to_f32(y.cpu().numpy().view(np.uint16))
+    xf = nf4.bf16_to_f32(x_bits).astype(np.float64)
+    wb = nf4.bf16_round(wdq).astype(np.float64)
+    lora = s * (xf @ A.T.astype(np.float64)) @ B.T.astype(np.float64)
+    exact = xf @ wb.T + lora
+    tol = 2.0 ** -8 * np.abs(exact) + 2e-3 * np.sqrt(np.mean(exact ** 2))
+    bad = np.abs(got - exact) > tol
+    assert not bad.any(), (bad.sum(), np.abs(got - exact).max())
+    oracle = xf @ wdq.T.astype(np.float64) + lora        # unrounded W
+    assert _rel_l2(got, oracle) <= 1e-2
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_proj_dx(api, M, N, K):
+    r, s = 16, 2.0
+    w_bits, packed, absmax, wdq = _weights(N, K)
+    dy_bits = synth.activations_bf16(M, N, key=2)
+    A, B = _lora(N, K, r)
+    dx = torch.empty((M, K), dtype=torch.float32, device="cuda")
+    scratch = torch.empty(api.proj_scratch_bytes(M, N, K, r), dtype=torch.uint8, device="cuda")
+    api.proj_dx(_dev(dy_bits), M, N, K, _dev(packed), _dev(absmax), None, _dev(A), _dev(B), r, s, dx, scratch)
+    torch.cuda.synchronize()
+    got = dx.cpu().numpy().astype(np.float64)
+    dyf = nf4.bf16_to_f32(dy_bits).astype(np.float64)
+    wb = nf4.bf16_round(wdq).astype(np.float64)
+    du = s * (dyf @ B.astype(np.float64))
+    exact = dyf @ wb + nf4.bf16_round(du.astype(np.float32)).astype(np.float64) @ \
+        nf4.bf16_round(A).astype(np.float64)
+    tol = 1e-4 * np.abs(exact) + 1e-3 * np.sqrt(np.mean(exact ** 2))
+    bad = np.abs(got - exact) > tol
+    assert not bad.any(), (bad.sum(), np.abs(got - exact).max())
+    oracle = dyf @ wdq.astype(np.float64) + du @ A.astype(np.float64)
+    assert _rel_l2(got, oracle) <= 1e-2
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 256, 256), (513, 1376, 256), (512, 4096, 14336)])
+def test_proj_lora_grad(api, M, N, K):
+    r, s = 16, 2.0
+    x_bits = synth.activations_bf16(M, K, key=3)
+    dy_bits = synth.activations_bf16(M, N, key=4)
+    A, B = _lora(N, K, r)
+    dA = torch.empty((r, K), dtype=torch.float32, device="cuda")
+    dB = torch.empty((N, r), dtype=torch.float32, device="cuda")
+    scratch = torch.empty(api.proj_scratch_bytes(M, N, K, r), dtype=torch.uint8, device="cuda")
+    api.proj_lora_grad(_dev(x_bits), _dev(dy_bits), M, N, K, _dev(A), _dev(B), r, s, dA, dB, scratch)
+    torch.cuda.synchronize()
+    xf = nf4.bf16_to_f32(x_bits).astype(np.float64)
+    dyf = nf4.bf16_to_f32(dy_bits).astype(np.float64)
+    u = xf @ A.T.astype(np.float64)
+    want_dB = s * dyf.T @ u
+    want_dA = s * (dyf @ B.astype(np.float64)).T @ xf
+    assert _rel_l2(dB.cpu().numpy(), want_dB) < 1e-5
+    assert _rel_l2(dA.cpu().numpy(), want_dA) < 1e-5
+
+
+def test_bf16_weight_path(api):
+    """bf16 base weights (the un-quantised streamed base) through the same kernels."""
+    M, N, K, r, s = 192, 512, 1024, 16, 2.0
+    w_bits = synth.normal_bf16(0, "layer", (9000, 1), (N, K), 0.02)
+    x_bits = synth.activations_bf16(M, K, key=5)
+    dy_bits = synth.activations_bf16(M, N, key=6)
+    A, B = _lora(N, K, r)
+    scratch = torch.empty(api.proj_scratch_bytes(M, N, K, r), dtype=torch.uint8, device="cuda")
+    y = torch.empty((M, N), dtype=torch.int16, device="cuda")
+    dx = torch.empty((M, K), dtype=torch.float32, device="cuda")
+    wd = _dev(w_bits)
+    api.proj_fwd(_dev(x_bits), M, N, K, None, None, wd, _dev(A), _dev(B), r, s, y, scratch)
+    api.proj_dx(_dev(dy_bits), M, N, K, None, None, wd, _dev(A), _dev(B), r, s, dx, scratch)
+    torch.cuda.synchronize()
+    w = nf4.bf16_to_f32(w_bits).astype(np.float64)
+    xf = nf4.bf16_to_f32(x_bits).astype(np.float64)
+    dyf = nf4.bf16_to_f32(dy_bits).astype(np.float64)
+    want_y = xf @ w.T + s * (xf @ A.T) @ B.T
+    want_dx = dyf @ w + s * (dyf @ B) @ A
+    assert _rel_l2(synth.bf16_bits_to_f32(y.cpu().numpy().view(np.uint16)), want_y) < 5e-3
+    assert _rel_l2(dx.cpu().numpy(), want_dx) < 5e-3

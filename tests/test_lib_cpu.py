@@ -1,0 +1,114 @@
+"""CPU checks of the C-ABI library: it loads without a GPU, exports every entry point the
+header declares, and its host-side logic (codebook, packer, shard layout, memory plan) agrees
+with the oracle.  No device work is launched here."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import nf4, sizes
+
+api = pytest.importorskip("nf4_dequant_gemm_blockwise_b300.api")
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "soup.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(soup_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol():
+    import ctypes
+    lib = ctypes.CDLL(api.LIB_PATH)
+    declared = _declared()
+    assert len(declared) >= 20
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_codebook_matches_oracle_bitwise():
+    assert np.array_equal(api.nf4_codebook().view(np.uint32), nf4.codebook().view(np.uint32))
+
+
+@pytest.mark.parametrize("n", [64 * 1000, 64 * 37 + 13, 688 * 256, 1])
+def test_host_packer_bit_exact(n):
+    rng = np.random.default_rng(n)
+    x = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    x[rng.integers(0, n, size=max(1, n // 500))] = 0.0
+    if n > 200:
+        x[64:128] = 0.0                                # an all-zero block
+    bits = synth.to_bf16_bits(x)
+    codes, absmax = api.nf4_quantize_host(bits, n_threads=4)
+    oc, oa = nf4.quantize(nf4.bf16_to_f32(bits))
+    assert np.array_equal(absmax.view(np.uint32), oa.view(np.uint32))
+    assert np.array_equal(codes, nf4.pack(oc[: n + (n % 2)]))
+
+
+def test_host_packer_ties_go_low():
+    m = nf4.midpoints()
+    x = np.zeros(64, np.float32)
+    x[0] = 1.0
+    x[1:16] = m
+    codes, _ = api.nf4_quantize_host(synth.to_bf16_bits(x))
+    # midpoints are not all bf16-representable: compare with the oracle on the same bf16 input
+    oc, _ = nf4.quantize(nf4.bf16_to_f32(synth.to_bf16_bits(x)))
+    assert np.array_equal(codes, nf4.pack(oc))
+
+
+@pytest.mark.parametrize("cfg", [synth.TINY, synth.LLAMA8B, synth.QWEN32B, synth.QWEN3B_BF16])
+def test_shard_layout_matches_payload(cfg):
+    lay = api.shard_layout_of(cfg)
+    assert lay.payload == sizes.shard_payload_bytes(cfg)
+    assert lay.stride % 4096 == 0 and lay.payload <= lay.stride < lay.payload + 16 * 1024
+    for g in range(4):
+        assert lay.w_off[g] % 1024 == 0 and lay.a_off[g] % 1024 == 0
+    assert lay.ln1_off % 1024 == 0 and lay.ln2_off % 1024 == 0
+
+
+def test_store_shard_bytes_match_oracle_packing():
+    cfg = synth.TINY
+    st = api.Store(cfg, allow_pageable=True)            # no GPU here: pageable fallback
+    src = [synth.layer_source(cfg, i) for i in range(cfg.n_layers)]
+    for i, s in enumerate(src):
+        st.put_layer(i, [s[t] for t in synth.LAYER_TENSORS])
+    lay = api.shard_layout_of(cfg)
+    groups = [("q", "k", "v"), ("o",), ("gate", "up"), ("down",)]
+    for i in range(cfg.n_layers):
+        sh = st.shard_bytes(i)
+        for g, names in enumerate(groups):
+            packed = np.concatenate([nf4.quantize_tensor(src[i][p])[0] for p in names])
+            absm = np.concatenate([nf4.quantize_tensor(src[i][p])[1] for p in names])
+            assert np.array_equal(sh[lay.w_off[g]: lay.w_off[g] + lay.w_bytes[g]], packed)
+            got_a = sh[lay.a_off[g]: lay.a_off[g] + lay.a_bytes[g]].view(np.float32)
+            assert np.array_equal(got_a.view(np.uint32), absm.view(np.uint32))
+        assert np.array_equal(sh[lay.ln1_off: lay.ln1_off + 2 * cfg.hidden].view(np.uint16), src[i]["ln1"])
+    st.free()
+
+
+def test_memory_plan_bounds_streaming_by_slots():
+    cfg = synth.LLAMA8B
+    lay = api.shard_layout_of(cfg)
+    ws2 = api.workspace_bytes(cfg, 1, 512, n_slots=2)
+    ws8 = api.workspace_bytes(cfg, 1, 512, n_slots=8)
+    wsr = api.workspace_bytes(cfg, 1, 512, resident=True)
+    # weights on the device: n_slots shards when streamed, every shard when resident
+    assert ws8 - ws2 == 6 * lay.stride
+    assert wsr - ws2 == (cfg.n_layers - 2) * lay.stride
+    tot, ws = api.peak_bytes(cfg, 1, 512, n_slots=2)
+    assert ws == ws2
+    assert tot - ws == sizes.resident_bytes(cfg)
+    # streaming keeps the device copy of the base to two shards (< 1/10 of the store here)
+    assert 2 * lay.stride < sizes.store_payload_bytes(cfg) / 10
+
+
+def test_invalid_config_is_rejected():
+    bad = synth.TINY.with_(head_dim=96)
+    with pytest.raises(api.SoupError) as e:
+        api.shard_layout_of(bad)
+    assert e.value.code == api.EINVAL
+    with pytest.raises(api.SoupError):
+        api.workspace_bytes(synth.TINY, 1, 64, n_slots=9)
