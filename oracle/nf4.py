@@ -64,8 +64,8 @@ def quantize(x: np.ndarray):
     nz = absmax > 0
     with np.errstate(divide="ignore", invalid="ignore"):
         q = (blocks[nz] / absmax[nz, None]).astype(np.float32)   # IEEE float32 divide
-    # count of midpoints strictly below q
-    codes[nz] = (q[..., None] > m[None, None, :]).sum(axis=-1).astype(np.uint8)
+    # count of midpoints strictly below q (searchsorted 'left' stops before an equal one)
+    codes[nz] = np.searchsorted(m, q, side="left").astype(np.uint8)
     codes = codes.reshape(-1)
     codes[n:] = 7
     return codes, absmax
