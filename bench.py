@@ -1,0 +1,395 @@
+#!/usr/bin/env python
+"""Streamed NF4 LoRA training step on the Llama-3.1-8B-shaped stack (B=1, S=512, r=16, two
+device slots), seeded synthetic weights and tokens.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  `value` = tokens/s of whole forward+backward steps timed
+with CUDA events on the compute stream, inputs already on the device; `e2e` = the same
+through host buffers (token ids copied in from pinned memory and the loss read back every
+step).  The weights are streamed from the pinned host store by the step itself in both.
+`roofline` covers the NF4-dequant tensor-core GEMMs (all base-weight projections of the
+step, forward, recompute and dX), timed live with CUDA events around each launch during
+the timed steps.  `cpu_baseline` times the CPU oracle on one decoder layer plus the output
+head, scaled to the whole stack.  With N > 1 (torchrun) every rank runs an independent
+replica ("replicas only": the step has no exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "streamed LoRA train tok/s (8B-shape NF4); dequant-GEMM % roofline; H2D GB/s"
+UNIT = "tokens/s"
+
+
+def _args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--batch", type=int, default=1)
+    p.add_argument("--seq", type=int, default=512)
+    p.add_argument("--slots", type=int, default=2)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-overlap", action="store_true", help="skip the resident comparison run")
+    return p.parse_args()
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm": d["hbm_gbs"], "bf16": d["bf16_tflops"], "bf16_sus": d["bf16_tflops_sustained"],
+                "src": "measured"}
+    return {"hbm": 6400.0, "bf16": 1800.0, "bf16_sus": 1400.0, "src": "fallback"}
+
+
+def _workload(cfg, slots):
+    return {"workload": f"{cfg.name}: streamed LoRA step (fwd+bwd), {cfg.n_layers} layers, hidden "
+                        f"{cfg.hidden}, inter {cfg.inter}, {cfg.n_heads}/{cfg.n_kv_heads} heads, vocab "
+                        f"{cfg.vocab}, NF4 base, r={cfg.lora_r}, {slots} device slots",
+            "global_batch": cfg.batch, "seq_len": cfg.seq, "tokens_per_step": cfg.batch * cfg.seq,
+            "parallelism": "replicas", "l2": "inputs larger than L2 (whole store re-streamed each step)"}
+
+
+# ------------------------------------------------------------------------------ clocks
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self) -> dict:
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.f.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------------------ oracle baseline
+def run_oracle_timed(cfg):
+    """Estimated oracle step time: L x (layer fwd + layer bwd) + head fwd + head bwd."""
+    import numpy as np
+
+    import synth
+    from oracle import model, nf4
+
+    src = synth.layer_source(cfg, 0)
+    W = model.weights_from_source(cfg, [src], synth.embedding(cfg.with_(vocab=2)),
+                                  synth.embedding(cfg.with_(vocab=2)), synth.final_norm(cfg)).layers[0]
+    lora = model.lora_dict(synth.lora_params(cfg.with_(n_layers=1))[0], np.float32)
+    w_lm = nf4.bf16_to_f32(synth.lm_head(cfg))
+    w_f = nf4.bf16_to_f32(synth.final_norm(cfg))
+    tok = synth.tokens(cfg)
+    h = nf4.bf16_to_f32(synth.embedding(cfg))[tok.astype(np.int64)]
+    cos, sin = model.rope_tables(cfg.seq, cfg.head_dim, cfg.rope_theta, np.float32)
+    M = cfg.batch * cfg.seq
+
+    def one():
+        ta = time.perf_counter()
+        out, cache = model.layer_forward(h, W, lora, cfg, cos, sin)
+        tb = time.perf_counter()
+        logits, (xn, r) = model.logits_of(out.reshape(M, -1), w_f, w_lm, cfg.rms_eps)
+        model.loss_of(logits.reshape(cfg.batch, cfg.seq, -1), tok)
+        dz = model.loss_backward(logits.reshape(cfg.batch, cfg.seq, -1), tok).reshape(M, -1)
+        dh = model.rmsnorm_backward(dz @ w_lm, out.reshape(M, -1), w_f, r).reshape(out.shape)
+        tc = time.perf_counter()
+        model.layer_backward(dh, cache, W, lora, cfg, cos, sin)
+        td = time.perf_counter()
+        layer = (tb - ta) + (td - tc)
+        head = tc - tb
+        return cfg.n_layers * layer + head, td - ta
+
+    return one
+
+
+def _threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+# ------------------------------------------------------------------------------ reference arm
+def run_reference(args, rank):
+    import synth
+    cfg = synth.LLAMA8B.with_(batch=args.batch, seq=args.seq)
+    if rank != 0:
+        return
+    one = run_oracle_timed(cfg)
+    for _ in range(args.warmup):
+        one()
+    est, wall = [], []
+    for _ in range(args.steps):
+        e, w = one()
+        est.append(e)
+        wall.append(w)
+    step_s = statistics.mean(est)
+    value = cfg.batch * cfg.seq / step_s
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": _workload(cfg, args.slots),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": _threads(), "kind": "oracle",
+                             "sample": "each step: one decoder layer forward+backward and the output "
+                                       "head forward+backward of the same workload, on the CPU "
+                                       f"oracle; step time = {cfg.n_layers} x layer + head"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------ our arm
+def h2d_peak_gbs(torch):
+    n = 1 << 30
+    h = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    h.fill_(1)
+    d = torch.empty(n, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    best = 0.0
+    for _ in range(10):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            a.record(s)
+            d.copy_(h, non_blocking=True)
+            b.record(s)
+        b.synchronize()
+        best = max(best, n / (a.elapsed_time(b) * 1e-3) / 1e9)
+    del h, d
+    return best
+
+
+def run_ours(args, rank, world, local_rank, dist):
+    import numpy as np
+    import torch
+
+    import synth
+    from nf4_dequant_gemm_blockwise_b300 import api
+    from nf4_dequant_gemm_blockwise_b300.session import StreamedLoRA
+
+    torch.cuda.set_device(local_rank)
+    cfg = synth.LLAMA8B.with_(batch=args.batch, seq=args.seq)
+    B, S = cfg.batch, cfg.seq
+    peaks = _peaks()
+    h2d_peak = h2d_peak_gbs(torch)
+
+    t_build = time.perf_counter()
+    store = api.Store(cfg, allow_pageable=True)
+    for i0 in range(0, cfg.n_layers, 8):
+        idx = list(range(i0, min(cfg.n_layers, i0 + 8)))
+        for i, src in zip(idx, synth.layer_sources(cfg, idx)):
+            store.put_layer(i, [src[t] for t in synth.LAYER_TENSORS])
+    t_build = time.perf_counter() - t_build
+    _, store_bytes, pinned = store.info()
+
+    torch.cuda.reset_peak_memory_stats()
+    lora = synth.lora_params(cfg)
+    sess = StreamedLoRA(cfg, None, synth.embedding(cfg), synth.lm_head(cfg), synth.final_norm(cfg),
+                        lora, B, S, n_slots=args.slots, store=store)
+    tok_host = torch.from_numpy(synth.tokens(cfg)).pin_memory()
+    tok_dev = tok_host.cuda()
+    loss_host = torch.zeros(1, dtype=torch.float32).pin_memory()
+
+    for _ in range(args.warmup):
+        sess.step(tok_dev)
+    sess.sync()
+    torch.cuda.synchronize()
+
+    # ---- timed region: device-resident inputs
+    clocks = Clocks(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    sess.stream.debug(api.DBG_PROFILE, 1)
+    sess.stream.stats(reset=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    l0 = api.kernel_launches()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(sess.compute)
+    for _ in range(args.steps):
+        sess.step(tok_dev)
+    e1.record(sess.compute)
+    sess.sync()
+    torch.cuda.synchronize()
+    launches = api.kernel_launches() - l0
+    ms_total = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    st = sess.stream.stats(reset=True)
+    sess.stream.debug(api.DBG_PROFILE, 0)
+    if dist is not None:
+        dist.barrier()
+    peak_alloc = torch.cuda.max_memory_allocated()
+
+    # ---- end to end: token ids in from pinned host memory, loss out, every step
+    for _ in range(2):
+        sess.step(tok_dev)
+    sess.sync()
+    torch.cuda.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(sess.compute)
+    for _ in range(args.steps):
+        with torch.cuda.stream(sess.compute):
+            tok_dev.copy_(tok_host, non_blocking=True)
+        sess.fwd(tok_dev)
+        sess.bwd()
+        with torch.cuda.stream(sess.compute):
+            loss_host.copy_(sess.loss, non_blocking=True)
+    f1.record(sess.compute)
+    sess.sync()
+    torch.cuda.synchronize()
+    ms_e2e = f0.elapsed_time(f1)
+    st_e2e = sess.stream.stats(reset=True)
+    loss_val = float(loss_host.item())
+
+    # ---- resident run of the same kernels: the compute-only step time (for the overlap)
+    ms_res = None
+    if not args.no_overlap:
+        sess_r = StreamedLoRA(cfg, None, synth.embedding(cfg), synth.lm_head(cfg), synth.final_norm(cfg),
+                              lora, B, S, resident=True, store=store)
+        for _ in range(args.warmup):
+            sess_r.step(tok_dev)
+        sess_r.sync()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(sess_r.compute)
+        for _ in range(args.steps):
+            sess_r.step(tok_dev)
+        g1.record(sess_r.compute)
+        sess_r.sync()
+        torch.cuda.synchronize()
+        ms_res = g0.elapsed_time(g1) / args.steps
+        sess_r.close()
+
+    # ---- max over ranks
+    ms_step = ms_total / args.steps
+    ms_e2e_step = ms_e2e / args.steps
+    if dist is not None:
+        t = torch.tensor([ms_step, ms_e2e_step], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step, ms_e2e_step = float(t[0]), float(t[1])
+    tokens = B * S
+    value = world * tokens / (ms_step * 1e-3)
+    e2e_value = world * tokens / (ms_e2e_step * 1e-3)
+
+    # roofline of the NF4 dequant GEMMs (tensor-bound at this token count)
+    gemm_tflops = st["gemm_flops"] / (st["gemm_ms"] * 1e-3) / 1e12 if st["gemm_ms"] else None
+    peak_tc = peaks["bf16_sus"]
+    copy_s = st["copy_ms"] * 1e-3
+    h2d_gbs = st["copy_bytes"] / copy_s / 1e9 if copy_s else None
+    t_copy = st["copy_ms"] / args.steps
+    overlap = None
+    if ms_res is not None:
+        exposed = ms_step - max(t_copy, ms_res)
+        overlap = {"t_step_ms": ms_step, "t_copy_ms": t_copy, "t_compute_resident_ms": ms_res,
+                   "hidden_fraction": 1.0 - max(exposed, 0.0) / min(t_copy, ms_res) if min(t_copy, ms_res) > 0 else None}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": _workload(cfg, args.slots),
+        "e2e": {"value": e2e_value, "unit": UNIT,
+                "h2d_bytes_per_step": tok_host.numel() * 4 + st_e2e["copy_bytes"] / args.steps,
+                "d2h_bytes_per_step": 4},
+        "gpu_launches": launches,
+        "roofline": {"kernel": "nf4_dequant_gemm (tcgen05; all base-weight projections, fwd + recompute + dX)",
+                     "bound": "tensor", "achieved": gemm_tflops, "peak": peak_tc, "unit": "TFLOP/s",
+                     "frac": gemm_tflops / peak_tc if gemm_tflops else None, "traffic": None,
+                     "peak_source": f"{peaks['src']} bf16 sustained", "launches": st["gemm_launches"],
+                     "avg_launch_us": st["gemm_ms"] * 1e3 / max(st["gemm_launches"], 1),
+                     "share_of_step": st["gemm_ms"] / ms_total if ms_total else None},
+        "h2d": {"achieved_gbs": h2d_gbs, "pinned_peak_gbs": h2d_peak,
+                "frac": h2d_gbs / h2d_peak if h2d_gbs else None, "bytes_per_step": st["copy_bytes"] / args.steps,
+                "copies_per_step": st["copies"] / args.steps, "store_bytes": store_bytes, "pinned": pinned},
+        "overlap": overlap,
+        "peak_vram_bytes": peak_alloc,
+        "store_build_s": t_build,
+        "loss": loss_val,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        one = run_oracle_timed(cfg)
+        est = [one()[0] for _ in range(2)]
+        step_s = min(est)
+        line["cpu_baseline"] = {"value": tokens / step_s, "unit": UNIT, "cores": _threads(), "kind": "oracle",
+                                "sample": f"one decoder layer fwd+bwd and the output head fwd+bwd of this "
+                                          f"workload on the CPU oracle (float32 NumPy), step time = "
+                                          f"{cfg.n_layers} x layer + head; best of 2"}
+    sess.close()
+    store.free()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = _args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as td
+        backend = "gloo" if args.impl == "reference" else "nccl"
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(local_rank)
+        td.init_process_group(backend)
+        dist = td
+    if args.impl == "reference":
+        run_reference(args, rank)
+    else:
+        run_ours(args, rank, world, local_rank, dist)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -106,6 +106,8 @@ typedef struct soup_stats {
 const char *soup_last_error(void);
 /* Library version string. */
 const char *soup_version(void);
+/* Number of kernels this library has launched in this process so far (all devices). */
+uint64_t soup_kernel_launches(void);
 
 /* The 16 NF4 code values, ascending, as this library derives them (float64 construction
  * from normal quantiles, rounded once to float): "Turn it on" names NF4 without printing
@@ -208,25 +210,32 @@ void soup_stream_free(soup_stream *h);
 /* One projection of the step, for the microbench and the kernel tests.  W is a weight
  * [N, K] (out x in) given as NF4 (codes dev uint8 [N*K/2] + absmax dev float [N*K/64]) or
  * bf16 (w_bf16 dev uint16 [N, K]; codes/absmax NULL).  LoRA: A dev float [r, K],
- * B dev float [N, r], s = alpha / r.  scratch: dev buffer of soup_proj_scratch_bytes().
- * Shapes: any M >= 1; the tensor-core path needs K % 256 == 0 and N % 16 == 0 for the
- * forward, N % 64 == 0 and K % 256 == 0 for dX; other shapes use a plain tiled kernel. */
+ * B dev float [N, r], s = alpha / r, 1 <= r <= 64.  scratch: dev buffer of
+ * soup_proj_scratch_bytes() bytes, 256-byte aligned, owned by the caller; its contents are
+ * overwritten.  Shapes: any M >= 1; the tensor-core path needs K % 256 == 0 (both
+ * directions) and N % 64 == 0 for dX; other shapes use a plain tiled kernel.
+ * 16-bit operand format: x_f16 != 0 means x (and y) are IEEE half and the GEMM runs on half
+ * operands (the step's forward); 0 means bf16.  dY and dx of the backward are bf16 / float. */
 int soup_proj_scratch_bytes(int M, int N, int K, int r, uint64_t *bytes);
 
-/* y[M, N] (bf16 out, dev uint16) = x W^T + s (x A^T) B^T,  x: dev bf16 [M, K]. */
+/* y[M, N] (16-bit out, dev uint16) = x W^T + s (x A^T) B^T,  x: dev 16-bit [M, K].
+ * "Layer streaming: fine-tune a model that does not fit in your card", "How it works": the
+ * projection runs on the streamed weight bytes; the weights are dequantised in the kernel. */
 int soup_proj_fwd(const uint16_t *x, int M, int N, int K, const uint8_t *codes,
                   const float *absmax, const uint16_t *w_bf16, const float *A, const float *B,
-                  int r, float s, uint16_t *y, void *scratch, uint64_t scratch_bytes,
+                  int r, float s, int x_f16, uint16_t *y, void *scratch, uint64_t scratch_bytes,
                   uintptr_t stream);
-/* dx[M, K] (float out) = dY W + s (dY B) A,  dY: dev bf16 [M, N]. */
+/* dx[M, K] (float out) = dY W + s (dY B) A,  dY: dev bf16 [M, N].  "How it works": the
+ * backward needs W^T dL/dy; the dequantisation is redone inside the GEMM, never cached. */
 int soup_proj_dx(const uint16_t *dy, int M, int N, int K, const uint8_t *codes,
                  const float *absmax, const uint16_t *w_bf16, const float *A, const float *B,
                  int r, float s, float *dx, void *scratch, uint64_t scratch_bytes,
                  uintptr_t stream);
-/* dA[r, K] = s (dY B)^T x,  dB[N, r] = s dY^T (x A^T); float outputs, fixed summation order. */
+/* dA[r, K] = s (dY B)^T x,  dB[N, r] = s dY^T (x A^T); float outputs, fixed summation order.
+ * x: dev 16-bit [M, K] (half if x_f16), dY: dev bf16 [M, N]. */
 int soup_proj_lora_grad(const uint16_t *x, const uint16_t *dy, int M, int N, int K,
-                        const float *A, const float *B, int r, float s, float *dA, float *dB,
-                        void *scratch, uint64_t scratch_bytes, uintptr_t stream);
+                        const float *A, const float *B, int r, float s, int x_f16, float *dA,
+                        float *dB, void *scratch, uint64_t scratch_bytes, uintptr_t stream);
 
 /* Dequantise n NF4 weights on the device: out_f32[i] = float(c[code_i] * absmax[i / 64])
  * and out_bf16[i] = that value rounded to nearest-even bf16 (either output may be NULL). */

@@ -59,6 +59,7 @@ def _load() -> C.CDLL:
     sig = {
         "soup_last_error": (C.c_char_p, []),
         "soup_version": (C.c_char_p, []),
+        "soup_kernel_launches": (C.c_uint64, []),
         "soup_nf4_codebook": (I32, [P]),
         "soup_shard_layout_of": (I32, [C.POINTER(soup_cfg), C.POINTER(soup_shard_layout)]),
         "soup_nf4_quantize_host": (I32, [P, C.c_int64, P, P, I32]),
@@ -78,9 +79,9 @@ def _load() -> C.CDLL:
         "soup_stream_debug": (I32, [VP, I32, I32]),
         "soup_stream_free": (None, [VP]),
         "soup_proj_scratch_bytes": (I32, [I32, I32, I32, I32, C.POINTER(U64)]),
-        "soup_proj_fwd": (I32, [P, I32, I32, I32, P, P, P, P, P, I32, F32, P, P, U64, C.c_size_t]),
+        "soup_proj_fwd": (I32, [P, I32, I32, I32, P, P, P, P, P, I32, F32, I32, P, P, U64, C.c_size_t]),
         "soup_proj_dx": (I32, [P, I32, I32, I32, P, P, P, P, P, I32, F32, P, P, U64, C.c_size_t]),
-        "soup_proj_lora_grad": (I32, [P, P, I32, I32, I32, P, P, I32, F32, P, P, P, U64, C.c_size_t]),
+        "soup_proj_lora_grad": (I32, [P, P, I32, I32, I32, P, P, I32, F32, I32, P, P, P, U64, C.c_size_t]),
         "soup_nf4_dequant": (I32, [P, P, C.c_int64, P, P, C.c_size_t]),
     }
     for name, (res, args) in sig.items():
@@ -108,6 +109,10 @@ def last_error() -> str:
 
 def version() -> str:
     return lib.soup_version().decode()
+
+
+def kernel_launches() -> int:
+    return int(lib.soup_kernel_launches())
 
 
 def _ptr(x) -> int | None:
@@ -281,9 +286,9 @@ def proj_scratch_bytes(M, N, K, r) -> int:
     return out.value
 
 
-def proj_fwd(x, M, N, K, codes, absmax, w_bf16, A, B, r, s, y, scratch, stream=0):
+def proj_fwd(x, M, N, K, codes, absmax, w_bf16, A, B, r, s, y, scratch, stream=0, x_f16=True):
     _check(lib.soup_proj_fwd(_ptr(x), M, N, K, _ptr(codes), _ptr(absmax), _ptr(w_bf16), _ptr(A),
-                             _ptr(B), r, s, _ptr(y), _ptr(scratch),
+                             _ptr(B), r, s, int(x_f16), _ptr(y), _ptr(scratch),
                              scratch.numel() * scratch.element_size(), _stream(stream)))
 
 
@@ -293,8 +298,8 @@ def proj_dx(dy, M, N, K, codes, absmax, w_bf16, A, B, r, s, dx, scratch, stream=
                             scratch.numel() * scratch.element_size(), _stream(stream)))
 
 
-def proj_lora_grad(x, dy, M, N, K, A, B, r, s, dA, dB, scratch, stream=0):
-    _check(lib.soup_proj_lora_grad(_ptr(x), _ptr(dy), M, N, K, _ptr(A), _ptr(B), r, s, _ptr(dA),
+def proj_lora_grad(x, dy, M, N, K, A, B, r, s, dA, dB, scratch, stream=0, x_f16=True):
+    _check(lib.soup_proj_lora_grad(_ptr(x), _ptr(dy), M, N, K, _ptr(A), _ptr(B), r, s, int(x_f16), _ptr(dA),
                                    _ptr(dB), _ptr(scratch), scratch.numel() * scratch.element_size(),
                                    _stream(stream)))
 

@@ -1,5 +1,7 @@
 // The C ABI declared in include/soup.h: argument checks, error strings, and thin wrappers
 // over the store, the step orchestrator and the single-projection kernels.
+#include <algorithm>
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -26,6 +28,11 @@ int set_error(int code, const char *fmt, ...) {
   return code;
 }
 void clear_error() { g_err.clear(); }
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+uint64_t launches_so_far() { return g_launches.load(std::memory_order_relaxed); }
 }  // namespace soup
 
 using namespace soup;
@@ -34,6 +41,7 @@ extern "C" {
 
 const char *soup_last_error(void) { return g_err.c_str(); }
 const char *soup_version(void) { return "soup-b300 0.1 (sm_103a)"; }
+uint64_t soup_kernel_launches(void) { return launches_so_far(); }
 
 int soup_nf4_codebook(float *out) {
   if (!out) return set_error(SOUP_EINVAL, "out is NULL");
@@ -139,7 +147,7 @@ void soup_stream_free(soup_stream *h) { soup_stream_free_impl(h); }
 // ------------------------------------------------------------------ single projection
 namespace {
 struct ProjScratch {
-  uint64_t u_f32, ul, vl, ac, du_f32, dul, err, total;
+  uint64_t u_f32, ul, vl, ac, du_f32, dul, part, err, total;
 };
 ProjScratch proj_plan(int M, int N, int K) {
   ProjScratch s;
@@ -155,6 +163,7 @@ ProjScratch proj_plan(int M, int N, int K) {
   s.ac = take(2ull * 64 * K);
   s.du_f32 = take(4ull * M * 64);
   s.dul = take(2ull * M * 64);
+  s.part = take(4ull * std::max(lora_partial_floats(std::max(M, 1), K), lora_partial_floats(std::max(M, 1), N)));
   s.err = take(64);
   s.total = off;
   return s;
@@ -207,8 +216,8 @@ int soup_proj_scratch_bytes(int M, int N, int K, int r, uint64_t *bytes) {
 }
 
 int soup_proj_fwd(const uint16_t *x, int M, int N, int K, const uint8_t *codes, const float *absmax,
-                  const uint16_t *w_bf16, const float *A, const float *B, int r, float s, uint16_t *y,
-                  void *scratch, uint64_t scratch_bytes, uintptr_t stream) {
+                  const uint16_t *w_bf16, const float *A, const float *B, int r, float s, int x_f16,
+                  uint16_t *y, void *scratch, uint64_t scratch_bytes, uintptr_t stream) {
   SOUP_TRY(proj_check(M, N, K, codes, absmax, w_bf16, A, B, r, scratch, scratch_bytes));
   if (M == 0) return 0;
   if (!x || !y) return set_error(SOUP_EINVAL, "NULL x or y");
@@ -216,13 +225,16 @@ int soup_proj_fwd(const uint16_t *x, int M, int N, int K, const uint8_t *codes, 
   const ProjScratch P = proj_plan(M, N, K);
   uint8_t *base = static_cast<uint8_t *>(scratch);
   LoraSeg L = one_seg(N, A, B, r, s, nullptr, nullptr);
+  const bool f16 = x_f16 != 0;
   k_lora_down(x, K, M, K, L, reinterpret_cast<float *>(base + P.u_f32),
-              reinterpret_cast<uint16_t *>(base + P.ul), st);
-  k_pack_fwd(L, N, reinterpret_cast<uint16_t *>(base + P.vl), st);
+              reinterpret_cast<uint16_t *>(base + P.ul), f16, f16,
+              reinterpret_cast<float *>(base + P.part), st);
+  k_pack_fwd(L, N, reinterpret_cast<uint16_t *>(base + P.vl), f16, st);
   GemmArgs g = proj_weight(GEMM_FWD, N, K, codes, absmax, w_bf16);
+  g.op_f16 = f16 ? 1 : 0;
   g.M = M; g.a = x; g.lda = K;
   g.ul = reinterpret_cast<uint16_t *>(base + P.ul); g.vl = reinterpret_cast<uint16_t *>(base + P.vl);
-  g.R = L.Rpad(); g.epi = EPI_BF16; g.out = y; g.ldo = N;
+  g.R = L.Rpad(); g.epi = EPI_16; g.out = y; g.ldo = N;
   g.err = reinterpret_cast<int *>(base + P.err);
   return gemm_launch(g, st);
 }
@@ -238,8 +250,9 @@ int soup_proj_dx(const uint16_t *dy, int M, int N, int K, const uint8_t *codes, 
   uint8_t *base = static_cast<uint8_t *>(scratch);
   LoraSeg L = one_seg(N, A, B, r, s, nullptr, nullptr);
   k_lora_du(dy, N, M, L, reinterpret_cast<float *>(base + P.du_f32),
-            reinterpret_cast<uint16_t *>(base + P.dul), st);
-  k_pack_bwd(L, K, reinterpret_cast<uint16_t *>(base + P.ac), st);
+            reinterpret_cast<uint16_t *>(base + P.dul), false, false,
+            reinterpret_cast<float *>(base + P.part), st);
+  k_pack_bwd(L, K, reinterpret_cast<uint16_t *>(base + P.ac), false, st);
   GemmArgs g = proj_weight(GEMM_DX, N, K, codes, absmax, w_bf16);
   g.M = M; g.a = dy; g.lda = N;
   g.ul = reinterpret_cast<uint16_t *>(base + P.dul); g.vl = reinterpret_cast<uint16_t *>(base + P.ac);
@@ -249,7 +262,7 @@ int soup_proj_dx(const uint16_t *dy, int M, int N, int K, const uint8_t *codes, 
 }
 
 int soup_proj_lora_grad(const uint16_t *x, const uint16_t *dy, int M, int N, int K, const float *A,
-                        const float *B, int r, float s, float *dA, float *dB, void *scratch,
+                        const float *B, int r, float s, int x_f16, float *dA, float *dB, void *scratch,
                         uint64_t scratch_bytes, uintptr_t stream) {
   if (!dA || !dB || !x || !dy) return set_error(SOUP_EINVAL, "NULL argument");
   if (M < 1 || N < 1 || K < 1 || r < 1 || r > 64 || !A || !B || !scratch)
@@ -259,12 +272,14 @@ int soup_proj_lora_grad(const uint16_t *x, const uint16_t *dy, int M, int N, int
   const ProjScratch P = proj_plan(M, N, K);
   uint8_t *base = static_cast<uint8_t *>(scratch);
   LoraSeg L = one_seg(N, A, B, r, s, dA, dB);
+  float *part = reinterpret_cast<float *>(base + P.part);
+  const bool f16 = x_f16 != 0;
   k_lora_down(x, K, M, K, L, reinterpret_cast<float *>(base + P.u_f32),
-              reinterpret_cast<uint16_t *>(base + P.ul), st);
+              reinterpret_cast<uint16_t *>(base + P.ul), f16, f16, part, st);
   k_lora_du(dy, N, M, L, reinterpret_cast<float *>(base + P.du_f32),
-            reinterpret_cast<uint16_t *>(base + P.dul), st);
-  k_lora_dB(dy, N, M, reinterpret_cast<float *>(base + P.u_f32), L, st);
-  k_lora_dA(reinterpret_cast<float *>(base + P.du_f32), x, K, M, K, L, st);
+            reinterpret_cast<uint16_t *>(base + P.dul), false, false, part, st);
+  k_lora_dB(dy, N, M, reinterpret_cast<float *>(base + P.u_f32), L, false, st);
+  k_lora_dA(reinterpret_cast<float *>(base + P.du_f32), x, K, M, K, L, f16, st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(SOUP_ECUDA, "lora grad launch: %s", cudaGetErrorString(e));
   return 0;

@@ -5,8 +5,10 @@
 //
 // Flash-style tiling: the S x S score matrix is never stored.  The forward keeps a running
 // row max and sum per query row and writes the base-2 log-sum-exp; the backward recomputes
-// the probabilities from it.  Tiles use the warp-level bf16 tensor-core MMA (m16n8k16,
-// float accumulation).  Determinism: every output element is accumulated by one thread in a
+// the probabilities from it.  Tiles use the warp-level tensor-core MMA (m16n8k16, float
+// accumulation).  q, k, v and the output are IEEE half (the forward's operand format); the
+// backward recomputes the scores from the same half q and k, then forms every product with
+// a gradient in bf16 (v, k and q are converted to bf16 when they are staged).  Determinism: every output element is accumulated by one thread in a
 // fixed order; the key/value gradients of the heads that share a key/value head are summed
 // by a separate kernel in head order (no atomics).
 #include <cmath>
@@ -19,12 +21,20 @@ namespace soup {
 namespace {
 using namespace soupk;
 
+template <bool F16>
 SOUP_DEV void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  if (F16)
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  else
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 SOUP_DEV void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -47,8 +57,8 @@ SOUP_DEV float quad_sum(float v) {
 SOUP_DEV uint32_t ld32(const uint16_t *p) { return *reinterpret_cast<const uint32_t *>(p); }
 
 // Copy rows [r0, r0+nrows) x D of one head (column offset col) into smem [nrows][D+8];
-// rows past S are zero.
-template <int D>
+// rows past S are zero.  TO_BF16: the source is half and is converted to bf16.
+template <int D, bool TO_BF16 = false>
 SOUP_DEV void load_tile(uint16_t *dst, const uint16_t *src, int ld, size_t rowbase, int r0,
                         int nrows, int S, int col) {
   constexpr int LDS = D + 8;
@@ -56,12 +66,18 @@ SOUP_DEV void load_tile(uint16_t *dst, const uint16_t *src, int ld, size_t rowba
     const int r = i / (D / 8), c = (i % (D / 8)) * 8;
     uint4 v = make_uint4(0, 0, 0, 0);
     if (r0 + r < S) v = *reinterpret_cast<const uint4 *>(src + (rowbase + r0 + r) * ld + col + c);
+    if (TO_BF16) {
+      v.x = pack_bf16x2(lo16<true>(v.x), hi16<true>(v.x));
+      v.y = pack_bf16x2(lo16<true>(v.y), hi16<true>(v.y));
+      v.z = pack_bf16x2(lo16<true>(v.z), hi16<true>(v.z));
+      v.w = pack_bf16x2(lo16<true>(v.w), hi16<true>(v.w));
+    }
     *reinterpret_cast<uint4 *>(dst + r * LDS + c) = v;
   }
 }
 
 // ------------------------------------------------------------------------ forward
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(128) attn_fwd_kernel(const uint16_t *qkv, int ld, int S, int nh,
                                                        int nkv, uint16_t *out, float *lse,
                                                        float scale_log2) {
@@ -106,7 +122,7 @@ __global__ void __launch_bounds__(128) attn_fwd_kernel(const uint16_t *qkv, int 
 #pragma unroll
       for (int kc = 0; kc < NC; ++kc) {
         const uint16_t *kp = Ks + (nt * 8 + gr) * LDS + kc * 16 + 2 * tq;
-        mma16816(sacc[nt], qf[kc], ld32(kp), ld32(kp + 8));
+        mma16816<F16>(sacc[nt], qf[kc], ld32(kp), ld32(kp + 8));
       }
     }
 #pragma unroll
@@ -145,17 +161,17 @@ __global__ void __launch_bounds__(128) attn_fwd_kernel(const uint16_t *qkv, int 
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       uint32_t a[4];
-      a[0] = pack_bf16x2(sacc[2 * j][0], sacc[2 * j][1]);
-      a[1] = pack_bf16x2(sacc[2 * j][2], sacc[2 * j][3]);
-      a[2] = pack_bf16x2(sacc[2 * j + 1][0], sacc[2 * j + 1][1]);
-      a[3] = pack_bf16x2(sacc[2 * j + 1][2], sacc[2 * j + 1][3]);
+      a[0] = pack16x2<F16>(sacc[2 * j][0], sacc[2 * j][1]);
+      a[1] = pack16x2<F16>(sacc[2 * j][2], sacc[2 * j][3]);
+      a[2] = pack16x2<F16>(sacc[2 * j + 1][0], sacc[2 * j + 1][1]);
+      a[3] = pack16x2<F16>(sacc[2 * j + 1][2], sacc[2 * j + 1][3]);
       const int key = j * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
       for (int dn = 0; dn < NC; ++dn) {
         uint32_t r0, r1, r2, r3;
         ldsm_x4_t(smem_u32(Vs + key * LDS + dn * 16 + (lane >> 4) * 8), r0, r1, r2, r3);
-        mma16816(oacc[2 * dn], a, r0, r1);
-        mma16816(oacc[2 * dn + 1], a, r2, r3);
+        mma16816<F16>(oacc[2 * dn], a, r0, r1);
+        mma16816<F16>(oacc[2 * dn + 1], a, r2, r3);
       }
     }
   }
@@ -169,7 +185,7 @@ __global__ void __launch_bounds__(128) attn_fwd_kernel(const uint16_t *qkv, int 
 #pragma unroll
     for (int dn = 0; dn < D / 8; ++dn)
       *reinterpret_cast<uint32_t *>(o + dn * 8 + 2 * tq) =
-          pack_bf16x2(oacc[dn][2 * r] * inv, oacc[dn][2 * r + 1] * inv);
+          pack16x2<F16>(oacc[dn][2 * r] * inv, oacc[dn][2 * r + 1] * inv);
     if (tq == 0) lse[((size_t)b * nh + h) * S + row] = mrow[r] + log2f(l);
   }
 }
@@ -187,7 +203,7 @@ __global__ void attn_dsum_kernel(const uint16_t *o, const uint16_t *dO, int M, i
   float s = 0.f;
   for (int i = lane * 2; i < D; i += 64) {
     const uint32_t x = ld32(a + i), y = ld32(g + i);
-    s += bf16_lo(x) * bf16_lo(y) + bf16_hi(x) * bf16_hi(y);
+    s += lo16<true>(x) * bf16_lo(y) + hi16<true>(x) * bf16_hi(y);
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
@@ -205,10 +221,11 @@ __global__ void __launch_bounds__(128) attn_bwd_dkdv_kernel(
     int nh, int nkv, float *part_k, float *part_v, float scale_log2, float scale) {
   constexpr int QT = 32, LDS = D + 8, NC = D / 16;
   extern __shared__ __align__(16) uint8_t smraw[];
-  uint16_t *Ks = reinterpret_cast<uint16_t *>(smraw);
-  uint16_t *Vs = Ks + 64 * LDS;
-  uint16_t *Qs = Vs + 64 * LDS;
-  uint16_t *dOs = Qs + QT * LDS;
+  uint16_t *Ks = reinterpret_cast<uint16_t *>(smraw);  // half
+  uint16_t *Vs = Ks + 64 * LDS;                         // bf16
+  uint16_t *Qs = Vs + 64 * LDS;                         // half
+  uint16_t *Qb = Qs + QT * LDS;                         // bf16
+  uint16_t *dOs = Qb + QT * LDS;                        // bf16
   float *lse_s = reinterpret_cast<float *>(dOs + QT * LDS);
   float *ds_s = lse_s + QT;
 
@@ -220,7 +237,7 @@ __global__ void __launch_bounds__(128) attn_bwd_dkdv_kernel(
   const size_t rowbase = (size_t)b * S;
 
   load_tile<D>(Ks, qkv, ld, rowbase, kb * 64, 64, S, (nh + g) * D);
-  load_tile<D>(Vs, qkv, ld, rowbase, kb * 64, 64, S, (nh + nkv + g) * D);
+  load_tile<D, true>(Vs, qkv, ld, rowbase, kb * 64, 64, S, (nh + nkv + g) * D);
 
   float dk[D / 8][4], dv[D / 8][4];
 #pragma unroll
@@ -232,6 +249,7 @@ __global__ void __launch_bounds__(128) attn_bwd_dkdv_kernel(
   for (int q0 = (kb * 64 / QT) * QT; q0 < S; q0 += QT) {
     __syncthreads();
     load_tile<D>(Qs, qkv, ld, rowbase, q0, QT, S, h * D);
+    load_tile<D, true>(Qb, qkv, ld, rowbase, q0, QT, S, h * D);
     load_tile<D>(dOs, dO, nh * D, rowbase, q0, QT, S, h * D);
     for (int i = threadIdx.x; i < QT; i += blockDim.x) {
       const bool ok = q0 + i < S;
@@ -254,9 +272,9 @@ __global__ void __launch_bounds__(128) attn_bwd_dkdv_kernel(
 #pragma unroll
       for (int nt = 0; nt < QT / 8; ++nt) {
         const uint16_t *qp = Qs + (nt * 8 + gr) * LDS + kc * 16 + 2 * tq;
-        mma16816(st[nt], ak, ld32(qp), ld32(qp + 8));
+        mma16816<true>(st[nt], ak, ld32(qp), ld32(qp + 8));
         const uint16_t *dp = dOs + (nt * 8 + gr) * LDS + kc * 16 + 2 * tq;
-        mma16816(dpt[nt], av, ld32(dp), ld32(dp + 8));
+        mma16816<false>(dpt[nt], av, ld32(dp), ld32(dp + 8));
       }
     }
 #pragma unroll
@@ -287,11 +305,11 @@ __global__ void __launch_bounds__(128) attn_bwd_dkdv_kernel(
         uint32_t r0, r1, r2, r3;
         const int col = dn * 16 + (lane >> 4) * 8;
         ldsm_x4_t(smem_u32(dOs + qr * LDS + col), r0, r1, r2, r3);
-        mma16816(dv[2 * dn], ap, r0, r1);
-        mma16816(dv[2 * dn + 1], ap, r2, r3);
-        ldsm_x4_t(smem_u32(Qs + qr * LDS + col), r0, r1, r2, r3);
-        mma16816(dk[2 * dn], as, r0, r1);
-        mma16816(dk[2 * dn + 1], as, r2, r3);
+        mma16816<false>(dv[2 * dn], ap, r0, r1);
+        mma16816<false>(dv[2 * dn + 1], ap, r2, r3);
+        ldsm_x4_t(smem_u32(Qb + qr * LDS + col), r0, r1, r2, r3);
+        mma16816<false>(dk[2 * dn], as, r0, r1);
+        mma16816<false>(dk[2 * dn + 1], as, r2, r3);
       }
     }
   }
@@ -341,8 +359,9 @@ __global__ void __launch_bounds__(128) attn_bwd_dq_kernel(const uint16_t *qkv, i
                                                           const float *dsum, int S, int nh, int nkv,
                                                           float *dqkv, float scale_log2, float scale) {
   constexpr int KT = 32, LDS = D + 8, NC = D / 16;
-  __shared__ __align__(16) uint16_t Ks[KT * LDS];
-  __shared__ __align__(16) uint16_t Vs[KT * LDS];
+  __shared__ __align__(16) uint16_t Ks[KT * LDS];  // half, for the scores
+  __shared__ __align__(16) uint16_t Kb[KT * LDS];  // bf16, for dQ
+  __shared__ __align__(16) uint16_t Vs[KT * LDS];  // bf16, for dP
   const int qb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int g = (h * nkv) / nh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -383,7 +402,8 @@ __global__ void __launch_bounds__(128) attn_bwd_dq_kernel(const uint16_t *qkv, i
     const int k0 = kt * KT;
     __syncthreads();
     load_tile<D>(Ks, qkv, ld, rowbase, k0, KT, S, (nh + g) * D);
-    load_tile<D>(Vs, qkv, ld, rowbase, k0, KT, S, (nh + nkv + g) * D);
+    load_tile<D, true>(Kb, qkv, ld, rowbase, k0, KT, S, (nh + g) * D);
+    load_tile<D, true>(Vs, qkv, ld, rowbase, k0, KT, S, (nh + nkv + g) * D);
     __syncthreads();
     if (k0 > q0 + 15) continue;
     float s[KT / 8][4], dp[KT / 8][4];
@@ -394,9 +414,9 @@ __global__ void __launch_bounds__(128) attn_bwd_dq_kernel(const uint16_t *qkv, i
 #pragma unroll
       for (int kc = 0; kc < NC; ++kc) {
         const uint16_t *kp = Ks + (nt * 8 + gr) * LDS + kc * 16 + 2 * tq;
-        mma16816(s[nt], qf[kc], ld32(kp), ld32(kp + 8));
+        mma16816<true>(s[nt], qf[kc], ld32(kp), ld32(kp + 8));
         const uint16_t *vp = Vs + (nt * 8 + gr) * LDS + kc * 16 + 2 * tq;
-        mma16816(dp[nt], df[kc], ld32(vp), ld32(vp + 8));
+        mma16816<false>(dp[nt], df[kc], ld32(vp), ld32(vp + 8));
       }
     }
 #pragma unroll
@@ -420,9 +440,9 @@ __global__ void __launch_bounds__(128) attn_bwd_dq_kernel(const uint16_t *qkv, i
 #pragma unroll
       for (int dn = 0; dn < NC; ++dn) {
         uint32_t r0, r1, r2, r3;
-        ldsm_x4_t(smem_u32(Ks + key * LDS + dn * 16 + (lane >> 4) * 8), r0, r1, r2, r3);
-        mma16816(dq[2 * dn], a, r0, r1);
-        mma16816(dq[2 * dn + 1], a, r2, r3);
+        ldsm_x4_t(smem_u32(Kb + key * LDS + dn * 16 + (lane >> 4) * 8), r0, r1, r2, r3);
+        mma16816<false>(dq[2 * dn], a, r0, r1);
+        mma16816<false>(dq[2 * dn + 1], a, r2, r3);
       }
     }
   }
@@ -454,7 +474,7 @@ int attn_bwd_impl(const uint16_t *qkv, int ld, const uint16_t *o, const uint16_t
   }
   dim3 grid((S + 63) / 64, nh, B);
   constexpr int LDS = D + 8;
-  const int smem = (2 * 64 + 2 * 32) * LDS * 2 + 2 * 32 * 4;
+  const int smem = (2 * 64 + 3 * 32) * LDS * 2 + 2 * 32 * 4;
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D>,
@@ -468,6 +488,7 @@ int attn_bwd_impl(const uint16_t *qkv, int ld, const uint16_t *o, const uint16_t
   attn_kv_reduce_kernel<<<(unsigned)std::min<int64_t>((nred + 255) / 256, 148 * 32), 256, 0, st>>>(
       part_k, part_v, B, S, nh, nkv, D, dqkv, ld);
   attn_bwd_dq_kernel<D><<<grid, 128, 0, st>>>(qkv, ld, dO, lse, dsum, S, nh, nkv, dqkv, scale_log2, scale);
+  count_launches(4);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(SOUP_ECUDA, "attention backward launch: %s", cudaGetErrorString(e));
   return 0;
@@ -483,9 +504,10 @@ int k_attn_fwd(const uint16_t *qkv, int ld, int B, int S, int nh, int nkv, int d
                float *lse, cudaStream_t st) {
   const float scale_log2 = (1.0f / sqrtf((float)d)) * 1.4426950408889634f;
   dim3 grid((S + 63) / 64, nh, B);
-  if (d == 128) attn_fwd_kernel<128><<<grid, 128, 0, st>>>(qkv, ld, S, nh, nkv, o, lse, scale_log2);
-  else if (d == 64) attn_fwd_kernel<64><<<grid, 128, 0, st>>>(qkv, ld, S, nh, nkv, o, lse, scale_log2);
+  if (d == 128) attn_fwd_kernel<128, true><<<grid, 128, 0, st>>>(qkv, ld, S, nh, nkv, o, lse, scale_log2);
+  else if (d == 64) attn_fwd_kernel<64, true><<<grid, 128, 0, st>>>(qkv, ld, S, nh, nkv, o, lse, scale_log2);
   else return set_error(SOUP_EINVAL, "attention: head_dim %d not supported (64 or 128)", d);
+  count_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(SOUP_ECUDA, "attention forward launch: %s", cudaGetErrorString(e));
   return 0;

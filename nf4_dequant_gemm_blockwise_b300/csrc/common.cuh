@@ -5,6 +5,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -33,6 +34,26 @@ SOUP_DEV uint16_t f_to_bf16(float f) {
   __nv_bfloat16 b = __float2bfloat16_rn(f);
   return *reinterpret_cast<uint16_t *>(&b);
 }
+
+// IEEE half helpers (the forward path's tensor-core operand format).
+SOUP_DEV uint32_t pack_h2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+SOUP_DEV float h16_to_f(uint16_t v) { return __half2float(__ushort_as_half(v)); }
+SOUP_DEV uint16_t f_to_h16(float f) { return __half_as_ushort(__float2half_rn(f)); }
+
+// 16-bit operand format chosen at compile time: F16 = IEEE half, else bf16.
+template <bool F16>
+SOUP_DEV float ld16(uint16_t v) { return F16 ? h16_to_f(v) : bf16_to_f(v); }
+template <bool F16>
+SOUP_DEV uint16_t st16(float f) { return F16 ? f_to_h16(f) : f_to_bf16(f); }
+template <bool F16>
+SOUP_DEV uint32_t pack16x2(float lo, float hi) { return F16 ? pack_h2(lo, hi) : pack_bf16x2(lo, hi); }
+template <bool F16>
+SOUP_DEV float lo16(uint32_t v) { return ld16<F16>((uint16_t)(v & 0xffffu)); }
+template <bool F16>
+SOUP_DEV float hi16(uint32_t v) { return ld16<F16>((uint16_t)(v >> 16)); }
 
 SOUP_DEV uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
@@ -157,12 +178,13 @@ SOUP_DEV uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   d |= (uint64_t)2 << 61;
   return d;
 }
-// Instruction descriptor for kind::f16 with bf16 A/B, f32 D, M x N tile.
-// b_mn_major: B operand stored with its N (output) dimension contiguous.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn_major, int b_mn_major) {
-  return (1u << 4)                       // D format: f32
-         | (1u << 7)                     // A format: bf16
-         | (1u << 10)                    // B format: bf16
+// Instruction descriptor for kind::f16, f32 D, M x N tile; A and B both f16 (f16 = 1) or
+// both bf16.  b_mn_major: B operand stored with its N (output) dimension contiguous.
+__host__ __device__ constexpr uint32_t idesc_16(int M, int N, int a_mn_major, int b_mn_major,
+                                                int f16) {
+  return (1u << 4)                                // D format: f32
+         | ((uint32_t)(f16 ? 0 : 1) << 7)         // A format: f16 (0) or bf16 (1)
+         | ((uint32_t)(f16 ? 0 : 1) << 10)        // B format: same as A
          | ((uint32_t)a_mn_major << 15)  // A major-ness
          | ((uint32_t)b_mn_major << 16)  // B major-ness
          | ((uint32_t)(N >> 3) << 17)    // N / 8

@@ -6,8 +6,10 @@
 // the backward dequantises, it never caches dequantised weights):
 //   forward  y  = x  deq(W)^T + s (x A^T) B^T
 //   backward dx = dY deq(W)   + s (dY B)   A
-// deq(W)[n,k] = bf16_rne(float(c[code] * absmax[block])), blocks of 64 along the flattened
-// [out, in] matrix.  The rank-r LoRA term is folded into the same tensor-core reduction as
+// deq(W)[n,k] = round16(float(c[code] * absmax[block])), blocks of 64 along the flattened
+// [out, in] matrix, where round16 rounds to nearest-even in the GEMM's 16-bit operand format:
+// IEEE half for the forward (activations are half there), bf16 for dX (gradients need the
+// exponent range).  The rank-r LoRA term is folded into the same tensor-core reduction as
 // extra 64-wide K tiles: the caller packs s(xA^T) (or s(dY B)) as bf16 [M, R] and the
 // matching B rows (or A rows) as bf16, zero-padded to R = 64 * ceil(segments * r / 64).
 //
@@ -42,9 +44,12 @@ constexpr int DQ_WARPS = 8;
 constexpr int THREADS = (DQ_WARPS + 2) * 32;
 enum BMode { B_NF4_K = 0, B_NF4_MN = 1, B_BF16_K = 2, B_BF16_MN = 3 };
 
-template <int BN, int BMODE>
+template <int BN, int BMODE, bool F16>
 struct TcCfg {
   static constexpr bool NF4 = (BMODE == B_NF4_K || BMODE == B_NF4_MN);
+  // bf16 weights feeding a half-precision GEMM are converted in shared memory, in place
+  static constexpr bool CONV = !NF4 && F16;
+  static constexpr bool PRODUCE = NF4 || CONV;  // the worker warps touch the B tile
   static constexpr bool MN = (BMODE == B_NF4_MN || BMODE == B_BF16_MN);
   static constexpr int A_BYTES = BM * 128;
   static constexpr int B_BYTES = BN * 128;
@@ -70,11 +75,12 @@ struct TcParams {
 };
 
 // Dequantise one 64-weight block: cw = 32 bytes of packed codes, a = the block's absmax.
-// out[c] = 8 bf16 weights c*8 .. c*8+7.
+// out[c] = 8 16-bit weights c*8 .. c*8+7 (half if F16, else bf16).
+template <bool F16>
 SOUP_DEV void dq_block64(const float *cb, const uint32_t (&cw)[8], float a, uint4 (&out)[8]) {
   uint32_t P[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) P[j] = pack_bf16x2(cb[2 * j] * a, cb[2 * j + 1] * a);
+  for (int j = 0; j < 8; ++j) P[j] = pack16x2<F16>(cb[2 * j] * a, cb[2 * j + 1] * a);
   uint32_t LO[4], HI[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -93,7 +99,7 @@ SOUP_DEV void dq_block64(const float *cb, const uint32_t (&cw)[8], float a, uint
       const uint32_t pick = ((s >> 1) & 0x4444u) | 0x3210u;  // +4 for codes 8..15
       const uint32_t lo = prmt(prmt(LO[0], LO[1], s7), prmt(LO[2], LO[3], s7), pick);
       const uint32_t hi = prmt(prmt(HI[0], HI[1], s7), prmt(HI[2], HI[3], s7), pick);
-      o[2 * h] = prmt(lo, hi, 0x4051);      // (even, odd) code of byte 0 -> bf16x2
+      o[2 * h] = prmt(lo, hi, 0x4051);      // (even, odd) code of byte 0 -> 16x2
       o[2 * h + 1] = prmt(lo, hi, 0x6273);  // byte 1
     }
     out[w] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -106,14 +112,14 @@ SOUP_DEV uint32_t sw128(int r, int c) {
   return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
-template <int BN, int BMODE, int EPI>
+template <int BN, int BMODE, int EPI, bool F16>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_b0,
                    const __grid_constant__ CUtensorMap map_b1,
                    const __grid_constant__ CUtensorMap map_ul,
                    const __grid_constant__ CUtensorMap map_vl, const TcParams p) {
-  using C = TcCfg<BN, BMODE>;
+  using C = TcCfg<BN, BMODE, F16>;
   constexpr int NS = C::NS;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
@@ -207,8 +213,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == DQ_WARPS + 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(BM, BN, 0, C::MN ? 1 : 0);
-      uint64_t *wait_bar = C::NF4 ? bready : full;
+      constexpr uint32_t idesc = idesc_16(BM, BN, 0, C::MN ? 1 : 0, F16 ? 1 : 0);
+      uint64_t *wait_bar = C::PRODUCE ? bready : full;
       for (int kt = 0; kt < n_total; ++kt) {
         const int s = kt % NS;
         if (!mbar_wait(&wait_bar[s], (kt / NS) & 1, p.err, abort_flag)) break;
@@ -231,9 +237,22 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     // ---------------------------------------------------------------- dequant warps
     const int t = threadIdx.x;  // 0 .. 255
-    for (int kt = 0; C::NF4 && kt < n_total; ++kt) {
+    for (int kt = 0; C::PRODUCE && kt < n_total; ++kt) {
       const int s = kt % NS;
       if (!mbar_wait(&full[s], (kt / NS) & 1, p.err, abort_flag)) break;
+      if (C::CONV && kt < p.n_main) {
+        // bf16 -> half, element by element; the byte layout (and so the swizzle) is unchanged
+        uint4 *Bs = reinterpret_cast<uint4 *>(B_s(s));
+        for (int i = t; i < C::B_BYTES / 16; i += DQ_WARPS * 32) {
+          uint4 v = Bs[i];
+          v.x = pack_h2(bf16_lo(v.x), bf16_hi(v.x));
+          v.y = pack_h2(bf16_lo(v.y), bf16_hi(v.y));
+          v.z = pack_h2(bf16_lo(v.z), bf16_hi(v.z));
+          v.w = pack_h2(bf16_lo(v.w), bf16_hi(v.w));
+          Bs[i] = v;
+        }
+        fence_async_smem();
+      }
       if (C::NF4 && kt < p.n_main) {
         uint8_t *Bs = B_s(s);
         const uint8_t *Rs = R_s(s);
@@ -245,7 +264,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const float a = *reinterpret_cast<const float *>(Ss + n * 16 + (kt & 3) * 4);
             const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
             uint4 o[8];
-            dq_block64(p.cb.v, cw, a, o);
+            dq_block64<F16>(p.cb.v, cw, a, o);
 #pragma unroll
             for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(Bs + sw128(n, c)) = o[c];
           }
@@ -257,7 +276,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const float a = *reinterpret_cast<const float *>(Ss + n * 16 + seg * 4);
             const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
             uint4 o[8];
-            dq_block64(p.cb.v, cw, a, o);
+            dq_block64<F16>(p.cb.v, cw, a, o);
 #pragma unroll
             for (int c = 0; c < 8; ++c)
               *reinterpret_cast<uint4 *>(Bs + seg * 8192 + sw128(n, c)) = o[c];
@@ -284,22 +303,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int n = n0 + col;
         if (n >= p.Ng) continue;
         const bool full_row = (n + 32 <= p.Ng);
-        if (EPI == EPI_BF16) {
+        if (EPI == EPI_16) {
           uint16_t *o = reinterpret_cast<uint16_t *>(p.out) + (size_t)m * p.ldo + n;
           if (full_row) {
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
-              w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
-              w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
-              w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+              w.x = pack16x2<F16>(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+              w.y = pack16x2<F16>(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+              w.z = pack16x2<F16>(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+              w.w = pack16x2<F16>(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
               *reinterpret_cast<uint4 *>(o + 8 * v) = w;
             }
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              if (n + j < p.Ng) o[j] = f_to_bf16(__uint_as_float(r[j]));
+              if (n + j < p.Ng) o[j] = st16<F16>(__uint_as_float(r[j]));
           }
         } else {
           float *o = reinterpret_cast<float *>(p.out) + (size_t)m * p.ldo + n;
@@ -344,6 +363,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 // unaligned strides).  Same operand definition, float accumulation, 64x64 tiles.
 struct FbParams {
   Codebook cb;
+  int f16;
   int mode, M, Ng, Kg, wfmt, Nw, Kw, ldw, lda, R, epi, ldo, ld_add;
   const uint16_t *a;
   const uint8_t *codes;
@@ -354,15 +374,19 @@ struct FbParams {
   const float *add_src;
 };
 
+SOUP_DEV float fb_round(const FbParams &p, float v) {
+  return p.f16 ? h16_to_f(f_to_h16(v)) : bf16_to_f(f_to_bf16(v));
+}
+SOUP_DEV float fb_ld16(const FbParams &p, uint16_t v) { return p.f16 ? h16_to_f(v) : bf16_to_f(v); }
 SOUP_DEV float fb_weight(const FbParams &p, int row, int col) {  // W[row, col] as used
   if (p.wfmt == W_NF4) {
     const int64_t f = (int64_t)row * p.Kw + col;
     const uint8_t b = p.codes[f >> 1];
     const int code = (f & 1) ? (b & 15) : (b >> 4);
     const float v = p.cb.v[code] * p.absmax[f >> 6];
-    return bf16_to_f(f_to_bf16(v));
+    return fb_round(p, v);
   }
-  return bf16_to_f(p.w[(int64_t)row * p.ldw + col]);
+  return fb_round(p, bf16_to_f(p.w[(int64_t)row * p.ldw + col]));
 }
 
 __global__ void __launch_bounds__(256) fallback_gemm_kernel(const FbParams p) {
@@ -379,8 +403,8 @@ __global__ void __launch_bounds__(256) fallback_gemm_kernel(const FbParams p) {
       const int m = m0 + mm, k = k0 + kk;
       float v = 0.f;
       if (m < p.M && k < k_total) {
-        if (k < k_main) v = bf16_to_f(p.a[(int64_t)m * p.lda + k]);
-        else v = bf16_to_f(p.ul[(int64_t)m * p.R + (k - k_main)]);
+        if (k < k_main) v = fb_ld16(p, p.a[(int64_t)m * p.lda + k]);
+        else v = fb_ld16(p, p.ul[(int64_t)m * p.R + (k - k_main)]);
       }
       As[kk][mm] = v;
       const int n = n0 + mm;
@@ -389,8 +413,8 @@ __global__ void __launch_bounds__(256) fallback_gemm_kernel(const FbParams p) {
         if (k < k_main) b = (p.mode == GEMM_FWD) ? fb_weight(p, n, k) : fb_weight(p, k, n);
         else {
           const int j = k - k_main;
-          b = (p.mode == GEMM_FWD) ? bf16_to_f(p.vl[(int64_t)n * p.R + j])
-                                   : bf16_to_f(p.vl[(int64_t)j * p.Ng + n]);
+          b = (p.mode == GEMM_FWD) ? fb_ld16(p, p.vl[(int64_t)n * p.R + j])
+                                   : fb_ld16(p, p.vl[(int64_t)j * p.Ng + n]);
         }
       }
       Bs[kk][mm] = b;
@@ -419,8 +443,8 @@ __global__ void __launch_bounds__(256) fallback_gemm_kernel(const FbParams p) {
       const int n = n0 + tx * 4 + j;
       if (n >= p.Ng) continue;
       const float v = acc[i][j];
-      if (p.epi == EPI_BF16) {
-        reinterpret_cast<uint16_t *>(p.out)[(int64_t)m * p.ldo + n] = f_to_bf16(v);
+      if (p.epi == EPI_16) {
+        reinterpret_cast<uint16_t *>(p.out)[(int64_t)m * p.ldo + n] = p.f16 ? f_to_h16(v) : f_to_bf16(v);
       } else {
         float *o = reinterpret_cast<float *>(p.out) + (int64_t)m * p.ldo + n;
         if (p.epi == EPI_F32) *o = v;
@@ -465,11 +489,11 @@ int make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t 
   return 0;
 }
 
-template <int BN, int BMODE, int EPI>
+template <int BN, int BMODE, int EPI, bool F16>
 int launch_tc(const GemmArgs &g, const CUtensorMap *maps, cudaStream_t st) {
-  using C = TcCfg<BN, BMODE>;
+  using C = TcCfg<BN, BMODE, F16>;
   static bool attr_done = false;  // per instantiation; set under g_mu
-  auto kern = tc_gemm_kernel<BN, BMODE, EPI>;
+  auto kern = tc_gemm_kernel<BN, BMODE, EPI, F16>;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!attr_done) {
@@ -491,19 +515,25 @@ int launch_tc(const GemmArgs &g, const CUtensorMap *maps, cudaStream_t st) {
   p.err = g.err;
   dim3 grid((p.Ng + BN - 1) / BN, (g.M + BM - 1) / BM);
   kern<<<grid, THREADS, C::SMEM, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
+  count_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(SOUP_ECUDA, "tc_gemm launch: %s", cudaGetErrorString(e));
   return 0;
 }
 
-template <int BN, int BMODE>
+template <int BN, int BMODE, bool F16>
 int launch_tc_epi(const GemmArgs &g, const CUtensorMap *maps, cudaStream_t st) {
   switch (g.epi) {
-    case EPI_BF16: return launch_tc<BN, BMODE, EPI_BF16>(g, maps, st);
-    case EPI_F32: return launch_tc<BN, BMODE, EPI_F32>(g, maps, st);
-    case EPI_F32_ADD: return launch_tc<BN, BMODE, EPI_F32_ADD>(g, maps, st);
-    default: return launch_tc<BN, BMODE, EPI_F32_ACC>(g, maps, st);
+    case EPI_16: return launch_tc<BN, BMODE, EPI_16, F16>(g, maps, st);
+    case EPI_F32: return launch_tc<BN, BMODE, EPI_F32, F16>(g, maps, st);
+    case EPI_F32_ADD: return launch_tc<BN, BMODE, EPI_F32_ADD, F16>(g, maps, st);
+    default: return launch_tc<BN, BMODE, EPI_F32_ACC, F16>(g, maps, st);
   }
+}
+template <int BN, int BMODE>
+int launch_tc_op(const GemmArgs &g, const CUtensorMap *maps, cudaStream_t st) {
+  return g.op_f16 ? launch_tc_epi<BN, BMODE, true>(g, maps, st)
+                  : launch_tc_epi<BN, BMODE, false>(g, maps, st);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -527,7 +557,7 @@ int gemm_uses_tc(const GemmArgs &g) {
     if (ldw % 8 || !aligned16(g.w)) return 0;
     if (g.mode == GEMM_DX && Ng % 8) return 0;
   }
-  if (g.epi == EPI_BF16 ? (g.ldo % 8) : (g.ldo % 4)) return 0;
+  if (g.epi == EPI_16 ? (g.ldo % 8) : (g.ldo % 4)) return 0;
   if (g.epi == EPI_F32_ADD && (g.ld_add % 4 || !aligned16(g.add_src))) return 0;
   if (!aligned16(g.out)) return 0;
   return 1;
@@ -540,7 +570,7 @@ double gemm_flops(const GemmArgs &g) {
 double gemm_bytes(const GemmArgs &g) {
   const double nw = (double)g.Nw * g.Kw;
   const double wb = g.wfmt == W_NF4 ? nw * 0.5 + nw / 64.0 * 4.0 : nw * 2.0;
-  const double out_b = g.epi == EPI_BF16 ? 2.0 : 4.0;
+  const double out_b = g.epi == EPI_16 ? 2.0 : 4.0;
   double b = wb + 2.0 * g.M * g.Kg() + out_b * g.M * (double)g.Ng();
   if (g.epi == EPI_F32_ADD || g.epi == EPI_F32_ACC) b += 4.0 * g.M * (double)g.Ng();
   b += 2.0 * g.R * ((double)g.M + g.Ng());
@@ -561,6 +591,7 @@ int gemm_launch(const GemmArgs &g, cudaStream_t st) {
   if (!gemm_uses_tc(g)) {
     FbParams p;
     p.cb = nf4_codebook_param();
+    p.f16 = g.op_f16;
     p.mode = g.mode; p.M = g.M; p.Ng = g.Ng(); p.Kg = g.Kg(); p.wfmt = g.wfmt;
     p.Nw = g.Nw; p.Kw = g.Kw; p.ldw = g.ldw ? g.ldw : g.Kw; p.lda = g.lda; p.R = g.R;
     p.epi = g.epi; p.ldo = g.ldo; p.ld_add = g.ld_add; p.a = g.a; p.codes = g.codes;
@@ -568,6 +599,7 @@ int gemm_launch(const GemmArgs &g, cudaStream_t st) {
     p.add_src = g.add_src;
     dim3 grid((p.Ng + 63) / 64, (g.M + 63) / 64);
     fallback_gemm_kernel<<<grid, 256, 0, st>>>(p);
+    count_launches(1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(SOUP_ECUDA, "fallback gemm launch: %s", cudaGetErrorString(e));
     return 0;
@@ -577,7 +609,8 @@ int gemm_launch(const GemmArgs &g, cudaStream_t st) {
   constexpr int BN = 256;
   const int Ng = g.Ng(), Kg = g.Kg();
   CUtensorMap maps[5];
-  rc = make_map(&maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.a, (uint64_t)Kg, (uint64_t)g.M,
+  const CUtensorMapDataType t16 = g.op_f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  rc = make_map(&maps[0], t16, g.a, (uint64_t)Kg, (uint64_t)g.M,
                 (uint64_t)g.lda * 2, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B, "activations");
   if (rc) return rc;
   int bmode;
@@ -612,14 +645,14 @@ int gemm_launch(const GemmArgs &g, cudaStream_t st) {
   }
   if (rc) return rc;
   if (g.R) {
-    rc = make_map(&maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.ul, (uint64_t)g.R, (uint64_t)g.M,
+    rc = make_map(&maps[3], t16, g.ul, (uint64_t)g.R, (uint64_t)g.M,
                   (uint64_t)g.R * 2, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B, "lora ul");
     if (rc) return rc;
     if (g.mode == GEMM_FWD)
-      rc = make_map(&maps[4], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.vl, (uint64_t)g.R, (uint64_t)Ng,
+      rc = make_map(&maps[4], t16, g.vl, (uint64_t)g.R, (uint64_t)Ng,
                     (uint64_t)g.R * 2, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B, "lora vl");
     else
-      rc = make_map(&maps[4], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.vl, (uint64_t)Ng, (uint64_t)g.R,
+      rc = make_map(&maps[4], t16, g.vl, (uint64_t)Ng, (uint64_t)g.R,
                     (uint64_t)Ng * 2, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B, "lora vl");
     if (rc) return rc;
   } else {
@@ -627,10 +660,10 @@ int gemm_launch(const GemmArgs &g, cudaStream_t st) {
     maps[4] = maps[0];
   }
   switch (bmode) {
-    case B_NF4_K: return launch_tc_epi<BN, B_NF4_K>(g, maps, st);
-    case B_NF4_MN: return launch_tc_epi<BN, B_NF4_MN>(g, maps, st);
-    case B_BF16_K: return launch_tc_epi<BN, B_BF16_K>(g, maps, st);
-    default: return launch_tc_epi<BN, B_BF16_MN>(g, maps, st);
+    case B_NF4_K: return launch_tc_op<BN, B_NF4_K>(g, maps, st);
+    case B_NF4_MN: return launch_tc_op<BN, B_NF4_MN>(g, maps, st);
+    case B_BF16_K: return launch_tc_op<BN, B_BF16_K>(g, maps, st);
+    default: return launch_tc_op<BN, B_BF16_MN>(g, maps, st);
   }
 }
 

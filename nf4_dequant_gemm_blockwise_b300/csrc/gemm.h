@@ -9,7 +9,7 @@ namespace soup {
 enum GemmMode { GEMM_FWD = 0, GEMM_DX = 1 };   // FWD: y = a W^T ; DX: y = a W
 enum WFmt { W_BF16 = 0, W_NF4 = 1 };
 enum Epi {
-  EPI_BF16 = 0,     // out bf16 = acc
+  EPI_16 = 0,       // out 16-bit (half if op_f16, else bf16) = acc
   EPI_F32 = 1,      // out f32 = acc
   EPI_F32_ADD = 2,  // out f32 = add_src + acc   (residual; add_src may alias out)
   EPI_F32_ACC = 3   // out f32 += acc
@@ -17,8 +17,9 @@ enum Epi {
 
 struct GemmArgs {
   int mode = GEMM_FWD;
+  int op_f16 = 0;               // 16-bit operands (a, ul, vl, 16-bit out) are half, else bf16
   int M = 0;
-  const uint16_t *a = nullptr;  // bf16 [M, Kg], row stride lda elements
+  const uint16_t *a = nullptr;  // [M, Kg], row stride lda elements
   int lda = 0;
   // base weight W [Nw, Kw] (out x in)
   int wfmt = W_NF4;
@@ -33,7 +34,7 @@ struct GemmArgs {
   const uint16_t *ul = nullptr;
   const uint16_t *vl = nullptr;
   int R = 0;
-  int epi = EPI_BF16;
+  int epi = EPI_16;
   void *out = nullptr;
   int ldo = 0;
   const float *add_src = nullptr;

@@ -8,10 +8,12 @@
 // x / sqrt(mean x^2 + eps) * w, rotate-half RoPE, SiLU-gated MLP, LoRA y += s (x A^T) B^T.
 // All arithmetic is float32; every reduction has a fixed order (warp shuffles and block
 // trees, never atomics), so results do not depend on scheduling.
+#include <algorithm>
 #include <cmath>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "util.h"
 
 namespace soup {
 namespace {
@@ -45,6 +47,7 @@ __global__ void embed_kernel(const int32_t *tok, const uint16_t *E, int V, int H
 }
 
 // ------------------------------------------------------------------ RMSNorm
+template <bool F16>
 __global__ void rmsnorm_fwd_kernel(const float *h, const uint16_t *w, float eps, int M, int H,
                                    uint16_t *out) {
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -63,8 +66,8 @@ __global__ void rmsnorm_fwd_kernel(const float *h, const uint16_t *w, float eps,
     const float4 v = *reinterpret_cast<const float4 *>(x + i);
     const uint2 wv = *reinterpret_cast<const uint2 *>(w + i);
     uint2 res;
-    res.x = pack_bf16x2(v.x * r * bf16_lo(wv.x), v.y * r * bf16_hi(wv.x));
-    res.y = pack_bf16x2(v.z * r * bf16_lo(wv.y), v.w * r * bf16_hi(wv.y));
+    res.x = pack16x2<F16>(v.x * r * bf16_lo(wv.x), v.y * r * bf16_hi(wv.x));
+    res.y = pack16x2<F16>(v.z * r * bf16_lo(wv.y), v.w * r * bf16_hi(wv.y));
     *reinterpret_cast<uint2 *>(o + i) = res;
   }
 }
@@ -113,6 +116,7 @@ __global__ void rmsnorm_bwd_kernel(const float *dy, const float *h, const uint16
 }
 
 // ------------------------------------------------------------------ RoPE (rotate-half)
+template <bool F16>
 __global__ void rope_fwd_kernel(uint16_t *qkv, int ld, const float *cs, const float *sn, int M,
                                 int S, int nheads_rot, int d) {
   const int half = d >> 1;
@@ -125,10 +129,10 @@ __global__ void rope_fwd_kernel(uint16_t *qkv, int ld, const float *cs, const fl
     const int m = (int)(rest / nheads_rot);
     const int pos = m % S;
     uint16_t *p = qkv + (size_t)m * ld + (size_t)head * d;
-    const float x1 = bf16_to_f(p[i]), x2 = bf16_to_f(p[i + half]);
+    const float x1 = ld16<F16>(p[i]), x2 = ld16<F16>(p[i + half]);
     const float c = cs[pos * half + i], s = sn[pos * half + i];
-    p[i] = f_to_bf16(x1 * c - x2 * s);
-    p[i + half] = f_to_bf16(x2 * c + x1 * s);
+    p[i] = st16<F16>(x1 * c - x2 * s);
+    p[i + half] = st16<F16>(x2 * c + x1 * s);
   }
 }
 
@@ -161,24 +165,26 @@ __global__ void rope_bwd_kernel(const float *dqkv, uint16_t *out, int ld, const 
 // ------------------------------------------------------------------ SwiGLU
 SOUP_DEV float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
 
+template <bool F16>
 __global__ void swiglu_fwd_kernel(const uint16_t *gu, int M, int I, uint16_t *act) {
   const int64_t total = (int64_t)M * I;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
        idx += (int64_t)gridDim.x * blockDim.x) {
     const int64_t m = idx / I, j = idx % I;
-    const float g = bf16_to_f(gu[m * 2 * I + j]);
-    const float u = bf16_to_f(gu[m * 2 * I + I + j]);
-    act[idx] = f_to_bf16(g * sigmoidf_(g) * u);
+    const float g = ld16<F16>(gu[m * 2 * I + j]);
+    const float u = ld16<F16>(gu[m * 2 * I + I + j]);
+    act[idx] = st16<F16>(g * sigmoidf_(g) * u);
   }
 }
 
+template <bool F16>
 __global__ void swiglu_bwd_kernel(const float *dact, const uint16_t *gu, int M, int I, uint16_t *dgu) {
   const int64_t total = (int64_t)M * I;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
        idx += (int64_t)gridDim.x * blockDim.x) {
     const int64_t m = idx / I, j = idx % I;
-    const float g = bf16_to_f(gu[m * 2 * I + j]);
-    const float u = bf16_to_f(gu[m * 2 * I + I + j]);
+    const float g = ld16<F16>(gu[m * 2 * I + j]);
+    const float u = ld16<F16>(gu[m * 2 * I + I + j]);
     const float da = dact[idx];
     const float sg = sigmoidf_(g);
     dgu[m * 2 * I + j] = f_to_bf16(da * u * (sg * (1.0f + g * (1.0f - sg))));
@@ -187,33 +193,33 @@ __global__ void swiglu_bwd_kernel(const float *dact, const uint16_t *gu, int M, 
 }
 
 // ------------------------------------------------------------------ LoRA projections
-// out[m, o] = sum_k X[m, k] * W_o(k) for o < nseg*r, with
+// part[split][m][o] = sum over k in the split's range of X[m, k] * W_o(k), o < 64, with
 //   DOWN: X = x [M, K], W_o(k) = A_seg[j, k]                       (u = x A^T)
 //   DU:   X = dY [M, Ng], W_o(k) = B_seg[k - off_seg, j] inside the segment, else 0
-// Tile: 32 rows x 64 outputs per 256-thread block, K in chunks of 64; fixed order.
-template <bool DU>
-__global__ void __launch_bounds__(256) lora_proj_kernel(const uint16_t *X, int ldx, int M, int K,
-                                                        const LoraSeg L, float *out_f32,
-                                                        uint16_t *out_bf16) {
+// Tile: 32 rows x 64 outputs per 256-thread block; blockIdx.y picks the K range.  The
+// splits are then summed in split order by lora_reduce_kernel (no atomics).
+template <bool DU, bool XF16>
+__global__ void __launch_bounds__(256) lora_part_kernel(const uint16_t *X, int ldx, int M, int K,
+                                                        int KS, const LoraSeg L, float *part) {
   __shared__ float xs[32][65];
   __shared__ float ws[64][65];
   const int t = threadIdx.x;
   const int m0 = blockIdx.x * 32;
+  const int kb = blockIdx.y * KS, ke = min(K, kb + KS);
   const int nout = L.nseg * L.r;
-  const int Rp = L.Rpad();
   const int row = t >> 3, cb = t & 7;
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  for (int k0 = 0; k0 < K; k0 += 64) {
+  for (int k0 = kb; k0 < ke; k0 += 64) {
     for (int i = t; i < 32 * 64; i += 256) {
       const int rr = i >> 6, kk = i & 63;
       const int m = m0 + rr, k = k0 + kk;
-      xs[rr][kk] = (m < M && k < K) ? bf16_to_f(X[(size_t)m * ldx + k]) : 0.f;
+      xs[rr][kk] = (m < M && k < ke) ? ld16<XF16>(X[(size_t)m * ldx + k]) : 0.f;
     }
     for (int i = t; i < 64 * 64; i += 256) {
       const int o = i >> 6, kk = i & 63;
       const int k = k0 + kk;
       float v = 0.f;
-      if (o < nout && k < K) {
+      if (o < nout && k < ke) {
         const int seg = o / L.r, j = o % L.r;
         if (!DU) {
           v = L.A[seg][(size_t)j * K + k];
@@ -234,21 +240,34 @@ __global__ void __launch_bounds__(256) lora_proj_kernel(const uint16_t *X, int l
   }
   const int m = m0 + row;
   if (m >= M) return;
+  float *dst = part + ((size_t)blockIdx.y * M + m) * 64;
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const int o = cb + 8 * c;
-    if (o < nout) {
-      const float v = DU ? L.s * acc[c] : acc[c];
-      out_f32[(size_t)m * nout + o] = v;
-      out_bf16[(size_t)m * Rp + o] = f_to_bf16(L.s * acc[c]);
-    } else if (o < Rp) {
-      out_bf16[(size_t)m * Rp + o] = 0;
+  for (int c = 0; c < 8; ++c) dst[cb + 8 * c] = acc[c];
+}
+
+// out_f32[m, o] = (DU ? s : 1) * sum_split part; out16[m, o] = 16-bit(s * sum), zero padded.
+template <bool DU, bool OF16>
+__global__ void lora_reduce_kernel(const float *part, int nsplit, int M, const LoraSeg L,
+                                   float *out_f32, uint16_t *out16) {
+  const int nout = L.nseg * L.r;
+  const int Rp = L.Rpad();
+  const int64_t total = (int64_t)M * Rp;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int m = (int)(idx / Rp), o = (int)(idx % Rp);
+    if (o >= nout) {
+      out16[idx] = 0;
+      continue;
     }
+    float acc = 0.f;
+    for (int ks = 0; ks < nsplit; ++ks) acc += part[((size_t)ks * M + m) * 64 + o];
+    out_f32[(size_t)m * nout + o] = DU ? L.s * acc : acc;
+    out16[idx] = st16<OF16>(L.s * acc);
   }
-  for (int o = 64 + cb; o < Rp; o += 8) out_bf16[(size_t)m * Rp + o] = 0;
 }
 
 // dB_seg[n - off, j] = s * sum_m dY[m, n] u[m, seg*r + j]; 64 columns per block.
+template <bool F16>
 __global__ void __launch_bounds__(256) lora_dB_kernel(const uint16_t *dy, int ldy, int M, int Ng,
                                                       const float *u, const LoraSeg L) {
   __shared__ float ys[32][65];
@@ -268,7 +287,7 @@ __global__ void __launch_bounds__(256) lora_dB_kernel(const uint16_t *dy, int ld
     for (int i = t; i < 32 * 64; i += 256) {
       const int rr = i >> 6, cc = i & 63;
       const int m = mb + rr, nn = n0 + cc;
-      ys[rr][cc] = (m < M && nn < Ng) ? bf16_to_f(dy[(size_t)m * ldy + nn]) : 0.f;
+      ys[rr][cc] = (m < M && nn < Ng) ? ld16<F16>(dy[(size_t)m * ldy + nn]) : 0.f;
     }
     for (int i = t; i < 32 * 64; i += 256) {
       const int rr = i >> 6, o = i & 63;
@@ -297,6 +316,7 @@ __global__ void __launch_bounds__(256) lora_dB_kernel(const uint16_t *dy, int ld
 }
 
 // dA_seg[j, k] = sum_m du[m, seg*r + j] x[m, k]; 64 columns per block.
+template <bool F16>
 __global__ void __launch_bounds__(256) lora_dA_kernel(const float *du, const uint16_t *x, int ldx,
                                                       int M, int K, const LoraSeg L) {
   __shared__ float xs[32][65];
@@ -313,7 +333,7 @@ __global__ void __launch_bounds__(256) lora_dA_kernel(const float *du, const uin
     for (int i = t; i < 32 * 64; i += 256) {
       const int rr = i >> 6, cc = i & 63;
       const int m = mb + rr, kk = k0 + cc;
-      xs[rr][cc] = (m < M && kk < K) ? bf16_to_f(x[(size_t)m * ldx + kk]) : 0.f;
+      xs[rr][cc] = (m < M && kk < K) ? ld16<F16>(x[(size_t)m * ldx + kk]) : 0.f;
       ds[rr][cc] = (m < M && cc < nout) ? du[(size_t)m * nout + cc] : 0.f;
     }
     __syncthreads();
@@ -332,6 +352,7 @@ __global__ void __launch_bounds__(256) lora_dA_kernel(const float *du, const uin
   }
 }
 
+template <bool F16>
 __global__ void pack_fwd_kernel(const LoraSeg L, int Ng, uint16_t *vl) {
   const int Rp = L.Rpad();
   const int64_t total = (int64_t)Ng * Rp;
@@ -342,10 +363,11 @@ __global__ void pack_fwd_kernel(const LoraSeg L, int Ng, uint16_t *vl) {
     const int seg = c / L.r;
     if (seg < L.nseg && n >= L.off[seg] && n < L.off[seg] + L.n[seg])
       v = L.B[seg][(size_t)(n - L.off[seg]) * L.r + (c % L.r)];
-    vl[idx] = f_to_bf16(v);
+    vl[idx] = st16<F16>(v);
   }
 }
 
+template <bool F16>
 __global__ void pack_bwd_kernel(const LoraSeg L, int K, uint16_t *acat) {
   const int Rp = L.Rpad();
   const int64_t total = (int64_t)Rp * K;
@@ -354,7 +376,7 @@ __global__ void pack_bwd_kernel(const LoraSeg L, int K, uint16_t *acat) {
     const int row = (int)(idx / K), k = (int)(idx % K);
     float v = 0.f;
     if (row < L.nseg * L.r) v = L.A[row / L.r][(size_t)(row % L.r) * K + k];
-    acat[idx] = f_to_bf16(v);
+    acat[idx] = st16<F16>(v);
   }
 }
 
@@ -467,84 +489,152 @@ int grid_for(int64_t n, int threads) {
 }  // namespace
 
 void k_embed(const int32_t *tok, const uint16_t *E, int V, int H, int M, float *out, cudaStream_t st) {
-  if (M > 0) embed_kernel<<<M, 128, 0, st>>>(tok, E, V, H, out);
+  if (M > 0) {
+    embed_kernel<<<M, 128, 0, st>>>(tok, E, V, H, out);
+    count_launches(1);
+  }
 }
 void k_rmsnorm_fwd(const float *h, const uint16_t *w, float eps, int M, int H, uint16_t *out,
-                   cudaStream_t st) {
-  if (M > 0) rmsnorm_fwd_kernel<<<cdiv(M, 8), 256, 0, st>>>(h, w, eps, M, H, out);
+                   bool out_f16, cudaStream_t st) {
+  if (M <= 0) return;
+  if (out_f16) rmsnorm_fwd_kernel<true><<<cdiv(M, 8), 256, 0, st>>>(h, w, eps, M, H, out);
+  else rmsnorm_fwd_kernel<false><<<cdiv(M, 8), 256, 0, st>>>(h, w, eps, M, H, out);
+  count_launches(1);
 }
 void k_rmsnorm_bwd(const float *dy, const float *h, const uint16_t *w, float eps, int M, int H,
                    const float *dres, float *out, uint16_t *out_bf16, cudaStream_t st) {
-  if (M > 0) rmsnorm_bwd_kernel<<<cdiv(M, 8), 256, 0, st>>>(dy, h, w, eps, M, H, dres, out, out_bf16);
+  if (M <= 0) return;
+  rmsnorm_bwd_kernel<<<cdiv(M, 8), 256, 0, st>>>(dy, h, w, eps, M, H, dres, out, out_bf16);
+  count_launches(1);
 }
 void k_rope_fwd(uint16_t *qkv, int ld, const float *cos, const float *sin, int M, int S, int nh,
-                int nkv, int d, cudaStream_t st) {
+                int nkv, int d, bool f16, cudaStream_t st) {
   const int64_t n = (int64_t)M * (nh + nkv) * (d / 2);
-  if (n > 0) rope_fwd_kernel<<<grid_for(n, 256), 256, 0, st>>>(qkv, ld, cos, sin, M, S, nh + nkv, d);
+  if (n <= 0) return;
+  if (f16) rope_fwd_kernel<true><<<grid_for(n, 256), 256, 0, st>>>(qkv, ld, cos, sin, M, S, nh + nkv, d);
+  else rope_fwd_kernel<false><<<grid_for(n, 256), 256, 0, st>>>(qkv, ld, cos, sin, M, S, nh + nkv, d);
+  count_launches(1);
 }
 void k_rope_bwd(const float *dqkv, uint16_t *out, int ld, const float *cos, const float *sin,
                 int M, int S, int nh, int nkv, int d, cudaStream_t st) {
   const int64_t n = (int64_t)M * (nh + 2 * nkv) * (d / 2);
-  if (n > 0)
-    rope_bwd_kernel<<<grid_for(n, 256), 256, 0, st>>>(dqkv, out, ld, cos, sin, M, S, nh + nkv,
-                                                      nh + 2 * nkv, d);
+  if (n <= 0) return;
+  rope_bwd_kernel<<<grid_for(n, 256), 256, 0, st>>>(dqkv, out, ld, cos, sin, M, S, nh + nkv,
+                                                    nh + 2 * nkv, d);
+  count_launches(1);
 }
-void k_swiglu_fwd(const uint16_t *gu, int M, int I, uint16_t *act, cudaStream_t st) {
+void k_swiglu_fwd(const uint16_t *gu, int M, int I, uint16_t *act, bool f16, cudaStream_t st) {
   const int64_t n = (int64_t)M * I;
-  if (n > 0) swiglu_fwd_kernel<<<grid_for(n, 256), 256, 0, st>>>(gu, M, I, act);
+  if (n <= 0) return;
+  if (f16) swiglu_fwd_kernel<true><<<grid_for(n, 256), 256, 0, st>>>(gu, M, I, act);
+  else swiglu_fwd_kernel<false><<<grid_for(n, 256), 256, 0, st>>>(gu, M, I, act);
+  count_launches(1);
 }
-void k_swiglu_bwd(const float *dact, const uint16_t *gu, int M, int I, uint16_t *dgu, cudaStream_t st) {
+void k_swiglu_bwd(const float *dact, const uint16_t *gu, int M, int I, uint16_t *dgu, bool gu_f16,
+                  cudaStream_t st) {
   const int64_t n = (int64_t)M * I;
-  if (n > 0) swiglu_bwd_kernel<<<grid_for(n, 256), 256, 0, st>>>(dact, gu, M, I, dgu);
+  if (n <= 0) return;
+  if (gu_f16) swiglu_bwd_kernel<true><<<grid_for(n, 256), 256, 0, st>>>(dact, gu, M, I, dgu);
+  else swiglu_bwd_kernel<false><<<grid_for(n, 256), 256, 0, st>>>(dact, gu, M, I, dgu);
+  count_launches(1);
+}
+
+int lora_splits(int M, int K, int *KS) {
+  const int rb = cdiv(M, 32);
+  int want = std::max(1, cdiv(296, rb));
+  want = std::min(want, cdiv(K, 64));
+  int ks = cdiv(cdiv(K, want), 64) * 64;
+  if (KS) *KS = ks;
+  return cdiv(K, ks);
+}
+size_t lora_partial_floats(int M, int K) { return (size_t)lora_splits(M, K, nullptr) * M * 64; }
+
+template <bool DU>
+static void lora_proj(const uint16_t *X, int ldx, int M, int K, const LoraSeg &L, float *out_f32,
+                      uint16_t *out16, bool x_f16, bool o_f16, float *part, cudaStream_t st) {
+  if (M <= 0) return;
+  int KS;
+  const int ns = lora_splits(M, K, &KS);
+  dim3 grid(cdiv(M, 32), ns);
+  if (x_f16) lora_part_kernel<DU, true><<<grid, 256, 0, st>>>(X, ldx, M, K, KS, L, part);
+  else lora_part_kernel<DU, false><<<grid, 256, 0, st>>>(X, ldx, M, K, KS, L, part);
+  const int64_t n = (int64_t)M * L.Rpad();
+  if (o_f16) lora_reduce_kernel<DU, true><<<grid_for(n, 256), 256, 0, st>>>(part, ns, M, L, out_f32, out16);
+  else lora_reduce_kernel<DU, false><<<grid_for(n, 256), 256, 0, st>>>(part, ns, M, L, out_f32, out16);
+  count_launches(2);
 }
 void k_lora_down(const uint16_t *x, int lda, int M, int K, const LoraSeg &L, float *u_f32,
-                 uint16_t *ul, cudaStream_t st) {
-  if (M > 0) lora_proj_kernel<false><<<cdiv(M, 32), 256, 0, st>>>(x, lda, M, K, L, u_f32, ul);
+                 uint16_t *ul, bool x_f16, bool ul_f16, float *part, cudaStream_t st) {
+  lora_proj<false>(x, lda, M, K, L, u_f32, ul, x_f16, ul_f16, part, st);
 }
 void k_lora_du(const uint16_t *dy, int ldy, int M, const LoraSeg &L, float *du_f32, uint16_t *dul,
+               bool dy_f16, bool dul_f16, float *part, cudaStream_t st) {
+  int Ng = 0;
+  for (int p = 0; p < L.nseg; ++p) Ng = L.off[p] + L.n[p] > Ng ? L.off[p] + L.n[p] : Ng;
+  lora_proj<true>(dy, ldy, M, Ng, L, du_f32, dul, dy_f16, dul_f16, part, st);
+}
+void k_lora_dB(const uint16_t *dy, int ldy, int M, const float *u_f32, const LoraSeg &L, bool dy_f16,
                cudaStream_t st) {
   int Ng = 0;
   for (int p = 0; p < L.nseg; ++p) Ng = L.off[p] + L.n[p] > Ng ? L.off[p] + L.n[p] : Ng;
-  if (M > 0) lora_proj_kernel<true><<<cdiv(M, 32), 256, 0, st>>>(dy, ldy, M, Ng, L, du_f32, dul);
-}
-void k_lora_dB(const uint16_t *dy, int ldy, int M, const float *u_f32, const LoraSeg &L, cudaStream_t st) {
-  int Ng = 0;
-  for (int p = 0; p < L.nseg; ++p) Ng = L.off[p] + L.n[p] > Ng ? L.off[p] + L.n[p] : Ng;
-  lora_dB_kernel<<<cdiv(Ng, 64), 256, 0, st>>>(dy, ldy, M, Ng, u_f32, L);
+  if (dy_f16) lora_dB_kernel<true><<<cdiv(Ng, 64), 256, 0, st>>>(dy, ldy, M, Ng, u_f32, L);
+  else lora_dB_kernel<false><<<cdiv(Ng, 64), 256, 0, st>>>(dy, ldy, M, Ng, u_f32, L);
+  count_launches(1);
 }
 void k_lora_dA(const float *du_f32, const uint16_t *x, int lda, int M, int K, const LoraSeg &L,
-               cudaStream_t st) {
-  lora_dA_kernel<<<cdiv(K, 64), 256, 0, st>>>(du_f32, x, lda, M, K, L);
+               bool x_f16, cudaStream_t st) {
+  if (x_f16) lora_dA_kernel<true><<<cdiv(K, 64), 256, 0, st>>>(du_f32, x, lda, M, K, L);
+  else lora_dA_kernel<false><<<cdiv(K, 64), 256, 0, st>>>(du_f32, x, lda, M, K, L);
+  count_launches(1);
 }
-void k_pack_fwd(const LoraSeg &L, int Ng, uint16_t *vl, cudaStream_t st) {
+void k_pack_fwd(const LoraSeg &L, int Ng, uint16_t *vl, bool f16, cudaStream_t st) {
   const int64_t n = (int64_t)Ng * L.Rpad();
-  pack_fwd_kernel<<<grid_for(n, 256), 256, 0, st>>>(L, Ng, vl);
+  if (f16) pack_fwd_kernel<true><<<grid_for(n, 256), 256, 0, st>>>(L, Ng, vl);
+  else pack_fwd_kernel<false><<<grid_for(n, 256), 256, 0, st>>>(L, Ng, vl);
+  count_launches(1);
 }
-void k_pack_bwd(const LoraSeg &L, int K, uint16_t *acat, cudaStream_t st) {
+void k_pack_bwd(const LoraSeg &L, int K, uint16_t *acat, bool f16, cudaStream_t st) {
   const int64_t n = (int64_t)L.Rpad() * K;
-  pack_bwd_kernel<<<grid_for(n, 256), 256, 0, st>>>(L, K, acat);
+  if (f16) pack_bwd_kernel<true><<<grid_for(n, 256), 256, 0, st>>>(L, K, acat);
+  else pack_bwd_kernel<false><<<grid_for(n, 256), 256, 0, st>>>(L, K, acat);
+  count_launches(1);
 }
 void k_ce_chunk_fwd(const float *z, int ldz, int v0, int vc, const int32_t *tok, int M, int S,
                     int first, float *rmax, float *rsum, float *zlab, cudaStream_t st) {
-  ce_chunk_fwd_kernel<<<M, 256, 0, st>>>(z, ldz, v0, vc, tok, M, S, first, rmax, rsum, zlab);
+  {
+    ce_chunk_fwd_kernel<<<M, 256, 0, st>>>(z, ldz, v0, vc, tok, M, S, first, rmax, rsum, zlab);
+    count_launches(1);
+  }
 }
 void k_ce_finalize(const float *rmax, const float *rsum, const float *zlab, int M, int S,
                    float *lse, float *loss, cudaStream_t st) {
-  ce_finalize_kernel<<<1, 1024, 0, st>>>(rmax, rsum, zlab, M, S, lse, loss);
+  {
+    ce_finalize_kernel<<<1, 1024, 0, st>>>(rmax, rsum, zlab, M, S, lse, loss);
+    count_launches(1);
+  }
 }
 void k_ce_chunk_bwd(const float *z, int ldz, int v0, int vc, const float *lse, const int32_t *tok,
                     int M, int S, float inv_n, uint16_t *dz, cudaStream_t st) {
   const int64_t n = (int64_t)M * vc;
-  ce_chunk_bwd_kernel<<<grid_for(n, 256), 256, 0, st>>>(z, ldz, v0, vc, lse, tok, M, S, inv_n, dz);
+  {
+    ce_chunk_bwd_kernel<<<grid_for(n, 256), 256, 0, st>>>(z, ldz, v0, vc, lse, tok, M, S, inv_n, dz);
+    count_launches(1);
+  }
 }
 void k_cast_bf16(const float *in, uint16_t *out, int64_t n, cudaStream_t st) {
-  if (n > 0) cast_bf16_kernel<<<grid_for(n, 256), 256, 0, st>>>(in, out, n);
+  if (n > 0) {
+    cast_bf16_kernel<<<grid_for(n, 256), 256, 0, st>>>(in, out, n);
+    count_launches(1);
+  }
 }
 void k_nf4_dequant(const uint8_t *codes, const float *absmax, int64_t n, float *out_f32,
                    uint16_t *out_bf16, cudaStream_t st) {
   if (n > 0)
+    {
     nf4_dequant_kernel<<<grid_for(n, 256), 256, 0, st>>>(codes, absmax, n, out_f32, out_bf16,
                                                          nf4_codebook_param());
+    count_launches(1);
+  }
 }
 
 }  // namespace soup

@@ -30,34 +30,43 @@ struct LoraSeg {
 };
 
 void k_embed(const int32_t *tok, const uint16_t *E, int V, int H, int M, float *out, cudaStream_t st);
+// Tensors in 16-bit are either IEEE half (the forward's tensor-core operands: normalised
+// inputs, qkv, attention output, gate/up, SwiGLU output, the forward LoRA packs) or bf16
+// (gradients, the loss head); each launcher takes a flag saying which.
 void k_rmsnorm_fwd(const float *h, const uint16_t *w, float eps, int M, int H, uint16_t *out,
-                   cudaStream_t st);
+                   bool out_f16, cudaStream_t st);
 // out = dres + rmsnorm_backward(dy); dres may be null (treated as 0) or alias out.
 void k_rmsnorm_bwd(const float *dy, const float *h, const uint16_t *w, float eps, int M, int H,
                    const float *dres, float *out, uint16_t *out_bf16, cudaStream_t st);
 void k_rope_fwd(uint16_t *qkv, int ld, const float *cos, const float *sin, int M, int S, int nh,
-                int nkv, int d, cudaStream_t st);
+                int nkv, int d, bool f16, cudaStream_t st);
 // in: dqkv float [M, ld]; out bf16 [M, ld]: q/k heads rotated back, v heads cast.
 void k_rope_bwd(const float *dqkv, uint16_t *out, int ld, const float *cos, const float *sin,
                 int M, int S, int nh, int nkv, int d, cudaStream_t st);
-void k_swiglu_fwd(const uint16_t *gu, int M, int I, uint16_t *act, cudaStream_t st);
-void k_swiglu_bwd(const float *dact, const uint16_t *gu, int M, int I, uint16_t *dgu, cudaStream_t st);
+void k_swiglu_fwd(const uint16_t *gu, int M, int I, uint16_t *act, bool f16, cudaStream_t st);
+void k_swiglu_bwd(const float *dact, const uint16_t *gu, int M, int I, uint16_t *dgu, bool gu_f16,
+                  cudaStream_t st);
 
-// u = x A^T per segment -> u_f32 [M, nseg*r]; ul = bf16(s * u) [M, Rpad] (zero padded)
+// Split of the reduction of a LoRA projection (deterministic split-K) and the float scratch
+// it needs: lora_partial_floats(M, K) floats.
+int lora_splits(int M, int K, int *KS);
+size_t lora_partial_floats(int M, int K);
+// u = x A^T per segment -> u_f32 [M, nseg*r]; ul = 16-bit(s * u) [M, Rpad] (zero padded)
 void k_lora_down(const uint16_t *x, int lda, int M, int K, const LoraSeg &L, float *u_f32,
-                 uint16_t *ul, cudaStream_t st);
-// du_p = s dY_p B_p -> du_f32 [M, nseg*r]; dul = bf16(du) [M, Rpad]
+                 uint16_t *ul, bool x_f16, bool ul_f16, float *part, cudaStream_t st);
+// du_p = s dY_p B_p -> du_f32 [M, nseg*r]; dul = 16-bit(du) [M, Rpad]
 void k_lora_du(const uint16_t *dy, int ldy, int M, const LoraSeg &L, float *du_f32, uint16_t *dul,
-               cudaStream_t st);
+               bool dy_f16, bool dul_f16, float *part, cudaStream_t st);
 // dB_p = s dY_p^T u_p   (written into L.dB)
-void k_lora_dB(const uint16_t *dy, int ldy, int M, const float *u_f32, const LoraSeg &L, cudaStream_t st);
+void k_lora_dB(const uint16_t *dy, int ldy, int M, const float *u_f32, const LoraSeg &L, bool dy_f16,
+               cudaStream_t st);
 // dA_p = du_p^T x       (written into L.dA)
 void k_lora_dA(const float *du_f32, const uint16_t *x, int lda, int M, int K, const LoraSeg &L,
-               cudaStream_t st);
-// Vl [Ng, Rpad]: row n of segment p holds bf16(B_p[n - off_p, :]) at columns p*r .. p*r+r-1
-void k_pack_fwd(const LoraSeg &L, int Ng, uint16_t *vl, cudaStream_t st);
-// Acat [Rpad, K]: row p*r + j holds bf16(A_p[j, :]); rows past nseg*r are zero
-void k_pack_bwd(const LoraSeg &L, int K, uint16_t *acat, cudaStream_t st);
+               bool x_f16, cudaStream_t st);
+// Vl [Ng, Rpad]: row n of segment p holds 16-bit(B_p[n - off_p, :]) at columns p*r .. p*r+r-1
+void k_pack_fwd(const LoraSeg &L, int Ng, uint16_t *vl, bool f16, cudaStream_t st);
+// Acat [Rpad, K]: row p*r + j holds 16-bit(A_p[j, :]); rows past nseg*r are zero
+void k_pack_bwd(const LoraSeg &L, int K, uint16_t *acat, bool f16, cudaStream_t st);
 
 // Vocabulary-chunked cross-entropy.  Rows are tokens b*S + t; row t has label tok[b*S+t+1]
 // for t < S-1 and none for t = S-1.
@@ -72,12 +81,13 @@ void k_cast_bf16(const float *in, uint16_t *out, int64_t n, cudaStream_t st);
 void k_nf4_dequant(const uint8_t *codes, const float *absmax, int64_t n, float *out_f32,
                    uint16_t *out_bf16, cudaStream_t st);
 
-// Causal GQA attention on the fused qkv buffer [M, ld] (q heads, then k heads, then v heads,
-// each head_dim wide), rows b*S + t.  o: bf16 [M, nh*d]; lse: float [B*nh*S] (base-2 log-sum
-// of exp2(scale*log2e*score)).  head_dim 64 or 128.
+// Causal GQA attention on the fused half-precision qkv buffer [M, ld] (q heads, then k heads,
+// then v heads, each head_dim wide), rows b*S + t.  o: half [M, nh*d]; lse: float [B*nh*S]
+// (base-2 log-sum of exp2(scale*log2e*score)).  head_dim 64 or 128.
 int k_attn_fwd(const uint16_t *qkv, int ld, int B, int S, int nh, int nkv, int d, uint16_t *o,
                float *lse, cudaStream_t st);
-// dO: bf16 [M, nh*d]; dqkv: float [M, ld] written completely (dq, dk, dv);
+// o: half [M, nh*d] (the forward output); dO: bf16 [M, nh*d]; dqkv: float [M, ld] written
+// completely (dq, dk, dv);
 // scratch: float [attn_bwd_scratch_floats()].
 size_t attn_bwd_scratch_floats(int B, int S, int nh, int d);
 int k_attn_bwd(const uint16_t *qkv, int ld, const uint16_t *o, const uint16_t *dO,

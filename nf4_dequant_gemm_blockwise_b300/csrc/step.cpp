@@ -80,6 +80,12 @@ int make_plan(const soup_cfg *c, int maxB, int maxS, int n_slots, int resident, 
   P->attn_scratch = take(4 * attn_bwd_scratch_floats(maxB, maxS, c->n_heads, c->head_dim));
   P->du_f32 = take(4 * M * 64);
   P->du_b = take(2 * M * 64);
+  {
+    const int Ks[6] = {(int)H, (int)qd, (int)I, (int)nqkv, (int)(2 * I), (int)H};
+    size_t mx = 0;
+    for (int k : Ks) mx = std::max(mx, lora_partial_floats((int)M, k));
+    P->lora_part = take(4 * mx);
+  }
   P->hn = take(2 * M * H);
   P->vc = ce_chunk_cols((int)M, c->vocab);
   P->z = take(4 * M * (uint64_t)P->vc);
@@ -306,41 +312,43 @@ int layer_forward(soup_stream *h, int li, const uint8_t *shard, bool recompute) 
   LoraSeg Lq = make_seg(h, li, SOUP_G_QKV, false), Lo = make_seg(h, li, SOUP_G_O, false),
           Lg = make_seg(h, li, SOUP_G_GU, false), Ld = make_seg(h, li, SOUP_G_DOWN, false);
 
-  k_rmsnorm_fwd(hin, ln1, c.rms_eps, M, H, B16(h, P.x1), st);
-  k_lora_down(B16(h, P.x1), H, M, H, Lq, F(h, P.u_f32[0]), B16(h, P.u_b[0]), st);
+  float *part = F(h, P.lora_part);
+  // the forward's tensor-core operands are IEEE half (x1, qkv, att, x2, gu, act, LoRA packs)
+  k_rmsnorm_fwd(hin, ln1, c.rms_eps, M, H, B16(h, P.x1), true, st);
+  k_lora_down(B16(h, P.x1), H, M, H, Lq, F(h, P.u_f32[0]), B16(h, P.u_b[0]), true, true, part, st);
   {
     GemmArgs g = weight_args(h, shard, SOUP_G_QKV, GEMM_FWD);
-    g.M = M; g.a = B16(h, P.x1); g.lda = H;
+    g.op_f16 = 1; g.M = M; g.a = B16(h, P.x1); g.lda = H;
     g.ul = B16(h, P.u_b[0]); g.vl = B16(h, P.vl[(size_t)li * 4 + 0]); g.R = Lq.Rpad();
-    g.epi = EPI_BF16; g.out = B16(h, P.qkv); g.ldo = nqkv;
+    g.epi = EPI_16; g.out = B16(h, P.qkv); g.ldo = nqkv;
     SOUP_TRY(timed_gemm(h, g));
   }
   k_rope_fwd(B16(h, P.qkv), nqkv, F(h, P.rope_cos), F(h, P.rope_sin), M, S, c.n_heads,
-             c.n_kv_heads, c.head_dim, st);
+             c.n_kv_heads, c.head_dim, true, st);
   SOUP_TRY(k_attn_fwd(B16(h, P.qkv), nqkv, B, S, c.n_heads, c.n_kv_heads, c.head_dim,
                       B16(h, P.att), F(h, P.lse), st));
-  k_lora_down(B16(h, P.att), qd, M, qd, Lo, F(h, P.u_f32[1]), B16(h, P.u_b[1]), st);
+  k_lora_down(B16(h, P.att), qd, M, qd, Lo, F(h, P.u_f32[1]), B16(h, P.u_b[1]), true, true, part, st);
   {
     GemmArgs g = weight_args(h, shard, SOUP_G_O, GEMM_FWD);
-    g.M = M; g.a = B16(h, P.att); g.lda = qd;
+    g.op_f16 = 1; g.M = M; g.a = B16(h, P.att); g.lda = qd;
     g.ul = B16(h, P.u_b[1]); g.vl = B16(h, P.vl[(size_t)li * 4 + 1]); g.R = Lo.Rpad();
     g.epi = EPI_F32_ADD; g.add_src = hin; g.ld_add = H; g.out = F(h, P.hm); g.ldo = H;
     SOUP_TRY(timed_gemm(h, g));
   }
-  k_rmsnorm_fwd(F(h, P.hm), ln2, c.rms_eps, M, H, B16(h, P.x2), st);
-  k_lora_down(B16(h, P.x2), H, M, H, Lg, F(h, P.u_f32[2]), B16(h, P.u_b[2]), st);
+  k_rmsnorm_fwd(F(h, P.hm), ln2, c.rms_eps, M, H, B16(h, P.x2), true, st);
+  k_lora_down(B16(h, P.x2), H, M, H, Lg, F(h, P.u_f32[2]), B16(h, P.u_b[2]), true, true, part, st);
   {
     GemmArgs g = weight_args(h, shard, SOUP_G_GU, GEMM_FWD);
-    g.M = M; g.a = B16(h, P.x2); g.lda = H;
+    g.op_f16 = 1; g.M = M; g.a = B16(h, P.x2); g.lda = H;
     g.ul = B16(h, P.u_b[2]); g.vl = B16(h, P.vl[(size_t)li * 4 + 2]); g.R = Lg.Rpad();
-    g.epi = EPI_BF16; g.out = B16(h, P.gu); g.ldo = 2 * I;
+    g.epi = EPI_16; g.out = B16(h, P.gu); g.ldo = 2 * I;
     SOUP_TRY(timed_gemm(h, g));
   }
-  k_swiglu_fwd(B16(h, P.gu), M, I, B16(h, P.act), st);
-  k_lora_down(B16(h, P.act), I, M, I, Ld, F(h, P.u_f32[3]), B16(h, P.u_b[3]), st);
+  k_swiglu_fwd(B16(h, P.gu), M, I, B16(h, P.act), true, st);
+  k_lora_down(B16(h, P.act), I, M, I, Ld, F(h, P.u_f32[3]), B16(h, P.u_b[3]), true, true, part, st);
   if (!recompute) {
     GemmArgs g = weight_args(h, shard, SOUP_G_DOWN, GEMM_FWD);
-    g.M = M; g.a = B16(h, P.act); g.lda = I;
+    g.op_f16 = 1; g.M = M; g.a = B16(h, P.act); g.lda = I;
     g.ul = B16(h, P.u_b[3]); g.vl = B16(h, P.vl[(size_t)li * 4 + 3]); g.R = Ld.Rpad();
     g.epi = EPI_F32_ADD; g.add_src = F(h, P.hm); g.ld_add = H;
     g.out = F(h, P.h_all) + (size_t)(li + 1) * M * H; g.ldo = H;
@@ -357,9 +365,10 @@ int group_backward(soup_stream *h, int li, const uint8_t *shard, int grp, const 
   const int M = h->B * h->S;
   LoraSeg L = make_seg(h, li, grp, true);
   const int K = h->lay.n_in[grp];
-  k_lora_du(dy, ldy, M, L, F(h, P.du_f32), B16(h, P.du_b), st);
-  k_lora_dB(dy, ldy, M, F(h, P.u_f32[grp]), L, st);
-  k_lora_dA(F(h, P.du_f32), x, ldx, M, K, L, st);
+  // gradients travel in bf16; the layer inputs x are the forward's half tensors
+  k_lora_du(dy, ldy, M, L, F(h, P.du_f32), B16(h, P.du_b), false, false, F(h, P.lora_part), st);
+  k_lora_dB(dy, ldy, M, F(h, P.u_f32[grp]), L, false, st);
+  k_lora_dA(F(h, P.du_f32), x, ldx, M, K, L, true, st);
   GemmArgs g = weight_args(h, shard, grp, GEMM_DX);
   g.M = M; g.a = dy; g.lda = ldy;
   g.ul = B16(h, P.du_b); g.vl = B16(h, P.ac[(size_t)li * 4 + grp]); g.R = L.Rpad();
@@ -380,7 +389,7 @@ int layer_backward(soup_stream *h, int li, const uint8_t *shard) {
 
   // dh / dh_b hold dL/dh_{li+1}
   SOUP_TRY(group_backward(h, li, shard, SOUP_G_DOWN, B16(h, P.dh_b), H, B16(h, P.act), I, F(h, P.dact)));
-  k_swiglu_bwd(F(h, P.dact), B16(h, P.gu), M, I, B16(h, P.dgu), st);
+  k_swiglu_bwd(F(h, P.dact), B16(h, P.gu), M, I, B16(h, P.dgu), true, st);
   SOUP_TRY(group_backward(h, li, shard, SOUP_G_GU, B16(h, P.dgu), 2 * I, B16(h, P.x2), H, F(h, P.dx)));
   k_rmsnorm_bwd(F(h, P.dx), F(h, P.hm), ln2, c.rms_eps, M, H, F(h, P.dh), F(h, P.dhm), B16(h, P.dhm_b), st);
   SOUP_TRY(group_backward(h, li, shard, SOUP_G_O, B16(h, P.dhm_b), H, B16(h, P.att), qd, F(h, P.datt)));
@@ -504,8 +513,8 @@ int step_fwd(soup_stream *h, const int32_t *tokens, int B, int S, const float *c
   for (int l = 0; l < L; ++l)
     for (int g = 0; g < 4; ++g) {
       LoraSeg Lg = make_seg(h, l, g, false);
-      k_pack_fwd(Lg, h->lay.n_out[g], B16(h, P.vl[(size_t)l * 4 + g]), st);
-      k_pack_bwd(Lg, h->lay.n_in[g], B16(h, P.ac[(size_t)l * 4 + g]), st);
+      k_pack_fwd(Lg, h->lay.n_out[g], B16(h, P.vl[(size_t)l * 4 + g]), true, st);
+      k_pack_bwd(Lg, h->lay.n_in[g], B16(h, P.ac[(size_t)l * 4 + g]), false, st);
     }
   k_embed(tokens, h->embed, c.vocab, H, M, F(h, P.h_all), st);
   std::vector<int> seq(L);
@@ -520,7 +529,7 @@ int step_fwd(soup_stream *h, const int32_t *tokens, int B, int S, const float *c
     if (!h->resident) SOUP_TRY(prefetch(h, seq, (size_t)i + 1, look - 1));
   }
   // final norm + vocabulary-chunked loss
-  k_rmsnorm_fwd(F(h, P.h_all) + (size_t)L * M * H, h->final_norm, c.rms_eps, M, H, B16(h, P.hn), st);
+  k_rmsnorm_fwd(F(h, P.h_all) + (size_t)L * M * H, h->final_norm, c.rms_eps, M, H, B16(h, P.hn), false, st);
   const int vc = P.vc;
   for (int v0 = 0, ci = 0; v0 < c.vocab; v0 += vc, ++ci) {
     const int n = std::min(vc, c.vocab - v0);

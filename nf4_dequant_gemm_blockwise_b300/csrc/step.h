@@ -16,7 +16,7 @@ struct Plan {
   uint64_t slots = 0, h_all = 0, hm = 0, x1 = 0, x2 = 0, qkv = 0, att = 0, lse = 0, gu = 0, act = 0;
   uint64_t u_f32[4] = {0, 0, 0, 0}, u_b[4] = {0, 0, 0, 0};
   uint64_t dh = 0, dhm = 0, dh_b = 0, dhm_b = 0, dact = 0, dgu = 0, dx = 0, datt = 0, datt_b = 0;
-  uint64_t dqkv = 0, dqkv_b = 0, attn_scratch = 0, du_f32 = 0, du_b = 0;
+  uint64_t dqkv = 0, dqkv_b = 0, attn_scratch = 0, du_f32 = 0, du_b = 0, lora_part = 0;
   uint64_t hn = 0, z = 0, dz = 0, dhn = 0, ce_max = 0, ce_sum = 0, ce_lab = 0, ce_lse = 0;
   std::vector<uint64_t> vl, ac;  // per (layer, group) LoRA operand packs
   uint64_t rope_cos = 0, rope_sin = 0, err = 0;

@@ -1,6 +1,7 @@
 // Host-side error reporting shared by the library's translation units.
 #pragma once
 #include <cuda_runtime.h>
+#include <stdint.h>
 
 #include "soup.h"
 
@@ -8,6 +9,9 @@ namespace soup {
 // Record a formatted message as this thread's last error and return `code`.
 int set_error(int code, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
 void clear_error();
+// Process-wide count of kernels this library has launched (for launch accounting).
+void count_launches(int n);
+uint64_t launches_so_far();
 }  // namespace soup
 
 #define SOUP_CUDA_TRY(call)                                                              \

@@ -1,10 +1,12 @@
 """GPU parity of the single-projection kernels against the oracle (all calls go through the
-C ABI).  Operands are the oracle's: NF4 codes and absmax from oracle.nf4, dequantised values
-from oracle.nf4.dequantize.  Two references are used:
+C ABI).  The forward runs on IEEE-half operands (as in the step) or bf16 ones; dX on bf16.
+Operands are the oracle's: NF4 codes and absmax from oracle.nf4, dequantised values from
+oracle.nf4.dequantize.  Two references are used:
 
-* the exact-operand reference: the same bf16 operands the kernel is defined on (bf16 x,
-  bf16-rounded dequantised W) multiplied in float64 — the tensor-core result must match it
-  to float32-accumulation accuracy plus the final output rounding;
+* the exact-operand reference: the same 16-bit operands the kernel is defined on (x and the
+  dequantised W rounded to the GEMM's 16-bit format) multiplied in float64 — the
+  tensor-core result must match it to float32-accumulation accuracy plus the final output
+  rounding;
 * the oracle's float32 layer maths (unrounded W) — relative L2 <= 1e-2, the step's bar.
 """
 import numpy as np
@@ -38,6 +40,11 @@ def _weights(N, K, seed=0):
     return w_bits, packed, absmax, wdq
 
 
+def _h16(x):
+    """float32 -> IEEE half values (round to nearest even), returned as float32."""
+    return np.asarray(x, np.float32).astype(np.float16).astype(np.float32)
+
+
 def _rel_l2(a, b):
     a = np.asarray(a, np.float64)
     b = np.asarray(b, np.float64)
@@ -68,25 +75,35 @@ def _lora(N, K, r=16):
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
-def test_proj_fwd(api, M, N, K):
+@pytest.mark.parametrize("f16", [True, False])
+def test_proj_fwd(api, M, N, K, f16):
     r, s = 16, 2.0
     w_bits, packed, absmax, wdq = _weights(N, K)
-    x_bits = synth.activations_bf16(M, K, key=1)
+    x32 = nf4.bf16_to_f32(synth.activations_bf16(M, K, key=1))
+    if f16:
+        x_in = x32.astype(np.float16).view(np.uint16)
+        rnd = _h16
+    else:
+        x_in = synth.to_bf16_bits(x32)
+        rnd = nf4.bf16_round
     A, B = _lora(N, K, r)
     y = torch.empty((M, N), dtype=torch.int16, device="cuda")
     scratch = torch.empty(api.proj_scratch_bytes(M, N, K, r), dtype=torch.uint8, device="cuda")
-    api.proj_fwd(_dev(x_bits), M, N, K, _dev(packed), _dev(absmax), None, _dev(A), _dev(B), r, s, y, scratch)
+    api.proj_fwd(_dev(x_in), M, N, K, _dev(packed), _dev(absmax), None, _dev(A), _dev(B), r, s, y,
+                 scratch, x_f16=f16)
     torch.cuda.synchronize()
-    got = synth.bf16_bits_to_f32(y.cpu().numpy().view(np.uint16))
-    xf = nf4.bf16_to_f32(x_bits).astype(np.float64)
-    wb = nf4.bf16_round(wdq).astype(np.float64)
+    yb = y.cpu().numpy().view(np.uint16)
+    got = yb.view(np.float16).astype(np.float32) if f16 else synth.bf16_bits_to_f32(yb)
+    xf = rnd(x32).astype(np.float64)
+    wb = rnd(wdq).astype(np.float64)
     lora = s * (xf @ A.T.astype(np.float64)) @ B.T.astype(np.float64)
     exact = xf @ wb.T + lora
-    tol = 2.0 ** -8 * np.abs(exact) + 2e-3 * np.sqrt(np.mean(exact ** 2))
+    ulp = 2.0 ** -10 if f16 else 2.0 ** -8
+    tol = ulp * np.abs(exact) + 2e-3 * np.sqrt(np.mean(exact ** 2))
     bad = np.abs(got - exact) > tol
     assert not bad.any(), (bad.sum(), np.abs(got - exact).max())
-    oracle = xf @ wdq.T.astype(np.float64) + lora        # unrounded W
-    assert _rel_l2(got, oracle) <= 1e-2
+    oracle = x32.astype(np.float64) @ wdq.T.astype(np.float64) + lora   # unrounded operands
+    assert _rel_l2(got, oracle) <= (2e-3 if f16 else 1e-2)
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
@@ -113,17 +130,20 @@ def test_proj_dx(api, M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [(64, 256, 256), (513, 1376, 256), (512, 4096, 14336)])
-def test_proj_lora_grad(api, M, N, K):
+@pytest.mark.parametrize("f16", [True, False])
+def test_proj_lora_grad(api, M, N, K, f16):
     r, s = 16, 2.0
-    x_bits = synth.activations_bf16(M, K, key=3)
+    x32 = nf4.bf16_to_f32(synth.activations_bf16(M, K, key=3))
+    x_in = x32.astype(np.float16).view(np.uint16) if f16 else synth.to_bf16_bits(x32)
     dy_bits = synth.activations_bf16(M, N, key=4)
     A, B = _lora(N, K, r)
     dA = torch.empty((r, K), dtype=torch.float32, device="cuda")
     dB = torch.empty((N, r), dtype=torch.float32, device="cuda")
     scratch = torch.empty(api.proj_scratch_bytes(M, N, K, r), dtype=torch.uint8, device="cuda")
-    api.proj_lora_grad(_dev(x_bits), _dev(dy_bits), M, N, K, _dev(A), _dev(B), r, s, dA, dB, scratch)
+    api.proj_lora_grad(_dev(x_in), _dev(dy_bits), M, N, K, _dev(A), _dev(B), r, s, dA, dB, scratch,
+                       x_f16=f16)
     torch.cuda.synchronize()
-    xf = nf4.bf16_to_f32(x_bits).astype(np.float64)
+    xf = (_h16(x32) if f16 else x32).astype(np.float64)
     dyf = nf4.bf16_to_f32(dy_bits).astype(np.float64)
     u = xf @ A.T.astype(np.float64)
     want_dB = s * dyf.T @ u
@@ -132,24 +152,29 @@ def test_proj_lora_grad(api, M, N, K):
     assert _rel_l2(dA.cpu().numpy(), want_dA) < 1e-5
 
 
-def test_bf16_weight_path(api):
-    """bf16 base weights (the un-quantised streamed base) through the same kernels."""
+@pytest.mark.parametrize("f16", [True, False])
+def test_bf16_weight_path(api, f16):
+    """bf16 base weights (the un-quantised streamed base) through the same kernels; with half
+    activations the weight tile is converted to half in shared memory."""
     M, N, K, r, s = 192, 512, 1024, 16, 2.0
     w_bits = synth.normal_bf16(0, "layer", (9000, 1), (N, K), 0.02)
-    x_bits = synth.activations_bf16(M, K, key=5)
+    x32 = nf4.bf16_to_f32(synth.activations_bf16(M, K, key=5))
+    x_in = x32.astype(np.float16).view(np.uint16) if f16 else synth.to_bf16_bits(x32)
     dy_bits = synth.activations_bf16(M, N, key=6)
     A, B = _lora(N, K, r)
     scratch = torch.empty(api.proj_scratch_bytes(M, N, K, r), dtype=torch.uint8, device="cuda")
     y = torch.empty((M, N), dtype=torch.int16, device="cuda")
     dx = torch.empty((M, K), dtype=torch.float32, device="cuda")
     wd = _dev(w_bits)
-    api.proj_fwd(_dev(x_bits), M, N, K, None, None, wd, _dev(A), _dev(B), r, s, y, scratch)
+    api.proj_fwd(_dev(x_in), M, N, K, None, None, wd, _dev(A), _dev(B), r, s, y, scratch, x_f16=f16)
     api.proj_dx(_dev(dy_bits), M, N, K, None, None, wd, _dev(A), _dev(B), r, s, dx, scratch)
     torch.cuda.synchronize()
     w = nf4.bf16_to_f32(w_bits).astype(np.float64)
-    xf = nf4.bf16_to_f32(x_bits).astype(np.float64)
+    xf = x32.astype(np.float64)
     dyf = nf4.bf16_to_f32(dy_bits).astype(np.float64)
     want_y = xf @ w.T + s * (xf @ A.T) @ B.T
     want_dx = dyf @ w + s * (dyf @ B) @ A
-    assert _rel_l2(synth.bf16_bits_to_f32(y.cpu().numpy().view(np.uint16)), want_y) < 5e-3
+    yb = y.cpu().numpy().view(np.uint16)
+    got_y = yb.view(np.float16).astype(np.float32) if f16 else synth.bf16_bits_to_f32(yb)
+    assert _rel_l2(got_y, want_y) < (2e-3 if f16 else 5e-3)
     assert _rel_l2(dx.cpu().numpy(), want_dx) < 5e-3
