@@ -43,6 +43,11 @@ def _args():
     p.add_argument("--slots", type=int, default=2)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-overlap", action="store_true", help="skip the resident comparison run")
+    p.add_argument("--micro", action="store_true",
+                   help="single-projection microbench instead of the step: one JSON line per (shape, M)")
+    p.add_argument("--micro-shape", default="14336x4096,4096x14336", help="NxK list")
+    p.add_argument("--micro-m", default="1,16,128,512,2048,8192")
+    p.add_argument("--micro-iters", type=int, default=10)
     return p.parse_args()
 
 
@@ -185,6 +190,78 @@ def run_reference(args, rank):
                                        f"oracle; step time = {cfg.n_layers} x layer + head"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------ microbench
+def run_micro(args):
+    """Single-projection NF4 dequant-GEMM + LoRA: forward (half operands), dX (bf16) and the
+    LoRA gradients, each launch timed alone with CUDA events after an L2 flush."""
+    import numpy as np
+    import torch
+
+    import synth
+    from nf4_dequant_gemm_blockwise_b300 import api
+
+    peaks = _peaks()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    r, s = synth.MICRO_R, 2.0
+    for shp in args.micro_shape.split(","):
+        N, K = (int(v) for v in shp.lower().split("x"))
+        codes, absmax = api.nf4_quantize_host(synth.micro_weight(N, K))
+        codes_d, absmax_d = torch.from_numpy(codes).cuda(), torch.from_numpy(absmax).cuda()
+        A, B = synth.micro_lora(N, K, r)
+        A_d, B_d = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+        for M in (int(v) for v in args.micro_m.split(",")):
+            x32 = synth.bf16_bits_to_f32(synth.activations_bf16(M, K, key=1))
+            x = torch.from_numpy(x32.astype(np.float16).view(np.int16)).cuda()
+            dy = torch.from_numpy(synth.activations_bf16(M, N, key=2).view(np.int16)).cuda()
+            y = torch.empty((M, N), dtype=torch.int16, device="cuda")
+            dx = torch.empty((M, K), dtype=torch.float32, device="cuda")
+            dA = torch.empty((r, K), dtype=torch.float32, device="cuda")
+            dB = torch.empty((N, r), dtype=torch.float32, device="cuda")
+            scratch = torch.empty(api.proj_scratch_bytes(M, N, K, r), dtype=torch.uint8, device="cuda")
+            st = torch.cuda.current_stream()
+            calls = {
+                "fwd": lambda: api.proj_fwd(x, M, N, K, codes_d, absmax_d, None, A_d, B_d, r, s, y, scratch, st),
+                "dx": lambda: api.proj_dx(dy, M, N, K, codes_d, absmax_d, None, A_d, B_d, r, s, dx, scratch, st),
+                "grad": lambda: api.proj_lora_grad(x, dy, M, N, K, A_d, B_d, r, s, dA, dB, scratch, st),
+                # the dequant GEMM kernel alone (no adapter: r = 0)
+                "fwd_gemm": lambda: api.proj_fwd(x, M, N, K, codes_d, absmax_d, None, None, None, 0, s, y, scratch, st),
+                "dx_gemm": lambda: api.proj_dx(dy, M, N, K, codes_d, absmax_d, None, None, None, 0, s, dx, scratch, st),
+            }
+            out = {"micro": True, "shape": [N, K], "M": M, "r": r}
+            wbytes = N * K * 0.5 + N * K / 64 * 4
+            for name, fn in calls.items():
+                for _ in range(2):
+                    fn()
+                ts = []
+                for _ in range(args.micro_iters):
+                    flush.fill_(1)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(st)
+                    fn()
+                    e1.record(st)
+                    e1.synchronize()
+                    ts.append(e0.elapsed_time(e1) * 1e-3)
+                t = statistics.median(ts)
+                rr = 0 if name.endswith("_gemm") else r
+                fwd_like = name.startswith("fwd")
+                if name == "grad":
+                    flops = 4.0 * M * r * (N + K)
+                    byts = 2.0 * M * (N + K) + 4.0 * r * (N + K) * 2
+                elif fwd_like:
+                    flops = 2.0 * M * N * K + 2.0 * M * rr * (N + K)
+                    byts = wbytes + 2.0 * M * K + 2.0 * M * N + 2.0 * rr * (N + K)
+                else:
+                    flops = 2.0 * M * N * K + 2.0 * M * rr * (N + K)
+                    byts = wbytes + 2.0 * M * N + 4.0 * M * K + 2.0 * rr * (N + K)
+                t_hbm = byts / (peaks["hbm"] * 1e9)
+                t_tc = flops / (peaks["bf16"] * 1e12)
+                bound = "hbm" if t_hbm >= t_tc else "tensor"
+                out[name] = {"us": t * 1e6, "tflops": flops / t / 1e12, "gbs": byts / t / 1e9,
+                             "bound": bound, "frac": max(t_hbm, t_tc) / t}
+            out["peak_source"] = f"{peaks['src']}: hbm {peaks['hbm']} GB/s, bf16 burst {peaks['bf16']} TFLOP/s"
+            print(json.dumps(out), flush=True)
 
 
 # ------------------------------------------------------------------------------ our arm
@@ -384,6 +461,9 @@ def main():
         dist = td
     if args.impl == "reference":
         run_reference(args, rank)
+    elif args.micro:
+        if rank == 0:
+            run_micro(args)
     else:
         run_ours(args, rank, world, local_rank, dist)
     if dist is not None:

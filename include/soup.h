@@ -210,7 +210,8 @@ void soup_stream_free(soup_stream *h);
 /* One projection of the step, for the microbench and the kernel tests.  W is a weight
  * [N, K] (out x in) given as NF4 (codes dev uint8 [N*K/2] + absmax dev float [N*K/64]) or
  * bf16 (w_bf16 dev uint16 [N, K]; codes/absmax NULL).  LoRA: A dev float [r, K],
- * B dev float [N, r], s = alpha / r, 1 <= r <= 64.  scratch: dev buffer of
+ * B dev float [N, r], s = alpha / r, 0 <= r <= 64 (r = 0: no adapter, A and B may be NULL;
+ * the plain dequant GEMM, used to time the kernel alone).  scratch: dev buffer of
  * soup_proj_scratch_bytes() bytes, 256-byte aligned, owned by the caller; its contents are
  * overwritten.  Shapes: any M >= 1; the tensor-core path needs K % 256 == 0 (both
  * directions) and N % 64 == 0 for dX; other shapes use a plain tiled kernel.

@@ -60,6 +60,7 @@ def _load() -> C.CDLL:
         "soup_last_error": (C.c_char_p, []),
         "soup_version": (C.c_char_p, []),
         "soup_kernel_launches": (C.c_uint64, []),
+
         "soup_nf4_codebook": (I32, [P]),
         "soup_shard_layout_of": (I32, [C.POINTER(soup_cfg), C.POINTER(soup_shard_layout)]),
         "soup_nf4_quantize_host": (I32, [P, C.c_int64, P, P, I32]),
@@ -113,6 +114,7 @@ def version() -> str:
 
 def kernel_launches() -> int:
     return int(lib.soup_kernel_launches())
+
 
 
 def _ptr(x) -> int | None:

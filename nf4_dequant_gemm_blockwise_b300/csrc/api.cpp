@@ -43,6 +43,7 @@ const char *soup_last_error(void) { return g_err.c_str(); }
 const char *soup_version(void) { return "soup-b300 0.1 (sm_103a)"; }
 uint64_t soup_kernel_launches(void) { return launches_so_far(); }
 
+
 int soup_nf4_codebook(float *out) {
   if (!out) return set_error(SOUP_EINVAL, "out is NULL");
   std::memcpy(out, nf4_codebook_param().v, 16 * sizeof(float));
@@ -147,7 +148,7 @@ void soup_stream_free(soup_stream *h) { soup_stream_free_impl(h); }
 // ------------------------------------------------------------------ single projection
 namespace {
 struct ProjScratch {
-  uint64_t u_f32, ul, vl, ac, du_f32, dul, part, err, total;
+  uint64_t u_f32, ul, vl, ac, du_f32, dul, part, gpart, gpart_floats, err, total;
 };
 ProjScratch proj_plan(int M, int N, int K) {
   ProjScratch s;
@@ -163,16 +164,20 @@ ProjScratch proj_plan(int M, int N, int K) {
   s.ac = take(2ull * 64 * K);
   s.du_f32 = take(4ull * M * 64);
   s.dul = take(2ull * M * 64);
-  s.part = take(4ull * std::max(lora_partial_floats(std::max(M, 1), K), lora_partial_floats(std::max(M, 1), N)));
+  s.part = take(4ull * std::max(lora_scratch_floats(std::max(M, 1), K, 64),
+                                 lora_scratch_floats(std::max(M, 1), N, 64)));
+  s.gpart_floats = std::min<uint64_t>(4ull * M * std::max(N, K), 1ull << 26);
+  s.gpart = take(4 * s.gpart_floats);
   s.err = take(64);
   s.total = off;
   return s;
 }
 int proj_check(int M, int N, int K, const uint8_t *codes, const float *absmax, const uint16_t *w,
                const float *A, const float *B, int r, void *scratch, uint64_t bytes) {
-  if (M < 0 || N < 1 || K < 1 || r < 1 || r > 64)
+  if (M < 0 || N < 1 || K < 1 || r < 0 || r > 64)
     return set_error(SOUP_EINVAL, "bad shape M=%d N=%d K=%d r=%d", M, N, K, r);
-  if (!A || !B || !scratch) return set_error(SOUP_EINVAL, "NULL LoRA or scratch pointer");
+  if (r > 0 && (!A || !B)) return set_error(SOUP_EINVAL, "NULL LoRA pointer with r > 0");
+  if (!scratch) return set_error(SOUP_EINVAL, "NULL scratch pointer");
   if (!(codes && absmax) && !w) return set_error(SOUP_EINVAL, "no weight given");
   if ((int64_t)N * K % 64 && codes) return set_error(SOUP_EINVAL, "N*K must be a multiple of 64");
   if (bytes < proj_plan(M, N, K).total) return set_error(SOUP_ENOMEM, "scratch too small");
@@ -210,7 +215,7 @@ GemmArgs proj_weight(int mode, int N, int K, const uint8_t *codes, const float *
 }  // namespace
 
 int soup_proj_scratch_bytes(int M, int N, int K, int r, uint64_t *bytes) {
-  if (!bytes || M < 0 || N < 1 || K < 1 || r < 1 || r > 64) return set_error(SOUP_EINVAL, "bad argument");
+  if (!bytes || M < 0 || N < 1 || K < 1 || r < 0 || r > 64) return set_error(SOUP_EINVAL, "bad argument");
   *bytes = proj_plan(M, N, K).total;
   return 0;
 }
@@ -226,16 +231,24 @@ int soup_proj_fwd(const uint16_t *x, int M, int N, int K, const uint8_t *codes, 
   uint8_t *base = static_cast<uint8_t *>(scratch);
   LoraSeg L = one_seg(N, A, B, r, s, nullptr, nullptr);
   const bool f16 = x_f16 != 0;
-  k_lora_down(x, K, M, K, L, reinterpret_cast<float *>(base + P.u_f32),
-              reinterpret_cast<uint16_t *>(base + P.ul), f16, f16,
-              reinterpret_cast<float *>(base + P.part), st);
-  k_pack_fwd(L, N, reinterpret_cast<uint16_t *>(base + P.vl), f16, st);
+  if (r > 0) {
+    k_lora_down(x, K, M, K, L, reinterpret_cast<float *>(base + P.u_f32),
+                reinterpret_cast<uint16_t *>(base + P.ul), f16, f16,
+                reinterpret_cast<float *>(base + P.part), st);
+    k_pack_fwd(L, N, reinterpret_cast<uint16_t *>(base + P.vl), f16, st);
+  }
   GemmArgs g = proj_weight(GEMM_FWD, N, K, codes, absmax, w_bf16);
   g.op_f16 = f16 ? 1 : 0;
   g.M = M; g.a = x; g.lda = K;
-  g.ul = reinterpret_cast<uint16_t *>(base + P.ul); g.vl = reinterpret_cast<uint16_t *>(base + P.vl);
-  g.R = L.Rpad(); g.epi = EPI_16; g.out = y; g.ldo = N;
+  if (r > 0) {
+    g.ul = reinterpret_cast<uint16_t *>(base + P.ul);
+    g.vl = reinterpret_cast<uint16_t *>(base + P.vl);
+    g.R = L.Rpad();
+  }
+  g.epi = EPI_16; g.out = y; g.ldo = N;
   g.err = reinterpret_cast<int *>(base + P.err);
+  g.part = reinterpret_cast<float *>(base + P.gpart);
+  g.part_floats = P.gpart_floats;
   return gemm_launch(g, st);
 }
 
@@ -249,15 +262,23 @@ int soup_proj_dx(const uint16_t *dy, int M, int N, int K, const uint8_t *codes, 
   const ProjScratch P = proj_plan(M, N, K);
   uint8_t *base = static_cast<uint8_t *>(scratch);
   LoraSeg L = one_seg(N, A, B, r, s, nullptr, nullptr);
-  k_lora_du(dy, N, M, L, reinterpret_cast<float *>(base + P.du_f32),
-            reinterpret_cast<uint16_t *>(base + P.dul), false, false,
-            reinterpret_cast<float *>(base + P.part), st);
-  k_pack_bwd(L, K, reinterpret_cast<uint16_t *>(base + P.ac), false, st);
+  if (r > 0) {
+    k_lora_du(dy, N, M, L, reinterpret_cast<float *>(base + P.du_f32),
+              reinterpret_cast<uint16_t *>(base + P.dul), false, false,
+              reinterpret_cast<float *>(base + P.part), st);
+    k_pack_bwd(L, K, reinterpret_cast<uint16_t *>(base + P.ac), false, st);
+  }
   GemmArgs g = proj_weight(GEMM_DX, N, K, codes, absmax, w_bf16);
   g.M = M; g.a = dy; g.lda = N;
-  g.ul = reinterpret_cast<uint16_t *>(base + P.dul); g.vl = reinterpret_cast<uint16_t *>(base + P.ac);
-  g.R = L.Rpad(); g.epi = EPI_F32; g.out = dx; g.ldo = K;
+  if (r > 0) {
+    g.ul = reinterpret_cast<uint16_t *>(base + P.dul);
+    g.vl = reinterpret_cast<uint16_t *>(base + P.ac);
+    g.R = L.Rpad();
+  }
+  g.epi = EPI_F32; g.out = dx; g.ldo = K;
   g.err = reinterpret_cast<int *>(base + P.err);
+  g.part = reinterpret_cast<float *>(base + P.gpart);
+  g.part_floats = P.gpart_floats;
   return gemm_launch(g, st);
 }
 
@@ -278,8 +299,8 @@ int soup_proj_lora_grad(const uint16_t *x, const uint16_t *dy, int M, int N, int
               reinterpret_cast<uint16_t *>(base + P.ul), f16, f16, part, st);
   k_lora_du(dy, N, M, L, reinterpret_cast<float *>(base + P.du_f32),
             reinterpret_cast<uint16_t *>(base + P.dul), false, false, part, st);
-  k_lora_dB(dy, N, M, reinterpret_cast<float *>(base + P.u_f32), L, false, st);
-  k_lora_dA(reinterpret_cast<float *>(base + P.du_f32), x, K, M, K, L, f16, st);
+  k_lora_dB(dy, N, M, reinterpret_cast<float *>(base + P.u_f32), L, false, part, st);
+  k_lora_dA(reinterpret_cast<float *>(base + P.du_f32), x, K, M, K, L, f16, part, st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(SOUP_ECUDA, "lora grad launch: %s", cudaGetErrorString(e));
   return 0;

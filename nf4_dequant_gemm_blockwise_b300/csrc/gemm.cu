@@ -13,14 +13,14 @@
 // extra 64-wide K tiles: the caller packs s(xA^T) (or s(dY B)) as bf16 [M, R] and the
 // matching B rows (or A rows) as bf16, zero-padded to R = 64 * ceil(segments * r / 64).
 //
-// Tensor-core kernel (tcgen05, one CTA per 128 x BN output tile, 320 threads):
-//   warp 8      TMA producer: activation tile (128 x 64 bf16, 128-byte swizzle), the raw
-//               4-bit codes and float absmax of the weight tile (or a bf16 weight tile)
-//   warps 0..7  dequantise codes -> bf16 into the swizzled shared-memory layout the tensor
-//               core reads (K-major for the forward, MN-major for dX), then run the
-//               epilogue from TMEM
-//   warp 9      allocates TMEM; one lane issues tcgen05.mma (M=128, N=BN, K=16) x 4 per
-//               stage and commits each stage back to the producer
+// Tensor-core kernel (tcgen05, one CTA per 128 x BN output tile, 576 threads):
+//   warp 16      TMA producer: activation tile (128 x 64, 128-byte swizzle), the raw 4-bit
+//                codes and float absmax of the weight tile (or a bf16 weight tile)
+//   warps 0..15  two groups of 8 worker warps taking alternate k-tiles: dequantise codes into
+//                the swizzled 16-bit layout the tensor core reads (K-major for the forward,
+//                MN-major for dX); afterwards all 16 run the epilogue from TMEM
+//   warp 17      allocates TMEM; one lane issues tcgen05.mma (M=128, N=BN, K=16) x 4 per
+//                k-tile and commits each stage back to the producer and the workers
 // Dequantisation uses a per-block table: the 16 products c_k * absmax rounded to bf16,
 // then byte permutes look up four codes at a time (no shared-memory table, no divergence).
 #include <cudaTypedefs.h>
@@ -40,8 +40,10 @@ using namespace soupk;
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int DQ_WARPS = 8;
-constexpr int THREADS = (DQ_WARPS + 2) * 32;
+constexpr int DQ_WARPS = 8;            // warps per worker group (one row-block per thread)
+constexpr int NGROUPS = 2;             // worker groups take alternate k-tiles
+constexpr int WORKERS = DQ_WARPS * NGROUPS;
+constexpr int THREADS = (WORKERS + 2) * 32;
 enum BMode { B_NF4_K = 0, B_NF4_MN = 1, B_BF16_K = 2, B_BF16_MN = 3 };
 
 template <int BN, int BMODE, bool F16>
@@ -51,22 +53,29 @@ struct TcCfg {
   static constexpr bool CONV = !NF4 && F16;
   static constexpr bool PRODUCE = NF4 || CONV;  // the worker warps touch the B tile
   static constexpr bool MN = (BMODE == B_NF4_MN || BMODE == B_BF16_MN);
+  // Two rings.  The load ring (NL stages) receives the activation tile and, for NF4, the raw
+  // codes; the B ring (NB stages) holds the 16-bit weight operand the tensor core reads
+  // (dequantised by the worker warps, or loaded directly for bf16 weights).  The float block
+  // scales are read by the workers straight from global memory (L1-cached, one k-tile ahead).
   static constexpr int A_BYTES = BM * 128;
   static constexpr int B_BYTES = BN * 128;
   static constexpr int RAW_BYTES = NF4 ? BN * 32 : 0;
-  static constexpr int ABS_BYTES = NF4 ? ((BN * 16 + 1023) / 1024) * 1024 : 0;
-  static constexpr int STAGE = A_BYTES + B_BYTES + RAW_BYTES + ABS_BYTES;
-  static constexpr int NS = NF4 ? 3 : 4;
-  static constexpr int SMEM = NS * STAGE + 1024 + 256;
-  // expected TMA bytes per main stage
-  static constexpr uint32_t TX_MAIN =
-      A_BYTES + (NF4 ? (BN * 32 + (MN ? 64 * 16 : BN * 16)) : B_BYTES);
+  static constexpr int LSTAGE = A_BYTES + RAW_BYTES;
+  static constexpr int NL = NF4 ? 5 : 6;
+  static constexpr int NB = 3;
+  static constexpr int SMEM = NL * LSTAGE + NB * B_BYTES + 1024 + 1024;
+  // expected TMA bytes per main / LoRA-extension k-tile (block scales are read by the workers)
+  static constexpr uint32_t TX_MAIN = A_BYTES + (NF4 ? BN * 32 : B_BYTES);
   static constexpr uint32_t TX_EXT = A_BYTES + B_BYTES;
 };
 
 struct TcParams {
   Codebook cb;
+  const float *absmax;  // NF4 block scales of W [Nw, Kw]: absmax[row * kblocks + col / 64]
+  int kblocks, Nw;
   int M, Ng, n_main, n_ext;
+  int splits, per_split;  // split-K: blockIdx.z takes k-tiles [z * per_split, ...); >1 -> partials
+  float *part;            // split-K partial tiles [splits, M, Ng] (float)
   void *out;
   int ldo;
   const float *add_src;
@@ -120,43 +129,59 @@ __global__ void __launch_bounds__(THREADS, 1)
                    const __grid_constant__ CUtensorMap map_ul,
                    const __grid_constant__ CUtensorMap map_vl, const TcParams p) {
   using C = TcCfg<BN, BMODE, F16>;
-  constexpr int NS = C::NS;
+  constexpr int NL = C::NL, NB = C::NB;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + (((raw_base + 1023u) & ~1023u) - raw_base);
-  uint8_t *stage0 = smem;
-  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + NS * C::STAGE);
-  uint64_t *full = bar;             // TMA landed
-  uint64_t *bready = bar + NS;      // B operand ready (dequantised)
-  uint64_t *empty = bar + 2 * NS;   // MMAs done reading the stage
-  uint64_t *accf = bar + 3 * NS;    // accumulator complete
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 3 * NS + 1);
+  uint8_t *lring = smem;                                   // NL x LSTAGE
+  uint8_t *bring = smem + NL * C::LSTAGE;                  // NB x B_BYTES
+  uint64_t *bar = reinterpret_cast<uint64_t *>(bring + NB * C::B_BYTES);
+  uint64_t *lfull = bar;              // load stage landed (TMA)
+  uint64_t *lempty = bar + NL;        // MMAs done with the load stage
+  uint64_t *bready = bar + 2 * NL;    // B stage written (dequantised / converted)
+  uint64_t *bempty = bar + 2 * NL + NB;  // MMAs done with the B stage
+  uint64_t *accf = bar + 2 * NL + 2 * NB;  // accumulator complete
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accf + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * BN;
   const int m0 = blockIdx.y * BM;
-  const int n_total = p.n_main + p.n_ext;
+  // this split's k-tiles, renumbered from 0: main tiles [kb, ke), then the LoRA extension
+  // tiles on the last split only
+  const int z = blockIdx.z;
+  const int kb = z * p.per_split;
+  const int ke = min(p.n_main, kb + p.per_split);
+  const int n_my_main = max(0, ke - kb);
+  const int n_total = n_my_main + (z == p.splits - 1 ? p.n_ext : 0);
 
-  auto A_s = [&](int s) { return stage0 + s * C::STAGE; };
-  auto B_s = [&](int s) { return stage0 + s * C::STAGE + C::A_BYTES; };
-  auto R_s = [&](int s) { return stage0 + s * C::STAGE + C::A_BYTES + C::B_BYTES; };
-  auto S_s = [&](int s) {
-    return stage0 + s * C::STAGE + C::A_BYTES + C::B_BYTES + C::RAW_BYTES;
-  };
+  auto A_s = [&](int s) { return lring + s * C::LSTAGE; };
+  auto R_s = [&](int s) { return lring + s * C::LSTAGE + C::A_BYTES; };
+  auto B_s = [&](int s) { return bring + s * C::B_BYTES; };
 
+  // the codebook goes through shared memory: indexing the parameter block with a run-time
+  // index would force a local copy of it
+  __shared__ float s_cb[16];
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&full[s], 1);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) s_cb[i] = p.cb.v[i];  // static indices: read in place
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NL; ++s) {
+      mbar_init(&lfull[s], 1);
+      mbar_init(&lempty[s], 1);
+    }
+    for (int s = 0; s < NB; ++s) {
       mbar_init(&bready[s], DQ_WARPS);
-      mbar_init(&empty[s], 1);
+      mbar_init(&bempty[s], 1);
     }
     mbar_init(accf, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == DQ_WARPS + 1) {
+  if (warp == WORKERS + 1) {
     tc_alloc(tmem_slot, BN);
     tc_relinquish();
   }
@@ -165,62 +190,66 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == DQ_WARPS) {
+  if (warp == WORKERS) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&map_a);
       tma_prefetch_desc(&map_b0);
       int issued = 0;
       for (int kt = 0; kt < n_total; ++kt) {
-        const int s = kt % NS;
-        if (kt >= NS && !mbar_wait(&empty[s], ((kt / NS) - 1) & 1, p.err, abort_flag)) break;
-        if (kt < p.n_main) {
-          mbar_arrive_expect_tx(&full[s], C::TX_MAIN);
-          tma_load_2d(A_s(s), &map_a, kt * BK, m0, &full[s]);
+        const int sl = kt % NL, sb = kt % NB;
+        if (kt >= NL && !mbar_wait(&lempty[sl], ((kt / NL) - 1) & 1, p.err, abort_flag)) break;
+        const bool b_direct = !C::NF4 || kt >= n_my_main;  // B arrives by TMA into the B ring
+        if (b_direct && kt >= NB && !mbar_wait(&bempty[sb], ((kt / NB) - 1) & 1, p.err, abort_flag)) break;
+        if (kt < n_my_main) {
+          const int g = kb + kt;  // global k-tile
+          mbar_arrive_expect_tx(&lfull[sl], C::TX_MAIN);
+          tma_load_2d(A_s(sl), &map_a, g * BK, m0, &lfull[sl]);
           if (BMODE == B_NF4_K) {
-            tma_load_2d(R_s(s), &map_b0, kt * (BK / 2), n0, &full[s]);
-            tma_load_2d(S_s(s), &map_b1, (kt & ~3), n0, &full[s]);
+            tma_load_2d(R_s(sl), &map_b0, g * (BK / 2), n0, &lfull[sl]);
           } else if (BMODE == B_NF4_MN) {
-            tma_load_2d(R_s(s), &map_b0, n0 / 2, kt * BK, &full[s]);
-            tma_load_2d(S_s(s), &map_b1, n0 / 64, kt * BK, &full[s]);
+            tma_load_2d(R_s(sl), &map_b0, n0 / 2, g * BK, &lfull[sl]);
           } else if (BMODE == B_BF16_K) {
-            tma_load_2d(B_s(s), &map_b0, kt * BK, n0, &full[s]);
+            tma_load_2d(B_s(sb), &map_b0, g * BK, n0, &lfull[sl]);
           } else {
 #pragma unroll
             for (int c = 0; c < BN / 64; ++c)
-              tma_load_2d(B_s(s) + c * 8192, &map_b0, n0 + 64 * c, kt * BK, &full[s]);
+              tma_load_2d(B_s(sb) + c * 8192, &map_b0, n0 + 64 * c, g * BK, &lfull[sl]);
           }
         } else {
-          const int e = kt - p.n_main;
-          mbar_arrive_expect_tx(&full[s], C::TX_EXT);
-          tma_load_2d(A_s(s), &map_ul, e * BK, m0, &full[s]);
+          const int e = kt - n_my_main;
+          mbar_arrive_expect_tx(&lfull[sl], C::TX_EXT);
+          tma_load_2d(A_s(sl), &map_ul, e * BK, m0, &lfull[sl]);
           if (!C::MN) {
-            tma_load_2d(B_s(s), &map_vl, e * BK, n0, &full[s]);
+            tma_load_2d(B_s(sb), &map_vl, e * BK, n0, &lfull[sl]);
           } else {
 #pragma unroll
             for (int c = 0; c < BN / 64; ++c)
-              tma_load_2d(B_s(s) + c * 8192, &map_vl, n0 + 64 * c, e * BK, &full[s]);
+              tma_load_2d(B_s(sb) + c * 8192, &map_vl, n0 + 64 * c, e * BK, &lfull[sl]);
           }
         }
         ++issued;
       }
       // never leave the CTA with copies still landing in its shared memory
-      for (int kt = (issued > NS ? issued - NS : 0); kt < issued; ++kt) {
+      for (int kt = (issued > NL ? issued - NL : 0); kt < issued; ++kt) {
         volatile int no_abort = 0;
-        mbar_wait(&full[kt % NS], (kt / NS) & 1, p.err, &no_abort);
+        mbar_wait(&lfull[kt % NL], (kt / NL) & 1, p.err, &no_abort);
       }
     }
-  } else if (warp == DQ_WARPS + 1) {
+  } else if (warp == WORKERS + 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_16(BM, BN, 0, C::MN ? 1 : 0, F16 ? 1 : 0);
-      uint64_t *wait_bar = C::PRODUCE ? bready : full;
       for (int kt = 0; kt < n_total; ++kt) {
-        const int s = kt % NS;
-        if (!mbar_wait(&wait_bar[s], (kt / NS) & 1, p.err, abort_flag)) break;
+        const int sl = kt % NL, sb = kt % NB;
+        // produce modes: the workers waited for the load stage before marking the B stage
+        // ready; direct modes: the load-stage barrier also counts the B tile's bytes
+        const bool ok = C::PRODUCE ? mbar_wait(&bready[sb], (kt / NB) & 1, p.err, abort_flag)
+                                   : mbar_wait(&lfull[sl], (kt / NL) & 1, p.err, abort_flag);
+        if (!ok) break;
         tc_fence_after();
-        const uint32_t a_addr = smem_u32(A_s(s));
-        const uint32_t b_addr = smem_u32(B_s(s));
+        const uint32_t a_addr = smem_u32(A_s(sl));
+        const uint32_t b_addr = smem_u32(B_s(sb));
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
           const uint64_t ad = smem_desc(a_addr + kk * 32, 16, 1024);
@@ -228,21 +257,66 @@ __global__ void __launch_bounds__(THREADS, 1)
                                     : smem_desc(b_addr + kk * 32, 16, 1024);
           tc_mma_bf16(tmem, ad, bd, idesc, (kt | kk) != 0);
         }
-        tc_commit(&empty[s]);
+        tc_commit(&lempty[sl]);
+        tc_commit(&bempty[sb]);
       }
       tc_commit(accf);
       volatile int no_abort = 0;
       mbar_wait(accf, 0, p.err, &no_abort);  // every MMA retired before TMEM is freed
     }
   } else {
-    // ---------------------------------------------------------------- dequant warps
-    const int t = threadIdx.x;  // 0 .. 255
-    for (int kt = 0; C::PRODUCE && kt < n_total; ++kt) {
-      const int s = kt % NS;
-      if (!mbar_wait(&full[s], (kt / NS) & 1, p.err, abort_flag)) break;
-      if (C::CONV && kt < p.n_main) {
+    // ---------------------------------------------------------------- worker warps
+    const int grp = warp / DQ_WARPS;
+    const int t = threadIdx.x - grp * DQ_WARPS * 32;  // 0 .. 255 within the group
+    float cbr[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) cbr[i] = s_cb[i];
+    // this thread's block scale for k-tile kt: forward = (row n0 + t, block kt); dX = (row
+    // kt * 64 + (t & 63), block n0 / 64 + (t >> 6)); rows past the weight read as 0
+    auto absmax_of = [&](int kt) -> float {
+      if (!C::NF4 || kt >= n_my_main) return 0.f;
+      const int g = kb + kt;
+      const int row = (BMODE == B_NF4_K) ? n0 + t : g * BK + (t & 63);
+      const int col = (BMODE == B_NF4_K) ? g : n0 / 64 + (t >> 6);
+      if (row >= p.Nw || col >= p.kblocks) return 0.f;
+      return __ldg(p.absmax + (size_t)row * p.kblocks + col);
+    };
+    float a_next = absmax_of(grp);
+    for (int kt = grp; C::PRODUCE && kt < n_total; kt += NGROUPS) {
+      const int sl = kt % NL, sb = kt % NB;
+      const float a = a_next;
+      a_next = absmax_of(kt + NGROUPS);  // in flight while this tile is waited for and dequantised
+      if (!mbar_wait(&lfull[sl], (kt / NL) & 1, p.err, abort_flag)) break;
+      if (C::NF4 && kt < n_my_main) {
+        if (kt >= NB && !mbar_wait(&bempty[sb], ((kt / NB) - 1) & 1, p.err, abort_flag)) break;
+        uint8_t *Bs = B_s(sb);
+        const uint8_t *Rs = R_s(sl);
+        if (BMODE == B_NF4_K) {
+          // BN == 256 rows: one row-block per thread
+          const int n = t;
+          const uint4 c0 = *reinterpret_cast<const uint4 *>(Rs + n * 32);
+          const uint4 c1 = *reinterpret_cast<const uint4 *>(Rs + n * 32 + 16);
+          const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          uint4 o[8];
+          dq_block64<F16>(cbr, cw, a, o);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(Bs + sw128(n, c)) = o[c];
+        } else {
+          // 64 reduction rows x (BN / 64) column segments: one row-block per thread
+          const int n = t & 63, seg = t >> 6;
+          const uint4 c0 = *reinterpret_cast<const uint4 *>(Rs + sw128(n, 2 * seg));
+          const uint4 c1 = *reinterpret_cast<const uint4 *>(Rs + sw128(n, 2 * seg + 1));
+          const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          uint4 o[8];
+          dq_block64<F16>(cbr, cw, a, o);
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4 *>(Bs + seg * 8192 + sw128(n, c)) = o[c];
+        }
+        fence_async_smem();
+      } else if (C::CONV && kt < n_my_main) {
         // bf16 -> half, element by element; the byte layout (and so the swizzle) is unchanged
-        uint4 *Bs = reinterpret_cast<uint4 *>(B_s(s));
+        uint4 *Bs = reinterpret_cast<uint4 *>(B_s(sb));
         for (int i = t; i < C::B_BYTES / 16; i += DQ_WARPS * 32) {
           uint4 v = Bs[i];
           v.x = pack_h2(bf16_lo(v.x), bf16_hi(v.x));
@@ -253,39 +327,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         fence_async_smem();
       }
-      if (C::NF4 && kt < p.n_main) {
-        uint8_t *Bs = B_s(s);
-        const uint8_t *Rs = R_s(s);
-        const uint8_t *Ss = S_s(s);
-        if (BMODE == B_NF4_K) {
-          for (int n = t; n < BN; n += DQ_WARPS * 32) {
-            const uint4 c0 = *reinterpret_cast<const uint4 *>(Rs + n * 32);
-            const uint4 c1 = *reinterpret_cast<const uint4 *>(Rs + n * 32 + 16);
-            const float a = *reinterpret_cast<const float *>(Ss + n * 16 + (kt & 3) * 4);
-            const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-            uint4 o[8];
-            dq_block64<F16>(p.cb.v, cw, a, o);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(Bs + sw128(n, c)) = o[c];
-          }
-        } else {
-          for (int it = t; it < 64 * (BN / 64); it += DQ_WARPS * 32) {
-            const int n = it & 63, seg = it >> 6;
-            const uint4 c0 = *reinterpret_cast<const uint4 *>(Rs + sw128(n, 2 * seg));
-            const uint4 c1 = *reinterpret_cast<const uint4 *>(Rs + sw128(n, 2 * seg + 1));
-            const float a = *reinterpret_cast<const float *>(Ss + n * 16 + seg * 4);
-            const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-            uint4 o[8];
-            dq_block64<F16>(p.cb.v, cw, a, o);
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-              *reinterpret_cast<uint4 *>(Bs + seg * 8192 + sw128(n, c)) = o[c];
-          }
-        }
-        fence_async_smem();
-      }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bready[s]);
+      if (lane == 0) mbar_arrive(&bready[sb]);
     }
     // ---------------------------------------------------------------- epilogue
     volatile int no_abort = 0;
@@ -294,8 +337,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (ok) {
       const int q = warp & 3;
       const int m = m0 + q * 32 + lane;
-      for (int cc = 0; cc < BN / 64; ++cc) {
-        const int col = (warp >> 2) * (BN / 2) + cc * 32;
+      constexpr int COLS = BN / (WORKERS / 4);  // columns per warp
+      for (int cc = 0; cc < COLS / 32; ++cc) {
+        const int col = (warp >> 2) * COLS + cc * 32;
         uint32_t r[32];
         tc_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + col, r);
         tc_wait_ld();
@@ -303,7 +347,20 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int n = n0 + col;
         if (n >= p.Ng) continue;
         const bool full_row = (n + 32 <= p.Ng);
-        if (EPI == EPI_16) {
+        if (p.splits > 1) {
+          float *o = p.part + ((size_t)z * p.M + m) * p.Ng + n;
+          if (full_row && (p.Ng & 3) == 0) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              *reinterpret_cast<float4 *>(o + 4 * v) =
+                  make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                              __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (n + j < p.Ng) o[j] = __uint_as_float(r[j]);
+          }
+        } else if (EPI == EPI_16) {
           uint16_t *o = reinterpret_cast<uint16_t *>(p.out) + (size_t)m * p.ldo + n;
           if (full_row) {
 #pragma unroll
@@ -351,7 +408,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_before();
   }
   __syncthreads();
-  if (warp == DQ_WARPS + 1) {
+  if (warp == WORKERS + 1) {
     __syncwarp();
     tc_fence_after();
     tc_dealloc(tmem, BN);
@@ -456,6 +513,33 @@ __global__ void __launch_bounds__(256) fallback_gemm_kernel(const FbParams p) {
 }
 
 // ---------------------------------------------------------------------------------------
+// Split-K reduction: out = epilogue(sum over splits, in split order) — deterministic.
+struct RedParams {
+  const float *part;
+  int splits, M, Ng, epi, f16, ldo, ld_add;
+  void *out;
+  const float *add_src;
+};
+__global__ void splitk_reduce_kernel(const RedParams p) {
+  const int64_t total = (int64_t)p.M * p.Ng;
+  const int64_t plane = total;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    float v = 0.f;
+    for (int z = 0; z < p.splits; ++z) v += p.part[(size_t)z * plane + idx];
+    const int m = (int)(idx / p.Ng), n = (int)(idx % p.Ng);
+    if (p.epi == EPI_16) {
+      reinterpret_cast<uint16_t *>(p.out)[(size_t)m * p.ldo + n] = p.f16 ? f_to_h16(v) : f_to_bf16(v);
+    } else {
+      float *o = reinterpret_cast<float *>(p.out) + (size_t)m * p.ldo + n;
+      if (p.epi == EPI_F32) *o = v;
+      else if (p.epi == EPI_F32_ADD) *o = p.add_src[(size_t)m * p.ld_add + n] + v;
+      else *o = *o + v;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------
 // host side
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::mutex g_mu;
@@ -504,18 +588,33 @@ int launch_tc(const GemmArgs &g, const CUtensorMap *maps, cudaStream_t st) {
   }
   TcParams p;
   p.cb = nf4_codebook_param();
+  p.absmax = g.absmax;
+  p.kblocks = g.Kw / 64;
+  p.Nw = g.Nw;
   p.M = g.M;
   p.Ng = g.Ng();
   p.n_main = (g.Kg() + BK - 1) / BK;
   p.n_ext = g.R / BK;
+  p.splits = g.splits > 1 ? g.splits : 1;
+  p.per_split = (p.n_main + p.splits - 1) / p.splits;
+  p.part = g.part;
   p.out = g.out;
   p.ldo = g.ldo;
   p.add_src = g.add_src;
   p.ld_add = g.ld_add;
   p.err = g.err;
-  dim3 grid((p.Ng + BN - 1) / BN, (g.M + BM - 1) / BM);
+  dim3 grid((p.Ng + BN - 1) / BN, (g.M + BM - 1) / BM, p.splits);
   kern<<<grid, THREADS, C::SMEM, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
   count_launches(1);
+  if (p.splits > 1) {
+    RedParams rp;
+    rp.part = g.part; rp.splits = p.splits; rp.M = g.M; rp.Ng = p.Ng; rp.epi = g.epi;
+    rp.f16 = g.op_f16; rp.ldo = g.ldo; rp.ld_add = g.ld_add; rp.out = g.out; rp.add_src = g.add_src;
+    const int64_t n = (int64_t)g.M * p.Ng;
+    const int blocks = (int)std::min<int64_t>((n + 255) / 256, 148 * 16);
+    splitk_reduce_kernel<<<blocks, 256, 0, st>>>(rp);
+    count_launches(1);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(SOUP_ECUDA, "tc_gemm launch: %s", cudaGetErrorString(e));
   return 0;
@@ -539,6 +638,29 @@ int launch_tc_op(const GemmArgs &g, const CUtensorMap *maps, cudaStream_t st) {
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 }  // namespace
+
+// Split-K factor for an under-filled grid: minimise waves(tiles * s) / s plus the cost of
+// writing and re-reading s partial planes, within the partial buffer the caller provides.
+int choose_splits(const GemmArgs &g, int bn) {
+  if (!g.part || g.part_floats == 0) return 1;
+  const int64_t tiles = (int64_t)((g.M + 127) / 128) * ((g.Ng() + bn - 1) / bn);
+  const int kt = (g.Kg() + 63) / 64;
+  const double t_ktile = 0.6e-6;                        // one 128 x 256 x 64 k-tile, seconds (measured)
+  const double bw = 6.0e12;                             // partial traffic (L2-resident), bytes / s
+  int best = 1;
+  double best_t = 1e30;
+  for (int s = 1; s <= 4; ++s) {
+    if (s > 1 && (kt / s < 4 || (double)s * g.M * g.Ng() > (double)g.part_floats)) break;
+    const int64_t waves = (tiles * s + 147) / 148;
+    const double t = (double)waves * ((kt + s - 1) / s) * t_ktile +
+                     (s > 1 ? 2.0 * s * g.M * (double)g.Ng() * 4.0 / bw : 0.0);
+    if (t < best_t * 0.97) {
+      best_t = t;
+      best = s;
+    }
+  }
+  return best;
+}
 
 int gemm_uses_tc(const GemmArgs &g) {
   if (g_force_fallback) return 0;
@@ -607,6 +729,15 @@ int gemm_launch(const GemmArgs &g, cudaStream_t st) {
   int rc = get_encode();
   if (rc) return rc;
   constexpr int BN = 256;
+  GemmArgs g2 = g;
+  g2.splits = choose_splits(g, BN);
+  if (g2.splits > 1 && g.splits_allowed == 0) g2.splits = 1;
+  return gemm_launch_tc(g2, st);
+}
+
+int gemm_launch_tc(const GemmArgs &g, cudaStream_t st) {
+  int rc = 0;
+  constexpr int BN = 256;
   const int Ng = g.Ng(), Kg = g.Kg();
   CUtensorMap maps[5];
   const CUtensorMapDataType t16 = g.op_f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -614,21 +745,17 @@ int gemm_launch(const GemmArgs &g, cudaStream_t st) {
                 (uint64_t)g.lda * 2, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B, "activations");
   if (rc) return rc;
   int bmode;
+  maps[2] = maps[0];
   if (g.wfmt == W_NF4) {
-    const uint64_t rowb = (uint64_t)g.Kw / 2, arow = (uint64_t)g.Kw / 64;
+    const uint64_t rowb = (uint64_t)g.Kw / 2;
     if (g.mode == GEMM_FWD) {
       bmode = B_NF4_K;
       rc = make_map(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, g.codes, rowb, (uint64_t)g.Nw, rowb,
                     32, BN, CU_TENSOR_MAP_SWIZZLE_NONE, "codes");
-      if (!rc) rc = make_map(&maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, g.absmax, arow,
-                             (uint64_t)g.Nw, arow * 4, 4, BN, CU_TENSOR_MAP_SWIZZLE_NONE, "absmax");
     } else {
       bmode = B_NF4_MN;
       rc = make_map(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, g.codes, rowb, (uint64_t)g.Nw, rowb,
                     BN / 2, BK, CU_TENSOR_MAP_SWIZZLE_128B, "codes");
-      if (!rc) rc = make_map(&maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, g.absmax, arow,
-                             (uint64_t)g.Nw, arow * 4, BN / 64, BK, CU_TENSOR_MAP_SWIZZLE_NONE,
-                             "absmax");
     }
   } else {
     const uint64_t ldw = g.ldw ? g.ldw : g.Kw;

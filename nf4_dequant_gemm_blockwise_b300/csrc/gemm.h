@@ -40,6 +40,12 @@ struct GemmArgs {
   const float *add_src = nullptr;
   int ld_add = 0;
   int *err = nullptr;              // device int: kernels OR error bits into it
+  // split-K scratch (optional): float buffer the kernel may use for partial tiles when the
+  // output grid under-fills the GPU; splits is chosen by gemm_launch
+  float *part = nullptr;
+  size_t part_floats = 0;
+  int splits_allowed = 1;
+  int splits = 1;
   // derived: Ng = output columns, Kg = reduction length
   int Ng() const { return mode == GEMM_FWD ? Nw : Kw; }
   int Kg() const { return mode == GEMM_FWD ? Kw : Nw; }
@@ -54,6 +60,9 @@ double gemm_bytes(const GemmArgs &g);
 int gemm_launch(const GemmArgs &g, cudaStream_t stream);
 // 1 if gemm_launch would take the tensor-core path for this shape.
 int gemm_uses_tc(const GemmArgs &g);
+// Split-K factor gemm_launch picks for this call (1 = none).
+int choose_splits(const GemmArgs &g, int bn);
+int gemm_launch_tc(const GemmArgs &g, cudaStream_t stream);
 // Force the fallback path (tests compare the two).
 void gemm_force_fallback(int on);
 

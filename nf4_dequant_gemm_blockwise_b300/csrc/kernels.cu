@@ -167,6 +167,28 @@ SOUP_DEV float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
 
 template <bool F16>
 __global__ void swiglu_fwd_kernel(const uint16_t *gu, int M, int I, uint16_t *act) {
+  // 8 consecutive outputs per item when I % 8 == 0 (16-byte loads of gate and up)
+  const int I8 = I / 8;
+  const int64_t total = (int64_t)M * I8;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t m = idx / I8, j = (idx % I8) * 8;
+    const uint4 g = *reinterpret_cast<const uint4 *>(gu + m * 2 * I + j);
+    const uint4 u = *reinterpret_cast<const uint4 *>(gu + m * 2 * I + I + j);
+    const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {u.x, u.y, u.z, u.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float g0 = lo16<F16>(gw[e]), g1 = hi16<F16>(gw[e]);
+      const float u0 = lo16<F16>(uw[e]), u1 = hi16<F16>(uw[e]);
+      o[e] = pack16x2<F16>(g0 * sigmoidf_(g0) * u0, g1 * sigmoidf_(g1) * u1);
+    }
+    *reinterpret_cast<uint4 *>(act + m * I + j) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+template <bool F16>
+__global__ void swiglu_fwd_scalar_kernel(const uint16_t *gu, int M, int I, uint16_t *act) {
   const int64_t total = (int64_t)M * I;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
        idx += (int64_t)gridDim.x * blockDim.x) {
@@ -196,53 +218,100 @@ __global__ void swiglu_bwd_kernel(const float *dact, const uint16_t *gu, int M, 
 // part[split][m][o] = sum over k in the split's range of X[m, k] * W_o(k), o < 64, with
 //   DOWN: X = x [M, K], W_o(k) = A_seg[j, k]                       (u = x A^T)
 //   DU:   X = dY [M, Ng], W_o(k) = B_seg[k - off_seg, j] inside the segment, else 0
-// Tile: 32 rows x 64 outputs per 256-thread block; blockIdx.y picks the K range.  The
-// splits are then summed in split order by lora_reduce_kernel (no atomics).
+// Tile: 64 rows x 64 outputs per 256-thread block, K in chunks of 64 staged in shared memory
+// as float; each thread owns 4 rows x 4 outputs and reads float4s.  blockIdx.y picks the K
+// range; lora_reduce_kernel sums the splits in split order (no atomics).
 template <bool DU, bool XF16>
 __global__ void __launch_bounds__(256) lora_part_kernel(const uint16_t *X, int ldx, int M, int K,
                                                         int KS, const LoraSeg L, float *part) {
-  __shared__ float xs[32][65];
-  __shared__ float ws[64][65];
+  __shared__ __align__(16) float xs[64][68];
+  __shared__ __align__(16) float ws[64][68];
   const int t = threadIdx.x;
-  const int m0 = blockIdx.x * 32;
+  const int tx = t & 15, ty = t >> 4;  // outputs tx + 16 j, rows ty * 4 + i
+  const int m0 = blockIdx.x * 64;
   const int kb = blockIdx.y * KS, ke = min(K, kb + KS);
   const int nout = L.nseg * L.r;
-  const int row = t >> 3, cb = t & 7;
-  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
   for (int k0 = kb; k0 < ke; k0 += 64) {
-    for (int i = t; i < 32 * 64; i += 256) {
-      const int rr = i >> 6, kk = i & 63;
-      const int m = m0 + rr, k = k0 + kk;
-      xs[rr][kk] = (m < M && k < ke) ? ld16<XF16>(X[(size_t)m * ldx + k]) : 0.f;
-    }
-    for (int i = t; i < 64 * 64; i += 256) {
-      const int o = i >> 6, kk = i & 63;
-      const int k = k0 + kk;
-      float v = 0.f;
-      if (o < nout && k < ke) {
-        const int seg = o / L.r, j = o % L.r;
-        if (!DU) {
-          v = L.A[seg][(size_t)j * K + k];
-        } else if (k >= L.off[seg] && k < L.off[seg] + L.n[seg]) {
-          v = L.B[seg][(size_t)(k - L.off[seg]) * L.r + j];
-        }
+    for (int i = t; i < 64 * 8; i += 256) {  // X tile: 8 elements per item
+      const int rr = i >> 3, c8 = (i & 7) * 8;
+      const int m = m0 + rr, k = k0 + c8;
+      float v[8];
+      if (m < M && k + 8 <= ke && ((ldx | k) & 7) == 0) {
+        const uint4 q = *reinterpret_cast<const uint4 *>(X + (size_t)m * ldx + k);
+        v[0] = lo16<XF16>(q.x); v[1] = hi16<XF16>(q.x); v[2] = lo16<XF16>(q.y); v[3] = hi16<XF16>(q.y);
+        v[4] = lo16<XF16>(q.z); v[5] = hi16<XF16>(q.z); v[6] = lo16<XF16>(q.w); v[7] = hi16<XF16>(q.w);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          v[e] = (m < M && k + e < ke) ? ld16<XF16>(X[(size_t)m * ldx + k + e]) : 0.f;
       }
-      ws[o][kk] = v;
+      *reinterpret_cast<float4 *>(&xs[rr][c8]) = make_float4(v[0], v[1], v[2], v[3]);
+      *reinterpret_cast<float4 *>(&xs[rr][c8 + 4]) = make_float4(v[4], v[5], v[6], v[7]);
+    }
+    if (!DU) {
+      for (int i = t; i < 64 * 16; i += 256) {  // W tile from A rows: 4 k per item
+        const int o = i >> 4, k4 = (i & 15) * 4;
+        const int k = k0 + k4;
+        float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (o < nout) {
+          const float *ar = L.A[o / L.r] + (size_t)(o % L.r) * K;
+          if (k + 4 <= ke && ((K | k) & 3) == 0) {
+            w = *reinterpret_cast<const float4 *>(ar + k);
+          } else {
+            w.x = k < ke ? ar[k] : 0.f;
+            w.y = k + 1 < ke ? ar[k + 1] : 0.f;
+            w.z = k + 2 < ke ? ar[k + 2] : 0.f;
+            w.w = k + 3 < ke ? ar[k + 3] : 0.f;
+          }
+        }
+        *reinterpret_cast<float4 *>(&ws[o][k4]) = w;
+      }
+    } else {
+      for (int i = t; i < 64 * 64; i += 256) {  // W tile from B rows (r contiguous floats)
+        const int kk = i >> 6, o = i & 63;
+        const int k = k0 + kk;
+        float v = 0.f;
+        if (o < nout && k < ke) {
+          const int seg = o / L.r;
+          if (k >= L.off[seg] && k < L.off[seg] + L.n[seg])
+            v = L.B[seg][(size_t)(k - L.off[seg]) * L.r + (o % L.r)];
+        }
+        ws[o][kk] = v;
+      }
     }
     __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < 64; ++kk) {
-      const float xv = xs[row][kk];
+#pragma unroll 4
+    for (int kk = 0; kk < 64; kk += 4) {
+      float4 a[4], w[4];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) acc[c] = fmaf(xv, ws[cb + 8 * c][kk], acc[c]);
+      for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4 *>(&xs[ty * 4 + i][kk]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w[j] = *reinterpret_cast<const float4 *>(&ws[tx + 16 * j][kk]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc[i][j] = fmaf(a[i].x, w[j].x, acc[i][j]);
+          acc[i][j] = fmaf(a[i].y, w[j].y, acc[i][j]);
+          acc[i][j] = fmaf(a[i].z, w[j].z, acc[i][j]);
+          acc[i][j] = fmaf(a[i].w, w[j].w, acc[i][j]);
+        }
     }
     __syncthreads();
   }
-  const int m = m0 + row;
-  if (m >= M) return;
-  float *dst = part + ((size_t)blockIdx.y * M + m) * 64;
 #pragma unroll
-  for (int c = 0; c < 8; ++c) dst[cb + 8 * c] = acc[c];
+  for (int i = 0; i < 4; ++i) {
+    const int m = m0 + ty * 4 + i;
+    if (m >= M) continue;
+    float *dst = part + ((size_t)blockIdx.y * M + m) * 64;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) dst[tx + 16 * j] = acc[i][j];
+  }
 }
 
 // out_f32[m, o] = (DU ? s : 1) * sum_split part; out16[m, o] = 16-bit(s * sum), zero padded.
@@ -266,89 +335,145 @@ __global__ void lora_reduce_kernel(const float *part, int nsplit, int M, const L
   }
 }
 
-// dB_seg[n - off, j] = s * sum_m dY[m, n] u[m, seg*r + j]; 64 columns per block.
-template <bool F16>
-__global__ void __launch_bounds__(256) lora_dB_kernel(const uint16_t *dy, int ldy, int M, int Ng,
-                                                      const float *u, const LoraSeg L) {
-  __shared__ float ys[32][65];
-  __shared__ float us[32][65];
+// dB partials: part[ms][n][j] = sum over the block's rows m of dY[m, n] u[m, seg(n) r + j].
+// 256 threads x 2 adjacent columns; rows in chunks of 32 with u staged in shared memory.
+template <bool F16, int RMAX>
+__global__ void __launch_bounds__(256) lora_dB_part_kernel(const uint16_t *dy, int ldy, int M,
+                                                           int Ng, int MC, const float *u,
+                                                           const LoraSeg L, float *part) {
+  __shared__ float us[32][64];
   const int t = threadIdx.x;
-  const int n0 = blockIdx.x * 64;
-  const int c = t & 63, jg = t >> 6;
-  const int n = n0 + c;
+  const int n = blockIdx.x * 512 + 2 * t;
+  const int mb = blockIdx.y * MC, me = min(M, mb + MC);
   const int nout = L.nseg * L.r;
-  int seg = -1;
-  for (int p = 0; p < L.nseg; ++p)
-    if (n >= L.off[p] && n < L.off[p] + L.n[p]) seg = p;
-  float acc[16];
+  int s0 = 0, s1 = 0;
+  for (int p = 0; p < L.nseg; ++p) {
+    if (n >= L.off[p] && n < L.off[p] + L.n[p]) s0 = p;
+    if (n + 1 >= L.off[p] && n + 1 < L.off[p] + L.n[p]) s1 = p;
+  }
+  const int b0 = s0 * L.r, b1 = s1 * L.r;
+  float a0[RMAX], a1[RMAX];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-  for (int mb = 0; mb < M; mb += 32) {
-    for (int i = t; i < 32 * 64; i += 256) {
-      const int rr = i >> 6, cc = i & 63;
-      const int m = mb + rr, nn = n0 + cc;
-      ys[rr][cc] = (m < M && nn < Ng) ? ld16<F16>(dy[(size_t)m * ldy + nn]) : 0.f;
-    }
+  for (int j = 0; j < RMAX; ++j) a0[j] = a1[j] = 0.f;
+  const bool pair = (n + 1 < Ng) && ((ldy & 1) == 0);
+  for (int m0 = mb; m0 < me; m0 += 32) {
     for (int i = t; i < 32 * 64; i += 256) {
       const int rr = i >> 6, o = i & 63;
-      const int m = mb + rr;
-      us[rr][o] = (m < M && o < nout) ? u[(size_t)m * nout + o] : 0.f;
+      const int m = m0 + rr;
+      us[rr][o] = (m < me && o < nout) ? u[(size_t)m * nout + o] : 0.f;
     }
     __syncthreads();
-    if (seg >= 0) {
-      for (int rr = 0; rr < 32; ++rr) {
-        const float yv = ys[rr][c];
+    if (n < Ng) {
+      const int rows = min(32, me - m0);
+      for (int rr = 0; rr < rows; ++rr) {
+        const uint16_t *row = dy + (size_t)(m0 + rr) * ldy + n;
+        float y0, y1;
+        if (pair) {
+          const uint32_t v = *reinterpret_cast<const uint32_t *>(row);
+          y0 = lo16<F16>(v);
+          y1 = hi16<F16>(v);
+        } else {
+          y0 = ld16<F16>(row[0]);
+          y1 = n + 1 < Ng ? ld16<F16>(row[1]) : 0.f;
+        }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int j = jg + 4 * i;
-          if (j < L.r) acc[i] = fmaf(yv, us[rr][seg * L.r + j], acc[i]);
+        for (int j = 0; j < RMAX; ++j) {
+          if (j < L.r) {
+            a0[j] = fmaf(y0, us[rr][b0 + j], a0[j]);
+            a1[j] = fmaf(y1, us[rr][b1 + j], a1[j]);
+          }
         }
       }
     }
     __syncthreads();
   }
-  if (seg < 0) return;
+  if (n >= Ng) return;
+  float *d0 = part + ((size_t)blockIdx.y * Ng + n) * L.r;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int j = jg + 4 * i;
-    if (j < L.r) L.dB[seg][(size_t)(n - L.off[seg]) * L.r + j] = L.s * acc[i];
+  for (int j = 0; j < RMAX; ++j)
+    if (j < L.r) {
+      d0[j] = a0[j];
+      if (n + 1 < Ng) d0[L.r + j] = a1[j];
+    }
+}
+
+__global__ void lora_dB_reduce_kernel(const float *part, int msplit, int Ng, const LoraSeg L) {
+  const int64_t total = (int64_t)Ng * L.r;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int n = (int)(idx / L.r), j = (int)(idx % L.r);
+    float acc = 0.f;
+    for (int ms = 0; ms < msplit; ++ms) acc += part[(size_t)ms * total + idx];
+    int seg = 0;
+    for (int p = 0; p < L.nseg; ++p)
+      if (n >= L.off[p] && n < L.off[p] + L.n[p]) seg = p;
+    L.dB[seg][(size_t)(n - L.off[seg]) * L.r + j] = L.s * acc;
   }
 }
 
-// dA_seg[j, k] = sum_m du[m, seg*r + j] x[m, k]; 64 columns per block.
+// dA partials: part[ms][o][k] = sum over the block's rows m of du[m, o] x[m, k]; 128 threads
+// x 2 adjacent columns, 16 outputs per block (blockIdx.z picks them).
 template <bool F16>
-__global__ void __launch_bounds__(256) lora_dA_kernel(const float *du, const uint16_t *x, int ldx,
-                                                      int M, int K, const LoraSeg L) {
-  __shared__ float xs[32][65];
-  __shared__ float ds[32][65];
+__global__ void __launch_bounds__(128) lora_dA_part_kernel(const float *du, const uint16_t *x, int ldx,
+                                                           int M, int K, int MC, int nout,
+                                                           float *part) {
+  __shared__ float ds[32][16];
   const int t = threadIdx.x;
-  const int k0 = blockIdx.x * 64;
-  const int c = t & 63, og = t >> 6;
-  const int k = k0 + c;
-  const int nout = L.nseg * L.r;
-  float acc[16];
+  const int k = blockIdx.x * 256 + 2 * t;
+  const int mb = blockIdx.y * MC, me = min(M, mb + MC);
+  const int o0 = blockIdx.z * 16;
+  float a0[16], a1[16];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-  for (int mb = 0; mb < M; mb += 32) {
-    for (int i = t; i < 32 * 64; i += 256) {
-      const int rr = i >> 6, cc = i & 63;
-      const int m = mb + rr, kk = k0 + cc;
-      xs[rr][cc] = (m < M && kk < K) ? ld16<F16>(x[(size_t)m * ldx + kk]) : 0.f;
-      ds[rr][cc] = (m < M && cc < nout) ? du[(size_t)m * nout + cc] : 0.f;
+  for (int c = 0; c < 16; ++c) a0[c] = a1[c] = 0.f;
+  const bool pair = (k + 1 < K) && ((ldx & 1) == 0);
+  for (int m0 = mb; m0 < me; m0 += 32) {
+    for (int i = t; i < 32 * 16; i += 128) {
+      const int rr = i >> 4, c = i & 15;
+      const int m = m0 + rr;
+      ds[rr][c] = (m < me && o0 + c < nout) ? du[(size_t)m * nout + o0 + c] : 0.f;
     }
     __syncthreads();
-    for (int rr = 0; rr < 32; ++rr) {
-      const float xv = xs[rr][c];
+    if (k < K) {
+      const int rows = min(32, me - m0);
+      for (int rr = 0; rr < rows; ++rr) {
+        const uint16_t *row = x + (size_t)(m0 + rr) * ldx + k;
+        float x0, x1;
+        if (pair) {
+          const uint32_t v = *reinterpret_cast<const uint32_t *>(row);
+          x0 = lo16<F16>(v);
+          x1 = hi16<F16>(v);
+        } else {
+          x0 = ld16<F16>(row[0]);
+          x1 = k + 1 < K ? ld16<F16>(row[1]) : 0.f;
+        }
 #pragma unroll
-      for (int i = 0; i < 16; ++i) acc[i] = fmaf(ds[rr][og + 4 * i], xv, acc[i]);
+        for (int c = 0; c < 16; ++c) {
+          a0[c] = fmaf(ds[rr][c], x0, a0[c]);
+          a1[c] = fmaf(ds[rr][c], x1, a1[c]);
+        }
+      }
     }
     __syncthreads();
   }
   if (k >= K) return;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int o = og + 4 * i;
-    if (o < nout) L.dA[o / L.r][(size_t)(o % L.r) * K + k] = acc[i];
+  for (int c = 0; c < 16; ++c) {
+    if (o0 + c >= nout) break;
+    float *d = part + ((size_t)blockIdx.y * nout + o0 + c) * K + k;
+    d[0] = a0[c];
+    if (k + 1 < K) d[1] = a1[c];
+  }
+}
+
+__global__ void lora_dA_reduce_kernel(const float *part, int msplit, int K, const LoraSeg L) {
+  const int nout = L.nseg * L.r;
+  const int64_t total = (int64_t)nout * K;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int o = (int)(idx / K), k = (int)(idx % K);
+    float acc = 0.f;
+    for (int ms = 0; ms < msplit; ++ms) acc += part[(size_t)ms * total + idx];
+    L.dA[o / L.r][(size_t)(o % L.r) * K + k] = acc;
   }
 }
 
@@ -497,14 +622,14 @@ void k_embed(const int32_t *tok, const uint16_t *E, int V, int H, int M, float *
 void k_rmsnorm_fwd(const float *h, const uint16_t *w, float eps, int M, int H, uint16_t *out,
                    bool out_f16, cudaStream_t st) {
   if (M <= 0) return;
-  if (out_f16) rmsnorm_fwd_kernel<true><<<cdiv(M, 8), 256, 0, st>>>(h, w, eps, M, H, out);
-  else rmsnorm_fwd_kernel<false><<<cdiv(M, 8), 256, 0, st>>>(h, w, eps, M, H, out);
+  if (out_f16) rmsnorm_fwd_kernel<true><<<cdiv(M, 2), 64, 0, st>>>(h, w, eps, M, H, out);
+  else rmsnorm_fwd_kernel<false><<<cdiv(M, 2), 64, 0, st>>>(h, w, eps, M, H, out);
   count_launches(1);
 }
 void k_rmsnorm_bwd(const float *dy, const float *h, const uint16_t *w, float eps, int M, int H,
                    const float *dres, float *out, uint16_t *out_bf16, cudaStream_t st) {
   if (M <= 0) return;
-  rmsnorm_bwd_kernel<<<cdiv(M, 8), 256, 0, st>>>(dy, h, w, eps, M, H, dres, out, out_bf16);
+  rmsnorm_bwd_kernel<<<cdiv(M, 2), 64, 0, st>>>(dy, h, w, eps, M, H, dres, out, out_bf16);
   count_launches(1);
 }
 void k_rope_fwd(uint16_t *qkv, int ld, const float *cos, const float *sin, int M, int S, int nh,
@@ -526,8 +651,14 @@ void k_rope_bwd(const float *dqkv, uint16_t *out, int ld, const float *cos, cons
 void k_swiglu_fwd(const uint16_t *gu, int M, int I, uint16_t *act, bool f16, cudaStream_t st) {
   const int64_t n = (int64_t)M * I;
   if (n <= 0) return;
-  if (f16) swiglu_fwd_kernel<true><<<grid_for(n, 256), 256, 0, st>>>(gu, M, I, act);
-  else swiglu_fwd_kernel<false><<<grid_for(n, 256), 256, 0, st>>>(gu, M, I, act);
+  if (I % 8 == 0) {
+    const int64_t n8 = n / 8;
+    if (f16) swiglu_fwd_kernel<true><<<grid_for(n8, 256), 256, 0, st>>>(gu, M, I, act);
+    else swiglu_fwd_kernel<false><<<grid_for(n8, 256), 256, 0, st>>>(gu, M, I, act);
+  } else {
+    if (f16) swiglu_fwd_scalar_kernel<true><<<grid_for(n, 256), 256, 0, st>>>(gu, M, I, act);
+    else swiglu_fwd_scalar_kernel<false><<<grid_for(n, 256), 256, 0, st>>>(gu, M, I, act);
+  }
   count_launches(1);
 }
 void k_swiglu_bwd(const float *dact, const uint16_t *gu, int M, int I, uint16_t *dgu, bool gu_f16,
@@ -540,14 +671,26 @@ void k_swiglu_bwd(const float *dact, const uint16_t *gu, int M, int I, uint16_t 
 }
 
 int lora_splits(int M, int K, int *KS) {
-  const int rb = cdiv(M, 32);
+  const int rb = cdiv(M, 64);
   int want = std::max(1, cdiv(296, rb));
   want = std::min(want, cdiv(K, 64));
   int ks = cdiv(cdiv(K, want), 64) * 64;
   if (KS) *KS = ks;
   return cdiv(K, ks);
 }
-size_t lora_partial_floats(int M, int K) { return (size_t)lora_splits(M, K, nullptr) * M * 64; }
+// Row split of the gradient reductions: about two waves of blocks in total.
+static int lora_msplit(int M, int col_blocks, int *MC) {
+  int ms = std::max(1, std::min(cdiv(296, col_blocks), cdiv(M, 32)));
+  int mc = cdiv(cdiv(M, ms), 32) * 32;
+  if (MC) *MC = mc;
+  return cdiv(M, mc);
+}
+size_t lora_scratch_floats(int M, int dim, int nout) {
+  const size_t proj = (size_t)lora_splits(M, dim, nullptr) * M * 64;
+  const size_t db = (size_t)lora_msplit(M, cdiv(dim, 512), nullptr) * dim * nout;
+  const size_t da = (size_t)lora_msplit(M, cdiv(dim, 256) * cdiv(nout, 16), nullptr) * dim * nout;
+  return std::max(proj, std::max(db, da));
+}
 
 template <bool DU>
 static void lora_proj(const uint16_t *X, int ldx, int M, int K, const LoraSeg &L, float *out_f32,
@@ -555,7 +698,7 @@ static void lora_proj(const uint16_t *X, int ldx, int M, int K, const LoraSeg &L
   if (M <= 0) return;
   int KS;
   const int ns = lora_splits(M, K, &KS);
-  dim3 grid(cdiv(M, 32), ns);
+  dim3 grid(cdiv(M, 64), ns);
   if (x_f16) lora_part_kernel<DU, true><<<grid, 256, 0, st>>>(X, ldx, M, K, KS, L, part);
   else lora_part_kernel<DU, false><<<grid, 256, 0, st>>>(X, ldx, M, K, KS, L, part);
   const int64_t n = (int64_t)M * L.Rpad();
@@ -563,29 +706,49 @@ static void lora_proj(const uint16_t *X, int ldx, int M, int K, const LoraSeg &L
   else lora_reduce_kernel<DU, false><<<grid_for(n, 256), 256, 0, st>>>(part, ns, M, L, out_f32, out16);
   count_launches(2);
 }
+static int seg_cols(const LoraSeg &L) {
+  int Ng = 0;
+  for (int p = 0; p < L.nseg; ++p) Ng = L.off[p] + L.n[p] > Ng ? L.off[p] + L.n[p] : Ng;
+  return Ng;
+}
 void k_lora_down(const uint16_t *x, int lda, int M, int K, const LoraSeg &L, float *u_f32,
                  uint16_t *ul, bool x_f16, bool ul_f16, float *part, cudaStream_t st) {
   lora_proj<false>(x, lda, M, K, L, u_f32, ul, x_f16, ul_f16, part, st);
 }
 void k_lora_du(const uint16_t *dy, int ldy, int M, const LoraSeg &L, float *du_f32, uint16_t *dul,
                bool dy_f16, bool dul_f16, float *part, cudaStream_t st) {
-  int Ng = 0;
-  for (int p = 0; p < L.nseg; ++p) Ng = L.off[p] + L.n[p] > Ng ? L.off[p] + L.n[p] : Ng;
-  lora_proj<true>(dy, ldy, M, Ng, L, du_f32, dul, dy_f16, dul_f16, part, st);
+  lora_proj<true>(dy, ldy, M, seg_cols(L), L, du_f32, dul, dy_f16, dul_f16, part, st);
+}
+template <bool F16>
+static void dB_launch(const uint16_t *dy, int ldy, int M, int Ng, int MC, int ms, const float *u,
+                      const LoraSeg &L, float *part, cudaStream_t st) {
+  dim3 grid(cdiv(Ng, 512), ms);
+  if (L.r <= 8) lora_dB_part_kernel<F16, 8><<<grid, 256, 0, st>>>(dy, ldy, M, Ng, MC, u, L, part);
+  else if (L.r <= 16) lora_dB_part_kernel<F16, 16><<<grid, 256, 0, st>>>(dy, ldy, M, Ng, MC, u, L, part);
+  else lora_dB_part_kernel<F16, 32><<<grid, 256, 0, st>>>(dy, ldy, M, Ng, MC, u, L, part);
 }
 void k_lora_dB(const uint16_t *dy, int ldy, int M, const float *u_f32, const LoraSeg &L, bool dy_f16,
-               cudaStream_t st) {
-  int Ng = 0;
-  for (int p = 0; p < L.nseg; ++p) Ng = L.off[p] + L.n[p] > Ng ? L.off[p] + L.n[p] : Ng;
-  if (dy_f16) lora_dB_kernel<true><<<cdiv(Ng, 64), 256, 0, st>>>(dy, ldy, M, Ng, u_f32, L);
-  else lora_dB_kernel<false><<<cdiv(Ng, 64), 256, 0, st>>>(dy, ldy, M, Ng, u_f32, L);
-  count_launches(1);
+               float *part, cudaStream_t st) {
+  if (M <= 0) return;
+  const int Ng = seg_cols(L);
+  int MC;
+  const int ms = lora_msplit(M, cdiv(Ng, 512), &MC);
+  if (dy_f16) dB_launch<true>(dy, ldy, M, Ng, MC, ms, u_f32, L, part, st);
+  else dB_launch<false>(dy, ldy, M, Ng, MC, ms, u_f32, L, part, st);
+  lora_dB_reduce_kernel<<<grid_for((int64_t)Ng * L.r, 256), 256, 0, st>>>(part, ms, Ng, L);
+  count_launches(2);
 }
 void k_lora_dA(const float *du_f32, const uint16_t *x, int lda, int M, int K, const LoraSeg &L,
-               bool x_f16, cudaStream_t st) {
-  if (x_f16) lora_dA_kernel<true><<<cdiv(K, 64), 256, 0, st>>>(du_f32, x, lda, M, K, L);
-  else lora_dA_kernel<false><<<cdiv(K, 64), 256, 0, st>>>(du_f32, x, lda, M, K, L);
-  count_launches(1);
+               bool x_f16, float *part, cudaStream_t st) {
+  if (M <= 0) return;
+  const int nout = L.nseg * L.r;
+  int MC;
+  const int ms = lora_msplit(M, cdiv(K, 256) * cdiv(nout, 16), &MC);
+  dim3 grid(cdiv(K, 256), ms, cdiv(nout, 16));
+  if (x_f16) lora_dA_part_kernel<true><<<grid, 128, 0, st>>>(du_f32, x, lda, M, K, MC, nout, part);
+  else lora_dA_part_kernel<false><<<grid, 128, 0, st>>>(du_f32, x, lda, M, K, MC, nout, part);
+  lora_dA_reduce_kernel<<<grid_for((int64_t)nout * K, 256), 256, 0, st>>>(part, ms, K, L);
+  count_launches(2);
 }
 void k_pack_fwd(const LoraSeg &L, int Ng, uint16_t *vl, bool f16, cudaStream_t st) {
   const int64_t n = (int64_t)Ng * L.Rpad();

@@ -47,10 +47,11 @@ void k_swiglu_fwd(const uint16_t *gu, int M, int I, uint16_t *act, bool f16, cud
 void k_swiglu_bwd(const float *dact, const uint16_t *gu, int M, int I, uint16_t *dgu, bool gu_f16,
                   cudaStream_t st);
 
-// Split of the reduction of a LoRA projection (deterministic split-K) and the float scratch
-// it needs: lora_partial_floats(M, K) floats.
+// LoRA reductions are split (over K for the projections, over M for the gradients) and the
+// partial sums are added in a fixed order by a second kernel.  Scratch they need, in floats,
+// for M rows, a reduction/output width `dim` and nout = segments * r outputs:
 int lora_splits(int M, int K, int *KS);
-size_t lora_partial_floats(int M, int K);
+size_t lora_scratch_floats(int M, int dim, int nout);
 // u = x A^T per segment -> u_f32 [M, nseg*r]; ul = 16-bit(s * u) [M, Rpad] (zero padded)
 void k_lora_down(const uint16_t *x, int lda, int M, int K, const LoraSeg &L, float *u_f32,
                  uint16_t *ul, bool x_f16, bool ul_f16, float *part, cudaStream_t st);
@@ -59,10 +60,10 @@ void k_lora_du(const uint16_t *dy, int ldy, int M, const LoraSeg &L, float *du_f
                bool dy_f16, bool dul_f16, float *part, cudaStream_t st);
 // dB_p = s dY_p^T u_p   (written into L.dB)
 void k_lora_dB(const uint16_t *dy, int ldy, int M, const float *u_f32, const LoraSeg &L, bool dy_f16,
-               cudaStream_t st);
+               float *part, cudaStream_t st);
 // dA_p = du_p^T x       (written into L.dA)
 void k_lora_dA(const float *du_f32, const uint16_t *x, int lda, int M, int K, const LoraSeg &L,
-               bool x_f16, cudaStream_t st);
+               bool x_f16, float *part, cudaStream_t st);
 // Vl [Ng, Rpad]: row n of segment p holds 16-bit(B_p[n - off_p, :]) at columns p*r .. p*r+r-1
 void k_pack_fwd(const LoraSeg &L, int Ng, uint16_t *vl, bool f16, cudaStream_t st);
 // Acat [Rpad, K]: row p*r + j holds 16-bit(A_p[j, :]); rows past nseg*r are zero

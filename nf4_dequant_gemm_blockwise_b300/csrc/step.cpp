@@ -81,11 +81,14 @@ int make_plan(const soup_cfg *c, int maxB, int maxS, int n_slots, int resident, 
   P->du_f32 = take(4 * M * 64);
   P->du_b = take(2 * M * 64);
   {
-    const int Ks[6] = {(int)H, (int)qd, (int)I, (int)nqkv, (int)(2 * I), (int)H};
+    const int dims[5] = {(int)H, (int)qd, (int)I, (int)nqkv, (int)(2 * I)};
     size_t mx = 0;
-    for (int k : Ks) mx = std::max(mx, lora_partial_floats((int)M, k));
+    for (int k : dims) mx = std::max(mx, lora_scratch_floats((int)M, k, 3 * c->lora_r));
     P->lora_part = take(4 * mx);
   }
+  // split-K partial tiles for the base GEMMs whose output grid under-fills the GPU
+  P->gemm_part_floats = 4ull * M * std::max<uint64_t>(std::max(nqkv, H), std::max(qd, (uint64_t)I));
+  P->gemm_part = take(4 * P->gemm_part_floats);
   P->hn = take(2 * M * H);
   P->vc = ce_chunk_cols((int)M, c->vocab);
   P->z = take(4 * M * (uint64_t)P->vc);
@@ -154,6 +157,8 @@ void harvest(soup_stream *h, bool block) {
 
 int timed_gemm(soup_stream *h, GemmArgs &g) {
   g.err = h->err_dev;
+  g.part = F(h, h->plan.gemm_part);
+  g.part_floats = h->plan.gemm_part_floats;
   if (!h->dbg_profile) return gemm_launch(g, h->cs);
   TimedEv e;
   e.flops = gemm_flops(g);
@@ -367,8 +372,8 @@ int group_backward(soup_stream *h, int li, const uint8_t *shard, int grp, const 
   const int K = h->lay.n_in[grp];
   // gradients travel in bf16; the layer inputs x are the forward's half tensors
   k_lora_du(dy, ldy, M, L, F(h, P.du_f32), B16(h, P.du_b), false, false, F(h, P.lora_part), st);
-  k_lora_dB(dy, ldy, M, F(h, P.u_f32[grp]), L, false, st);
-  k_lora_dA(F(h, P.du_f32), x, ldx, M, K, L, true, st);
+  k_lora_dB(dy, ldy, M, F(h, P.u_f32[grp]), L, false, F(h, P.lora_part), st);
+  k_lora_dA(F(h, P.du_f32), x, ldx, M, K, L, true, F(h, P.lora_part), st);
   GemmArgs g = weight_args(h, shard, grp, GEMM_DX);
   g.M = M; g.a = dy; g.lda = ldy;
   g.ul = B16(h, P.du_b); g.vl = B16(h, P.ac[(size_t)li * 4 + grp]); g.R = L.Rpad();

@@ -20,6 +20,7 @@ struct Plan {
   uint64_t hn = 0, z = 0, dz = 0, dhn = 0, ce_max = 0, ce_sum = 0, ce_lab = 0, ce_lse = 0;
   std::vector<uint64_t> vl, ac;  // per (layer, group) LoRA operand packs
   uint64_t rope_cos = 0, rope_sin = 0, err = 0;
+  uint64_t gemm_part = 0, gemm_part_floats = 0;
 };
 
 struct Slot {
