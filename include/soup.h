@@ -238,6 +238,24 @@ int soup_proj_lora_grad(const uint16_t *x, const uint16_t *dy, int M, int N, int
                         const float *A, const float *B, int r, float s, int x_f16, float *dA,
                         float *dB, void *scratch, uint64_t scratch_bytes, uintptr_t stream);
 
+/* soup_proj_fwd without caller-provided scratch, for callers that cannot allocate device
+ * memory (a host application that owns the whole device-memory budget, or a latency-critical
+ * caller that cannot take cudaMalloc's implicit synchronisation).  The pages have no
+ * counterpart: this is a deployment convenience, same arguments and result as soup_proj_fwd
+ * minus the scratch pair.
+ *   Working memory comes from one static 16 MiB device array inside the library, reserved on
+ *   every GPU that loads it until the process exits.  A call needing more (large M or N) is
+ *   rejected with SOUP_EINVAL before anything is enqueued.  The first call on a device looks up
+ *   the array's address (cudaGetSymbolAddress); make it before any stream capture there.
+ *   Every call shares the array and it keeps the last call's contents: calls whose GPU work
+ *   overlaps race on it, so issue them in order on one stream.  No split-K partials are used,
+ *   so results can differ from soup_proj_fwd by float summation order.
+ *   Allocates nothing (no cudaMalloc / cudaFree). */
+int soup_proj_fwd_noalloc(const uint16_t *x, int M, int N, int K, const uint8_t *codes,
+                          const float *absmax, const uint16_t *w_bf16, const float *A,
+                          const float *B, int r, float s, int x_f16, uint16_t *y,
+                          uintptr_t stream);
+
 /* Dequantise n NF4 weights on the device: out_f32[i] = float(c[code_i] * absmax[i / 64])
  * and out_bf16[i] = that value rounded to nearest-even bf16 (either output may be NULL). */
 int soup_nf4_dequant(const uint8_t *codes, const float *absmax, int64_t n, float *out_f32,

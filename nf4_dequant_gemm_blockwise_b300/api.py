@@ -84,6 +84,7 @@ def _load() -> C.CDLL:
         "soup_proj_dx": (I32, [P, I32, I32, I32, P, P, P, P, P, I32, F32, P, P, U64, C.c_size_t]),
         "soup_proj_lora_grad": (I32, [P, P, I32, I32, I32, P, P, I32, F32, I32, P, P, P, U64, C.c_size_t]),
         "soup_nf4_dequant": (I32, [P, P, C.c_int64, P, P, C.c_size_t]),
+        "soup_proj_fwd_noalloc": (I32, [P, I32, I32, I32, P, P, P, P, P, I32, F32, I32, P, C.c_size_t]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -292,6 +293,12 @@ def proj_fwd(x, M, N, K, codes, absmax, w_bf16, A, B, r, s, y, scratch, stream=0
     _check(lib.soup_proj_fwd(_ptr(x), M, N, K, _ptr(codes), _ptr(absmax), _ptr(w_bf16), _ptr(A),
                              _ptr(B), r, s, int(x_f16), _ptr(y), _ptr(scratch),
                              scratch.numel() * scratch.element_size(), _stream(stream)))
+
+
+def proj_fwd_noalloc(x, M, N, K, codes, absmax, w_bf16, A, B, r, s, y, stream=0, x_f16=True):
+    """soup_proj_fwd with the library's static device scratch (no allocation by anyone)."""
+    _check(lib.soup_proj_fwd_noalloc(_ptr(x), M, N, K, _ptr(codes), _ptr(absmax), _ptr(w_bf16),
+                                     _ptr(A), _ptr(B), r, s, int(x_f16), _ptr(y), _stream(stream)))
 
 
 def proj_dx(dy, M, N, K, codes, absmax, w_bf16, A, B, r, s, dx, scratch, stream=0):
