@@ -46,7 +46,7 @@ constexpr int WORKERS = DQ_WARPS * NGROUPS;
 constexpr int THREADS = (WORKERS + 2) * 32;
 enum BMode { B_NF4_K = 0, B_NF4_MN = 1, B_BF16_K = 2, B_BF16_MN = 3 };
 
-template <int BN, int BMODE, bool F16>
+template <int BN, int BMODE, bool F16, int MT>
 struct TcCfg {
   static constexpr bool NF4 = (BMODE == B_NF4_K || BMODE == B_NF4_MN);
   // bf16 weights feeding a half-precision GEMM are converted in shared memory, in place
@@ -57,16 +57,20 @@ struct TcCfg {
   // codes; the B ring (NB stages) holds the 16-bit weight operand the tensor core reads
   // (dequantised by the worker warps, or loaded directly for bf16 weights).  The float block
   // scales are read by the workers straight from global memory (L1-cached, one k-tile ahead).
+  // MT m-tiles of 128 rows per CTA share every B tile (MT accumulators of BN TMEM columns)
   static constexpr int A_BYTES = BM * 128;
   static constexpr int B_BYTES = BN * 128;
   static constexpr int RAW_BYTES = NF4 ? BN * 32 : 0;
-  static constexpr int LSTAGE = A_BYTES + RAW_BYTES;
-  static constexpr int NL = NF4 ? 5 : 6;
+  static constexpr int LSTAGE = MT * A_BYTES + RAW_BYTES;
   static constexpr int NB = 3;
+  static constexpr int BUDGET = 225 * 1024 - NB * B_BYTES - 2048;
+  static constexpr int NL0 = BUDGET / LSTAGE;
+  static constexpr int NL = NL0 > 6 ? 6 : NL0;
   static constexpr int SMEM = NL * LSTAGE + NB * B_BYTES + 1024 + 1024;
+  static constexpr int TMEM_COLS = MT * BN;
   // expected TMA bytes per main / LoRA-extension k-tile (block scales are read by the workers)
-  static constexpr uint32_t TX_MAIN = A_BYTES + (NF4 ? BN * 32 : B_BYTES);
-  static constexpr uint32_t TX_EXT = A_BYTES + B_BYTES;
+  static constexpr uint32_t TX_MAIN = MT * A_BYTES + (NF4 ? BN * 32 : B_BYTES);
+  static constexpr uint32_t TX_EXT = MT * A_BYTES + B_BYTES;
 };
 
 struct TcParams {
@@ -121,14 +125,14 @@ SOUP_DEV uint32_t sw128(int r, int c) {
   return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
-template <int BN, int BMODE, int EPI, bool F16>
+template <int BN, int BMODE, int EPI, bool F16, int MT>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_b0,
                    const __grid_constant__ CUtensorMap map_b1,
                    const __grid_constant__ CUtensorMap map_ul,
                    const __grid_constant__ CUtensorMap map_vl, const TcParams p) {
-  using C = TcCfg<BN, BMODE, F16>;
+  using C = TcCfg<BN, BMODE, F16, MT>;
   constexpr int NL = C::NL, NB = C::NB;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
@@ -147,7 +151,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * BN;
-  const int m0 = blockIdx.y * BM;
+  const int m0 = blockIdx.y * BM * MT;
   // this split's k-tiles, renumbered from 0: main tiles [kb, ke), then the LoRA extension
   // tiles on the last split only
   const int z = blockIdx.z;
@@ -157,7 +161,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int n_total = n_my_main + (z == p.splits - 1 ? p.n_ext : 0);
 
   auto A_s = [&](int s) { return lring + s * C::LSTAGE; };
-  auto R_s = [&](int s) { return lring + s * C::LSTAGE + C::A_BYTES; };
+  auto R_s = [&](int s) { return lring + s * C::LSTAGE + MT * C::A_BYTES; };
   auto B_s = [&](int s) { return bring + s * C::B_BYTES; };
 
   // the codebook goes through shared memory: indexing the parameter block with a run-time
@@ -182,7 +186,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     fence_mbar_init();
   }
   if (warp == WORKERS + 1) {
-    tc_alloc(tmem_slot, BN);
+    tc_alloc(tmem_slot, C::TMEM_COLS);
     tc_relinquish();
   }
   tc_fence_before();
@@ -204,7 +208,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (kt < n_my_main) {
           const int g = kb + kt;  // global k-tile
           mbar_arrive_expect_tx(&lfull[sl], C::TX_MAIN);
-          tma_load_2d(A_s(sl), &map_a, g * BK, m0, &lfull[sl]);
+#pragma unroll
+          for (int i = 0; i < MT; ++i)
+            tma_load_2d(A_s(sl) + i * C::A_BYTES, &map_a, g * BK, m0 + i * BM, &lfull[sl]);
           if (BMODE == B_NF4_K) {
             tma_load_2d(R_s(sl), &map_b0, g * (BK / 2), n0, &lfull[sl]);
           } else if (BMODE == B_NF4_MN) {
@@ -219,7 +225,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         } else {
           const int e = kt - n_my_main;
           mbar_arrive_expect_tx(&lfull[sl], C::TX_EXT);
-          tma_load_2d(A_s(sl), &map_ul, e * BK, m0, &lfull[sl]);
+#pragma unroll
+          for (int i = 0; i < MT; ++i)
+            tma_load_2d(A_s(sl) + i * C::A_BYTES, &map_ul, e * BK, m0 + i * BM, &lfull[sl]);
           if (!C::MN) {
             tma_load_2d(B_s(sb), &map_vl, e * BK, n0, &lfull[sl]);
           } else {
@@ -252,10 +260,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t b_addr = smem_u32(B_s(sb));
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint64_t ad = smem_desc(a_addr + kk * 32, 16, 1024);
           const uint64_t bd = C::MN ? smem_desc(b_addr + kk * 2048, 8192, 1024)
                                     : smem_desc(b_addr + kk * 32, 16, 1024);
-          tc_mma_bf16(tmem, ad, bd, idesc, (kt | kk) != 0);
+#pragma unroll
+          for (int i = 0; i < MT; ++i) {
+            const uint64_t ad = smem_desc(a_addr + i * C::A_BYTES + kk * 32, 16, 1024);
+            tc_mma_bf16(tmem + i * BN, ad, bd, idesc, (kt | kk) != 0);
+          }
         }
         tc_commit(&lempty[sl]);
         tc_commit(&bempty[sb]);
@@ -336,12 +347,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     if (ok) {
       const int q = warp & 3;
-      const int m = m0 + q * 32 + lane;
       constexpr int COLS = BN / (WORKERS / 4);  // columns per warp
-      for (int cc = 0; cc < COLS / 32; ++cc) {
+      for (int it = 0; it < MT * (COLS / 32); ++it) {
+        const int mt = it / (COLS / 32), cc = it % (COLS / 32);
+        const int m = m0 + mt * BM + q * 32 + lane;
         const int col = (warp >> 2) * COLS + cc * 32;
         uint32_t r[32];
-        tc_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + col, r);
+        tc_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + mt * BN + col, r);
         tc_wait_ld();
         if (m >= p.M) continue;
         const int n = n0 + col;
@@ -411,7 +423,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == WORKERS + 1) {
     __syncwarp();
     tc_fence_after();
-    tc_dealloc(tmem, BN);
+    tc_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
@@ -573,11 +585,11 @@ int make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t 
   return 0;
 }
 
-template <int BN, int BMODE, int EPI, bool F16>
+template <int BN, int BMODE, int EPI, bool F16, int MT>
 int launch_tc(const GemmArgs &g, const CUtensorMap *maps, cudaStream_t st) {
-  using C = TcCfg<BN, BMODE, F16>;
+  using C = TcCfg<BN, BMODE, F16, MT>;
   static bool attr_done = false;  // per instantiation; set under g_mu
-  auto kern = tc_gemm_kernel<BN, BMODE, EPI, F16>;
+  auto kern = tc_gemm_kernel<BN, BMODE, EPI, F16, MT>;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!attr_done) {
@@ -603,7 +615,7 @@ int launch_tc(const GemmArgs &g, const CUtensorMap *maps, cudaStream_t st) {
   p.add_src = g.add_src;
   p.ld_add = g.ld_add;
   p.err = g.err;
-  dim3 grid((p.Ng + BN - 1) / BN, (g.M + BM - 1) / BM, p.splits);
+  dim3 grid((p.Ng + BN - 1) / BN, (g.M + BM * MT - 1) / (BM * MT), p.splits);
   kern<<<grid, THREADS, C::SMEM, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
   count_launches(1);
   if (p.splits > 1) {
@@ -620,19 +632,22 @@ int launch_tc(const GemmArgs &g, const CUtensorMap *maps, cudaStream_t st) {
   return 0;
 }
 
-template <int BN, int BMODE, bool F16>
+template <int BN, int BMODE, bool F16, int MT>
 int launch_tc_epi(const GemmArgs &g, const CUtensorMap *maps, cudaStream_t st) {
   switch (g.epi) {
-    case EPI_16: return launch_tc<BN, BMODE, EPI_16, F16>(g, maps, st);
-    case EPI_F32: return launch_tc<BN, BMODE, EPI_F32, F16>(g, maps, st);
-    case EPI_F32_ADD: return launch_tc<BN, BMODE, EPI_F32_ADD, F16>(g, maps, st);
-    default: return launch_tc<BN, BMODE, EPI_F32_ACC, F16>(g, maps, st);
+    case EPI_16: return launch_tc<BN, BMODE, EPI_16, F16, MT>(g, maps, st);
+    case EPI_F32: return launch_tc<BN, BMODE, EPI_F32, F16, MT>(g, maps, st);
+    case EPI_F32_ADD: return launch_tc<BN, BMODE, EPI_F32_ADD, F16, MT>(g, maps, st);
+    default: return launch_tc<BN, BMODE, EPI_F32_ACC, F16, MT>(g, maps, st);
   }
 }
 template <int BN, int BMODE>
 int launch_tc_op(const GemmArgs &g, const CUtensorMap *maps, cudaStream_t st) {
-  return g.op_f16 ? launch_tc_epi<BN, BMODE, true>(g, maps, st)
-                  : launch_tc_epi<BN, BMODE, false>(g, maps, st);
+  if (g.mtiles == 2)
+    return g.op_f16 ? launch_tc_epi<BN, BMODE, true, 2>(g, maps, st)
+                    : launch_tc_epi<BN, BMODE, false, 2>(g, maps, st);
+  return g.op_f16 ? launch_tc_epi<BN, BMODE, true, 1>(g, maps, st)
+                  : launch_tc_epi<BN, BMODE, false, 1>(g, maps, st);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -730,7 +745,11 @@ int gemm_launch(const GemmArgs &g, cudaStream_t st) {
   if (rc) return rc;
   constexpr int BN = 256;
   GemmArgs g2 = g;
-  g2.splits = choose_splits(g, BN);
+  // two m-tiles per CTA halve the dequantisation per flop; use them while the grid still
+  // covers at least two waves of the GPU
+  const int64_t ntile = (g.Ng() + BN - 1) / BN;
+  g2.mtiles = ((int64_t)((g.M + 255) / 256) * ntile >= 2 * 148) ? 2 : 1;
+  g2.splits = g2.mtiles == 1 ? choose_splits(g, BN) : 1;
   if (g2.splits > 1 && g.splits_allowed == 0) g2.splits = 1;
   return gemm_launch_tc(g2, st);
 }

@@ -46,6 +46,7 @@ struct GemmArgs {
   size_t part_floats = 0;
   int splits_allowed = 1;
   int splits = 1;
+  int mtiles = 1;                  // 128-row m-tiles per CTA (1 or 2), chosen by gemm_launch
   // derived: Ng = output columns, Kg = reduction length
   int Ng() const { return mode == GEMM_FWD ? Nw : Kw; }
   int Kg() const { return mode == GEMM_FWD ? Kw : Nw; }
