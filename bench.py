@@ -43,6 +43,8 @@ def _args():
     p.add_argument("--slots", type=int, default=2)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-overlap", action="store_true", help="skip the resident comparison run")
+    p.add_argument("--no-variants", action="store_true",
+                   help="skip the extra batch-4 / eight-slot measurements")
     p.add_argument("--micro", action="store_true",
                    help="single-projection microbench instead of the step: one JSON line per (shape, M)")
     p.add_argument("--micro-shape", default="14336x4096,4096x14336", help="NxK list")
@@ -431,6 +433,34 @@ def run_ours(args, rank, world, local_rank, dist):
         "loss": loss_val,
         "clocks": clk,
     }
+    # ---- extra configurations of the same store: batch 4 (the pages' other 8B batch) and
+    # eight device slots (stream_buffers' upper bound); same timing method, fewer steps
+    if not args.no_variants:
+        variants = []
+        for vb, vslots in ((4, args.slots), (1, 8), (4, 8)):
+            vcfg = cfg.with_(batch=vb)
+            vs = StreamedLoRA(vcfg, None, synth.embedding(cfg), synth.lm_head(cfg), synth.final_norm(cfg),
+                              lora, vb, S, n_slots=vslots, store=store)
+            vtok = torch.from_numpy(synth.tokens(vcfg)).cuda()
+            for _ in range(args.warmup):
+                vs.step(vtok)
+            vs.sync()
+            torch.cuda.synchronize()
+            nsteps = max(3, args.steps // 2)
+            v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            v0.record(vs.compute)
+            for _ in range(nsteps):
+                vs.step(vtok)
+            v1.record(vs.compute)
+            vs.sync()
+            torch.cuda.synchronize()
+            vms = v0.elapsed_time(v1) / nsteps
+            vst = vs.stream.stats(reset=True)
+            variants.append({"batch": vb, "slots": vslots, "tokens_per_step": vb * S,
+                             "value": world * vb * S / (vms * 1e-3), "ms_per_step": vms,
+                             "copies_per_step": vst["copies"] / nsteps, "steps": nsteps})
+            vs.close()
+        line["variants"] = variants
     if rank == 0 and not args.no_cpu_baseline:
         one = run_oracle_timed(cfg)
         est = [one()[0] for _ in range(2)]
