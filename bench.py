@@ -239,6 +239,9 @@ def run_micro(args):
                 ts = []
                 for _ in range(args.micro_iters):
                     flush.fill_(1)
+                    # keep the stream busy while the host enqueues the call, so the timed
+                    # region holds device work only (no host launch latency)
+                    torch.cuda._sleep(1_000_000)
                     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     e0.record(st)
                     fn()
@@ -446,6 +449,7 @@ def run_ours(args, rank, world, local_rank, dist):
                 vs.step(vtok)
             vs.sync()
             torch.cuda.synchronize()
+            vs.stream.stats(reset=True)          # count the timed steps' copies only
             nsteps = max(3, args.steps // 2)
             v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             v0.record(vs.compute)

@@ -238,6 +238,13 @@ int soup_proj_lora_grad(const uint16_t *x, const uint16_t *dy, int M, int N, int
                         const float *A, const float *B, int r, float s, int x_f16, float *dA,
                         float *dB, void *scratch, uint64_t scratch_bytes, uintptr_t stream);
 
+/* Status of the projections that used `scratch` (same M, N, K as those calls): waits for
+ * `stream`, reads the scratch's device error flag, clears it, and returns SOUP_OK, or
+ * SOUP_ETIMEDOUT if a kernel's bounded wait gave up (its outputs are then unusable).  The flag
+ * lives in the scratch: zero-fill a new scratch buffer (or pass it here once) before relying
+ * on the result. */
+int soup_proj_status(void *scratch, int M, int N, int K, uintptr_t stream);
+
 /* soup_proj_fwd without caller-provided scratch, for callers that cannot allocate device
  * memory (a host application that owns the whole device-memory budget, or a latency-critical
  * caller that cannot take cudaMalloc's implicit synchronisation).  The pages have no

@@ -85,6 +85,7 @@ def _load() -> C.CDLL:
         "soup_proj_lora_grad": (I32, [P, P, I32, I32, I32, P, P, I32, F32, I32, P, P, P, U64, C.c_size_t]),
         "soup_nf4_dequant": (I32, [P, P, C.c_int64, P, P, C.c_size_t]),
         "soup_proj_fwd_noalloc": (I32, [P, I32, I32, I32, P, P, P, P, P, I32, F32, I32, P, C.c_size_t]),
+        "soup_proj_status": (I32, [P, I32, I32, I32, C.c_size_t]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -305,6 +306,12 @@ def proj_dx(dy, M, N, K, codes, absmax, w_bf16, A, B, r, s, dx, scratch, stream=
     _check(lib.soup_proj_dx(_ptr(dy), M, N, K, _ptr(codes), _ptr(absmax), _ptr(w_bf16), _ptr(A),
                             _ptr(B), r, s, _ptr(dx), _ptr(scratch),
                             scratch.numel() * scratch.element_size(), _stream(stream)))
+
+
+def proj_status(scratch, M, N, K, stream=0):
+    """Raise SoupError(ETIMEDOUT) if a kernel of the projections that used `scratch` gave up a
+    bounded wait; clears the flag.  Waits for the stream."""
+    _check(lib.soup_proj_status(_ptr(scratch), M, N, K, _stream(stream)))
 
 
 def proj_lora_grad(x, dy, M, N, K, A, B, r, s, dA, dB, scratch, stream=0, x_f16=True):

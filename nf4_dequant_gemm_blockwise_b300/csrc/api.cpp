@@ -167,6 +167,9 @@ ProjScratch proj_plan(int M, int N, int K) {
   s.part = take(4ull * std::max(lora_scratch_floats(std::max(M, 1), K, 64),
                                  lora_scratch_floats(std::max(M, 1), N, 64)));
   s.gpart_floats = std::min<uint64_t>(4ull * M * std::max(N, K), 1ull << 26);
+  if (M <= 16)  // the small-M path's per-CTA partial strips
+    s.gpart_floats = std::max<uint64_t>(s.gpart_floats, std::max(gemv_part_floats(GEMM_FWD),
+                                                                 gemv_part_floats(GEMM_DX)));
   s.gpart = take(4 * s.gpart_floats);
   s.err = take(64);
   s.total = off;
@@ -231,24 +234,27 @@ int soup_proj_fwd(const uint16_t *x, int M, int N, int K, const uint8_t *codes, 
   uint8_t *base = static_cast<uint8_t *>(scratch);
   LoraSeg L = one_seg(N, A, B, r, s, nullptr, nullptr);
   const bool f16 = x_f16 != 0;
-  if (r > 0) {
-    k_lora_down(x, K, M, K, L, reinterpret_cast<float *>(base + P.u_f32),
-                reinterpret_cast<uint16_t *>(base + P.ul), f16, f16,
-                reinterpret_cast<float *>(base + P.part), st);
-    k_pack_fwd(L, N, reinterpret_cast<uint16_t *>(base + P.vl), f16, st);
-  }
   GemmArgs g = proj_weight(GEMM_FWD, N, K, codes, absmax, w_bf16);
   g.op_f16 = f16 ? 1 : 0;
   g.M = M; g.a = x; g.lda = K;
-  if (r > 0) {
-    g.ul = reinterpret_cast<uint16_t *>(base + P.ul);
-    g.vl = reinterpret_cast<uint16_t *>(base + P.vl);
-    g.R = L.Rpad();
-  }
   g.epi = EPI_16; g.out = y; g.ldo = N;
   g.err = reinterpret_cast<int *>(base + P.err);
   g.part = reinterpret_cast<float *>(base + P.gpart);
   g.part_floats = P.gpart_floats;
+  if (r > 0) {
+    k_lora_down(x, K, M, K, L, reinterpret_cast<float *>(base + P.u_f32),
+                reinterpret_cast<uint16_t *>(base + P.ul), f16, f16,
+                reinterpret_cast<float *>(base + P.part), st);
+    g.lora_u = reinterpret_cast<float *>(base + P.u_f32);
+    g.lseg = L;
+    g.after_lora = 1;
+    if (!gemv_eligible(g)) {  // the tensor-core path takes the LoRA term as 16-bit K tiles
+      k_pack_fwd(L, N, reinterpret_cast<uint16_t *>(base + P.vl), f16, st);
+      g.ul = reinterpret_cast<uint16_t *>(base + P.ul);
+      g.vl = reinterpret_cast<uint16_t *>(base + P.vl);
+      g.R = L.Rpad();
+    }
+  }
   return gemm_launch(g, st);
 }
 
@@ -262,23 +268,26 @@ int soup_proj_dx(const uint16_t *dy, int M, int N, int K, const uint8_t *codes, 
   const ProjScratch P = proj_plan(M, N, K);
   uint8_t *base = static_cast<uint8_t *>(scratch);
   LoraSeg L = one_seg(N, A, B, r, s, nullptr, nullptr);
-  if (r > 0) {
-    k_lora_du(dy, N, M, L, reinterpret_cast<float *>(base + P.du_f32),
-              reinterpret_cast<uint16_t *>(base + P.dul), false, false,
-              reinterpret_cast<float *>(base + P.part), st);
-    k_pack_bwd(L, K, reinterpret_cast<uint16_t *>(base + P.ac), false, st);
-  }
   GemmArgs g = proj_weight(GEMM_DX, N, K, codes, absmax, w_bf16);
   g.M = M; g.a = dy; g.lda = N;
-  if (r > 0) {
-    g.ul = reinterpret_cast<uint16_t *>(base + P.dul);
-    g.vl = reinterpret_cast<uint16_t *>(base + P.ac);
-    g.R = L.Rpad();
-  }
   g.epi = EPI_F32; g.out = dx; g.ldo = K;
   g.err = reinterpret_cast<int *>(base + P.err);
   g.part = reinterpret_cast<float *>(base + P.gpart);
   g.part_floats = P.gpart_floats;
+  if (r > 0) {
+    k_lora_du(dy, N, M, L, reinterpret_cast<float *>(base + P.du_f32),
+              reinterpret_cast<uint16_t *>(base + P.dul), false, false,
+              reinterpret_cast<float *>(base + P.part), st);
+    g.lora_u = reinterpret_cast<float *>(base + P.du_f32);
+    g.lseg = L;
+    g.after_lora = 1;
+    if (!gemv_eligible(g)) {
+      k_pack_bwd(L, K, reinterpret_cast<uint16_t *>(base + P.ac), false, st);
+      g.ul = reinterpret_cast<uint16_t *>(base + P.dul);
+      g.vl = reinterpret_cast<uint16_t *>(base + P.ac);
+      g.R = L.Rpad();
+    }
+  }
   return gemm_launch(g, st);
 }
 
@@ -303,6 +312,18 @@ int soup_proj_lora_grad(const uint16_t *x, const uint16_t *dy, int M, int N, int
   k_lora_dA(reinterpret_cast<float *>(base + P.du_f32), x, K, M, K, L, f16, part, st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(SOUP_ECUDA, "lora grad launch: %s", cudaGetErrorString(e));
+  return 0;
+}
+
+int soup_proj_status(void *scratch, int M, int N, int K, uintptr_t stream) {
+  if (!scratch || M < 0 || N < 1 || K < 1) return set_error(SOUP_EINVAL, "bad argument");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int *err = reinterpret_cast<int *>(static_cast<uint8_t *>(scratch) + proj_plan(M, N, K).err);
+  int flags = 0;
+  SOUP_CUDA_TRY(cudaMemcpyAsync(&flags, err, sizeof(int), cudaMemcpyDeviceToHost, st));
+  SOUP_CUDA_TRY(cudaStreamSynchronize(st));
+  SOUP_CUDA_TRY(cudaMemsetAsync(err, 0, sizeof(int), st));
+  if (flags) return set_error(SOUP_ETIMEDOUT, "a kernel's bounded wait gave up (flags 0x%x)", flags);
   return 0;
 }
 

@@ -62,11 +62,17 @@ struct TcCfg {
   static constexpr int B_BYTES = BN * 128;
   static constexpr int RAW_BYTES = NF4 ? BN * 32 : 0;
   static constexpr int LSTAGE = MT * A_BYTES + RAW_BYTES;
-  static constexpr int NB = 3;
-  static constexpr int BUDGET = 225 * 1024 - NB * B_BYTES - 2048;
-  static constexpr int NL0 = BUDGET / LSTAGE;
-  static constexpr int NL = NL0 > 6 ? 6 : NL0;
+  // Both ring depths are multiples of the number of worker groups: the groups take alternate
+  // k-tiles, so every stage then belongs to one group, which waits on each of its phases in
+  // turn.  (With an odd depth a group could meet a stage two phases on and its parity wait
+  // would pass on the stale phase.)
+  // (a group dequantises into registers before it waits for its B stage, so one B stage per
+  // group keeps the tensor core fed; the rest of the budget deepens the load ring)
+  static constexpr int NL = MT == 1 ? 6 : 4;
+  static constexpr int NB = 2;
+  static_assert(NL % NGROUPS == 0 && NB % NGROUPS == 0, "ring depths must split between groups");
   static constexpr int SMEM = NL * LSTAGE + NB * B_BYTES + 1024 + 1024;
+  static_assert(SMEM <= 232448, "over the 227 KB shared-memory limit per CTA");
   static constexpr int TMEM_COLS = MT * BN;
   // expected TMA bytes per main / LoRA-extension k-tile (block scales are read by the workers)
   static constexpr uint32_t TX_MAIN = MT * A_BYTES + (NF4 ? BN * 32 : B_BYTES);
@@ -299,27 +305,32 @@ __global__ void __launch_bounds__(THREADS, 1)
       a_next = absmax_of(kt + NGROUPS);  // in flight while this tile is waited for and dequantised
       if (!mbar_wait(&lfull[sl], (kt / NL) & 1, p.err, abort_flag)) break;
       if (C::NF4 && kt < n_my_main) {
-        if (kt >= NB && !mbar_wait(&bempty[sb], ((kt / NB) - 1) & 1, p.err, abort_flag)) break;
+        // dequantise into registers first, then wait for the B stage (the MMAs of this
+        // group's previous tile in it) and store
         uint8_t *Bs = B_s(sb);
         const uint8_t *Rs = R_s(sl);
+        uint4 o[8];
         if (BMODE == B_NF4_K) {
           // BN == 256 rows: one row-block per thread
           const int n = t;
           const uint4 c0 = *reinterpret_cast<const uint4 *>(Rs + n * 32);
           const uint4 c1 = *reinterpret_cast<const uint4 *>(Rs + n * 32 + 16);
           const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-          uint4 o[8];
           dq_block64<F16>(cbr, cw, a, o);
-#pragma unroll
-          for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(Bs + sw128(n, c)) = o[c];
         } else {
           // 64 reduction rows x (BN / 64) column segments: one row-block per thread
           const int n = t & 63, seg = t >> 6;
           const uint4 c0 = *reinterpret_cast<const uint4 *>(Rs + sw128(n, 2 * seg));
           const uint4 c1 = *reinterpret_cast<const uint4 *>(Rs + sw128(n, 2 * seg + 1));
           const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-          uint4 o[8];
           dq_block64<F16>(cbr, cw, a, o);
+        }
+        if (kt >= NB && !mbar_wait(&bempty[sb], ((kt / NB) - 1) & 1, p.err, abort_flag)) break;
+        if (BMODE == B_NF4_K) {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(Bs + sw128(t, c)) = o[c];
+        } else {
+          const int n = t & 63, seg = t >> 6;
 #pragma unroll
           for (int c = 0; c < 8; ++c)
             *reinterpret_cast<uint4 *>(Bs + seg * 8192 + sw128(n, c)) = o[c];
@@ -654,6 +665,13 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 }  // namespace
 
+int tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t outer,
+            uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw,
+            const char *what) {
+  SOUP_TRY(get_encode());
+  return make_map(m, dt, base, inner, outer, row_bytes, box_inner, box_outer, sw, what);
+}
+
 // Split-K factor for an under-filled grid: minimise waves(tiles * s) / s plus the cost of
 // writing and re-reading s partial planes, within the partial buffer the caller provides.
 int choose_splits(const GemmArgs &g, int bn) {
@@ -725,6 +743,7 @@ int gemm_launch(const GemmArgs &g, cudaStream_t st) {
   if (g.R && (!g.ul || !g.vl || g.R % 64)) return set_error(SOUP_EINVAL, "gemm: bad LoRA extension");
   if ((g.epi == EPI_F32_ADD) && !g.add_src) return set_error(SOUP_EINVAL, "gemm: residual missing");
 
+  if (!g_force_fallback && gemv_eligible(g)) return gemv_launch(g, st);
   if (!gemm_uses_tc(g)) {
     FbParams p;
     p.cb = nf4_codebook_param();

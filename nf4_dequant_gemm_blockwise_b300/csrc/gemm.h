@@ -1,8 +1,11 @@
 // Internal interface of the base-weight GEMMs (NF4-dequant or bf16 weights, with the rank-r
 // LoRA term folded in as extra reduction tiles).  Not part of the C ABI.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include "kernels.h"
 
 namespace soup {
 
@@ -47,6 +50,15 @@ struct GemmArgs {
   int splits_allowed = 1;
   int splits = 1;
   int mtiles = 1;                  // 128-row m-tiles per CTA (1 or 2), chosen by gemm_launch
+  // LoRA term in float for the small-M path (which ignores ul / vl / R):
+  //   FWD y[m, n]  += s * sum_j lora_u[m, p r + j] * B_p[n - off_p, j]   (lora_u = x A^T)
+  //   DX  dx[m, k] += sum_p sum_j lora_u[m, p r + j] * A_p[j, k]          (lora_u = s dY B)
+  // lseg.nseg == 0: no LoRA term on that path.
+  const float *lora_u = nullptr;   // [M, nseg * r]
+  LoraSeg lseg;
+  // set when the kernel enqueued just before this GEMM is the LoRA projection that writes
+  // lora_u (k_lora_down / k_lora_du): the small-M path then overlaps with it
+  int after_lora = 0;
   // derived: Ng = output columns, Kg = reduction length
   int Ng() const { return mode == GEMM_FWD ? Nw : Kw; }
   int Kg() const { return mode == GEMM_FWD ? Kw : Nw; }
@@ -66,5 +78,20 @@ int choose_splits(const GemmArgs &g, int bn);
 int gemm_launch_tc(const GemmArgs &g, cudaStream_t stream);
 // Force the fallback path (tests compare the two).
 void gemm_force_fallback(int on);
+
+// 2-D tiled TMA tensor map of a row-major [outer, inner] array (element type dt, rows
+// row_bytes apart), box [box_outer, box_inner]; 0 or SOUP_E* with the message set.
+int tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t outer,
+            uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw,
+            const char *what);
+
+// Small-M path (1 <= M <= 16, NF4 weights; forward on half activations, dX on bf16
+// gradients): weight-stationary mma.sync kernels, stream-K over the weight.  gemm_launch takes
+// it whenever gemv_eligible() holds.
+constexpr int GV_MAX_CTAS = 8 * 160;
+// Float scratch the small-M path needs in GemmArgs::part (upper bound over devices).
+size_t gemv_part_floats(int mode);
+int gemv_eligible(const GemmArgs &g);
+int gemv_launch(const GemmArgs &g, cudaStream_t stream);
 
 }  // namespace soup

@@ -318,20 +318,28 @@ __global__ void __launch_bounds__(256) lora_part_kernel(const uint16_t *X, int l
 template <bool DU, bool OF16>
 __global__ void lora_reduce_kernel(const float *part, int nsplit, int M, const LoraSeg L,
                                    float *out_f32, uint16_t *out16) {
+  pdl_trigger();
+  pdl_wait();  // launched as a dependent of the partial kernel
+  // one warp per output: lanes take the splits lane, lane + 32, ... and the lane sums are
+  // combined by a fixed butterfly, so the order of additions never changes
   const int nout = L.nseg * L.r;
   const int Rp = L.Rpad();
   const int64_t total = (int64_t)M * Rp;
-  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
-       idx += (int64_t)gridDim.x * blockDim.x) {
+  const int lane = threadIdx.x & 31;
+  const int64_t wpb = blockDim.x >> 5;
+  for (int64_t idx = blockIdx.x * wpb + (threadIdx.x >> 5); idx < total; idx += (int64_t)gridDim.x * wpb) {
     const int m = (int)(idx / Rp), o = (int)(idx % Rp);
     if (o >= nout) {
-      out16[idx] = 0;
+      if (lane == 0) out16[idx] = 0;
       continue;
     }
     float acc = 0.f;
-    for (int ks = 0; ks < nsplit; ++ks) acc += part[((size_t)ks * M + m) * 64 + o];
-    out_f32[(size_t)m * nout + o] = DU ? L.s * acc : acc;
-    out16[idx] = st16<OF16>(L.s * acc);
+    for (int ks = lane; ks < nsplit; ks += 32) acc += part[((size_t)ks * M + m) * 64 + o];
+    acc = warp_sum(acc);
+    if (lane == 0) {
+      out_f32[(size_t)m * nout + o] = DU ? L.s * acc : acc;
+      out16[idx] = st16<OF16>(L.s * acc);
+    }
   }
 }
 
@@ -701,9 +709,9 @@ static void lora_proj(const uint16_t *X, int ldx, int M, int K, const LoraSeg &L
   dim3 grid(cdiv(M, 64), ns);
   if (x_f16) lora_part_kernel<DU, true><<<grid, 256, 0, st>>>(X, ldx, M, K, KS, L, part);
   else lora_part_kernel<DU, false><<<grid, 256, 0, st>>>(X, ldx, M, K, KS, L, part);
-  const int64_t n = (int64_t)M * L.Rpad();
-  if (o_f16) lora_reduce_kernel<DU, true><<<grid_for(n, 256), 256, 0, st>>>(part, ns, M, L, out_f32, out16);
-  else lora_reduce_kernel<DU, false><<<grid_for(n, 256), 256, 0, st>>>(part, ns, M, L, out_f32, out16);
+  const int64_t n = (int64_t)M * L.Rpad() * 32;  // one warp per output
+  if (o_f16) launch_pdl(lora_reduce_kernel<DU, true>, dim3(grid_for(n, 256)), dim3(256), 0, st, part, ns, M, L, out_f32, out16);
+  else launch_pdl(lora_reduce_kernel<DU, false>, dim3(grid_for(n, 256)), dim3(256), 0, st, part, ns, M, L, out_f32, out16);
   count_launches(2);
 }
 static int seg_cols(const LoraSeg &L) {

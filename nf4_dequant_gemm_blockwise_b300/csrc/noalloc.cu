@@ -56,7 +56,7 @@ int scratch_address(void **out) {
 }
 
 struct Layout {
-  uint64_t u_f32, ul, vl, part, err, total;
+  uint64_t u_f32, ul, vl, part, gpart, gpart_floats, err, total;
 };
 Layout layout(int M, int N, int K) {
   Layout s;
@@ -70,6 +70,9 @@ Layout layout(int M, int N, int K) {
   s.ul = take(2ull * M * 64);
   s.vl = take(2ull * N * 64);
   s.part = take(4ull * lora_splits(M, K, nullptr) * M * 64);  // the down-projection's partials
+  // small-M path: per-CTA partial strips (no split-K buffer for the tensor-core path)
+  s.gpart_floats = M <= 16 ? gemv_part_floats(GEMM_FWD) : 0;
+  s.gpart = take(4 * s.gpart_floats);
   s.err = take(64);
   s.total = off;
   return s;
@@ -124,15 +127,6 @@ extern "C" int soup_proj_fwd_noalloc(const uint16_t *x, int M, int N, int K, con
     g.wfmt = W_BF16;
     g.w = w_bf16;
   }
-  if (r > 0) {
-    k_lora_down(x, K, M, K, seg, reinterpret_cast<float *>(base + L.u_f32),
-                reinterpret_cast<uint16_t *>(base + L.ul), f16, f16,
-                reinterpret_cast<float *>(base + L.part), st);
-    k_pack_fwd(seg, N, reinterpret_cast<uint16_t *>(base + L.vl), f16, st);
-    g.ul = reinterpret_cast<uint16_t *>(base + L.ul);
-    g.vl = reinterpret_cast<uint16_t *>(base + L.vl);
-    g.R = seg.Rpad();
-  }
   g.op_f16 = f16 ? 1 : 0;
   g.M = M;
   g.a = x;
@@ -141,6 +135,23 @@ extern "C" int soup_proj_fwd_noalloc(const uint16_t *x, int M, int N, int K, con
   g.out = y;
   g.ldo = N;
   g.err = reinterpret_cast<int *>(base + L.err);
-  // no split-K partial buffer: the static array only covers the fixed working set
+  // partial strips of the small-M path only; the tensor-core path runs without split-K here
+  g.part = L.gpart_floats ? reinterpret_cast<float *>(base + L.gpart) : nullptr;
+  g.part_floats = L.gpart_floats;
+  g.splits_allowed = 0;
+  if (r > 0) {
+    k_lora_down(x, K, M, K, seg, reinterpret_cast<float *>(base + L.u_f32),
+                reinterpret_cast<uint16_t *>(base + L.ul), f16, f16,
+                reinterpret_cast<float *>(base + L.part), st);
+    g.lora_u = reinterpret_cast<float *>(base + L.u_f32);
+    g.lseg = seg;
+    g.after_lora = 1;
+    if (!gemv_eligible(g)) {
+      k_pack_fwd(seg, N, reinterpret_cast<uint16_t *>(base + L.vl), f16, st);
+      g.ul = reinterpret_cast<uint16_t *>(base + L.ul);
+      g.vl = reinterpret_cast<uint16_t *>(base + L.vl);
+      g.R = seg.Rpad();
+    }
+  }
   return gemm_launch(g, st);
 }

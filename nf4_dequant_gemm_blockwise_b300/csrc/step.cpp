@@ -325,6 +325,7 @@ int layer_forward(soup_stream *h, int li, const uint8_t *shard, bool recompute) 
     GemmArgs g = weight_args(h, shard, SOUP_G_QKV, GEMM_FWD);
     g.op_f16 = 1; g.M = M; g.a = B16(h, P.x1); g.lda = H;
     g.ul = B16(h, P.u_b[0]); g.vl = B16(h, P.vl[(size_t)li * 4 + 0]); g.R = Lq.Rpad();
+    g.lora_u = F(h, P.u_f32[0]); g.lseg = Lq; g.after_lora = 1;
     g.epi = EPI_16; g.out = B16(h, P.qkv); g.ldo = nqkv;
     SOUP_TRY(timed_gemm(h, g));
   }
@@ -337,6 +338,7 @@ int layer_forward(soup_stream *h, int li, const uint8_t *shard, bool recompute) 
     GemmArgs g = weight_args(h, shard, SOUP_G_O, GEMM_FWD);
     g.op_f16 = 1; g.M = M; g.a = B16(h, P.att); g.lda = qd;
     g.ul = B16(h, P.u_b[1]); g.vl = B16(h, P.vl[(size_t)li * 4 + 1]); g.R = Lo.Rpad();
+    g.lora_u = F(h, P.u_f32[1]); g.lseg = Lo; g.after_lora = 1;
     g.epi = EPI_F32_ADD; g.add_src = hin; g.ld_add = H; g.out = F(h, P.hm); g.ldo = H;
     SOUP_TRY(timed_gemm(h, g));
   }
@@ -346,6 +348,7 @@ int layer_forward(soup_stream *h, int li, const uint8_t *shard, bool recompute) 
     GemmArgs g = weight_args(h, shard, SOUP_G_GU, GEMM_FWD);
     g.op_f16 = 1; g.M = M; g.a = B16(h, P.x2); g.lda = H;
     g.ul = B16(h, P.u_b[2]); g.vl = B16(h, P.vl[(size_t)li * 4 + 2]); g.R = Lg.Rpad();
+    g.lora_u = F(h, P.u_f32[2]); g.lseg = Lg; g.after_lora = 1;
     g.epi = EPI_16; g.out = B16(h, P.gu); g.ldo = 2 * I;
     SOUP_TRY(timed_gemm(h, g));
   }
@@ -355,6 +358,7 @@ int layer_forward(soup_stream *h, int li, const uint8_t *shard, bool recompute) 
     GemmArgs g = weight_args(h, shard, SOUP_G_DOWN, GEMM_FWD);
     g.op_f16 = 1; g.M = M; g.a = B16(h, P.act); g.lda = I;
     g.ul = B16(h, P.u_b[3]); g.vl = B16(h, P.vl[(size_t)li * 4 + 3]); g.R = Ld.Rpad();
+    g.lora_u = F(h, P.u_f32[3]); g.lseg = Ld; g.after_lora = 1;
     g.epi = EPI_F32_ADD; g.add_src = F(h, P.hm); g.ld_add = H;
     g.out = F(h, P.h_all) + (size_t)(li + 1) * M * H; g.ldo = H;
     SOUP_TRY(timed_gemm(h, g));
@@ -372,13 +376,15 @@ int group_backward(soup_stream *h, int li, const uint8_t *shard, int grp, const 
   const int K = h->lay.n_in[grp];
   // gradients travel in bf16; the layer inputs x are the forward's half tensors
   k_lora_du(dy, ldy, M, L, F(h, P.du_f32), B16(h, P.du_b), false, false, F(h, P.lora_part), st);
-  k_lora_dB(dy, ldy, M, F(h, P.u_f32[grp]), L, false, F(h, P.lora_part), st);
-  k_lora_dA(F(h, P.du_f32), x, ldx, M, K, L, true, F(h, P.lora_part), st);
   GemmArgs g = weight_args(h, shard, grp, GEMM_DX);
   g.M = M; g.a = dy; g.lda = ldy;
   g.ul = B16(h, P.du_b); g.vl = B16(h, P.ac[(size_t)li * 4 + grp]); g.R = L.Rpad();
+  g.lora_u = F(h, P.du_f32); g.lseg = L; g.after_lora = 1;
   g.epi = EPI_F32; g.out = dx_out; g.ldo = K;
-  return timed_gemm(h, g);
+  SOUP_TRY(timed_gemm(h, g));
+  k_lora_dB(dy, ldy, M, F(h, P.u_f32[grp]), L, false, F(h, P.lora_part), st);
+  k_lora_dA(F(h, P.du_f32), x, ldx, M, K, L, true, F(h, P.lora_part), st);
+  return 0;
 }
 
 int layer_backward(soup_stream *h, int li, const uint8_t *shard) {
@@ -514,13 +520,6 @@ int step_fwd(soup_stream *h, const int32_t *tokens, int B, int S, const float *c
   const Plan &P = h->plan;
   cudaStream_t st = h->cs;
   const int M = B * S, H = c.hidden;
-  // bf16 LoRA operands for the tensor-core GEMMs of every layer
-  for (int l = 0; l < L; ++l)
-    for (int g = 0; g < 4; ++g) {
-      LoraSeg Lg = make_seg(h, l, g, false);
-      k_pack_fwd(Lg, h->lay.n_out[g], B16(h, P.vl[(size_t)l * 4 + g]), true, st);
-      k_pack_bwd(Lg, h->lay.n_in[g], B16(h, P.ac[(size_t)l * 4 + g]), false, st);
-    }
   k_embed(tokens, h->embed, c.vocab, H, M, F(h, P.h_all), st);
   std::vector<int> seq(L);
   for (int i = 0; i < L; ++i) seq[i] = i;
@@ -528,6 +527,14 @@ int step_fwd(soup_stream *h, const int32_t *tokens, int B, int S, const float *c
   for (int i = 0; i < L; ++i) {
     const uint8_t *shard;
     int s;
+    // 16-bit LoRA operands of this layer's tensor-core GEMMs (forward: half B rows; dX:
+    // bf16 A rows), packed just before first use so that the first layer's kernels, and so
+    // the first slot release, are not queued behind every layer's packing
+    for (int g = 0; g < 4; ++g) {
+      LoraSeg Lg = make_seg(h, i, g, false);
+      k_pack_fwd(Lg, h->lay.n_out[g], B16(h, P.vl[(size_t)i * 4 + g]), true, st);
+      k_pack_bwd(Lg, h->lay.n_in[g], B16(h, P.ac[(size_t)i * 4 + g]), false, st);
+    }
     SOUP_TRY(acquire(h, seq, (size_t)i, &shard, &s));
     SOUP_TRY(layer_forward(h, i, shard, false));
     SOUP_TRY(release(h, s));

@@ -8,6 +8,11 @@ oracle.nf4.dequantize.  Two references are used:
   tensor-core result must match it to float32-accumulation accuracy plus the final output
   rounding;
 * the oracle's float32 layer maths (unrounded W) — relative L2 <= 1e-2, the step's bar.
+
+Token counts up to 16 take the small-M path, whose operands differ: the 16-bit operand is the
+codebook value itself and the block scale is applied in float (forward: to each 64-wide
+block's partial dot product; dX: to the gradient before its bf16 rounding), with the LoRA
+term in float.  Its exact-operand reference models exactly those operands.
 """
 import numpy as np
 import pytest
@@ -66,11 +71,44 @@ def test_dequant_bit_exact(api):
 
 SHAPES = [  # (M, N, K): tiles, ragged M / N, the fallback (K % 256 != 0), microbench shapes;
     # (130, 4096, 14336) takes split-K; (2100, 14336, 4096) forward and (2100, 4096, 14336) dX
-    # take two 128-row m-tiles per CTA with a ragged last m-tile
+    # take two 128-row m-tiles per CTA with a ragged last m-tile.  M <= 16 takes the small-M
+    # path: (9, 32, 1024) has more CTAs than strips, so every strip is summed from partials;
+    # (3, 48, 4096), (5, 4096, 14336) and (16, 14336, 4096) cut strips at CTA boundaries.
     (128, 256, 256), (200, 512, 512), (64, 1376, 256), (64, 256, 688), (1, 256, 256),
     (130, 4096, 14336), (128, 14336, 4096), (16, 14336, 4096), (2100, 14336, 4096),
-    (2100, 4096, 14336),
+    (2100, 4096, 14336), (9, 32, 1024), (3, 48, 4096), (5, 4096, 14336), (1, 14336, 4096),
 ]
+
+
+def _small_m(M, N, K):
+    """Whether the library takes the small-M path for this NF4 projection."""
+    return 1 <= M <= 16 and N % 16 == 0 and K % 64 == 0
+
+
+def _codes(packed, N, K):
+    return nf4.unpack(packed, N * K).reshape(N, K // 64, 64)
+
+
+def _small_fwd_exact(xh, packed, absmax, N, K):
+    """y = sum over blocks b of absmax[n, b] * (x_b . half(c[code_b])), in float64."""
+    codes = _codes(packed, N, K)
+    table = nf4.codebook().astype(np.float16).astype(np.float64)
+    a = absmax.reshape(N, K // 64).astype(np.float64)
+    y = np.zeros((xh.shape[0], N))
+    for b in range(K // 64):
+        y += (xh[:, 64 * b:64 * b + 64] @ table[codes[:, b, :]].T) * a[:, b]
+    return y
+
+
+def _small_dx_exact(dy32, packed, absmax, N, K):
+    """dx[:, block b] = bf16(dY * absmax[:, b]) . bf16(c[code_b]), in float64."""
+    codes = _codes(packed, N, K)
+    table = nf4.bf16_round(nf4.codebook()).astype(np.float64)
+    dx = np.empty((dy32.shape[0], K))
+    for b in range(K // 64):
+        dya = nf4.bf16_round((dy32 * absmax.reshape(N, K // 64)[:, b][None, :]).astype(np.float32))
+        dx[:, 64 * b:64 * b + 64] = dya.astype(np.float64) @ table[codes[:, b, :]]
+    return dx
 
 
 def _rows(M):
@@ -96,9 +134,10 @@ def test_proj_fwd(api, M, N, K, f16):
         rnd = nf4.bf16_round
     A, B = _lora(N, K, r)
     y = torch.empty((M, N), dtype=torch.int16, device="cuda")
-    scratch = torch.empty(api.proj_scratch_bytes(M, N, K, r), dtype=torch.uint8, device="cuda")
+    scratch = torch.zeros(api.proj_scratch_bytes(M, N, K, r), dtype=torch.uint8, device="cuda")
     api.proj_fwd(_dev(x_in), M, N, K, _dev(packed), _dev(absmax), None, _dev(A), _dev(B), r, s, y,
                  scratch, x_f16=f16)
+    api.proj_status(scratch, M, N, K)
     torch.cuda.synchronize()
     rows = _rows(M)
     yb = y.cpu().numpy().view(np.uint16)[rows]
@@ -107,9 +146,13 @@ def test_proj_fwd(api, M, N, K, f16):
     xf = rnd(x32).astype(np.float64)
     wb = rnd(wdq).astype(np.float64)
     lora = s * (xf @ A.T.astype(np.float64)) @ B.T.astype(np.float64)
-    exact = xf @ wb.T + lora
     ulp = 2.0 ** -10 if f16 else 2.0 ** -8
-    tol = ulp * np.abs(exact) + 2e-3 * np.sqrt(np.mean(exact ** 2))
+    if f16 and _small_m(M, N, K):
+        exact = _small_fwd_exact(xf, packed, absmax, N, K) + lora
+        tol = ulp * np.abs(exact) + 1e-4 * np.sqrt(np.mean(exact ** 2))
+    else:
+        exact = xf @ wb.T + lora
+        tol = ulp * np.abs(exact) + 2e-3 * np.sqrt(np.mean(exact ** 2))
     bad = np.abs(got - exact) > tol
     assert not bad.any(), (bad.sum(), np.abs(got - exact).max())
     oracle = x32.astype(np.float64) @ wdq.T.astype(np.float64) + lora   # unrounded operands
@@ -123,21 +166,47 @@ def test_proj_dx(api, M, N, K):
     dy_bits = synth.activations_bf16(M, N, key=2)
     A, B = _lora(N, K, r)
     dx = torch.empty((M, K), dtype=torch.float32, device="cuda")
-    scratch = torch.empty(api.proj_scratch_bytes(M, N, K, r), dtype=torch.uint8, device="cuda")
+    scratch = torch.zeros(api.proj_scratch_bytes(M, N, K, r), dtype=torch.uint8, device="cuda")
     api.proj_dx(_dev(dy_bits), M, N, K, _dev(packed), _dev(absmax), None, _dev(A), _dev(B), r, s, dx, scratch)
+    api.proj_status(scratch, M, N, K)      # no kernel gave up a bounded wait
     torch.cuda.synchronize()
     rows = _rows(M)
     got = dx.cpu().numpy().astype(np.float64)[rows]
     dyf = nf4.bf16_to_f32(dy_bits).astype(np.float64)[rows]
     wb = nf4.bf16_round(wdq).astype(np.float64)
     du = s * (dyf @ B.astype(np.float64))
-    exact = dyf @ wb + nf4.bf16_round(du.astype(np.float32)).astype(np.float64) @ \
-        nf4.bf16_round(A).astype(np.float64)
-    tol = 1e-4 * np.abs(exact) + 1e-3 * np.sqrt(np.mean(exact ** 2))
+    if _small_m(M, N, K):
+        # float LoRA term on this path
+        exact = _small_dx_exact(dyf.astype(np.float32), packed, absmax, N, K) + du @ A.astype(np.float64)
+        tol = 1e-4 * np.abs(exact) + 1e-4 * np.sqrt(np.mean(exact ** 2))
+    else:
+        exact = dyf @ wb + nf4.bf16_round(du.astype(np.float32)).astype(np.float64) @ \
+            nf4.bf16_round(A).astype(np.float64)
+        tol = 1e-4 * np.abs(exact) + 1e-3 * np.sqrt(np.mean(exact ** 2))
     bad = np.abs(got - exact) > tol
     assert not bad.any(), (bad.sum(), np.abs(got - exact).max())
     oracle = dyf @ wdq.astype(np.float64) + du @ A.astype(np.float64)
     assert _rel_l2(got, oracle) <= 1e-2
+
+
+@pytest.mark.parametrize("rep", range(6))
+def test_proj_dx_two_mtile_repeat(api, rep):
+    """dX with two 128-row m-tiles per CTA, a ragged last m-tile and the LoRA extension,
+    repeated: the result must be identical every time (fixed summation order)."""
+    M, N, K, r, s = 2100, 4096, 14336, 16, 2.0
+    _, packed, absmax, _ = _weights(N, K)
+    dy = _dev(synth.activations_bf16(M, N, key=2))
+    A, B = _lora(N, K, r)
+    args = (_dev(packed), _dev(absmax), None, _dev(A), _dev(B), r, s)
+    scratch = torch.zeros(api.proj_scratch_bytes(M, N, K, r), dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(2):
+        dx = torch.full((M, K), float("nan"), dtype=torch.float32, device="cuda")
+        api.proj_dx(dy, M, N, K, *args, dx, scratch)
+        api.proj_status(scratch, M, N, K)
+        outs.append(dx.cpu().numpy())
+    assert np.isfinite(outs[0]).all()
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
 
 
 @pytest.mark.parametrize("M,N,K", [(64, 256, 256), (513, 1376, 256), (512, 4096, 14336)])

@@ -148,6 +148,42 @@ def test_tiny_stale_slot_control_is_caught(tiny):
     _assert_bit_equal(clean, tiny["resident"])
 
 
+@pytest.mark.parametrize("batch,seq", [(1, 16), (2, 4)])
+def test_small_token_count_step(batch, seq):
+    """B*S <= 16 tokens: every base projection (the fused q/k/v with three LoRA segments, the
+    residual-adding o and down projections, the dX GEMMs) takes the small-M path.  Same bars:
+    bit-exact streamed vs resident, and the oracle tolerances."""
+    cfg = synth.TINY.with_(batch=batch, seq=seq)
+    s = _session(cfg, resident=False)
+    r = _session(cfg, resident=True, store=s.store)
+    try:
+        gs, gr = _run(s, cfg), _run(r, cfg)
+    finally:
+        r.close()
+        s.close()
+    _assert_bit_equal(gs, gr)
+    W = model.weights_from_source(cfg, [synth.layer_source(cfg, i) for i in range(cfg.n_layers)],
+                                  synth.embedding(cfg), synth.lm_head(cfg), synth.final_norm(cfg))
+    tok = synth.tokens(cfg)
+    lora = synth.lora_params(cfg)
+    fwd = model.forward(cfg, W, tok, lora)
+    grads, dhs = model.backward(cfg, W, tok, lora, fwd)
+    M = batch * seq
+    for i in range(cfg.n_layers + 1):
+        assert rel_l2(gs["layers"][i], fwd["hs"][i].reshape(M, -1)) <= TOL_FWD_REL, i
+    lo = fwd["logits"].reshape(M, -1)
+    assert rel_l2(gs["logits"], lo) <= TOL_FWD_REL
+    assert np.abs(gs["logits"] - lo).max() <= TOL_LOGIT_ABS
+    for li in range(cfg.n_layers):
+        for p in range(7):
+            for w in range(2):
+                got, want = gs["grads"][li][p][w], grads[li][p][w]
+                assert rel_l2(got, want) <= TOL_GRAD_REL, (li, p, w, rel_l2(got, want))
+                assert cosine(got, want) >= TOL_GRAD_COS, (li, p, w)
+    for i in range(cfg.n_layers + 1):
+        assert rel_l2(gs["dh"][i], dhs[i].reshape(M, -1)) <= TOL_GRAD_REL, i
+
+
 def test_tiny_b_zero_gives_exact_zero_dA():
     cfg = synth.TINY
     s = _session(cfg, resident=False, lora=synth.lora_params(cfg, b_zero=True))
