@@ -66,10 +66,8 @@ struct TcCfg {
   // k-tiles, so every stage then belongs to one group, which waits on each of its phases in
   // turn.  (With an odd depth a group could meet a stage two phases on and its parity wait
   // would pass on the stale phase.)
-  // (a group dequantises into registers before it waits for its B stage, so one B stage per
-  // group keeps the tensor core fed; the rest of the budget deepens the load ring)
-  static constexpr int NL = MT == 1 ? 6 : 4;
-  static constexpr int NB = 2;
+  static constexpr int NL = 4;
+  static constexpr int NB = MT == 1 ? 4 : 2;
   static_assert(NL % NGROUPS == 0 && NB % NGROUPS == 0, "ring depths must split between groups");
   static constexpr int SMEM = NL * LSTAGE + NB * B_BYTES + 1024 + 1024;
   static_assert(SMEM <= 232448, "over the 227 KB shared-memory limit per CTA");

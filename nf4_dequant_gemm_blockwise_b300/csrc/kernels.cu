@@ -215,102 +215,158 @@ __global__ void swiglu_bwd_kernel(const float *dact, const uint16_t *gu, int M, 
 }
 
 // ------------------------------------------------------------------ LoRA projections
+// The four LoRA products are skinny GEMMs (one side is nseg * r <= 64) and run on the tensor
+// cores as TF32 mma.sync (m16n8k8, float accumulation).  The 16-bit activations / gradients
+// are exact in TF32; the float LoRA parameters and intermediates are rounded to TF32 (nearest,
+// ties away) when they are staged.  Every reduction is split into partial tiles that a second
+// kernel adds in a fixed order (no atomics).
+SOUP_DEV uint32_t to_tf32(float f) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(f));
+  return r;
+}
+SOUP_DEV void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Segment of fused output column n (the one whose range holds it; 0 if none).
+SOUP_DEV int seg_of(const LoraSeg &L, int n) {
+  int q = 0;
+  for (int k = 1; k < L.nseg; ++k)
+    if (n >= L.off[k] && n < L.off[k] + L.n[k]) q = k;
+  return q;
+}
+
 // part[split][m][o] = sum over k in the split's range of X[m, k] * W_o(k), o < 64, with
 //   DOWN: X = x [M, K], W_o(k) = A_seg[j, k]                       (u = x A^T)
 //   DU:   X = dY [M, Ng], W_o(k) = B_seg[k - off_seg, j] inside the segment, else 0
-// Tile: 64 rows x 64 outputs per 256-thread block, K in chunks of 64 staged in shared memory
-// as float; each thread owns 4 rows x 4 outputs and reads float4s.  blockIdx.y picks the K
-// range; lora_reduce_kernel sums the splits in split order (no atomics).
+// o = seg * r + j.  Tile: 64 rows x 64 outputs per 128-thread block (warp w: rows 16w..16w+15,
+// all outputs), K in chunks of 32 staged in shared memory.  blockIdx.y picks the K range.
 template <bool DU, bool XF16>
-__global__ void __launch_bounds__(256) lora_part_kernel(const uint16_t *X, int ldx, int M, int K,
+__global__ void __launch_bounds__(128) lora_part_kernel(const uint16_t *X, int ldx, int M, int K,
                                                         int KS, const LoraSeg L, float *part) {
-  __shared__ __align__(16) float xs[64][68];
-  __shared__ __align__(16) float ws[64][68];
-  const int t = threadIdx.x;
-  const int tx = t & 15, ty = t >> 4;  // outputs tx + 16 j, rows ty * 4 + i
+  __shared__ uint32_t xs[64][36];  // [row][k]
+  __shared__ uint32_t ws[64][36];  // [o][k]
+  const int t = threadIdx.x, w = t >> 5, lane = t & 31, g = lane >> 2, q = lane & 3;
   const int m0 = blockIdx.x * 64;
   const int kb = blockIdx.y * KS, ke = min(K, kb + KS);
   const int nout = L.nseg * L.r;
-  float acc[4][4];
+  const int NT = (nout + 7) / 8;  // live 8-wide output tiles
+  // the next chunk's operands are fetched into registers while the current one is computed
+  uint4 xr[2];
+  float wr[16];
+  auto load = [&](int k0) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-  for (int k0 = kb; k0 < ke; k0 += 64) {
-    for (int i = t; i < 64 * 8; i += 256) {  // X tile: 8 elements per item
-      const int rr = i >> 3, c8 = (i & 7) * 8;
+    for (int it = 0; it < 2; ++it) {  // X: 64 rows x 32 k, 8 elements per item
+      const int i = t + 128 * it, rr = i >> 2, c8 = (i & 3) * 8;
       const int m = m0 + rr, k = k0 + c8;
-      float v[8];
       if (m < M && k + 8 <= ke && ((ldx | k) & 7) == 0) {
-        const uint4 q = *reinterpret_cast<const uint4 *>(X + (size_t)m * ldx + k);
-        v[0] = lo16<XF16>(q.x); v[1] = hi16<XF16>(q.x); v[2] = lo16<XF16>(q.y); v[3] = hi16<XF16>(q.y);
-        v[4] = lo16<XF16>(q.z); v[5] = hi16<XF16>(q.z); v[6] = lo16<XF16>(q.w); v[7] = hi16<XF16>(q.w);
+        xr[it] = *reinterpret_cast<const uint4 *>(X + (size_t)m * ldx + k);
       } else {
+        uint32_t h[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          v[e] = (m < M && k + e < ke) ? ld16<XF16>(X[(size_t)m * ldx + k + e]) : 0.f;
+        for (int e = 0; e < 8; ++e) h[e] = (m < M && k + e < ke) ? X[(size_t)m * ldx + k + e] : 0u;
+        xr[it] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
       }
-      *reinterpret_cast<float4 *>(&xs[rr][c8]) = make_float4(v[0], v[1], v[2], v[3]);
-      *reinterpret_cast<float4 *>(&xs[rr][c8 + 4]) = make_float4(v[4], v[5], v[6], v[7]);
     }
     if (!DU) {
-      for (int i = t; i < 64 * 16; i += 256) {  // W tile from A rows: 4 k per item
-        const int o = i >> 4, k4 = (i & 15) * 4;
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {  // A rows: 64 o x 32 k, 4 k per item
+        const int i = t + 128 * it, o = i >> 3, k4 = (i & 7) * 4;
         const int k = k0 + k4;
-        float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
         if (o < nout) {
           const float *ar = L.A[o / L.r] + (size_t)(o % L.r) * K;
           if (k + 4 <= ke && ((K | k) & 3) == 0) {
-            w = *reinterpret_cast<const float4 *>(ar + k);
+            a4 = *reinterpret_cast<const float4 *>(ar + k);
           } else {
-            w.x = k < ke ? ar[k] : 0.f;
-            w.y = k + 1 < ke ? ar[k + 1] : 0.f;
-            w.z = k + 2 < ke ? ar[k + 2] : 0.f;
-            w.w = k + 3 < ke ? ar[k + 3] : 0.f;
+            a4.x = k < ke ? ar[k] : 0.f;
+            a4.y = k + 1 < ke ? ar[k + 1] : 0.f;
+            a4.z = k + 2 < ke ? ar[k + 2] : 0.f;
+            a4.w = k + 3 < ke ? ar[k + 3] : 0.f;
           }
         }
-        *reinterpret_cast<float4 *>(&ws[o][k4]) = w;
+        wr[4 * it] = a4.x;
+        wr[4 * it + 1] = a4.y;
+        wr[4 * it + 2] = a4.z;
+        wr[4 * it + 3] = a4.w;
       }
     } else {
-      for (int i = t; i < 64 * 64; i += 256) {  // W tile from B rows (r contiguous floats)
-        const int kk = i >> 6, o = i & 63;
+#pragma unroll
+      for (int it = 0; it < 16; ++it) {  // W[o][kk] = B_seg[k - off, j], o = seg r + j
+        const int i = t + 128 * it, o = i >> 5, kk = i & 31;
         const int k = k0 + kk;
         float v = 0.f;
         if (o < nout && k < ke) {
-          const int seg = o / L.r;
-          if (k >= L.off[seg] && k < L.off[seg] + L.n[seg])
-            v = L.B[seg][(size_t)(k - L.off[seg]) * L.r + (o % L.r)];
+          const int sg = o / L.r;
+          if (k >= L.off[sg] && k < L.off[sg] + L.n[sg]) v = L.B[sg][(size_t)(k - L.off[sg]) * L.r + (o % L.r)];
         }
-        ws[o][kk] = v;
+        wr[it] = v;
       }
     }
+  };
+  auto store = [&]() {
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {  // 16-bit values are exact in TF32
+      const int i = t + 128 * it, rr = i >> 2, c8 = (i & 3) * 8;
+      const uint4 u4 = xr[it];
+      const uint32_t wv[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        xs[rr][c8 + 2 * e] = __float_as_uint(lo16<XF16>(wv[e]));
+        xs[rr][c8 + 2 * e + 1] = __float_as_uint(hi16<XF16>(wv[e]));
+      }
+    }
+    if (!DU) {
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int i = t + 128 * it, o = i >> 3, k4 = (i & 7) * 4;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) ws[o][k4 + e] = to_tf32(wr[4 * it + e]);
+      }
+    } else {
+#pragma unroll
+      for (int it = 0; it < 16; ++it) {
+        const int i = t + 128 * it;
+        ws[i >> 5][i & 31] = to_tf32(wr[it]);
+      }
+    }
+  };
+  float acc[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+  if (kb < ke) load(kb);
+  for (int k0 = kb; k0 < ke; k0 += 32) {
+    store();
     __syncthreads();
-#pragma unroll 4
-    for (int kk = 0; kk < 64; kk += 4) {
-      float4 a[4], w[4];
+    if (k0 + 32 < ke) load(k0 + 32);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4 *>(&xs[ty * 4 + i][kk]);
+    for (int k8 = 0; k8 < 32; k8 += 8) {
+      const uint32_t a[4] = {xs[16 * w + g][k8 + q], xs[16 * w + g + 8][k8 + q], xs[16 * w + g][k8 + q + 4],
+                             xs[16 * w + g + 8][k8 + q + 4]};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) w[j] = *reinterpret_cast<const float4 *>(&ws[tx + 16 * j][kk]);
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          acc[i][j] = fmaf(a[i].x, w[j].x, acc[i][j]);
-          acc[i][j] = fmaf(a[i].y, w[j].y, acc[i][j]);
-          acc[i][j] = fmaf(a[i].z, w[j].z, acc[i][j]);
-          acc[i][j] = fmaf(a[i].w, w[j].w, acc[i][j]);
-        }
+      for (int nt = 0; nt < 8; ++nt)
+        if (nt < NT) mma_tf32(acc[nt], a, ws[8 * nt + g][k8 + q], ws[8 * nt + g][k8 + q + 4]);
     }
     __syncthreads();
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int m = m0 + ty * 4 + i;
-    if (m >= M) continue;
-    float *dst = part + ((size_t)blockIdx.y * M + m) * 64;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) dst[tx + 16 * j] = acc[i][j];
+  for (int nt = 0; nt < 8; ++nt) {
+    if (nt >= NT) break;
+    const int m = m0 + 16 * w + g, o = 8 * nt + 2 * q;
+    if (m < M) {
+      float *d = part + ((size_t)blockIdx.y * M + m) * 64 + o;
+      d[0] = acc[nt][0];
+      d[1] = acc[nt][1];
+    }
+    if (m + 8 < M) {
+      float *d = part + ((size_t)blockIdx.y * M + m + 8) * 64 + o;
+      d[0] = acc[nt][2];
+      d[1] = acc[nt][3];
+    }
   }
 }
 
@@ -344,68 +400,105 @@ __global__ void lora_reduce_kernel(const float *part, int nsplit, int M, const L
 }
 
 // dB partials: part[ms][n][j] = sum over the block's rows m of dY[m, n] u[m, seg(n) r + j].
-// 256 threads x 2 adjacent columns; rows in chunks of 32 with u staged in shared memory.
-template <bool F16, int RMAX>
-__global__ void __launch_bounds__(256) lora_dB_part_kernel(const uint16_t *dy, int ldy, int M,
+// D[n, j] = sum_m dY^T[n, m] u[m, j]: tile 64 n x r per 128-thread block (warp w: n rows
+// 16w..16w+15), rows m in chunks of 32 staged in shared memory.  A tile that straddles a
+// segment boundary runs once per segment with the other segment's rows masked.
+template <bool F16>
+__global__ void __launch_bounds__(128) lora_dB_part_kernel(const uint16_t *dy, int ldy, int M,
                                                            int Ng, int MC, const float *u,
                                                            const LoraSeg L, float *part) {
-  __shared__ float us[32][64];
-  const int t = threadIdx.x;
-  const int n = blockIdx.x * 512 + 2 * t;
+  __shared__ uint32_t ds[32][72];  // [m][n]
+  __shared__ uint32_t us[32][72];  // [m][o], o < nout
+  const int t = threadIdx.x, w = t >> 5, lane = t & 31, g = lane >> 2, q = lane & 3;
+  const int n0 = blockIdx.x * 64;
   const int mb = blockIdx.y * MC, me = min(M, mb + MC);
   const int nout = L.nseg * L.r;
-  int s0 = 0, s1 = 0;
-  for (int p = 0; p < L.nseg; ++p) {
-    if (n >= L.off[p] && n < L.off[p] + L.n[p]) s0 = p;
-    if (n + 1 >= L.off[p] && n + 1 < L.off[p] + L.n[p]) s1 = p;
-  }
-  const int b0 = s0 * L.r, b1 = s1 * L.r;
-  float a0[RMAX], a1[RMAX];
+  const int JT = (L.r + 7) / 8;
+  const int s_lo = seg_of(L, n0), s_hi = seg_of(L, min(n0 + 63, Ng - 1));
+  const int na = n0 + 16 * w + g, nb = na + 8;  // this lane's two rows
+  // the next chunk's operands are fetched into registers while the current one is computed
+  uint4 dr[2];
+  float ur[16];
+  auto load = [&](int m0) {
 #pragma unroll
-  for (int j = 0; j < RMAX; ++j) a0[j] = a1[j] = 0.f;
-  const bool pair = (n + 1 < Ng) && ((ldy & 1) == 0);
-  for (int m0 = mb; m0 < me; m0 += 32) {
-    for (int i = t; i < 32 * 64; i += 256) {
-      const int rr = i >> 6, o = i & 63;
+    for (int it = 0; it < 2; ++it) {  // dY: 32 m x 64 n, 8 elements per item
+      const int i = t + 128 * it, rr = i >> 3, c8 = (i & 7) * 8;
+      const int m = m0 + rr, n = n0 + c8;
+      if (m < me && n + 8 <= Ng && ((ldy | n) & 7) == 0) {
+        dr[it] = *reinterpret_cast<const uint4 *>(dy + (size_t)m * ldy + n);
+      } else {
+        uint32_t h[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) h[e] = (m < me && n + e < Ng) ? dy[(size_t)m * ldy + n + e] : 0u;
+        dr[it] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+      }
+    }
+#pragma unroll
+    for (int it = 0; it < 16; ++it) {  // u: 32 m x 64 o
+      const int i = t + 128 * it, rr = i >> 6, o = i & 63;
       const int m = m0 + rr;
-      us[rr][o] = (m < me && o < nout) ? u[(size_t)m * nout + o] : 0.f;
+      ur[it] = (m < me && o < nout) ? u[(size_t)m * nout + o] : 0.f;
+    }
+  };
+  float acc[3][4];
+#pragma unroll
+  for (int i = 0; i < 3; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+  if (mb < me) load(mb);
+  for (int m0 = mb; m0 < me; m0 += 32) {
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+      const int i = t + 128 * it, rr = i >> 3, c8 = (i & 7) * 8;
+      const uint32_t wv[4] = {dr[it].x, dr[it].y, dr[it].z, dr[it].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        ds[rr][c8 + 2 * e] = __float_as_uint(lo16<F16>(wv[e]));
+        ds[rr][c8 + 2 * e + 1] = __float_as_uint(hi16<F16>(wv[e]));
+      }
+    }
+#pragma unroll
+    for (int it = 0; it < 16; ++it) {
+      const int i = t + 128 * it;
+      us[i >> 6][i & 63] = to_tf32(ur[it]);
     }
     __syncthreads();
-    if (n < Ng) {
-      const int rows = min(32, me - m0);
-      for (int rr = 0; rr < rows; ++rr) {
-        const uint16_t *row = dy + (size_t)(m0 + rr) * ldy + n;
-        float y0, y1;
-        if (pair) {
-          const uint32_t v = *reinterpret_cast<const uint32_t *>(row);
-          y0 = lo16<F16>(v);
-          y1 = hi16<F16>(v);
-        } else {
-          y0 = ld16<F16>(row[0]);
-          y1 = n + 1 < Ng ? ld16<F16>(row[1]) : 0.f;
-        }
+    if (m0 + 32 < me) load(m0 + 32);
+    for (int sg = s_lo; sg <= s_hi; ++sg) {
+      const bool ina = na < Ng && seg_of(L, na) == sg, inb = nb < Ng && seg_of(L, nb) == sg;
 #pragma unroll
-        for (int j = 0; j < RMAX; ++j) {
-          if (j < L.r) {
-            a0[j] = fmaf(y0, us[rr][b0 + j], a0[j]);
-            a1[j] = fmaf(y1, us[rr][b1 + j], a1[j]);
-          }
+      for (int k8 = 0; k8 < 32; k8 += 8) {
+        const uint32_t a[4] = {ina ? ds[k8 + q][na - n0] : 0u, inb ? ds[k8 + q][nb - n0] : 0u,
+                               ina ? ds[k8 + q + 4][na - n0] : 0u, inb ? ds[k8 + q + 4][nb - n0] : 0u};
+#pragma unroll
+        for (int jt = 0; jt < 3; ++jt) {
+          if (jt >= JT) break;
+          const int j = 8 * jt + g;
+          const uint32_t b0 = j < L.r ? us[k8 + q][sg * L.r + j] : 0u;
+          const uint32_t b1 = j < L.r ? us[k8 + q + 4][sg * L.r + j] : 0u;
+          mma_tf32(acc[jt], a, b0, b1);
         }
       }
     }
     __syncthreads();
   }
-  if (n >= Ng) return;
-  float *d0 = part + ((size_t)blockIdx.y * Ng + n) * L.r;
 #pragma unroll
-  for (int j = 0; j < RMAX; ++j)
-    if (j < L.r) {
-      d0[j] = a0[j];
-      if (n + 1 < Ng) d0[L.r + j] = a1[j];
+  for (int jt = 0; jt < 3; ++jt) {
+    if (jt >= JT) break;
+    const int j = 8 * jt + 2 * q;
+    if (na < Ng) {
+      float *d = part + ((size_t)blockIdx.y * Ng + na) * L.r;
+      if (j < L.r) d[j] = acc[jt][0];
+      if (j + 1 < L.r) d[j + 1] = acc[jt][1];
     }
+    if (nb < Ng) {
+      float *d = part + ((size_t)blockIdx.y * Ng + nb) * L.r;
+      if (j < L.r) d[j] = acc[jt][2];
+      if (j + 1 < L.r) d[j + 1] = acc[jt][3];
+    }
+  }
 }
 
 __global__ void lora_dB_reduce_kernel(const float *part, int msplit, int Ng, const LoraSeg L) {
+  pdl_wait();  // launched as a dependent of the partial kernel
   const int64_t total = (int64_t)Ng * L.r;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
        idx += (int64_t)gridDim.x * blockDim.x) {
@@ -419,61 +512,100 @@ __global__ void lora_dB_reduce_kernel(const float *part, int msplit, int Ng, con
   }
 }
 
-// dA partials: part[ms][o][k] = sum over the block's rows m of du[m, o] x[m, k]; 128 threads
-// x 2 adjacent columns, 16 outputs per block (blockIdx.z picks them).
-template <bool F16>
+// dA partials: part[ms][o][k] = sum over the block's rows m of du[m, o] x[m, k].
+// D[o, k] = sum_m du^T[o, m] x[m, k]: OT 16-row output tiles (OT = ceil(nout / 16)) x KW
+// features per 128-thread block (warp w: output tile w % OT, features (w / OT) * 64 .. + 64),
+// rows m in chunks of 32 staged in shared memory.
+template <bool F16, int OT>
 __global__ void __launch_bounds__(128) lora_dA_part_kernel(const float *du, const uint16_t *x, int ldx,
                                                            int M, int K, int MC, int nout,
                                                            float *part) {
-  __shared__ float ds[32][16];
-  const int t = threadIdx.x;
-  const int k = blockIdx.x * 256 + 2 * t;
+  constexpr int KW = (4 / OT) * 64;
+  constexpr int DN = OT * 16 * 32 / 128;  // du values per thread and chunk
+  constexpr int XN = KW / 32;             // 8-element x items per thread and chunk
+  __shared__ uint32_t dus[32][OT * 16 + 8];  // [m][o]
+  __shared__ uint32_t xs[32][KW + 8];        // [m][k]
+  const int t = threadIdx.x, w = t >> 5, lane = t & 31, g = lane >> 2, q = lane & 3;
+  const int ot = w % OT, kg = w / OT;
+  const int k0 = blockIdx.x * KW;
   const int mb = blockIdx.y * MC, me = min(M, mb + MC);
-  const int o0 = blockIdx.z * 16;
-  float a0[16], a1[16];
+  // the next chunk's operands are fetched into registers while the current one is computed
+  float dr[DN];
+  uint4 xr[XN];
+  auto load = [&](int m0) {
 #pragma unroll
-  for (int c = 0; c < 16; ++c) a0[c] = a1[c] = 0.f;
-  const bool pair = (k + 1 < K) && ((ldx & 1) == 0);
-  for (int m0 = mb; m0 < me; m0 += 32) {
-    for (int i = t; i < 32 * 16; i += 128) {
-      const int rr = i >> 4, c = i & 15;
+    for (int it = 0; it < DN; ++it) {
+      const int i = t + 128 * it, rr = i / (OT * 16), o = i % (OT * 16);
       const int m = m0 + rr;
-      ds[rr][c] = (m < me && o0 + c < nout) ? du[(size_t)m * nout + o0 + c] : 0.f;
+      dr[it] = (m < me && o < nout) ? du[(size_t)m * nout + o] : 0.f;
+    }
+#pragma unroll
+    for (int it = 0; it < XN; ++it) {  // x: 32 m x KW k, 8 elements per item
+      const int i = t + 128 * it, rr = i / (KW / 8), c8 = (i % (KW / 8)) * 8;
+      const int m = m0 + rr, k = k0 + c8;
+      if (m < me && k + 8 <= K && ((ldx | k) & 7) == 0) {
+        xr[it] = *reinterpret_cast<const uint4 *>(x + (size_t)m * ldx + k);
+      } else {
+        uint32_t h[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) h[e] = (m < me && k + e < K) ? x[(size_t)m * ldx + k + e] : 0u;
+        xr[it] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+      }
+    }
+  };
+  float acc[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+  if (mb < me) load(mb);
+  for (int m0 = mb; m0 < me; m0 += 32) {
+#pragma unroll
+    for (int it = 0; it < DN; ++it) {
+      const int i = t + 128 * it;
+      dus[i / (OT * 16)][i % (OT * 16)] = to_tf32(dr[it]);
+    }
+#pragma unroll
+    for (int it = 0; it < XN; ++it) {
+      const int i = t + 128 * it, rr = i / (KW / 8), c8 = (i % (KW / 8)) * 8;
+      const uint32_t wv[4] = {xr[it].x, xr[it].y, xr[it].z, xr[it].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        xs[rr][c8 + 2 * e] = __float_as_uint(lo16<F16>(wv[e]));
+        xs[rr][c8 + 2 * e + 1] = __float_as_uint(hi16<F16>(wv[e]));
+      }
     }
     __syncthreads();
-    if (k < K) {
-      const int rows = min(32, me - m0);
-      for (int rr = 0; rr < rows; ++rr) {
-        const uint16_t *row = x + (size_t)(m0 + rr) * ldx + k;
-        float x0, x1;
-        if (pair) {
-          const uint32_t v = *reinterpret_cast<const uint32_t *>(row);
-          x0 = lo16<F16>(v);
-          x1 = hi16<F16>(v);
-        } else {
-          x0 = ld16<F16>(row[0]);
-          x1 = k + 1 < K ? ld16<F16>(row[1]) : 0.f;
-        }
+    if (m0 + 32 < me) load(m0 + 32);
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          a0[c] = fmaf(ds[rr][c], x0, a0[c]);
-          a1[c] = fmaf(ds[rr][c], x1, a1[c]);
-        }
+    for (int k8 = 0; k8 < 32; k8 += 8) {
+      const int oa = 16 * ot + g;
+      const uint32_t a[4] = {dus[k8 + q][oa], dus[k8 + q][oa + 8], dus[k8 + q + 4][oa], dus[k8 + q + 4][oa + 8]};
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        const int kc = kg * 64 + 8 * nt + g;
+        mma_tf32(acc[nt], a, xs[k8 + q][kc], xs[k8 + q + 4][kc]);
       }
     }
     __syncthreads();
   }
-  if (k >= K) return;
+  const int oa = 16 * ot + g;
 #pragma unroll
-  for (int c = 0; c < 16; ++c) {
-    if (o0 + c >= nout) break;
-    float *d = part + ((size_t)blockIdx.y * nout + o0 + c) * K + k;
-    d[0] = a0[c];
-    if (k + 1 < K) d[1] = a1[c];
+  for (int nt = 0; nt < 8; ++nt) {
+    const int k = k0 + kg * 64 + 8 * nt + 2 * q;
+    if (oa < nout) {
+      float *d = part + ((size_t)blockIdx.y * nout + oa) * K;
+      if (k < K) d[k] = acc[nt][0];
+      if (k + 1 < K) d[k + 1] = acc[nt][1];
+    }
+    if (oa + 8 < nout) {
+      float *d = part + ((size_t)blockIdx.y * nout + oa + 8) * K;
+      if (k < K) d[k] = acc[nt][2];
+      if (k + 1 < K) d[k + 1] = acc[nt][3];
+    }
   }
 }
 
 __global__ void lora_dA_reduce_kernel(const float *part, int msplit, int K, const LoraSeg L) {
+  pdl_wait();  // launched as a dependent of the partial kernel
   const int nout = L.nseg * L.r;
   const int64_t total = (int64_t)nout * K;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
@@ -678,25 +810,32 @@ void k_swiglu_bwd(const float *dact, const uint16_t *gu, int M, int I, uint16_t 
   count_launches(1);
 }
 
+// Splits of the LoRA reductions: enough 128-thread blocks to keep several resident per SM
+// (they are latency-bound), while the float partials stay well below the operand traffic.
 int lora_splits(int M, int K, int *KS) {
   const int rb = cdiv(M, 64);
-  int want = std::max(1, cdiv(296, rb));
-  want = std::min(want, cdiv(K, 64));
+  int want = std::max(1, cdiv(148 * 8, rb));
+  want = std::min(want, std::max(1, cdiv(K, 128)));
   int ks = cdiv(cdiv(K, want), 64) * 64;
   if (KS) *KS = ks;
   return cdiv(K, ks);
 }
-// Row split of the gradient reductions: about two waves of blocks in total.
+// Row split of the gradient reductions: several blocks per SM; at most one split per 128 rows
+// so that the float partials stay below the 16-bit operand traffic.
 static int lora_msplit(int M, int col_blocks, int *MC) {
-  int ms = std::max(1, std::min(cdiv(296, col_blocks), cdiv(M, 32)));
+  int ms = std::max(1, std::min(cdiv(148 * 8, col_blocks), cdiv(M, 128)));
   int mc = cdiv(cdiv(M, ms), 32) * 32;
   if (MC) *MC = mc;
   return cdiv(M, mc);
 }
+static int da_ot(int nout) { return nout <= 16 ? 1 : nout <= 32 ? 2 : 4; }
+static int da_kw(int nout) { return (4 / da_ot(nout)) * 64; }
 size_t lora_scratch_floats(int M, int dim, int nout) {
   const size_t proj = (size_t)lora_splits(M, dim, nullptr) * M * 64;
-  const size_t db = (size_t)lora_msplit(M, cdiv(dim, 512), nullptr) * dim * nout;
-  const size_t da = (size_t)lora_msplit(M, cdiv(dim, 256) * cdiv(nout, 16), nullptr) * dim * nout;
+  const size_t db = (size_t)lora_msplit(M, cdiv(dim, 64), nullptr) * dim * nout;
+  size_t da = 0;
+  for (int n = 16; n <= 64; n += 16)  // any output count up to nout
+    if (n - 16 < nout) da = std::max(da, (size_t)lora_msplit(M, cdiv(dim, da_kw(n)), nullptr) * dim * nout);
   return std::max(proj, std::max(db, da));
 }
 
@@ -707,8 +846,8 @@ static void lora_proj(const uint16_t *X, int ldx, int M, int K, const LoraSeg &L
   int KS;
   const int ns = lora_splits(M, K, &KS);
   dim3 grid(cdiv(M, 64), ns);
-  if (x_f16) lora_part_kernel<DU, true><<<grid, 256, 0, st>>>(X, ldx, M, K, KS, L, part);
-  else lora_part_kernel<DU, false><<<grid, 256, 0, st>>>(X, ldx, M, K, KS, L, part);
+  if (x_f16) lora_part_kernel<DU, true><<<grid, 128, 0, st>>>(X, ldx, M, K, KS, L, part);
+  else lora_part_kernel<DU, false><<<grid, 128, 0, st>>>(X, ldx, M, K, KS, L, part);
   const int64_t n = (int64_t)M * L.Rpad() * 32;  // one warp per output
   if (o_f16) launch_pdl(lora_reduce_kernel<DU, true>, dim3(grid_for(n, 256)), dim3(256), 0, st, part, ns, M, L, out_f32, out16);
   else launch_pdl(lora_reduce_kernel<DU, false>, dim3(grid_for(n, 256)), dim3(256), 0, st, part, ns, M, L, out_f32, out16);
@@ -727,35 +866,37 @@ void k_lora_du(const uint16_t *dy, int ldy, int M, const LoraSeg &L, float *du_f
                bool dy_f16, bool dul_f16, float *part, cudaStream_t st) {
   lora_proj<true>(dy, ldy, M, seg_cols(L), L, du_f32, dul, dy_f16, dul_f16, part, st);
 }
-template <bool F16>
-static void dB_launch(const uint16_t *dy, int ldy, int M, int Ng, int MC, int ms, const float *u,
-                      const LoraSeg &L, float *part, cudaStream_t st) {
-  dim3 grid(cdiv(Ng, 512), ms);
-  if (L.r <= 8) lora_dB_part_kernel<F16, 8><<<grid, 256, 0, st>>>(dy, ldy, M, Ng, MC, u, L, part);
-  else if (L.r <= 16) lora_dB_part_kernel<F16, 16><<<grid, 256, 0, st>>>(dy, ldy, M, Ng, MC, u, L, part);
-  else lora_dB_part_kernel<F16, 32><<<grid, 256, 0, st>>>(dy, ldy, M, Ng, MC, u, L, part);
-}
 void k_lora_dB(const uint16_t *dy, int ldy, int M, const float *u_f32, const LoraSeg &L, bool dy_f16,
                float *part, cudaStream_t st) {
   if (M <= 0) return;
   const int Ng = seg_cols(L);
   int MC;
-  const int ms = lora_msplit(M, cdiv(Ng, 512), &MC);
-  if (dy_f16) dB_launch<true>(dy, ldy, M, Ng, MC, ms, u_f32, L, part, st);
-  else dB_launch<false>(dy, ldy, M, Ng, MC, ms, u_f32, L, part, st);
-  lora_dB_reduce_kernel<<<grid_for((int64_t)Ng * L.r, 256), 256, 0, st>>>(part, ms, Ng, L);
+  const int ms = lora_msplit(M, cdiv(Ng, 64), &MC);
+  dim3 grid(cdiv(Ng, 64), ms);
+  if (dy_f16) lora_dB_part_kernel<true><<<grid, 128, 0, st>>>(dy, ldy, M, Ng, MC, u_f32, L, part);
+  else lora_dB_part_kernel<false><<<grid, 128, 0, st>>>(dy, ldy, M, Ng, MC, u_f32, L, part);
+  launch_pdl(lora_dB_reduce_kernel, dim3(grid_for((int64_t)Ng * L.r, 256)), dim3(256), 0, st, part, ms, Ng, L);
   count_launches(2);
+}
+template <int OT>
+static void dA_launch(const float *du, const uint16_t *x, int lda, int M, int K, int MC, int ms,
+                      int nout, bool x_f16, float *part, cudaStream_t st) {
+  dim3 grid(cdiv(K, (4 / OT) * 64), ms);
+  if (x_f16) lora_dA_part_kernel<true, OT><<<grid, 128, 0, st>>>(du, x, lda, M, K, MC, nout, part);
+  else lora_dA_part_kernel<false, OT><<<grid, 128, 0, st>>>(du, x, lda, M, K, MC, nout, part);
 }
 void k_lora_dA(const float *du_f32, const uint16_t *x, int lda, int M, int K, const LoraSeg &L,
                bool x_f16, float *part, cudaStream_t st) {
   if (M <= 0) return;
   const int nout = L.nseg * L.r;
   int MC;
-  const int ms = lora_msplit(M, cdiv(K, 256) * cdiv(nout, 16), &MC);
-  dim3 grid(cdiv(K, 256), ms, cdiv(nout, 16));
-  if (x_f16) lora_dA_part_kernel<true><<<grid, 128, 0, st>>>(du_f32, x, lda, M, K, MC, nout, part);
-  else lora_dA_part_kernel<false><<<grid, 128, 0, st>>>(du_f32, x, lda, M, K, MC, nout, part);
-  lora_dA_reduce_kernel<<<grid_for((int64_t)nout * K, 256), 256, 0, st>>>(part, ms, K, L);
+  const int ms = lora_msplit(M, cdiv(K, da_kw(nout)), &MC);
+  switch (da_ot(nout)) {
+    case 1: dA_launch<1>(du_f32, x, lda, M, K, MC, ms, nout, x_f16, part, st); break;
+    case 2: dA_launch<2>(du_f32, x, lda, M, K, MC, ms, nout, x_f16, part, st); break;
+    default: dA_launch<4>(du_f32, x, lda, M, K, MC, ms, nout, x_f16, part, st); break;
+  }
+  launch_pdl(lora_dA_reduce_kernel, dim3(grid_for((int64_t)nout * K, 256)), dim3(256), 0, st, part, ms, K, L);
   count_launches(2);
 }
 void k_pack_fwd(const LoraSeg &L, int Ng, uint16_t *vl, bool f16, cudaStream_t st) {

@@ -50,6 +50,13 @@ def _h16(x):
     return np.asarray(x, np.float32).astype(np.float16).astype(np.float32)
 
 
+def _tf32(x):
+    """float32 -> TF32 (10 explicit mantissa bits; nearest, ties away from zero), as float64."""
+    b = np.asarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    b = ((b + 0x1000) & 0xFFFFE000).astype(np.uint32)
+    return b.view(np.float32).astype(np.float64)
+
+
 def _rel_l2(a, b):
     a = np.asarray(a, np.float64)
     b = np.asarray(b, np.float64)
@@ -223,13 +230,22 @@ def test_proj_lora_grad(api, M, N, K, f16):
     api.proj_lora_grad(_dev(x_in), _dev(dy_bits), M, N, K, _dev(A), _dev(B), r, s, dA, dB, scratch,
                        x_f16=f16)
     torch.cuda.synchronize()
+    # exact-operand reference: the 16-bit x and dY are exact in TF32; the float operands A, B,
+    # u = x A^T and du = s dY B are rounded to TF32 where the kernels stage them
     xf = (_h16(x32) if f16 else x32).astype(np.float64)
     dyf = nf4.bf16_to_f32(dy_bits).astype(np.float64)
-    u = xf @ A.T.astype(np.float64)
-    want_dB = s * dyf.T @ u
-    want_dA = s * (dyf @ B.astype(np.float64)).T @ xf
-    assert _rel_l2(dB.cpu().numpy(), want_dB) < 1e-5
-    assert _rel_l2(dA.cpu().numpy(), want_dA) < 1e-5
+    u = xf @ _tf32(A).T
+    du = s * (dyf @ _tf32(B))
+    want_dB = s * dyf.T @ _tf32(u)
+    want_dA = _tf32(du).T @ xf
+    # 2e-4: u and du are float intermediates whose last bits depend on the tensor core's
+    # accumulation order, so an element near a TF32 rounding boundary may round the other way
+    # than in this model (one TF32 step, 2^-11, on that element)
+    assert _rel_l2(dB.cpu().numpy(), want_dB) < 2e-4
+    assert _rel_l2(dA.cpu().numpy(), want_dA) < 2e-4
+    # and the unrounded product, to the step's gradient bar
+    assert _rel_l2(dB.cpu().numpy(), s * dyf.T @ (xf @ A.T.astype(np.float64))) < 2e-3
+    assert _rel_l2(dA.cpu().numpy(), s * (dyf @ B.astype(np.float64)).T @ xf) < 2e-3
 
 
 @pytest.mark.parametrize("f16", [True, False])
