@@ -16,8 +16,9 @@
 // Error flags written by kernels into a device int (bitwise OR).
 enum : int { SOUP_KERR_WAIT_TIMEOUT = 1, SOUP_KERR_BAD_ARG = 2 };
 
-// ~2 s at 2 GHz: far beyond any legitimate wait in these kernels.
-#define SOUP_WAIT_CYCLES (4000000000ll)
+// ~0.2 s at 2 GHz: far beyond any legitimate wait in these kernels (the longest, a CTA's
+// whole main loop before its epilogue, is well under a millisecond).
+#define SOUP_WAIT_CYCLES (400000000ll)
 
 namespace soupk {
 

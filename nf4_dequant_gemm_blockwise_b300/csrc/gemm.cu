@@ -107,13 +107,16 @@ SOUP_DEV void dq_block64(const float *cb, const uint32_t (&cw)[8], float a, uint
 #pragma unroll
   for (int w = 0; w < 8; ++w) {
     const uint32_t x = cw[w];
+    // selectors of the eight codes of this word (a byte holds even code << 4 | odd code):
+    // the low three bits pick a byte of a register pair, bit 3 picks the pair (+4); byte
+    // permutes read the low 16 bits of a selector, so the upper half is shifted down
+    const uint32_t x7 = x & 0x77777777u;
+    const uint32_t pk = ((x >> 1) & 0x44444444u) | 0x32103210u;
     uint32_t o[4];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      // four selectors = four codes; a byte holds (even code << 4 | odd code)
-      const uint32_t s = (x >> (16 * h)) & 0xFFFFu;
-      const uint32_t s7 = s & 0x7777u;
-      const uint32_t pick = ((s >> 1) & 0x4444u) | 0x3210u;  // +4 for codes 8..15
+      const uint32_t s7 = h ? x7 >> 16 : x7;
+      const uint32_t pick = h ? pk >> 16 : pk;
       const uint32_t lo = prmt(prmt(LO[0], LO[1], s7), prmt(LO[2], LO[3], s7), pick);
       const uint32_t hi = prmt(prmt(HI[0], HI[1], s7), prmt(HI[2], HI[3], s7), pick);
       o[2 * h] = prmt(lo, hi, 0x4051);      // (even, odd) code of byte 0 -> 16x2

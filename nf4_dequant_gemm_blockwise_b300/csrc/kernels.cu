@@ -47,60 +47,88 @@ __global__ void embed_kernel(const int32_t *tok, const uint16_t *E, int V, int H
 }
 
 // ------------------------------------------------------------------ RMSNorm
+// One row per 256-thread block: the row is read once into registers (up to RMS_V float4s per
+// thread, H <= 8192) and reused after the sum of squares; the block sum adds the eight warp
+// sums in warp order.
+constexpr int RMS_T = 256, RMS_V = 8;
+
+SOUP_DEV float block_sum256(float v, float *sh) {
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) sh[w] = v;
+  __syncthreads();
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < RMS_T / 32; ++i) s += sh[i];
+  __syncthreads();
+  return s;
+}
+
 template <bool F16>
-__global__ void rmsnorm_fwd_kernel(const float *h, const uint16_t *w, float eps, int M, int H,
-                                   uint16_t *out) {
-  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= M) return;
+__global__ void __launch_bounds__(RMS_T) rmsnorm_fwd_kernel(const float *h, const uint16_t *w, float eps,
+                                                            int M, int H, uint16_t *out) {
+  __shared__ float sh[RMS_T / 32];
+  const int row = blockIdx.x;
   const float *x = h + (size_t)row * H;
+  float4 v[RMS_V];
   float ss = 0.f;
-  for (int i = lane * 4; i < H; i += 128) {
-    const float4 v = *reinterpret_cast<const float4 *>(x + i);
-    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+#pragma unroll
+  for (int it = 0; it < RMS_V; ++it) {
+    const int i = (threadIdx.x + it * RMS_T) * 4;
+    v[it] = i < H ? *reinterpret_cast<const float4 *>(x + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    ss += v[it].x * v[it].x + v[it].y * v[it].y + v[it].z * v[it].z + v[it].w * v[it].w;
   }
-  ss = warp_sum(ss);
+  ss = block_sum256(ss, sh);
   const float r = 1.0f / sqrtf(ss / (float)H + eps);
   uint16_t *o = out + (size_t)row * H;
-  for (int i = lane * 4; i < H; i += 128) {
-    const float4 v = *reinterpret_cast<const float4 *>(x + i);
+#pragma unroll
+  for (int it = 0; it < RMS_V; ++it) {
+    const int i = (threadIdx.x + it * RMS_T) * 4;
+    if (i >= H) break;
     const uint2 wv = *reinterpret_cast<const uint2 *>(w + i);
     uint2 res;
-    res.x = pack16x2<F16>(v.x * r * bf16_lo(wv.x), v.y * r * bf16_hi(wv.x));
-    res.y = pack16x2<F16>(v.z * r * bf16_lo(wv.y), v.w * r * bf16_hi(wv.y));
+    res.x = pack16x2<F16>(v[it].x * r * bf16_lo(wv.x), v[it].y * r * bf16_hi(wv.x));
+    res.y = pack16x2<F16>(v[it].z * r * bf16_lo(wv.y), v[it].w * r * bf16_hi(wv.y));
     *reinterpret_cast<uint2 *>(o + i) = res;
   }
 }
 
-__global__ void rmsnorm_bwd_kernel(const float *dy, const float *h, const uint16_t *w, float eps,
-                                   int M, int H, const float *dres, float *out, uint16_t *out_bf16) {
-  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= M) return;
+__global__ void __launch_bounds__(RMS_T) rmsnorm_bwd_kernel(const float *dy, const float *h, const uint16_t *w,
+                                                            float eps, int M, int H, const float *dres,
+                                                            float *out, uint16_t *out_bf16) {
+  __shared__ float sh[RMS_T / 32];
+  const int row = blockIdx.x;
   const float *x = h + (size_t)row * H;
   const float *g = dy + (size_t)row * H;
+  float4 v[RMS_V], gw[RMS_V];  // x, and dy * w
   float ss = 0.f, sgh = 0.f;
-  for (int i = lane * 4; i < H; i += 128) {
-    const float4 v = *reinterpret_cast<const float4 *>(x + i);
-    const float4 d = *reinterpret_cast<const float4 *>(g + i);
-    const uint2 wv = *reinterpret_cast<const uint2 *>(w + i);
-    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-    sgh += d.x * bf16_lo(wv.x) * v.x + d.y * bf16_hi(wv.x) * v.y + d.z * bf16_lo(wv.y) * v.z +
-           d.w * bf16_hi(wv.y) * v.w;
+#pragma unroll
+  for (int it = 0; it < RMS_V; ++it) {
+    const int i = (threadIdx.x + it * RMS_T) * 4;
+    if (i < H) {
+      v[it] = *reinterpret_cast<const float4 *>(x + i);
+      const float4 d = *reinterpret_cast<const float4 *>(g + i);
+      const uint2 wv = *reinterpret_cast<const uint2 *>(w + i);
+      gw[it] = make_float4(d.x * bf16_lo(wv.x), d.y * bf16_hi(wv.x), d.z * bf16_lo(wv.y), d.w * bf16_hi(wv.y));
+    } else {
+      v[it] = gw[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    ss += v[it].x * v[it].x + v[it].y * v[it].y + v[it].z * v[it].z + v[it].w * v[it].w;
+    sgh += gw[it].x * v[it].x + gw[it].y * v[it].y + gw[it].z * v[it].z + gw[it].w * v[it].w;
   }
-  ss = warp_sum(ss);
-  sgh = warp_sum(sgh);
+  ss = block_sum256(ss, sh);
+  sgh = block_sum256(sgh, sh);
   const float r = 1.0f / sqrtf(ss / (float)H + eps);
-  const float c = r * r * r * sgh / (float)H;  // dx = r*g - x * r^3 * sum(g*x) / H
+  const float c = r * r * r * sgh / (float)H;  // dx = r*g*w - x * r^3 * sum(g*w*x) / H
   float *o = out + (size_t)row * H;
   const float *dr = dres ? dres + (size_t)row * H : nullptr;
   uint16_t *ob = out_bf16 ? out_bf16 + (size_t)row * H : nullptr;
-  for (int i = lane * 4; i < H; i += 128) {
-    const float4 v = *reinterpret_cast<const float4 *>(x + i);
-    const float4 d = *reinterpret_cast<const float4 *>(g + i);
-    const uint2 wv = *reinterpret_cast<const uint2 *>(w + i);
-    float4 res = make_float4(r * d.x * bf16_lo(wv.x) - v.x * c, r * d.y * bf16_hi(wv.x) - v.y * c,
-                             r * d.z * bf16_lo(wv.y) - v.z * c, r * d.w * bf16_hi(wv.y) - v.w * c);
+#pragma unroll
+  for (int it = 0; it < RMS_V; ++it) {
+    const int i = (threadIdx.x + it * RMS_T) * 4;
+    if (i >= H) break;
+    float4 res = make_float4(r * gw[it].x - v[it].x * c, r * gw[it].y - v[it].y * c,
+                             r * gw[it].z - v[it].z * c, r * gw[it].w - v[it].w * c);
     if (dr) {
       const float4 a = *reinterpret_cast<const float4 *>(dr + i);
       res.x += a.x; res.y += a.y; res.z += a.z; res.w += a.w;
@@ -199,18 +227,38 @@ __global__ void swiglu_fwd_scalar_kernel(const uint16_t *gu, int M, int I, uint1
   }
 }
 
+// 8 consecutive columns per item (inter % 8 == 0): 32-byte dact loads, 16-byte gate / up loads
+// and dgu stores.
 template <bool F16>
 __global__ void swiglu_bwd_kernel(const float *dact, const uint16_t *gu, int M, int I, uint16_t *dgu) {
-  const int64_t total = (int64_t)M * I;
+  const int I8 = I / 8;
+  const int64_t total = (int64_t)M * I8;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
        idx += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t m = idx / I, j = idx % I;
-    const float g = ld16<F16>(gu[m * 2 * I + j]);
-    const float u = ld16<F16>(gu[m * 2 * I + I + j]);
-    const float da = dact[idx];
-    const float sg = sigmoidf_(g);
-    dgu[m * 2 * I + j] = f_to_bf16(da * u * (sg * (1.0f + g * (1.0f - sg))));
-    dgu[m * 2 * I + I + j] = f_to_bf16(da * g * sg);
+    const int64_t m = idx / I8, j = (idx % I8) * 8;
+    const uint4 gv = *reinterpret_cast<const uint4 *>(gu + m * 2 * I + j);
+    const uint4 uv = *reinterpret_cast<const uint4 *>(gu + m * 2 * I + I + j);
+    const float4 d0 = *reinterpret_cast<const float4 *>(dact + m * I + j);
+    const float4 d1 = *reinterpret_cast<const float4 *>(dact + m * I + j + 4);
+    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, uw[4] = {uv.x, uv.y, uv.z, uv.w};
+    const float da[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+    uint32_t og[4], ou[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float dg[2], du[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float g = h ? hi16<F16>(gw[e]) : lo16<F16>(gw[e]);
+        const float u = h ? hi16<F16>(uw[e]) : lo16<F16>(uw[e]);
+        const float sg = sigmoidf_(g);
+        dg[h] = da[2 * e + h] * u * (sg * (1.0f + g * (1.0f - sg)));
+        du[h] = da[2 * e + h] * g * sg;
+      }
+      og[e] = pack_bf16x2(dg[0], dg[1]);
+      ou[e] = pack_bf16x2(du[0], du[1]);
+    }
+    *reinterpret_cast<uint4 *>(dgu + m * 2 * I + j) = make_uint4(og[0], og[1], og[2], og[3]);
+    *reinterpret_cast<uint4 *>(dgu + m * 2 * I + I + j) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
   }
 }
 
@@ -762,14 +810,14 @@ void k_embed(const int32_t *tok, const uint16_t *E, int V, int H, int M, float *
 void k_rmsnorm_fwd(const float *h, const uint16_t *w, float eps, int M, int H, uint16_t *out,
                    bool out_f16, cudaStream_t st) {
   if (M <= 0) return;
-  if (out_f16) rmsnorm_fwd_kernel<true><<<cdiv(M, 2), 64, 0, st>>>(h, w, eps, M, H, out);
-  else rmsnorm_fwd_kernel<false><<<cdiv(M, 2), 64, 0, st>>>(h, w, eps, M, H, out);
+  if (out_f16) rmsnorm_fwd_kernel<true><<<M, RMS_T, 0, st>>>(h, w, eps, M, H, out);
+  else rmsnorm_fwd_kernel<false><<<M, RMS_T, 0, st>>>(h, w, eps, M, H, out);
   count_launches(1);
 }
 void k_rmsnorm_bwd(const float *dy, const float *h, const uint16_t *w, float eps, int M, int H,
                    const float *dres, float *out, uint16_t *out_bf16, cudaStream_t st) {
   if (M <= 0) return;
-  rmsnorm_bwd_kernel<<<cdiv(M, 2), 64, 0, st>>>(dy, h, w, eps, M, H, dres, out, out_bf16);
+  rmsnorm_bwd_kernel<<<M, RMS_T, 0, st>>>(dy, h, w, eps, M, H, dres, out, out_bf16);
   count_launches(1);
 }
 void k_rope_fwd(uint16_t *qkv, int ld, const float *cos, const float *sin, int M, int S, int nh,
@@ -805,8 +853,9 @@ void k_swiglu_bwd(const float *dact, const uint16_t *gu, int M, int I, uint16_t 
                   cudaStream_t st) {
   const int64_t n = (int64_t)M * I;
   if (n <= 0) return;
-  if (gu_f16) swiglu_bwd_kernel<true><<<grid_for(n, 256), 256, 0, st>>>(dact, gu, M, I, dgu);
-  else swiglu_bwd_kernel<false><<<grid_for(n, 256), 256, 0, st>>>(dact, gu, M, I, dgu);
+  const int64_t n8 = n / 8;  // inter % 8 == 0 (checked with the configuration)
+  if (gu_f16) swiglu_bwd_kernel<true><<<grid_for(n8, 256), 256, 0, st>>>(dact, gu, M, I, dgu);
+  else swiglu_bwd_kernel<false><<<grid_for(n8, 256), 256, 0, st>>>(dact, gu, M, I, dgu);
   count_launches(1);
 }
 

@@ -132,6 +132,8 @@ int validate_cfg(const soup_cfg *c) {
     return set_error(SOUP_EINVAL, "cfg: head_dim must be 64 or 128");
   if (c->hidden % 64 || c->inter % 8)
     return set_error(SOUP_EINVAL, "cfg: hidden must be a multiple of 64 and inter of 8");
+  if (c->hidden > 8192)
+    return set_error(SOUP_EINVAL, "cfg: hidden must be at most 8192 (one row per norm block)");
   if (c->lora_r < 1 || 3 * c->lora_r > 64)
     return set_error(SOUP_EINVAL, "cfg: lora_r must be in [1, 21]");
   if (c->base_fmt != SOUP_FMT_BF16 && c->base_fmt != SOUP_FMT_NF4)
