@@ -32,6 +32,22 @@ METRIC = "streamed LoRA train tok/s (8B-shape NF4); dequant-GEMM % roofline; H2D
 UNIT = "tokens/s"
 
 
+def max_over_ranks(dist, values, device="cpu"):
+    """Entry-wise maximum over ranks (the slowest replica sets the job's step time)."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def job_tokens_per_s(world, tokens_per_rank, ms_per_step):
+    """Whole-job throughput: every rank steps its own replica over tokens_per_rank tokens, and
+    the job advances at the pace of the slowest rank (ms_per_step = max over ranks)."""
+    return world * tokens_per_rank / (ms_per_step * 1e-3)
+
+
 def _args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -391,15 +407,10 @@ def run_ours(args, rank, world, local_rank, dist):
         sess_r.close()
 
     # ---- max over ranks
-    ms_step = ms_total / args.steps
-    ms_e2e_step = ms_e2e / args.steps
-    if dist is not None:
-        t = torch.tensor([ms_step, ms_e2e_step], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step, ms_e2e_step = float(t[0]), float(t[1])
+    ms_step, ms_e2e_step = max_over_ranks(dist, [ms_total / args.steps, ms_e2e / args.steps], "cuda")
     tokens = B * S
-    value = world * tokens / (ms_step * 1e-3)
-    e2e_value = world * tokens / (ms_e2e_step * 1e-3)
+    value = job_tokens_per_s(world, tokens, ms_step)
+    e2e_value = job_tokens_per_s(world, tokens, ms_e2e_step)
 
     # roofline of the NF4 dequant GEMMs (tensor-bound at this token count)
     gemm_tflops = st["gemm_flops"] / (st["gemm_ms"] * 1e-3) / 1e12 if st["gemm_ms"] else None
