@@ -696,6 +696,27 @@ int choose_splits(const GemmArgs &g, int bn) {
   return best;
 }
 
+// One or two 128-row m-tiles per CTA.  Two halve the dequantisation per flop (the NF4 kernel's
+// limit at one m-tile: ~900 cycles of byte-permute work per 256 x 64 B tile against 512 tensor
+// cycles per m-tile), at the cost of half as many CTAs: compare waves x per-k-tile time, the
+// one-m-tile side with its split-K choice.
+int choose_mtiles(const GemmArgs &g, int bn) {
+  const int64_t ntile = (g.Ng() + bn - 1) / bn;
+  const int kt = (g.Kg() + 63) / 64;
+  const bool nf4 = g.wfmt == W_NF4;
+  auto per_ktile = [&](int mt) {  // cycles of one k-tile: tensor vs dequantisation
+    const double tc = 512.0 * mt;
+    return nf4 ? std::max(tc, 900.0) : tc;
+  };
+  const int64_t c2 = (int64_t)((g.M + 255) / 256) * ntile;
+  const double t2 = (double)((c2 + 147) / 148) * kt * per_ktile(2);
+  const int s1 = (g.part && g.part_floats && g.splits_allowed) ? choose_splits(g, bn) : 1;
+  const int64_t c1 = (int64_t)((g.M + 127) / 128) * ntile * s1;
+  const double t1 = (double)((c1 + 147) / 148) * ((kt + s1 - 1) / s1) * per_ktile(1) +
+                    (s1 > 1 ? 2.0 * s1 * g.M * (double)g.Ng() * 4.0 / 6.0e12 * 1.9e9 : 0.0);
+  return (g.M > 128 && t2 < 0.95 * t1) ? 2 : 1;
+}
+
 int gemm_uses_tc(const GemmArgs &g) {
   if (g_force_fallback) return 0;
   const int Ng = g.Ng();
@@ -765,10 +786,7 @@ int gemm_launch(const GemmArgs &g, cudaStream_t st) {
   if (rc) return rc;
   constexpr int BN = 256;
   GemmArgs g2 = g;
-  // two m-tiles per CTA halve the dequantisation per flop; use them while the grid still
-  // covers at least two waves of the GPU
-  const int64_t ntile = (g.Ng() + BN - 1) / BN;
-  g2.mtiles = ((int64_t)((g.M + 255) / 256) * ntile >= 2 * 148) ? 2 : 1;
+  g2.mtiles = choose_mtiles(g, BN);
   g2.splits = g2.mtiles == 1 ? choose_splits(g, BN) : 1;
   if (g2.splits > 1 && g.splits_allowed == 0) g2.splits = 1;
   return gemm_launch_tc(g2, st);

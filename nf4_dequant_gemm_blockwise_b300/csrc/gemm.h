@@ -75,6 +75,8 @@ int gemm_launch(const GemmArgs &g, cudaStream_t stream);
 int gemm_uses_tc(const GemmArgs &g);
 // Split-K factor gemm_launch picks for this call (1 = none).
 int choose_splits(const GemmArgs &g, int bn);
+// 128-row m-tiles per CTA (1 or 2) gemm_launch picks for this call.
+int choose_mtiles(const GemmArgs &g, int bn);
 int gemm_launch_tc(const GemmArgs &g, cudaStream_t stream);
 // Force the fallback path (tests compare the two).
 void gemm_force_fallback(int on);

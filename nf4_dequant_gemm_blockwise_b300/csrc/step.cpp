@@ -560,6 +560,7 @@ int step_fwd(soup_stream *h, const int32_t *tokens, int B, int S, const float *c
                                   cudaMemcpyDeviceToDevice, st));
   SOUP_CUDA_TRY(cudaEventRecord(h->done, st));
   h->fwd_ready = 1;
+  h->last_layer_fresh = 1;  // the last layer's activations are still in the scratch buffers
   h->stats.steps_fwd += 1;
   return check_cuda("step_fwd");
 }
@@ -609,7 +610,11 @@ int step_bwd(soup_stream *h, float *const *dA, float *const *dB, float *dh_out) 
     const uint8_t *shard;
     int s;
     SOUP_TRY(acquire(h, seq, (size_t)j, &shard, &s));
-    SOUP_TRY(layer_forward(h, li, shard, true));
+    // the forward's last layer left its activations in the scratch buffers (the loss head
+    // between uses separate ones): its backward reuses them instead of recomputing them, which
+    // would reproduce the same values with the same kernels
+    if (!(j == 0 && h->last_layer_fresh)) SOUP_TRY(layer_forward(h, li, shard, true));
+    h->last_layer_fresh = 0;
     SOUP_TRY(layer_backward(h, li, shard));
     SOUP_TRY(release(h, s));
     if (!h->resident) SOUP_TRY(prefetch(h, seq, (size_t)j + 1, look - 1));

@@ -57,6 +57,7 @@ struct soup_stream {
   cudaEvent_t done = nullptr;
   // per-step state
   int B = 0, S = 0, fwd_ready = 0, in_bwd = 0;
+  int last_layer_fresh = 0;  // set by step_fwd: the last layer's activations are intact
   const int32_t *tokens = nullptr;
   std::vector<const float *> lora_A, lora_B;
   std::vector<float *> grad_A, grad_B;
