@@ -673,49 +673,42 @@ int tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t i
   return make_map(m, dt, base, inner, outer, row_bytes, box_inner, box_outer, sw, what);
 }
 
-// Split-K factor for an under-filled grid: minimise waves(tiles * s) / s plus the cost of
-// writing and re-reading s partial planes, within the partial buffer the caller provides.
-int choose_splits(const GemmArgs &g, int bn) {
-  if (!g.part || g.part_floats == 0) return 1;
-  const int64_t tiles = (int64_t)((g.M + 127) / 128) * ((g.Ng() + bn - 1) / bn);
+// Tiling of one call: m-tiles per CTA (1 or 2) and split-K factor (1..4), minimising a model
+// of waves x k-tiles per CTA x time per k-tile, plus the cost of writing and re-reading the
+// float partial planes.  Two m-tiles halve the dequantisation per flop: an NF4 k-tile costs
+// max(512 x MT tensor cycles, ~900 cycles of byte-permute work for the 256 x 64 B tile);
+// bf16 weights have no dequantisation.  Split-K needs the caller's partial buffer.
+struct Tiling {
+  int mt, s;
+};
+Tiling choose_tiling(const GemmArgs &g, int bn) {
+  const int64_t ntile = (g.Ng() + bn - 1) / bn;
   const int kt = (g.Kg() + 63) / 64;
-  const double t_ktile = 0.6e-6;                        // one 128 x 256 x 64 k-tile, seconds (measured)
-  const double bw = 6.0e12;                             // partial traffic (L2-resident), bytes / s
-  int best = 1;
-  double best_t = 1e30;
-  for (int s = 1; s <= 4; ++s) {
-    if (s > 1 && (kt / s < 4 || (double)s * g.M * g.Ng() > (double)g.part_floats)) break;
-    const int64_t waves = (tiles * s + 147) / 148;
-    const double t = (double)waves * ((kt + s - 1) / s) * t_ktile +
-                     (s > 1 ? 2.0 * s * g.M * (double)g.Ng() * 4.0 / bw : 0.0);
-    if (t < best_t * 0.97) {
-      best_t = t;
-      best = s;
+  const bool nf4 = g.wfmt == W_NF4;
+  const bool can_split = g.part && g.part_floats > 0 && g.splits_allowed;
+  const double cyc_per_s = 1.9e9, bw = 6.0e12;  // partial traffic (mostly L2-resident), bytes / s
+  Tiling best{1, 1};
+  double best_t = 1e300;
+  for (int mt = 1; mt <= 2; ++mt) {
+    if (mt == 2 && g.M <= 128) break;
+    const double per_ktile = nf4 ? std::max(512.0 * mt, 900.0) : 512.0 * mt;
+    const int64_t tiles = (int64_t)((g.M + 128 * mt - 1) / (128 * mt)) * ntile;
+    for (int s = 1; s <= 4; ++s) {
+      if (s > 1 && (!can_split || kt / s < 4 || (double)s * g.M * g.Ng() > (double)g.part_floats)) break;
+      const int64_t waves = (tiles * s + 147) / 148;
+      const double t = (double)waves * ((kt + s - 1) / s) * per_ktile +
+                       (s > 1 ? 2.0 * s * g.M * (double)g.Ng() * 4.0 / bw * cyc_per_s : 0.0);
+      if (t < best_t * 0.97) {  // a clear gain only: fewer CTAs, fewer partial planes first
+        best_t = t;
+        best = {mt, s};
+      }
     }
   }
   return best;
 }
 
-// One or two 128-row m-tiles per CTA.  Two halve the dequantisation per flop (the NF4 kernel's
-// limit at one m-tile: ~900 cycles of byte-permute work per 256 x 64 B tile against 512 tensor
-// cycles per m-tile), at the cost of half as many CTAs: compare waves x per-k-tile time, the
-// one-m-tile side with its split-K choice.
-int choose_mtiles(const GemmArgs &g, int bn) {
-  const int64_t ntile = (g.Ng() + bn - 1) / bn;
-  const int kt = (g.Kg() + 63) / 64;
-  const bool nf4 = g.wfmt == W_NF4;
-  auto per_ktile = [&](int mt) {  // cycles of one k-tile: tensor vs dequantisation
-    const double tc = 512.0 * mt;
-    return nf4 ? std::max(tc, 900.0) : tc;
-  };
-  const int64_t c2 = (int64_t)((g.M + 255) / 256) * ntile;
-  const double t2 = (double)((c2 + 147) / 148) * kt * per_ktile(2);
-  const int s1 = (g.part && g.part_floats && g.splits_allowed) ? choose_splits(g, bn) : 1;
-  const int64_t c1 = (int64_t)((g.M + 127) / 128) * ntile * s1;
-  const double t1 = (double)((c1 + 147) / 148) * ((kt + s1 - 1) / s1) * per_ktile(1) +
-                    (s1 > 1 ? 2.0 * s1 * g.M * (double)g.Ng() * 4.0 / 6.0e12 * 1.9e9 : 0.0);
-  return (g.M > 128 && t2 < 0.95 * t1) ? 2 : 1;
-}
+int choose_splits(const GemmArgs &g, int bn) { return choose_tiling(g, bn).s; }
+int choose_mtiles(const GemmArgs &g, int bn) { return choose_tiling(g, bn).mt; }
 
 int gemm_uses_tc(const GemmArgs &g) {
   if (g_force_fallback) return 0;
@@ -786,9 +779,9 @@ int gemm_launch(const GemmArgs &g, cudaStream_t st) {
   if (rc) return rc;
   constexpr int BN = 256;
   GemmArgs g2 = g;
-  g2.mtiles = choose_mtiles(g, BN);
-  g2.splits = g2.mtiles == 1 ? choose_splits(g, BN) : 1;
-  if (g2.splits > 1 && g.splits_allowed == 0) g2.splits = 1;
+  const Tiling tl = choose_tiling(g, BN);
+  g2.mtiles = tl.mt;
+  g2.splits = tl.s;
   return gemm_launch_tc(g2, st);
 }
 

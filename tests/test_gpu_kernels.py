@@ -84,6 +84,8 @@ SHAPES = [  # (M, N, K): tiles, ragged M / N, the fallback (K % 256 != 0), micro
     (128, 256, 256), (200, 512, 512), (64, 1376, 256), (64, 256, 688), (1, 256, 256),
     (130, 4096, 14336), (128, 14336, 4096), (16, 14336, 4096), (2100, 14336, 4096),
     (2100, 4096, 14336), (9, 32, 1024), (3, 48, 4096), (5, 4096, 14336), (1, 14336, 4096),
+    # two m-tiles per CTA with split-K (and a ragged second m-tile pair at M=300)
+    (512, 4096, 4096), (300, 4096, 14336),
 ]
 
 
