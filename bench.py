@@ -32,6 +32,31 @@ METRIC = "streamed LoRA train tok/s (8B-shape NF4); dequant-GEMM % roofline; H2D
 UNIT = "tokens/s"
 
 
+# DRAM traffic of the NF4 GEMM launches of a step, from one ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum over 11 consecutive launches of the timed step; command and figures in
+# profiles/tc_gemm_step_traffic_llama8b_b1_s512.md).  Valid only for the GEMM source it was
+# taken on: reported while the hash of these files matches, null otherwise.
+GEMM_TRAFFIC = None  # {"sha256": ..., "bytes_per_launch": ..., "algorithmic_bytes_per_launch": ...}
+GEMM_SOURCES = ("nf4_dequant_gemm_blockwise_b300/csrc/gemm.cu", "nf4_dequant_gemm_blockwise_b300/csrc/gemm.h",
+                "nf4_dequant_gemm_blockwise_b300/csrc/common.cuh")
+
+
+def gemm_source_sha256():
+    import hashlib
+    h = hashlib.sha256()
+    for rel in GEMM_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def gemm_traffic():
+    """Measured bytes per GEMM launch if the capture matches the current kernel source."""
+    if not GEMM_TRAFFIC or GEMM_TRAFFIC.get("sha256") != gemm_source_sha256():
+        return None
+    return GEMM_TRAFFIC["bytes_per_launch"]
+
+
 def max_over_ranks(dist, values, device="cpu"):
     """Entry-wise maximum over ranks (the slowest replica sets the job's step time)."""
     if dist is None:
@@ -434,7 +459,7 @@ def run_ours(args, rank, world, local_rank, dist):
         "gpu_launches": launches,
         "roofline": {"kernel": "nf4_dequant_gemm (tcgen05; all base-weight projections, fwd + recompute + dX)",
                      "bound": "tensor", "achieved": gemm_tflops, "peak": peak_tc, "unit": "TFLOP/s",
-                     "frac": gemm_tflops / peak_tc if gemm_tflops else None, "traffic": None,
+                     "frac": gemm_tflops / peak_tc if gemm_tflops else None, "traffic": gemm_traffic(),
                      "peak_source": f"{peaks['src']} bf16 sustained", "launches": st["gemm_launches"],
                      "avg_launch_us": st["gemm_ms"] * 1e3 / max(st["gemm_launches"], 1),
                      "share_of_step": st["gemm_ms"] / ms_total if ms_total else None},
