@@ -155,6 +155,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accf + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
+  pdl_trigger();  // a dependent split-K reduction may be scheduled now; it waits for this grid
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * BN;
@@ -544,21 +545,43 @@ struct RedParams {
   void *out;
   const float *add_src;
 };
+// Sum of the split partial planes in split order, then the epilogue.  Launched as a
+// programmatic dependent of the GEMM: waits for it before reading the partials.  V = 4: four
+// consecutive columns per item (Ng, ldo, ld_add multiples of 4, 16-byte aligned buffers).
+template <int V>
 __global__ void splitk_reduce_kernel(const RedParams p) {
-  const int64_t total = (int64_t)p.M * p.Ng;
-  const int64_t plane = total;
+  pdl_wait();
+  const int nv = p.Ng / V;
+  const int64_t total = (int64_t)p.M * nv;
+  const int64_t plane = (int64_t)p.M * p.Ng;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
        idx += (int64_t)gridDim.x * blockDim.x) {
-    float v = 0.f;
-    for (int z = 0; z < p.splits; ++z) v += p.part[(size_t)z * plane + idx];
-    const int m = (int)(idx / p.Ng), n = (int)(idx % p.Ng);
+    const int m = (int)(idx / nv), n = (int)(idx - (int64_t)m * nv) * V;
+    const size_t e = (size_t)m * p.Ng + n;
+    float v[V];
+    if constexpr (V == 4) {
+      float4 a = *reinterpret_cast<const float4 *>(p.part + e);
+      for (int z = 1; z < p.splits; ++z) {
+        const float4 b = *reinterpret_cast<const float4 *>(p.part + (size_t)z * plane + e);
+        a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+      }
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    } else {
+      v[0] = p.part[e];
+      for (int z = 1; z < p.splits; ++z) v[0] += p.part[(size_t)z * plane + e];
+    }
     if (p.epi == EPI_16) {
-      reinterpret_cast<uint16_t *>(p.out)[(size_t)m * p.ldo + n] = p.f16 ? f_to_h16(v) : f_to_bf16(v);
+      uint16_t *o = reinterpret_cast<uint16_t *>(p.out) + (size_t)m * p.ldo + n;
+#pragma unroll
+      for (int j = 0; j < V; ++j) o[j] = p.f16 ? f_to_h16(v[j]) : f_to_bf16(v[j]);
     } else {
       float *o = reinterpret_cast<float *>(p.out) + (size_t)m * p.ldo + n;
-      if (p.epi == EPI_F32) *o = v;
-      else if (p.epi == EPI_F32_ADD) *o = p.add_src[(size_t)m * p.ld_add + n] + v;
-      else *o = *o + v;
+#pragma unroll
+      for (int j = 0; j < V; ++j) {
+        if (p.epi == EPI_F32) o[j] = v[j];
+        else if (p.epi == EPI_F32_ADD) o[j] = p.add_src[(size_t)m * p.ld_add + n + j] + v[j];
+        else o[j] = o[j] + v[j];
+      }
     }
   }
 }
@@ -634,9 +657,13 @@ int launch_tc(const GemmArgs &g, const CUtensorMap *maps, cudaStream_t st) {
     RedParams rp;
     rp.part = g.part; rp.splits = p.splits; rp.M = g.M; rp.Ng = p.Ng; rp.epi = g.epi;
     rp.f16 = g.op_f16; rp.ldo = g.ldo; rp.ld_add = g.ld_add; rp.out = g.out; rp.add_src = g.add_src;
-    const int64_t n = (int64_t)g.M * p.Ng;
+    const bool vec = p.Ng % 4 == 0 && g.ldo % 4 == 0 && (g.epi != EPI_F32_ADD || g.ld_add % 4 == 0) &&
+                     (reinterpret_cast<uintptr_t>(g.part) & 15) == 0;
+    const int64_t n = (int64_t)g.M * p.Ng / (vec ? 4 : 1);
     const int blocks = (int)std::min<int64_t>((n + 255) / 256, 148 * 16);
-    splitk_reduce_kernel<<<blocks, 256, 0, st>>>(rp);
+    cudaError_t le = vec ? launch_pdl(splitk_reduce_kernel<4>, dim3(blocks), dim3(256), 0, st, rp)
+                         : launch_pdl(splitk_reduce_kernel<1>, dim3(blocks), dim3(256), 0, st, rp);
+    if (le != cudaSuccess) return set_error(SOUP_ECUDA, "split-K reduce launch: %s", cudaGetErrorString(le));
     count_launches(1);
   }
   cudaError_t e = cudaGetLastError();
