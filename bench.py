@@ -36,7 +36,8 @@ UNIT = "tokens/s"
 # dram__bytes_write.sum over 11 consecutive launches of the timed step; command and figures in
 # profiles/tc_gemm_step_traffic_llama8b_b1_s512.md).  Valid only for the GEMM source it was
 # taken on: reported while the hash of these files matches, null otherwise.
-GEMM_TRAFFIC = None  # {"sha256": ..., "bytes_per_launch": ..., "algorithmic_bytes_per_launch": ...}
+GEMM_TRAFFIC = {"sha256": "b2010d82c497c3bccd1e29c44c1bd8a7ba54e067ce34d9ae7c02a7bbda4371a4",
+                "bytes_per_launch": 42.09e6, "algorithmic_bytes_per_launch": 55.43e6}
 GEMM_SOURCES = ("nf4_dequant_gemm_blockwise_b300/csrc/gemm.cu", "nf4_dequant_gemm_blockwise_b300/csrc/gemm.h",
                 "nf4_dequant_gemm_blockwise_b300/csrc/common.cuh")
 
