@@ -62,9 +62,7 @@ SOUP_DEV void load_tile(uint16_t *dst, const uint16_t *src, int ld, size_t rowba
 }
 
 // ------------------------------------------------------------------------ forward
-// QR query rows per CTA (QR / 16 warps of 16 rows): 32-row CTAs halve the work of the heaviest
-// (last, causal) query tile and double the number of CTAs.
-template <int D, bool F16, int QR = 32>
+template <int D, bool F16>
 __global__ void __launch_bounds__(128) attn_fwd_kernel(const uint16_t *qkv, int ld, int S, int nh,
                                                        int nkv, uint16_t *out, float *lse,
                                                        float scale_log2) {
@@ -75,7 +73,7 @@ __global__ void __launch_bounds__(128) attn_fwd_kernel(const uint16_t *qkv, int 
   const int g = (h * nkv) / nh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gr = lane >> 2, tq = lane & 3;
-  const int q0 = qb * QR + warp * 16;
+  const int q0 = qb * 64 + warp * 16;
   const size_t rowbase = (size_t)b * S;
   const uint16_t *Qg = qkv + (size_t)h * D;
 
@@ -93,7 +91,7 @@ __global__ void __launch_bounds__(128) attn_fwd_kernel(const uint16_t *qkv, int 
   for (int i = 0; i < D / 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
   float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
 
-  const int q_end = min(S, qb * QR + QR);
+  const int q_end = min(S, qb * 64 + 64);
   const int n_tiles = (q_end + KT - 1) / KT;
   for (int kt = 0; kt < n_tiles; ++kt) {
     const int k0 = kt * KT;
@@ -340,7 +338,7 @@ __global__ void attn_kv_reduce_kernel(const float *part_k, const float *part_v, 
   }
 }
 
-template <int D, int QR = 32>
+template <int D>
 __global__ void __launch_bounds__(128) attn_bwd_dq_kernel(const uint16_t *qkv, int ld,
                                                           const uint16_t *dO, const float *lse,
                                                           const float *dsum, int S, int nh, int nkv,
@@ -353,7 +351,7 @@ __global__ void __launch_bounds__(128) attn_bwd_dq_kernel(const uint16_t *qkv, i
   const int g = (h * nkv) / nh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gr = lane >> 2, tq = lane & 3;
-  const int q0 = qb * QR + warp * 16;
+  const int q0 = qb * 64 + warp * 16;
   const size_t rowbase = (size_t)b * S;
   const uint16_t *Qg = qkv + (size_t)h * D;
   const uint16_t *dOg = dO + (size_t)h * D;
@@ -383,7 +381,7 @@ __global__ void __launch_bounds__(128) attn_bwd_dq_kernel(const uint16_t *qkv, i
 #pragma unroll
   for (int i = 0; i < D / 8; ++i) dq[i][0] = dq[i][1] = dq[i][2] = dq[i][3] = 0.f;
 
-  const int q_end = min(S, qb * QR + QR);
+  const int q_end = min(S, qb * 64 + 64);
   const int n_tiles = (q_end + KT - 1) / KT;
   for (int kt = 0; kt < n_tiles; ++kt) {
     const int k0 = kt * KT;
@@ -474,9 +472,7 @@ int attn_bwd_impl(const uint16_t *qkv, int ld, const uint16_t *o, const uint16_t
   const int64_t nred = (int64_t)B * S * nkv * D;
   attn_kv_reduce_kernel<<<(unsigned)std::min<int64_t>((nred + 255) / 256, 148 * 32), 256, 0, st>>>(
       part_k, part_v, B, S, nh, nkv, D, dqkv, ld);
-  constexpr int QR = 32;  // query rows per dq CTA (QR / 16 warps)
-  dim3 gq((S + QR - 1) / QR, nh, B);
-  attn_bwd_dq_kernel<D, QR><<<gq, QR * 2, 0, st>>>(qkv, ld, dO, lse, dsum, S, nh, nkv, dqkv, scale_log2, scale);
+  attn_bwd_dq_kernel<D><<<grid, 128, 0, st>>>(qkv, ld, dO, lse, dsum, S, nh, nkv, dqkv, scale_log2, scale);
   count_launches(4);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(SOUP_ECUDA, "attention backward launch: %s", cudaGetErrorString(e));
@@ -492,10 +488,9 @@ size_t attn_bwd_scratch_floats(int B, int S, int nh, int d) {
 int k_attn_fwd(const uint16_t *qkv, int ld, int B, int S, int nh, int nkv, int d, uint16_t *o,
                float *lse, cudaStream_t st) {
   const float scale_log2 = (1.0f / sqrtf((float)d)) * 1.4426950408889634f;
-  constexpr int QR = 32;  // query rows per CTA (QR / 16 warps)
-  dim3 grid((S + QR - 1) / QR, nh, B);
-  if (d == 128) attn_fwd_kernel<128, true, QR><<<grid, QR * 2, 0, st>>>(qkv, ld, S, nh, nkv, o, lse, scale_log2);
-  else if (d == 64) attn_fwd_kernel<64, true, QR><<<grid, QR * 2, 0, st>>>(qkv, ld, S, nh, nkv, o, lse, scale_log2);
+  dim3 grid((S + 63) / 64, nh, B);
+  if (d == 128) attn_fwd_kernel<128, true><<<grid, 128, 0, st>>>(qkv, ld, S, nh, nkv, o, lse, scale_log2);
+  else if (d == 64) attn_fwd_kernel<64, true><<<grid, 128, 0, st>>>(qkv, ld, S, nh, nkv, o, lse, scale_log2);
   else return set_error(SOUP_EINVAL, "attention: head_dim %d not supported (64 or 128)", d);
   count_launches(1);
   cudaError_t e = cudaGetLastError();
