@@ -10,6 +10,7 @@ Modules
   nf4     NF4 codebook, blockwise quantise / dequantise, nibble packing, bf16 rounding
   model   Llama-shaped decoder layer with LoRA: forward, hand-derived backward, loss
   sizes   byte counts of a shard and of the resident tensors (the peak-memory bound)
+  optim   AdamW on the adapters, gradient accumulation, several training steps
 
 Every function cites the passage of the pages it follows as
 (page title, section).  Where the pages say nothing the reading taken is stated
