@@ -4,8 +4,9 @@ device slots), seeded synthetic weights and tokens.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Prints ONE JSON line (rank 0).  `value` = tokens/s of whole forward+backward steps timed
-with CUDA events on the compute stream, inputs already on the device; `e2e` = the same
+Prints ONE JSON line (rank 0).  `value` = tokens/s of whole training steps (forward,
+backward, AdamW on the adapters) timed with CUDA events on the compute stream, inputs
+already on the device; `e2e` = the same
 through host buffers (token ids copied in from pinned memory and the loss read back every
 step).  The weights are streamed from the pinned host store by the step itself in both.
 `roofline` covers the NF4-dequant tensor-core GEMMs (all base-weight projections of the
@@ -30,6 +31,13 @@ sys.path.insert(0, ROOT)
 
 METRIC = "streamed LoRA train tok/s (8B-shape NF4); dequant-GEMM % roofline; H2D GB/s"
 UNIT = "tokens/s"
+LR = 2e-4  # AdamW learning rate of the timed steps (a usual LoRA rate; the pages give none)
+
+
+def _train_step(sess, tok):
+    """One training step: streamed forward + backward, then AdamW on every adapter."""
+    sess.step(tok)
+    sess.optimizer_step(LR)
 
 
 # DRAM traffic of the NF4 GEMM launches of a step, from one ncu capture (dram__bytes_read.sum +
@@ -107,7 +115,8 @@ def _peaks():
 def _workload(cfg, slots):
     return {"workload": f"{cfg.name}: streamed LoRA step (fwd+bwd), {cfg.n_layers} layers, hidden "
                         f"{cfg.hidden}, inter {cfg.inter}, {cfg.n_heads}/{cfg.n_kv_heads} heads, vocab "
-                        f"{cfg.vocab}, NF4 base, r={cfg.lora_r}, {slots} device slots",
+                        f"{cfg.vocab}, NF4 base, r={cfg.lora_r}, {slots} device slots, AdamW on the "
+                        f"adapters (lr {LR}) every step",
             "global_batch": cfg.batch, "seq_len": cfg.seq, "tokens_per_step": cfg.batch * cfg.seq,
             "parallelism": "replicas", "l2": "inputs larger than L2 (whole store re-streamed each step)"}
 
@@ -162,11 +171,12 @@ class Clocks:
 
 # ------------------------------------------------------------------------------ oracle baseline
 def run_oracle_timed(cfg):
-    """Estimated oracle step time: L x (layer fwd + layer bwd) + head fwd + head bwd."""
+    """Estimated oracle step time: L x (layer fwd + layer bwd + AdamW on the layer's adapters)
+    + head fwd + head bwd."""
     import numpy as np
 
     import synth
-    from oracle import model, nf4
+    from oracle import model, nf4, optim
 
     src = synth.layer_source(cfg, 0)
     W = model.weights_from_source(cfg, [src], synth.embedding(cfg.with_(vocab=2)),
@@ -188,7 +198,10 @@ def run_oracle_timed(cfg):
         dz = model.loss_backward(logits.reshape(cfg.batch, cfg.seq, -1), tok).reshape(M, -1)
         dh = model.rmsnorm_backward(dz @ w_lm, out.reshape(M, -1), w_f, r).reshape(out.shape)
         tc = time.perf_counter()
-        model.layer_backward(dh, cache, W, lora, cfg, cos, sin)
+        _, grads = model.layer_backward(dh, cache, W, lora, cfg, cos, sin)
+        for p in model.PROJ:
+            for t, g in zip(lora[p], grads[p]):
+                optim.adamw_step(t, g, np.zeros_like(g), np.zeros_like(g), 1, LR)
         td = time.perf_counter()
         layer = (tb - ta) + (td - tc)
         head = tc - tb
@@ -229,7 +242,7 @@ def run_reference(args, rank):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic", "config": _workload(cfg, args.slots),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": _threads(), "kind": "oracle",
-                             "sample": "each step: one decoder layer forward+backward and the output "
+                             "sample": "each step: one decoder layer forward+backward+AdamW and the output "
                                        "head forward+backward of the same workload, on the CPU "
                                        f"oracle; step time = {cfg.n_layers} x layer + head"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -363,7 +376,7 @@ def run_ours(args, rank, world, local_rank, dist):
     loss_host = torch.zeros(1, dtype=torch.float32).pin_memory()
 
     for _ in range(args.warmup):
-        sess.step(tok_dev)
+        _train_step(sess, tok_dev)
     sess.sync()
     torch.cuda.synchronize()
 
@@ -380,7 +393,7 @@ def run_ours(args, rank, world, local_rank, dist):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(sess.compute)
     for _ in range(args.steps):
-        sess.step(tok_dev)
+        _train_step(sess, tok_dev)
     e1.record(sess.compute)
     sess.sync()
     torch.cuda.synchronize()
@@ -393,9 +406,19 @@ def run_ours(args, rank, world, local_rank, dist):
         dist.barrier()
     peak_alloc = torch.cuda.max_memory_allocated()
 
+    # ---- the AdamW launch alone (all adapters, one launch; 1.2 GB of state > L2)
+    o0, o1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    o0.record(sess.compute)
+    for _ in range(5):
+        sess.optimizer_step(LR)
+    o1.record(sess.compute)
+    sess.sync()
+    opt_ms = o0.elapsed_time(o1) / 5
+    opt_gbs = 28 * sess.n_params / (opt_ms * 1e-3) / 1e9  # p, g, m, v read; p, m, v written
+
     # ---- end to end: token ids in from pinned host memory, loss out, every step
     for _ in range(2):
-        sess.step(tok_dev)
+        _train_step(sess, tok_dev)
     sess.sync()
     torch.cuda.synchronize()
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -405,6 +428,7 @@ def run_ours(args, rank, world, local_rank, dist):
             tok_dev.copy_(tok_host, non_blocking=True)
         sess.fwd(tok_dev)
         sess.bwd()
+        sess.optimizer_step(LR)
         with torch.cuda.stream(sess.compute):
             loss_host.copy_(sess.loss, non_blocking=True)
     f1.record(sess.compute)
@@ -420,12 +444,12 @@ def run_ours(args, rank, world, local_rank, dist):
         sess_r = StreamedLoRA(cfg, None, synth.embedding(cfg), synth.lm_head(cfg), synth.final_norm(cfg),
                               lora, B, S, resident=True, store=store)
         for _ in range(args.warmup):
-            sess_r.step(tok_dev)
+            _train_step(sess_r, tok_dev)
         sess_r.sync()
         g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         g0.record(sess_r.compute)
         for _ in range(args.steps):
-            sess_r.step(tok_dev)
+            _train_step(sess_r, tok_dev)
         g1.record(sess_r.compute)
         sess_r.sync()
         torch.cuda.synchronize()
@@ -468,7 +492,11 @@ def run_ours(args, rank, world, local_rank, dist):
                 "frac": h2d_gbs / h2d_peak if h2d_gbs else None, "bytes_per_step": st["copy_bytes"] / args.steps,
                 "copies_per_step": st["copies"] / args.steps, "store_bytes": store_bytes, "pinned": pinned},
         "overlap": overlap,
+        "optimizer": {"kernel": "adamw (float32 state, one launch over all adapters)",
+                      "params": sess.n_params, "ms": opt_ms, "bound": "hbm", "achieved_gbs": opt_gbs,
+                      "frac": opt_gbs / peaks["hbm"], "bytes_per_param": 28},
         "peak_vram_bytes": peak_alloc,
+        "peak_vram_predicted_bytes": api.peak_bytes(cfg, B, S, n_slots=args.slots)[0],
         "store_build_s": t_build,
         "loss": loss_val,
         "clocks": clk,
@@ -483,7 +511,7 @@ def run_ours(args, rank, world, local_rank, dist):
                               lora, vb, S, n_slots=vslots, store=store)
             vtok = torch.from_numpy(synth.tokens(vcfg)).cuda()
             for _ in range(args.warmup):
-                vs.step(vtok)
+                _train_step(vs, vtok)
             vs.sync()
             torch.cuda.synchronize()
             vs.stream.stats(reset=True)          # count the timed steps' copies only
@@ -491,7 +519,7 @@ def run_ours(args, rank, world, local_rank, dist):
             v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             v0.record(vs.compute)
             for _ in range(nsteps):
-                vs.step(vtok)
+                _train_step(vs, vtok)
             v1.record(vs.compute)
             vs.sync()
             torch.cuda.synchronize()
@@ -507,7 +535,7 @@ def run_ours(args, rank, world, local_rank, dist):
         est = [one()[0] for _ in range(2)]
         step_s = min(est)
         line["cpu_baseline"] = {"value": tokens / step_s, "unit": UNIT, "cores": _threads(), "kind": "oracle",
-                                "sample": f"one decoder layer fwd+bwd and the output head fwd+bwd of this "
+                                "sample": f"one decoder layer fwd+bwd+AdamW and the output head fwd+bwd of this "
                                           f"workload on the CPU oracle (float32 NumPy), step time = "
                                           f"{cfg.n_layers} x layer + head; best of 2"}
     sess.close()

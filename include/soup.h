@@ -151,8 +151,8 @@ void soup_store_free(soup_store *st);
  * scratch, LoRA operand packs and the vocabulary chunk of the loss. Writes *ws_bytes. */
 int soup_workspace_bytes(const soup_cfg *cfg, int max_batch, int max_seq, int n_slots,
                          int resident, uint64_t *ws_bytes);
-/* Device bytes of a whole run: workspace + caller-side resident tensors (embedding, untied
- * head, final norm, LoRA A/B and their gradients).  The pages bound peak VRAM by a single
+/* Device bytes of a whole training run: workspace + caller-side resident tensors (embedding,
+ * untied head, final norm, float32 LoRA A/B, their gradients and the two AdamW moments).  The pages bound peak VRAM by a single
  * layer plus the resident parts ("About Soup"); this is that bound made exact.
  * Returns 0 for an invalid cfg. workspace_bytes (optional) receives the workspace part. */
 uint64_t soup_peak_bytes(const soup_cfg *cfg, int batch, int seq, int n_slots, int resident,
@@ -193,6 +193,17 @@ int soup_step_fwd(soup_stream *h, const int32_t *tokens_dev, int B, int S,
  *   [out_p, r].  dh_out_dev (optional): dev float [(n_layers + 1), B*S, hidden], dL/dh of the
  *   residual stream at each layer boundary.  SOUP_ESTATE without a preceding forward. */
 int soup_step_bwd(soup_stream *h, float *const *dA, float *const *dB, float *dh_out_dev);
+
+/* soup_step_bwd with flags.  SOUP_BWD_ACCUMULATE adds this step's LoRA gradients to the ones
+ * already in dA/dB instead of overwriting them (gradient accumulation over micro-batches,
+ * "Layer streaming: fine-tune a model that does not fit in your card", "Full config":
+ * gradient_accumulation_steps).  Each element becomes old + g in one float addition, where g
+ * is exactly the value soup_step_bwd would have written, so accumulating k micro-batches
+ * equals summing k separately computed gradients in float, left to right, bit for bit.
+ * flags = 0 is soup_step_bwd.  Unknown flag bits: SOUP_EINVAL. */
+enum { SOUP_BWD_ACCUMULATE = 1 };
+int soup_step_bwd_ex(soup_stream *h, float *const *dA, float *const *dB, float *dh_out_dev,
+                     int flags);
 
 /* Host-side bounded wait for all work enqueued on the handle: polls, never spins on the
  * device.  Returns SOUP_ETIMEDOUT after timeout_ms, or the error a kernel reported. */
@@ -262,6 +273,28 @@ int soup_proj_fwd_noalloc(const uint16_t *x, int M, int N, int K, const uint8_t 
                           const float *absmax, const uint16_t *w_bf16, const float *A,
                           const float *B, int r, float s, int x_f16, uint16_t *y,
                           uintptr_t stream);
+
+/* ------------------------------------------------------------------ optimizer */
+
+/* AdamW hyper-parameters.  grad_scale multiplies the gradient before it enters the moments
+ * (1/k after accumulating k micro-batches). */
+typedef struct soup_adamw {
+  float lr, beta1, beta2, eps, weight_decay, grad_scale;
+} soup_adamw;
+
+/* One AdamW step over n float parameters in place (the pages' runs train the adapters with
+ * an AdamW, "Layer streaming: fine-tune a model that does not fit in your card", "Measured
+ * numbers"; here with float32 state).  With g = grad_scale * grad[i] and step number t >= 1:
+ *   m = beta1 m + (1 - beta1) g;  v = beta2 v + (1 - beta2) g^2
+ *   p = p - lr weight_decay p - lr (m / (1 - beta1^t)) / (sqrt(v / (1 - beta2^t)) + eps)
+ * (Adam's bias-corrected moments, Kingma & Ba; decay decoupled from the gradient, Loshchilov
+ * & Hutter).  param, m, v: dev float [n], updated in place; grad: dev float [n], read only.
+ * The four buffers must not overlap; any alignment is accepted (16-byte aligned buffers take
+ * the vectorised path).  m and v start at zero for t = 1.  One kernel launch on `stream`;
+ * n = 0 enqueues nothing.  SOUP_EINVAL for NULL pointers, n < 0, t < 1 or beta outside
+ * [0, 1). */
+int soup_adamw_step(float *param, const float *grad, float *m, float *v, int64_t n,
+                    const soup_adamw *hp, int64_t step, uintptr_t stream);
 
 /* Dequantise n NF4 weights on the device: out_f32[i] = float(c[code_i] * absmax[i / 64])
  * and out_bf16[i] = that value rounded to nearest-even bf16 (either output may be NULL). */

@@ -51,6 +51,14 @@ class soup_stats(C.Structure):
         return {f: getattr(self, f) for f, _ in self._fields_}
 
 
+class soup_adamw(C.Structure):
+    _fields_ = [("lr", C.c_float), ("beta1", C.c_float), ("beta2", C.c_float),
+                ("eps", C.c_float), ("weight_decay", C.c_float), ("grad_scale", C.c_float)]
+
+
+BWD_ACCUMULATE = 1
+
+
 def _load() -> C.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is not built; run python -m nf4_dequant_gemm_blockwise_b300.build")
@@ -75,6 +83,9 @@ def _load() -> C.CDLL:
                                    C.c_size_t, I32, I32, C.POINTER(VP)]),
         "soup_step_fwd": (I32, [VP, P, I32, I32, C.POINTER(P), C.POINTER(P), P, P, P]),
         "soup_step_bwd": (I32, [VP, C.POINTER(P), C.POINTER(P), P]),
+        "soup_step_bwd_ex": (I32, [VP, C.POINTER(P), C.POINTER(P), P, I32]),
+        "soup_adamw_step": (I32, [P, P, P, P, C.c_int64, C.POINTER(soup_adamw), C.c_int64,
+                                  C.c_size_t]),
         "soup_sync": (I32, [VP, I32]),
         "soup_stream_stats": (I32, [VP, C.POINTER(soup_stats), I32]),
         "soup_stream_debug": (I32, [VP, I32, I32]),
@@ -255,11 +266,14 @@ class Stream:
         _check(lib.soup_step_fwd(self.handle, _ptr(tokens), B, S, a, b, _ptr(loss), _ptr(logits),
                                  _ptr(layer_out)))
 
-    def bwd(self, dA, dB, dh_out=None):
+    def bwd(self, dA, dB, dh_out=None, accumulate=False):
         n = len(dA)
         a = (C.c_void_p * n)(*[_ptr(t) for t in dA])
         b = (C.c_void_p * n)(*[_ptr(t) for t in dB])
-        _check(lib.soup_step_bwd(self.handle, a, b, _ptr(dh_out)))
+        if accumulate:
+            _check(lib.soup_step_bwd_ex(self.handle, a, b, _ptr(dh_out), BWD_ACCUMULATE))
+        else:
+            _check(lib.soup_step_bwd(self.handle, a, b, _ptr(dh_out)))
 
     def sync(self, timeout_ms: int = 60000):
         _check(lib.soup_sync(self.handle, timeout_ms))
@@ -323,6 +337,14 @@ def proj_lora_grad(x, dy, M, N, K, A, B, r, s, dA, dB, scratch, stream=0, x_f16=
 def nf4_dequant(codes, absmax, n, out_f32=None, out_bf16=None, stream=0):
     _check(lib.soup_nf4_dequant(_ptr(codes), _ptr(absmax), n, _ptr(out_f32), _ptr(out_bf16),
                                 _stream(stream)))
+
+
+def adamw_step(param, grad, m, v, n, step, lr, beta1=0.9, beta2=0.999, eps=1e-8,
+               weight_decay=0.0, grad_scale=1.0, stream=0):
+    """One in-place AdamW step over n floats of device buffers (soup_adamw_step)."""
+    hp = soup_adamw(lr, beta1, beta2, eps, weight_decay, grad_scale)
+    _check(lib.soup_adamw_step(_ptr(param), _ptr(grad), _ptr(m), _ptr(v), n, C.byref(hp), step,
+                               _stream(stream)))
 
 
 def _stream(s) -> int:

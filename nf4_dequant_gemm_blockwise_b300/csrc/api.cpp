@@ -116,7 +116,8 @@ uint64_t soup_peak_bytes(const soup_cfg *cfg, int batch, int seq, int n_slots, i
   const uint64_t ins[7] = {H, H, H, (uint64_t)qd, H, H, (uint64_t)cfg->inter};
   for (int p = 0; p < 7; ++p) lora += r * (outs[p] + ins[p]);
   lora *= (uint64_t)cfg->n_layers;
-  const uint64_t resident_t = 2 * V * H + (cfg->tied ? 0 : 2 * V * H) + 2 * H + 2 * 4 * lora;
+  // float32 adapters, their gradients and the two AdamW moments
+  const uint64_t resident_t = 2 * V * H + (cfg->tied ? 0 : 2 * V * H) + 2 * H + 4 * 4 * lora;
   return P.total + resident_t;
 }
 
@@ -132,7 +133,11 @@ int soup_step_fwd(soup_stream *h, const int32_t *tokens_dev, int B, int S, const
   return step_fwd(h, tokens_dev, B, S, lora_A, lora_B, loss_dev, logits_dev, layer_out_dev);
 }
 int soup_step_bwd(soup_stream *h, float *const *dA, float *const *dB, float *dh_out_dev) {
-  return step_bwd(h, dA, dB, dh_out_dev);
+  return step_bwd(h, dA, dB, dh_out_dev, 0);
+}
+int soup_step_bwd_ex(soup_stream *h, float *const *dA, float *const *dB, float *dh_out_dev,
+                     int flags) {
+  return step_bwd(h, dA, dB, dh_out_dev, flags);
 }
 int soup_sync(soup_stream *h, int timeout_ms) { return stream_sync(h, timeout_ms); }
 int soup_stream_stats(soup_stream *h, soup_stats *out, int reset) { return stream_stats(h, out, reset); }
@@ -333,6 +338,25 @@ int soup_nf4_dequant(const uint8_t *codes, const float *absmax, int64_t n, float
   k_nf4_dequant(codes, absmax, n, out_f32, out_bf16, reinterpret_cast<cudaStream_t>(stream));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(SOUP_ECUDA, "dequant launch: %s", cudaGetErrorString(e));
+  return 0;
+}
+
+int soup_adamw_step(float *param, const float *grad, float *m, float *v, int64_t n,
+                    const soup_adamw *hp, int64_t step, uintptr_t stream) {
+  if (!hp || n < 0) return set_error(SOUP_EINVAL, "adamw: NULL hyper-parameters or n < 0");
+  if (n > 0 && (!param || !grad || !m || !v)) return set_error(SOUP_EINVAL, "adamw: NULL buffer");
+  if (step < 1) return set_error(SOUP_EINVAL, "adamw: step numbers start at 1 (got %lld)", (long long)step);
+  if (!(hp->beta1 >= 0.f && hp->beta1 < 1.f && hp->beta2 >= 0.f && hp->beta2 < 1.f))
+    return set_error(SOUP_EINVAL, "adamw: betas must lie in [0, 1)");
+  const uintptr_t lo[4] = {(uintptr_t)param, (uintptr_t)grad, (uintptr_t)m, (uintptr_t)v};
+  for (int i = 0; i < 4 && n > 0; ++i)
+    for (int j = i + 1; j < 4; ++j)
+      if (lo[i] < lo[j] + 4ull * n && lo[j] < lo[i] + 4ull * n)
+        return set_error(SOUP_EINVAL, "adamw: buffers %d and %d overlap", i, j);
+  k_adamw(param, grad, m, v, n, hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay,
+          hp->grad_scale, step, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(SOUP_ECUDA, "adamw launch: %s", cudaGetErrorString(e));
   return 0;
 }
 

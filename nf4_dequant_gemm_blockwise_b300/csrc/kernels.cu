@@ -556,7 +556,9 @@ __global__ void lora_dB_reduce_kernel(const float *part, int msplit, int Ng, con
     int seg = 0;
     for (int p = 0; p < L.nseg; ++p)
       if (n >= L.off[p] && n < L.off[p] + L.n[p]) seg = p;
-    L.dB[seg][(size_t)(n - L.off[seg]) * L.r + j] = L.s * acc;
+    float *dst = L.dB[seg] + (size_t)(n - L.off[seg]) * L.r + j;
+    const float g = L.s * acc;
+    *dst = L.accumulate ? *dst + g : g;
   }
 }
 
@@ -661,7 +663,8 @@ __global__ void lora_dA_reduce_kernel(const float *part, int msplit, int K, cons
     const int o = (int)(idx / K), k = (int)(idx % K);
     float acc = 0.f;
     for (int ms = 0; ms < msplit; ++ms) acc += part[(size_t)ms * total + idx];
-    L.dA[o / L.r][(size_t)(o % L.r) * K + k] = acc;
+    float *dst = L.dA[o / L.r] + (size_t)(o % L.r) * K + k;
+    *dst = L.accumulate ? *dst + acc : acc;
   }
 }
 

@@ -26,6 +26,7 @@ struct LoraSeg {
   float *dA[MAX_SEG] = {nullptr, nullptr, nullptr};
   float *dB[MAX_SEG] = {nullptr, nullptr, nullptr};
   float s = 1.f;
+  bool accumulate = false;  // dA/dB reductions add to the existing gradient (old + g)
   __host__ __device__ int Rpad() const { return ((nseg * r + 63) / 64) * 64; }
 };
 
@@ -79,6 +80,10 @@ void k_ce_chunk_bwd(const float *z, int ldz, int v0, int vc, const float *lse, c
                     int M, int S, float inv_n, uint16_t *dz, cudaStream_t st);
 
 void k_cast_bf16(const float *in, uint16_t *out, int64_t n, cudaStream_t st);
+// One AdamW step in place over n floats (optim.cu); step >= 1, betas in [0, 1).
+void k_adamw(float *p, const float *g, float *m, float *v, int64_t n, float lr, float beta1,
+             float beta2, float eps, float weight_decay, float grad_scale, int64_t step,
+             cudaStream_t st);
 void k_nf4_dequant(const uint8_t *codes, const float *absmax, int64_t n, float *out_f32,
                    uint16_t *out_bf16, cudaStream_t st);
 

@@ -214,6 +214,7 @@ LoraSeg make_seg(soup_stream *h, int layer, int g, bool grads) {
       L.dB[p] = h->grad_B[idx];
     }
   }
+  L.accumulate = grads && h->grad_accumulate;
   return L;
 }
 
@@ -565,8 +566,9 @@ int step_fwd(soup_stream *h, const int32_t *tokens, int B, int S, const float *c
   return check_cuda("step_fwd");
 }
 
-int step_bwd(soup_stream *h, float *const *dA, float *const *dB, float *dh_out) {
+int step_bwd(soup_stream *h, float *const *dA, float *const *dB, float *dh_out, int flags) {
   if (!h || !dA || !dB) return set_error(SOUP_EINVAL, "step_bwd: NULL argument");
+  if (flags & ~SOUP_BWD_ACCUMULATE) return set_error(SOUP_EINVAL, "step_bwd: unknown flags 0x%x", flags);
   if (!h->fwd_ready) return set_error(SOUP_ESTATE, "step_bwd without a preceding step_fwd");
   const soup_cfg &c = h->cfg;
   const int L = c.n_layers;
@@ -574,6 +576,7 @@ int step_bwd(soup_stream *h, float *const *dA, float *const *dB, float *dh_out) 
     if (!dA[i] || !dB[i]) return set_error(SOUP_EINVAL, "step_bwd: gradient pointer %d is NULL", i);
   h->grad_A.assign(dA, dA + (size_t)L * 7);
   h->grad_B.assign(dB, dB + (size_t)L * 7);
+  h->grad_accumulate = (flags & SOUP_BWD_ACCUMULATE) != 0;
   h->in_bwd = 1;
   harvest(h, false);
   const Plan &P = h->plan;

@@ -61,6 +61,7 @@ struct soup_stream {
   const int32_t *tokens = nullptr;
   std::vector<const float *> lora_A, lora_B;
   std::vector<float *> grad_A, grad_B;
+  int grad_accumulate = 0;  // this backward adds to grad_A/grad_B (SOUP_BWD_ACCUMULATE)
   // measurement
   soup_stats stats{};
   std::vector<soup::TimedEv> copy_ev, gemm_ev;
@@ -73,7 +74,7 @@ int stream_init(soup_store *st, const soup_cfg *c, int maxB, int maxS, void *ws,
                 uintptr_t xs, int n_slots, int resident, soup_stream **out);
 int step_fwd(soup_stream *h, const int32_t *tokens, int B, int S, const float *const *lA,
              const float *const *lB, float *loss, float *logits, float *layer_out);
-int step_bwd(soup_stream *h, float *const *dA, float *const *dB, float *dh_out);
+int step_bwd(soup_stream *h, float *const *dA, float *const *dB, float *dh_out, int flags);
 int stream_sync(soup_stream *h, int timeout_ms);
 int stream_stats(soup_stream *h, soup_stats *out, int reset);
 void soup_stream_free_impl(soup_stream *h);

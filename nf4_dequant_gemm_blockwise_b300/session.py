@@ -38,10 +38,29 @@ class StreamedLoRA:
         self.embed = _bits_to_dev(embed_bits)
         self.lm_head = None if cfg.tied else _bits_to_dev(lm_head_bits)
         self.final = _bits_to_dev(final_bits)
-        self.lora_A = [torch.from_numpy(np.ascontiguousarray(a)).cuda() for layer in lora for a, _ in layer]
-        self.lora_B = [torch.from_numpy(np.ascontiguousarray(b)).cuda() for layer in lora for _, b in layer]
-        self.dA = [torch.zeros_like(a) for a in self.lora_A]
-        self.dB = [torch.zeros_like(b) for b in self.lora_B]
+        # adapters, gradients and AdamW moments each live in one flat float buffer (tensors
+        # at 256-byte aligned offsets), so the optimizer is a single launch over all of them
+        shapes = [t.shape for layer in lora for pair in layer for t in pair]
+        offs, n = [], 0
+        for sh in shapes:
+            offs.append(n)
+            n += -(-int(np.prod(sh)) // 64) * 64
+        self.n_params = n
+        host = np.zeros(n, np.float32)
+        flat = [t for layer in lora for pair in layer for t in pair]
+        for o, t in zip(offs, flat):
+            host[o:o + t.size] = np.asarray(t, np.float32).ravel()
+        self.params = torch.from_numpy(host).cuda()
+        self.grad_flat = torch.zeros(n, dtype=torch.float32, device="cuda")
+        self.exp_avg = torch.zeros(n, dtype=torch.float32, device="cuda")
+        self.exp_avg_sq = torch.zeros(n, dtype=torch.float32, device="cuda")
+        self.opt_step = 0
+
+        def views(buf):
+            return [buf[o:o + int(np.prod(sh))].view(*sh) for o, sh in zip(offs, shapes)]
+        pv, gv = views(self.params), views(self.grad_flat)
+        self.lora_A, self.lora_B = pv[0::2], pv[1::2]
+        self.dA, self.dB = gv[0::2], gv[1::2]
         nbytes = api.workspace_bytes(cfg, max_batch, max_seq, n_slots, resident)
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
         self.compute = torch.cuda.Stream()
@@ -57,12 +76,41 @@ class StreamedLoRA:
         self.compute.wait_stream(torch.cuda.current_stream())
         self.stream.fwd(tokens, B, S, self.lora_A, self.lora_B, self.loss, logits, layer_out)
 
-    def bwd(self, dh_out=None):
-        self.stream.bwd(self.dA, self.dB, dh_out)
+    def bwd(self, dh_out=None, accumulate=False):
+        """accumulate: add this backward's LoRA gradients to the ones held (micro-batches)."""
+        self.stream.bwd(self.dA, self.dB, dh_out, accumulate=accumulate)
 
     def step(self, tokens: torch.Tensor, logits=None, layer_out=None, dh_out=None):
         self.fwd(tokens, logits, layer_out)
         self.bwd(dh_out)
+
+    def optimizer_step(self, lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0,
+                       grad_scale=1.0):
+        """One AdamW step of every adapter on the compute stream, after the backward."""
+        self.opt_step += 1
+        api.adamw_step(self.params, self.grad_flat, self.exp_avg, self.exp_avg_sq, self.n_params,
+                       self.opt_step, lr, beta1, beta2, eps, weight_decay, grad_scale,
+                       stream=self.compute)
+
+    def train_step(self, micro_batches, losses: torch.Tensor, lr, **adamw):
+        """One optimizer step over k micro-batches ("Layer streaming: fine-tune a model that
+        does not fit in your card", "Full config": gradient_accumulation_steps): forward and
+        backward of each, gradients summed, AdamW with the sum scaled by 1/k.  losses: device
+        float [>= k], micro-batch i's loss lands in losses[i]."""
+        k = len(micro_batches)
+        for i, tok in enumerate(micro_batches):
+            B, S = tok.shape
+            self.compute.wait_stream(torch.cuda.current_stream())
+            self.stream.fwd(tok, B, S, self.lora_A, self.lora_B, losses[i:i + 1])
+            self.bwd(accumulate=i > 0)
+        self.optimizer_step(lr, grad_scale=1.0 / k, **adamw)
+
+    def adapters(self):
+        """Host copies of the adapters: list over layers of 7 (A, B)."""
+        L = self.cfg.n_layers
+        A = [t.cpu().numpy() for t in self.lora_A]
+        Bm = [t.cpu().numpy() for t in self.lora_B]
+        return [[(A[i * 7 + p], Bm[i * 7 + p]) for p in range(7)] for i in range(L)]
 
     def sync(self, timeout_ms: int = 600000):
         self.stream.sync(timeout_ms)

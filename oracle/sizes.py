@@ -38,7 +38,8 @@ def lora_param_count(cfg) -> int:
 
 
 def resident_bytes(cfg) -> int:
-    """Embedding, untied head, final norm (bf16), LoRA A/B and their gradients (float32)."""
+    """Embedding, untied head, final norm (bf16); LoRA A/B, their gradients and the two
+    AdamW moments (float32) — everything of a training run but the streamed base."""
     emb = 2 * cfg.vocab * cfg.hidden
     head = 0 if cfg.tied else 2 * cfg.vocab * cfg.hidden
-    return emb + head + 2 * cfg.hidden + 2 * 4 * lora_param_count(cfg)
+    return emb + head + 2 * cfg.hidden + 4 * 4 * lora_param_count(cfg)

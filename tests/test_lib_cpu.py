@@ -112,3 +112,23 @@ def test_invalid_config_is_rejected():
     assert e.value.code == api.EINVAL
     with pytest.raises(api.SoupError):
         api.workspace_bytes(synth.TINY, 1, 64, n_slots=9)
+
+
+def test_adamw_and_accumulate_arguments_are_checked_before_any_launch():
+    # every case below fails validation on the host, so no CUDA call is made
+    def rc(*args, **kw):
+        with pytest.raises(api.SoupError) as e:
+            api.adamw_step(*args, **kw)
+        return e.value.code
+    n = 1024
+    a, b, c, d = 1 << 20, 2 << 20, 3 << 20, 4 << 20  # disjoint fake device addresses
+    assert rc(a, b, c, d, n, 0, 1e-3) == api.EINVAL                 # step numbers start at 1
+    assert rc(a, b, c, d, n, 1, 1e-3, beta1=1.0) == api.EINVAL      # beta outside [0, 1)
+    assert rc(a, b, c, d, n, 1, 1e-3, beta2=-0.5) == api.EINVAL
+    assert rc(a, b, c, d, -1, 1, 1e-3) == api.EINVAL                # negative size
+    assert rc(a, None, c, d, n, 1, 1e-3) == api.EINVAL              # NULL buffer
+    assert rc(a, a + 4 * n - 4, c, d, n, 1, 1e-3) == api.EINVAL     # param and grad overlap
+    assert rc(a, b, c, c + 8, n, 1, 1e-3) == api.EINVAL             # m and v overlap
+    assert "overlap" in api.last_error()
+    arr = (api.C.c_void_p * 1)()
+    assert api.lib.soup_step_bwd_ex(None, arr, arr, None, api.BWD_ACCUMULATE) == api.EINVAL
