@@ -413,6 +413,7 @@ def run_ours(args, rank, world, local_rank, dist):
         sess.optimizer_step(LR)
     o1.record(sess.compute)
     sess.sync()
+    torch.cuda.synchronize()
     opt_ms = o0.elapsed_time(o1) / 5
     opt_gbs = 28 * sess.n_params / (opt_ms * 1e-3) / 1e9  # p, g, m, v read; p, m, v written
 
