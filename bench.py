@@ -113,10 +113,9 @@ def _peaks():
 
 
 def _workload(cfg, slots):
-    return {"workload": f"{cfg.name}: streamed LoRA step (fwd+bwd), {cfg.n_layers} layers, hidden "
+    return {"workload": f"{cfg.name}: streamed LoRA training step (fwd+bwd+AdamW), {cfg.n_layers} layers, hidden "
                         f"{cfg.hidden}, inter {cfg.inter}, {cfg.n_heads}/{cfg.n_kv_heads} heads, vocab "
-                        f"{cfg.vocab}, NF4 base, r={cfg.lora_r}, {slots} device slots, AdamW on the "
-                        f"adapters (lr {LR}) every step",
+                        f"{cfg.vocab}, NF4 base, r={cfg.lora_r}, {slots} device slots, AdamW lr {LR}",
             "global_batch": cfg.batch, "seq_len": cfg.seq, "tokens_per_step": cfg.batch * cfg.seq,
             "parallelism": "replicas", "l2": "inputs larger than L2 (whole store re-streamed each step)"}
 
