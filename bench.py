@@ -501,14 +501,16 @@ def run_ours(args, rank, world, local_rank, dist):
         "loss": loss_val,
         "clocks": clk,
     }
-    # ---- extra configurations of the same store: batch 4 (the pages' other 8B batch) and
-    # eight device slots (stream_buffers' upper bound); same timing method, fewer steps
+    # ---- extra configurations of the same store: batch 4 (the pages' other 8B batch), eight
+    # device slots (stream_buffers' upper bound) and kept activations (stream_recompute: off);
+    # same timing method, fewer steps
     if not args.no_variants:
         variants = []
-        for vb, vslots in ((4, args.slots), (1, 8), (4, 8)):
+        for vb, vslots, keep in ((4, args.slots, False), (1, 8, False), (4, 8, False),
+                                 (1, args.slots, True), (4, args.slots, True)):
             vcfg = cfg.with_(batch=vb)
             vs = StreamedLoRA(vcfg, None, synth.embedding(cfg), synth.lm_head(cfg), synth.final_norm(cfg),
-                              lora, vb, S, n_slots=vslots, store=store)
+                              lora, vb, S, n_slots=vslots, store=store, keep_activations=keep)
             vtok = torch.from_numpy(synth.tokens(vcfg)).cuda()
             for _ in range(args.warmup):
                 _train_step(vs, vtok)
@@ -525,7 +527,7 @@ def run_ours(args, rank, world, local_rank, dist):
             torch.cuda.synchronize()
             vms = v0.elapsed_time(v1) / nsteps
             vst = vs.stream.stats(reset=True)
-            variants.append({"batch": vb, "slots": vslots, "tokens_per_step": vb * S,
+            variants.append({"batch": vb, "slots": vslots, "keep_activations": keep, "tokens_per_step": vb * S,
                              "value": world * vb * S / (vms * 1e-3), "ms_per_step": vms,
                              "copies_per_step": vst["copies"] / nsteps, "steps": nsteps})
             vs.close()

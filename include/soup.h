@@ -146,16 +146,28 @@ void soup_store_free(soup_store *st);
 
 /* ------------------------------------------------------------------ memory plan */
 
+/* Stream modes: the `mode` argument of soup_workspace_bytes, soup_peak_bytes and
+ * soup_stream_init is a bit set (0 = the streamed default).
+ *   SOUP_MODE_RESIDENT: every shard lives in the workspace, copied once at init; no streaming.
+ *   SOUP_MODE_KEEP_ACTIVATIONS: the forward keeps every layer's activations for the backward,
+ *     which then skips re-running each layer's forward but still reads every layer's weights
+ *     again ("Layer streaming: fine-tune a model that does not fit in your card", "How it
+ *     works": training.stream_recompute: off).  Costs one activation set per layer.
+ * Other bits: SOUP_EINVAL. */
+enum { SOUP_MODE_RESIDENT = 1, SOUP_MODE_KEEP_ACTIVATIONS = 2 };
+
 /* Device bytes of the workspace a stream handle needs for batches up to max_batch x max_seq:
- * n_slots shard slots (or every layer when resident != 0), saved activations, per-layer
- * scratch, LoRA operand packs and the vocabulary chunk of the loss. Writes *ws_bytes. */
+ * n_slots shard slots (or every layer in SOUP_MODE_RESIDENT), saved activations (one layer's
+ * set, or every layer's in SOUP_MODE_KEEP_ACTIVATIONS), per-layer scratch, LoRA operand packs
+ * and the vocabulary chunk of the loss. Writes *ws_bytes. */
 int soup_workspace_bytes(const soup_cfg *cfg, int max_batch, int max_seq, int n_slots,
-                         int resident, uint64_t *ws_bytes);
+                         int mode, uint64_t *ws_bytes);
 /* Device bytes of a whole training run: workspace + caller-side resident tensors (embedding,
- * untied head, final norm, float32 LoRA A/B, their gradients and the two AdamW moments).  The pages bound peak VRAM by a single
- * layer plus the resident parts ("About Soup"); this is that bound made exact.
- * Returns 0 for an invalid cfg. workspace_bytes (optional) receives the workspace part. */
-uint64_t soup_peak_bytes(const soup_cfg *cfg, int batch, int seq, int n_slots, int resident,
+ * untied head, final norm, float32 LoRA A/B, their gradients and the two AdamW moments).
+ * The pages bound peak VRAM by a single layer plus the resident parts ("About Soup"); this
+ * is that bound made exact.  Returns 0 for an invalid cfg or mode.  workspace_bytes
+ * (optional) receives the workspace part. */
+uint64_t soup_peak_bytes(const soup_cfg *cfg, int batch, int seq, int n_slots, int mode,
                          uint64_t *workspace_bytes);
 
 /* ------------------------------------------------------------------ streamed step */
@@ -165,13 +177,16 @@ uint64_t soup_peak_bytes(const soup_cfg *cfg, int batch, int seq, int n_slots, i
  *   embed: dev bf16 [vocab, hidden]; lm_head: dev bf16 [vocab, hidden] or NULL when tied;
  *   final_norm: dev bf16 [hidden].
  *   compute_stream / copy_stream: distinct streams ("How it works": a dedicated copy stream).
- *   n_slots in [2, 8] ("Turn it on": stream_buffers).  resident != 0 copies every shard to
- *   the workspace once here (synchronously) and then runs the same kernels with no copies —
- *   the reference the streamed run must match bit for bit. */
+ *   n_slots in [2, 8] ("Turn it on": stream_buffers).
+ *   mode (bits above): SOUP_MODE_RESIDENT copies every shard to the workspace once here
+ *   (synchronously) and then runs the same kernels with no copies — the reference the
+ *   streamed run must match bit for bit.  SOUP_MODE_KEEP_ACTIVATIONS skips the backward's
+ *   recompute; results are bitwise those of the recomputing stream (same kernels, same
+ *   inputs). */
 int soup_stream_init(soup_store *st, const soup_cfg *cfg, int max_batch, int max_seq,
                      void *dev_ws, uint64_t ws_bytes, const void *embed, const void *lm_head,
                      const void *final_norm, uintptr_t compute_stream, uintptr_t copy_stream,
-                     int n_slots, int resident, soup_stream **out);
+                     int n_slots, int mode, soup_stream **out);
 
 /* Forward over all layers plus the vocabulary-chunked loss.
  *   tokens_dev: dev int32 [B, S], ids in [0, vocab) (ids out of range are clamped).

@@ -57,6 +57,11 @@ class soup_adamw(C.Structure):
 
 
 BWD_ACCUMULATE = 1
+MODE_RESIDENT, MODE_KEEP_ACTIVATIONS = 1, 2
+
+
+def _mode(resident, keep_activations) -> int:
+    return (MODE_RESIDENT if resident else 0) | (MODE_KEEP_ACTIVATIONS if keep_activations else 0)
 
 
 def _load() -> C.CDLL:
@@ -176,18 +181,20 @@ def nf4_quantize_host(src_bf16_bits: np.ndarray, n_threads: int = 0):
     return codes, absmax
 
 
-def workspace_bytes(cfg, max_batch, max_seq, n_slots=2, resident=False) -> int:
+def workspace_bytes(cfg, max_batch, max_seq, n_slots=2, resident=False, keep_activations=False) -> int:
     c = make_cfg(cfg)
     out = C.c_uint64()
-    _check(lib.soup_workspace_bytes(C.byref(c), max_batch, max_seq, n_slots, int(resident), C.byref(out)))
+    _check(lib.soup_workspace_bytes(C.byref(c), max_batch, max_seq, n_slots,
+                                    _mode(resident, keep_activations), C.byref(out)))
     return out.value
 
 
-def peak_bytes(cfg, batch, seq, n_slots=2, resident=False):
+def peak_bytes(cfg, batch, seq, n_slots=2, resident=False, keep_activations=False):
     """(total device bytes of a run, workspace part)."""
     c = make_cfg(cfg)
     ws = C.c_uint64()
-    tot = lib.soup_peak_bytes(C.byref(c), batch, seq, n_slots, int(resident), C.byref(ws))
+    tot = lib.soup_peak_bytes(C.byref(c), batch, seq, n_slots, _mode(resident, keep_activations),
+                              C.byref(ws))
     if tot == 0:
         raise SoupError(EINVAL, last_error())
     return tot, ws.value
@@ -244,18 +251,19 @@ class Stream:
     """A stream handle: a store bound to a device workspace and two CUDA streams."""
 
     def __init__(self, store: Store, max_batch, max_seq, workspace, embed, lm_head, final_norm,
-                 compute_stream, copy_stream, n_slots=2, resident=False):
+                 compute_stream, copy_stream, n_slots=2, resident=False, keep_activations=False):
         self.store = store
         self.cfg = store.cfg
         ws_need = C.c_uint64()
-        _check(lib.soup_workspace_bytes(C.byref(self.cfg), max_batch, max_seq, n_slots, int(resident),
+        mode = _mode(resident, keep_activations)
+        _check(lib.soup_workspace_bytes(C.byref(self.cfg), max_batch, max_seq, n_slots, mode,
                                         C.byref(ws_need)))
         self.keep = (workspace, embed, lm_head, final_norm)
         h = C.c_void_p()
         _check(lib.soup_stream_init(store.handle, C.byref(self.cfg), max_batch, max_seq, _ptr(workspace),
                                     workspace.numel() * workspace.element_size(), _ptr(embed),
                                     _ptr(lm_head), _ptr(final_norm), compute_stream.cuda_stream,
-                                    copy_stream.cuda_stream, n_slots, int(resident), C.byref(h)))
+                                    copy_stream.cuda_stream, n_slots, mode, C.byref(h)))
         self.handle = h
 
     def fwd(self, tokens, B, S, lora_A, lora_B, loss, logits=None, layer_out=None):

@@ -92,19 +92,19 @@ int soup_store_info(const soup_store *st, void **base, uint64_t *bytes, int *pin
 }
 void soup_store_free(soup_store *st) { store_free(st); }
 
-int soup_workspace_bytes(const soup_cfg *cfg, int max_batch, int max_seq, int n_slots, int resident,
+int soup_workspace_bytes(const soup_cfg *cfg, int max_batch, int max_seq, int n_slots, int mode,
                          uint64_t *ws_bytes) {
   if (!ws_bytes) return set_error(SOUP_EINVAL, "ws_bytes is NULL");
   Plan P;
-  SOUP_TRY(make_plan(cfg, max_batch, max_seq, n_slots, resident, &P));
+  SOUP_TRY(make_plan(cfg, max_batch, max_seq, n_slots, mode, &P));
   *ws_bytes = P.total;
   return 0;
 }
 
-uint64_t soup_peak_bytes(const soup_cfg *cfg, int batch, int seq, int n_slots, int resident,
+uint64_t soup_peak_bytes(const soup_cfg *cfg, int batch, int seq, int n_slots, int mode,
                          uint64_t *workspace_bytes) {
   Plan P;
-  if (make_plan(cfg, batch, seq, n_slots, resident, &P) < 0) return 0;
+  if (make_plan(cfg, batch, seq, n_slots, mode, &P) < 0) return 0;
   if (workspace_bytes) *workspace_bytes = P.total;
   const uint64_t V = cfg->vocab, H = cfg->hidden, r = cfg->lora_r;
   uint64_t lora = 0;
@@ -123,10 +123,10 @@ uint64_t soup_peak_bytes(const soup_cfg *cfg, int batch, int seq, int n_slots, i
 
 int soup_stream_init(soup_store *st, const soup_cfg *cfg, int max_batch, int max_seq, void *dev_ws,
                      uint64_t ws_bytes, const void *embed, const void *lm_head, const void *final_norm,
-                     uintptr_t compute_stream, uintptr_t copy_stream, int n_slots, int resident,
+                     uintptr_t compute_stream, uintptr_t copy_stream, int n_slots, int mode,
                      soup_stream **out) {
   return stream_init(st, cfg, max_batch, max_seq, dev_ws, ws_bytes, embed, lm_head, final_norm,
-                     compute_stream, copy_stream, n_slots, resident, out);
+                     compute_stream, copy_stream, n_slots, mode, out);
 }
 int soup_step_fwd(soup_stream *h, const int32_t *tokens_dev, int B, int S, const float *const *lora_A,
                   const float *const *lora_B, float *loss_dev, float *logits_dev, float *layer_out_dev) {

@@ -35,8 +35,11 @@ int ce_chunk_cols(int M, int V) {
   return std::max(vc, 256);
 }
 
-int make_plan(const soup_cfg *c, int maxB, int maxS, int n_slots, int resident, Plan *P) {
+int make_plan(const soup_cfg *c, int maxB, int maxS, int n_slots, int mode, Plan *P) {
   SOUP_TRY(validate_cfg(c));
+  if (mode & ~(SOUP_MODE_RESIDENT | SOUP_MODE_KEEP_ACTIVATIONS))
+    return set_error(SOUP_EINVAL, "unknown stream mode bits 0x%x", mode);
+  const bool resident = (mode & SOUP_MODE_RESIDENT) != 0;
   if (maxB < 1 || maxS < 2) return set_error(SOUP_EINVAL, "max_batch >= 1 and max_seq >= 2 required");
   if (!resident && (n_slots < 2 || n_slots > 8)) return set_error(SOUP_EINVAL, "n_slots must be in [2, 8]");
   soup_shard_layout L;
@@ -65,6 +68,10 @@ int make_plan(const soup_cfg *c, int maxB, int maxS, int n_slots, int resident, 
   for (int g = 0; g < 4; ++g) {
     P->u_f32[g] = take(4 * M * 64);
     P->u_b[g] = take(2 * M * 64);
+  }
+  if (mode & SOUP_MODE_KEEP_ACTIVATIONS) {  // layers 1 .. L-1 get their own copies
+    P->act_stride = off - P->hm;
+    take(P->act_stride * (uint64_t)(c->n_layers - 1));
   }
   P->dh = take(4 * M * H);
   P->dhm = take(4 * M * H);
@@ -305,9 +312,28 @@ int release(soup_stream *h, int slot) {
 }
 
 // ---------------------------------------------------------------- layer maths
+// Activation buffers of layer li: one set reused by every layer (the backward recomputes
+// them), or one set per layer when the stream keeps activations (no recompute).
+struct LayerBufs {
+  uint64_t hm, x1, x2, qkv, att, lse, gu, act, u_f32[4], u_b[4];
+};
+LayerBufs bufs_of(const soup_stream *h, int li) {
+  const Plan &P = h->plan;
+  const uint64_t o = h->keep_act ? (uint64_t)li * P.act_stride : 0;
+  LayerBufs b;
+  b.hm = P.hm + o; b.x1 = P.x1 + o; b.x2 = P.x2 + o; b.qkv = P.qkv + o; b.att = P.att + o;
+  b.lse = P.lse + o; b.gu = P.gu + o; b.act = P.act + o;
+  for (int g = 0; g < 4; ++g) {
+    b.u_f32[g] = P.u_f32[g] + o;
+    b.u_b[g] = P.u_b[g] + o;
+  }
+  return b;
+}
+
 int layer_forward(soup_stream *h, int li, const uint8_t *shard, bool recompute) {
   const soup_cfg &c = h->cfg;
   const Plan &P = h->plan;
+  const LayerBufs Lb = bufs_of(h, li);
   const soup_shard_layout &SL = h->lay;
   cudaStream_t st = h->cs;
   const int B = h->B, S = h->S, M = B * S, H = c.hidden, I = c.inter;
@@ -320,47 +346,47 @@ int layer_forward(soup_stream *h, int li, const uint8_t *shard, bool recompute) 
 
   float *part = F(h, P.lora_part);
   // the forward's tensor-core operands are IEEE half (x1, qkv, att, x2, gu, act, LoRA packs)
-  k_rmsnorm_fwd(hin, ln1, c.rms_eps, M, H, B16(h, P.x1), true, st);
-  k_lora_down(B16(h, P.x1), H, M, H, Lq, F(h, P.u_f32[0]), B16(h, P.u_b[0]), true, true, part, st);
+  k_rmsnorm_fwd(hin, ln1, c.rms_eps, M, H, B16(h, Lb.x1), true, st);
+  k_lora_down(B16(h, Lb.x1), H, M, H, Lq, F(h, Lb.u_f32[0]), B16(h, Lb.u_b[0]), true, true, part, st);
   {
     GemmArgs g = weight_args(h, shard, SOUP_G_QKV, GEMM_FWD);
-    g.op_f16 = 1; g.M = M; g.a = B16(h, P.x1); g.lda = H;
-    g.ul = B16(h, P.u_b[0]); g.vl = B16(h, P.vl[(size_t)li * 4 + 0]); g.R = Lq.Rpad();
-    g.lora_u = F(h, P.u_f32[0]); g.lseg = Lq; g.after_lora = 1;
-    g.epi = EPI_16; g.out = B16(h, P.qkv); g.ldo = nqkv;
+    g.op_f16 = 1; g.M = M; g.a = B16(h, Lb.x1); g.lda = H;
+    g.ul = B16(h, Lb.u_b[0]); g.vl = B16(h, P.vl[(size_t)li * 4 + 0]); g.R = Lq.Rpad();
+    g.lora_u = F(h, Lb.u_f32[0]); g.lseg = Lq; g.after_lora = 1;
+    g.epi = EPI_16; g.out = B16(h, Lb.qkv); g.ldo = nqkv;
     SOUP_TRY(timed_gemm(h, g));
   }
-  k_rope_fwd(B16(h, P.qkv), nqkv, F(h, P.rope_cos), F(h, P.rope_sin), M, S, c.n_heads,
+  k_rope_fwd(B16(h, Lb.qkv), nqkv, F(h, P.rope_cos), F(h, P.rope_sin), M, S, c.n_heads,
              c.n_kv_heads, c.head_dim, true, st);
-  SOUP_TRY(k_attn_fwd(B16(h, P.qkv), nqkv, B, S, c.n_heads, c.n_kv_heads, c.head_dim,
-                      B16(h, P.att), F(h, P.lse), st));
-  k_lora_down(B16(h, P.att), qd, M, qd, Lo, F(h, P.u_f32[1]), B16(h, P.u_b[1]), true, true, part, st);
+  SOUP_TRY(k_attn_fwd(B16(h, Lb.qkv), nqkv, B, S, c.n_heads, c.n_kv_heads, c.head_dim,
+                      B16(h, Lb.att), F(h, Lb.lse), st));
+  k_lora_down(B16(h, Lb.att), qd, M, qd, Lo, F(h, Lb.u_f32[1]), B16(h, Lb.u_b[1]), true, true, part, st);
   {
     GemmArgs g = weight_args(h, shard, SOUP_G_O, GEMM_FWD);
-    g.op_f16 = 1; g.M = M; g.a = B16(h, P.att); g.lda = qd;
-    g.ul = B16(h, P.u_b[1]); g.vl = B16(h, P.vl[(size_t)li * 4 + 1]); g.R = Lo.Rpad();
-    g.lora_u = F(h, P.u_f32[1]); g.lseg = Lo; g.after_lora = 1;
-    g.epi = EPI_F32_ADD; g.add_src = hin; g.ld_add = H; g.out = F(h, P.hm); g.ldo = H;
+    g.op_f16 = 1; g.M = M; g.a = B16(h, Lb.att); g.lda = qd;
+    g.ul = B16(h, Lb.u_b[1]); g.vl = B16(h, P.vl[(size_t)li * 4 + 1]); g.R = Lo.Rpad();
+    g.lora_u = F(h, Lb.u_f32[1]); g.lseg = Lo; g.after_lora = 1;
+    g.epi = EPI_F32_ADD; g.add_src = hin; g.ld_add = H; g.out = F(h, Lb.hm); g.ldo = H;
     SOUP_TRY(timed_gemm(h, g));
   }
-  k_rmsnorm_fwd(F(h, P.hm), ln2, c.rms_eps, M, H, B16(h, P.x2), true, st);
-  k_lora_down(B16(h, P.x2), H, M, H, Lg, F(h, P.u_f32[2]), B16(h, P.u_b[2]), true, true, part, st);
+  k_rmsnorm_fwd(F(h, Lb.hm), ln2, c.rms_eps, M, H, B16(h, Lb.x2), true, st);
+  k_lora_down(B16(h, Lb.x2), H, M, H, Lg, F(h, Lb.u_f32[2]), B16(h, Lb.u_b[2]), true, true, part, st);
   {
     GemmArgs g = weight_args(h, shard, SOUP_G_GU, GEMM_FWD);
-    g.op_f16 = 1; g.M = M; g.a = B16(h, P.x2); g.lda = H;
-    g.ul = B16(h, P.u_b[2]); g.vl = B16(h, P.vl[(size_t)li * 4 + 2]); g.R = Lg.Rpad();
-    g.lora_u = F(h, P.u_f32[2]); g.lseg = Lg; g.after_lora = 1;
-    g.epi = EPI_16; g.out = B16(h, P.gu); g.ldo = 2 * I;
+    g.op_f16 = 1; g.M = M; g.a = B16(h, Lb.x2); g.lda = H;
+    g.ul = B16(h, Lb.u_b[2]); g.vl = B16(h, P.vl[(size_t)li * 4 + 2]); g.R = Lg.Rpad();
+    g.lora_u = F(h, Lb.u_f32[2]); g.lseg = Lg; g.after_lora = 1;
+    g.epi = EPI_16; g.out = B16(h, Lb.gu); g.ldo = 2 * I;
     SOUP_TRY(timed_gemm(h, g));
   }
-  k_swiglu_fwd(B16(h, P.gu), M, I, B16(h, P.act), true, st);
-  k_lora_down(B16(h, P.act), I, M, I, Ld, F(h, P.u_f32[3]), B16(h, P.u_b[3]), true, true, part, st);
+  k_swiglu_fwd(B16(h, Lb.gu), M, I, B16(h, Lb.act), true, st);
+  k_lora_down(B16(h, Lb.act), I, M, I, Ld, F(h, Lb.u_f32[3]), B16(h, Lb.u_b[3]), true, true, part, st);
   if (!recompute) {
     GemmArgs g = weight_args(h, shard, SOUP_G_DOWN, GEMM_FWD);
-    g.op_f16 = 1; g.M = M; g.a = B16(h, P.act); g.lda = I;
-    g.ul = B16(h, P.u_b[3]); g.vl = B16(h, P.vl[(size_t)li * 4 + 3]); g.R = Ld.Rpad();
-    g.lora_u = F(h, P.u_f32[3]); g.lseg = Ld; g.after_lora = 1;
-    g.epi = EPI_F32_ADD; g.add_src = F(h, P.hm); g.ld_add = H;
+    g.op_f16 = 1; g.M = M; g.a = B16(h, Lb.act); g.lda = I;
+    g.ul = B16(h, Lb.u_b[3]); g.vl = B16(h, P.vl[(size_t)li * 4 + 3]); g.R = Ld.Rpad();
+    g.lora_u = F(h, Lb.u_f32[3]); g.lseg = Ld; g.after_lora = 1;
+    g.epi = EPI_F32_ADD; g.add_src = F(h, Lb.hm); g.ld_add = H;
     g.out = F(h, P.h_all) + (size_t)(li + 1) * M * H; g.ldo = H;
     SOUP_TRY(timed_gemm(h, g));
   }
@@ -371,6 +397,7 @@ int layer_forward(soup_stream *h, int li, const uint8_t *shard, bool recompute) 
 int group_backward(soup_stream *h, int li, const uint8_t *shard, int grp, const uint16_t *dy,
                    int ldy, const uint16_t *x, int ldx, float *dx_out) {
   const Plan &P = h->plan;
+  const LayerBufs Lb = bufs_of(h, li);
   cudaStream_t st = h->cs;
   const int M = h->B * h->S;
   LoraSeg L = make_seg(h, li, grp, true);
@@ -383,7 +410,7 @@ int group_backward(soup_stream *h, int li, const uint8_t *shard, int grp, const 
   g.lora_u = F(h, P.du_f32); g.lseg = L; g.after_lora = 1;
   g.epi = EPI_F32; g.out = dx_out; g.ldo = K;
   SOUP_TRY(timed_gemm(h, g));
-  k_lora_dB(dy, ldy, M, F(h, P.u_f32[grp]), L, false, F(h, P.lora_part), st);
+  k_lora_dB(dy, ldy, M, F(h, Lb.u_f32[grp]), L, false, F(h, P.lora_part), st);
   k_lora_dA(F(h, P.du_f32), x, ldx, M, K, L, true, F(h, P.lora_part), st);
   return 0;
 }
@@ -391,6 +418,7 @@ int group_backward(soup_stream *h, int li, const uint8_t *shard, int grp, const 
 int layer_backward(soup_stream *h, int li, const uint8_t *shard) {
   const soup_cfg &c = h->cfg;
   const Plan &P = h->plan;
+  const LayerBufs Lb = bufs_of(h, li);
   const soup_shard_layout &SL = h->lay;
   cudaStream_t st = h->cs;
   const int B = h->B, S = h->S, M = B * S, H = c.hidden, I = c.inter;
@@ -400,17 +428,17 @@ int layer_backward(soup_stream *h, int li, const uint8_t *shard) {
   const uint16_t *ln2 = reinterpret_cast<const uint16_t *>(shard + SL.ln2_off);
 
   // dh / dh_b hold dL/dh_{li+1}
-  SOUP_TRY(group_backward(h, li, shard, SOUP_G_DOWN, B16(h, P.dh_b), H, B16(h, P.act), I, F(h, P.dact)));
-  k_swiglu_bwd(F(h, P.dact), B16(h, P.gu), M, I, B16(h, P.dgu), true, st);
-  SOUP_TRY(group_backward(h, li, shard, SOUP_G_GU, B16(h, P.dgu), 2 * I, B16(h, P.x2), H, F(h, P.dx)));
-  k_rmsnorm_bwd(F(h, P.dx), F(h, P.hm), ln2, c.rms_eps, M, H, F(h, P.dh), F(h, P.dhm), B16(h, P.dhm_b), st);
-  SOUP_TRY(group_backward(h, li, shard, SOUP_G_O, B16(h, P.dhm_b), H, B16(h, P.att), qd, F(h, P.datt)));
+  SOUP_TRY(group_backward(h, li, shard, SOUP_G_DOWN, B16(h, P.dh_b), H, B16(h, Lb.act), I, F(h, P.dact)));
+  k_swiglu_bwd(F(h, P.dact), B16(h, Lb.gu), M, I, B16(h, P.dgu), true, st);
+  SOUP_TRY(group_backward(h, li, shard, SOUP_G_GU, B16(h, P.dgu), 2 * I, B16(h, Lb.x2), H, F(h, P.dx)));
+  k_rmsnorm_bwd(F(h, P.dx), F(h, Lb.hm), ln2, c.rms_eps, M, H, F(h, P.dh), F(h, P.dhm), B16(h, P.dhm_b), st);
+  SOUP_TRY(group_backward(h, li, shard, SOUP_G_O, B16(h, P.dhm_b), H, B16(h, Lb.att), qd, F(h, P.datt)));
   k_cast_bf16(F(h, P.datt), B16(h, P.datt_b), (int64_t)M * qd, st);
-  SOUP_TRY(k_attn_bwd(B16(h, P.qkv), nqkv, B16(h, P.att), B16(h, P.datt_b), F(h, P.lse), B, S,
+  SOUP_TRY(k_attn_bwd(B16(h, Lb.qkv), nqkv, B16(h, Lb.att), B16(h, P.datt_b), F(h, Lb.lse), B, S,
                       c.n_heads, c.n_kv_heads, c.head_dim, F(h, P.attn_scratch), F(h, P.dqkv), st));
   k_rope_bwd(F(h, P.dqkv), B16(h, P.dqkv_b), nqkv, F(h, P.rope_cos), F(h, P.rope_sin), M, S,
              c.n_heads, c.n_kv_heads, c.head_dim, st);
-  SOUP_TRY(group_backward(h, li, shard, SOUP_G_QKV, B16(h, P.dqkv_b), nqkv, B16(h, P.x1), H, F(h, P.dx)));
+  SOUP_TRY(group_backward(h, li, shard, SOUP_G_QKV, B16(h, P.dqkv_b), nqkv, B16(h, Lb.x1), H, F(h, P.dx)));
   k_rmsnorm_bwd(F(h, P.dx), hin, ln1, c.rms_eps, M, H, F(h, P.dhm), F(h, P.dh), B16(h, P.dh_b), st);
   return check_cuda("layer backward");
 }
@@ -422,7 +450,7 @@ const uint16_t *lm_weight(soup_stream *h) { return h->lm_head ? h->lm_head : h->
 // ------------------------------------------------------------------------------------------
 int stream_init(soup_store *st, const soup_cfg *c, int maxB, int maxS, void *ws, uint64_t ws_bytes,
                 const void *embed, const void *lm_head, const void *final_norm, uintptr_t cs,
-                uintptr_t xs, int n_slots, int resident, soup_stream **out) {
+                uintptr_t xs, int n_slots, int mode, soup_stream **out) {
   if (!out) return set_error(SOUP_EINVAL, "out is NULL");
   *out = nullptr;
   if (!st || !c || !ws || !embed || !final_norm)
@@ -432,10 +460,11 @@ int stream_init(soup_store *st, const soup_cfg *c, int maxB, int maxS, void *ws,
     return set_error(SOUP_EINVAL, "stream_init: cfg differs from the store's");
   for (int l = 0; l < c->n_layers; ++l)
     if (!st->filled[l]) return set_error(SOUP_ESTATE, "store layer %d was never filled", l);
+  const int resident = (mode & SOUP_MODE_RESIDENT) != 0;
   if (cs == xs && !resident) return set_error(SOUP_EINVAL, "compute and copy streams must differ");
   if (reinterpret_cast<uintptr_t>(ws) % 256) return set_error(SOUP_EINVAL, "workspace must be 256-byte aligned");
   Plan P;
-  SOUP_TRY(make_plan(c, maxB, maxS, n_slots, resident, &P));
+  SOUP_TRY(make_plan(c, maxB, maxS, n_slots, mode, &P));
   if (ws_bytes < P.total)
     return set_error(SOUP_ENOMEM, "workspace %llu bytes < required %llu",
                      (unsigned long long)ws_bytes, (unsigned long long)P.total);
@@ -447,7 +476,8 @@ int stream_init(soup_store *st, const soup_cfg *c, int maxB, int maxS, void *ws,
   h->lay = st->lay;
   h->maxB = maxB;
   h->maxS = maxS;
-  h->resident = resident ? 1 : 0;
+  h->resident = resident;
+  h->keep_act = (mode & SOUP_MODE_KEEP_ACTIVATIONS) != 0;
   h->cs = reinterpret_cast<cudaStream_t>(cs);
   h->xs = reinterpret_cast<cudaStream_t>(xs);
   h->ws = static_cast<uint8_t *>(ws);
@@ -615,8 +645,9 @@ int step_bwd(soup_stream *h, float *const *dA, float *const *dB, float *dh_out, 
     SOUP_TRY(acquire(h, seq, (size_t)j, &shard, &s));
     // the forward's last layer left its activations in the scratch buffers (the loss head
     // between uses separate ones): its backward reuses them instead of recomputing them, which
-    // would reproduce the same values with the same kernels
-    if (!(j == 0 && h->last_layer_fresh)) SOUP_TRY(layer_forward(h, li, shard, true));
+    // would reproduce the same values with the same kernels.  With kept activations every
+    // layer's are still there ("stream_recompute: off"); only the weights are read again.
+    if (!h->keep_act && !(j == 0 && h->last_layer_fresh)) SOUP_TRY(layer_forward(h, li, shard, true));
     h->last_layer_fresh = 0;
     SOUP_TRY(layer_backward(h, li, shard));
     SOUP_TRY(release(h, s));

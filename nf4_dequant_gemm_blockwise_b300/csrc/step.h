@@ -21,6 +21,8 @@ struct Plan {
   std::vector<uint64_t> vl, ac;  // per (layer, group) LoRA operand packs
   uint64_t rope_cos = 0, rope_sin = 0, err = 0;
   uint64_t gemm_part = 0, gemm_part_floats = 0;
+  // keep-activations mode: hm .. u_b[3] repeat once per layer at this stride (0 otherwise)
+  uint64_t act_stride = 0;
 };
 
 struct Slot {
@@ -37,7 +39,8 @@ struct TimedEv {
   double flops = 0, bytes = 0;
 };
 
-int make_plan(const soup_cfg *c, int maxB, int maxS, int n_slots, int resident, Plan *P);
+// mode: SOUP_MODE_RESIDENT | SOUP_MODE_KEEP_ACTIVATIONS bits (soup.h)
+int make_plan(const soup_cfg *c, int maxB, int maxS, int n_slots, int mode, Plan *P);
 int ce_chunk_cols(int M, int V);
 
 }  // namespace soup
@@ -48,6 +51,7 @@ struct soup_stream {
   soup_store *store = nullptr;
   soup::Plan plan;
   int maxB = 0, maxS = 0, resident = 0;
+  int keep_act = 0;  // every layer's activations stay from the forward; no recompute
   cudaStream_t cs = nullptr, xs = nullptr;
   uint8_t *ws = nullptr;
   const uint16_t *embed = nullptr, *lm_head = nullptr, *final_norm = nullptr;
@@ -71,7 +75,7 @@ struct soup_stream {
 namespace soup {
 int stream_init(soup_store *st, const soup_cfg *c, int maxB, int maxS, void *ws, uint64_t ws_bytes,
                 const void *embed, const void *lm_head, const void *final_norm, uintptr_t cs,
-                uintptr_t xs, int n_slots, int resident, soup_stream **out);
+                uintptr_t xs, int n_slots, int mode, soup_stream **out);
 int step_fwd(soup_stream *h, const int32_t *tokens, int B, int S, const float *const *lA,
              const float *const *lB, float *loss, float *logits, float *layer_out);
 int step_bwd(soup_stream *h, float *const *dA, float *const *dB, float *dh_out, int flags);

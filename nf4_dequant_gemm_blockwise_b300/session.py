@@ -23,10 +23,12 @@ def _bits_to_dev(bits: np.ndarray) -> torch.Tensor:
 class StreamedLoRA:
     """cfg: any object with the stack's fields (see api.make_cfg).
     layer_source(i) -> dict of the nine bf16-bit host arrays of layer i.
-    lora: list over layers of 7 (A [r, in], B [out, r]) float32 host arrays."""
+    lora: list over layers of 7 (A [r, in], B [out, r]) float32 host arrays.
+    keep_activations: keep every layer's activations for the backward instead of re-running
+    each layer's forward ("How it works": stream_recompute: off); weights are still re-read."""
 
     def __init__(self, cfg, layer_source, embed_bits, lm_head_bits, final_bits, lora, max_batch,
-                 max_seq, n_slots=2, resident=False, store=None, threads=0):
+                 max_seq, n_slots=2, resident=False, store=None, threads=0, keep_activations=False):
         self.cfg = cfg
         self.own_store = store is None
         if store is None:
@@ -61,14 +63,14 @@ class StreamedLoRA:
         pv, gv = views(self.params), views(self.grad_flat)
         self.lora_A, self.lora_B = pv[0::2], pv[1::2]
         self.dA, self.dB = gv[0::2], gv[1::2]
-        nbytes = api.workspace_bytes(cfg, max_batch, max_seq, n_slots, resident)
+        nbytes = api.workspace_bytes(cfg, max_batch, max_seq, n_slots, resident, keep_activations)
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
         self.compute = torch.cuda.Stream()
         self.copy = torch.cuda.Stream()
         self.loss = torch.zeros(1, dtype=torch.float32, device="cuda")
         self.stream = api.Stream(store, max_batch, max_seq, self.workspace, self.embed, self.lm_head,
                                  self.final, self.compute, self.copy, n_slots=n_slots,
-                                 resident=resident)
+                                 resident=resident, keep_activations=keep_activations)
         torch.cuda.synchronize()
 
     def fwd(self, tokens: torch.Tensor, logits=None, layer_out=None):

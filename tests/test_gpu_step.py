@@ -38,12 +38,13 @@ def cosine(a, b):
     return float(a @ b / max(np.linalg.norm(a) * np.linalg.norm(b), 1e-300))
 
 
-def _session(cfg, resident, store=None, n_slots=2, lora=None):
+def _session(cfg, resident, store=None, n_slots=2, lora=None, keep_activations=False):
     from nf4_dequant_gemm_blockwise_b300.session import StreamedLoRA
     return StreamedLoRA(cfg, lambda i: synth.layer_source(cfg, i), synth.embedding(cfg),
                         synth.lm_head(cfg), synth.final_norm(cfg),
                         lora if lora is not None else synth.lora_params(cfg),
-                        cfg.batch, cfg.seq, n_slots=n_slots, resident=resident, store=store)
+                        cfg.batch, cfg.seq, n_slots=n_slots, resident=resident, store=store,
+                        keep_activations=keep_activations)
 
 
 def _run(sess, cfg, want_logits=True):
@@ -146,6 +147,21 @@ def test_tiny_stale_slot_control_is_caught(tiny):
     assert differs > 0
     clean = _run(s, tiny["cfg"])
     _assert_bit_equal(clean, tiny["resident"])
+
+
+@pytest.mark.parametrize("resident", [False, True])
+def test_tiny_kept_activations_equal_recompute_bitwise(tiny, resident):
+    """"How it works": with stream_recompute off the backward uses the forward's activations
+    of every layer instead of re-running each layer; the same kernels produced them from the
+    same inputs, so every output and gradient is bitwise that of the recomputing stream."""
+    s = _session(tiny["cfg"], resident=resident, store=tiny["s"].store, keep_activations=True)
+    try:
+        k1 = _run(s, tiny["cfg"])
+        k2 = _run(s, tiny["cfg"])  # a second step over the kept buffers
+    finally:
+        s.close()
+    _assert_bit_equal(tiny["stream"], k1)
+    _assert_bit_equal(tiny["stream"], k2)
 
 
 @pytest.mark.parametrize("batch,seq", [(1, 16), (2, 4)])

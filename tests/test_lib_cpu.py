@@ -132,3 +132,27 @@ def test_adamw_and_accumulate_arguments_are_checked_before_any_launch():
     assert "overlap" in api.last_error()
     arr = (api.C.c_void_p * 1)()
     assert api.lib.soup_step_bwd_ex(None, arr, arr, None, api.BWD_ACCUMULATE) == api.EINVAL
+
+
+def test_keep_activations_plan_adds_one_activation_set_per_layer():
+    # the activation set of one layer: mid residual (float), x1, x2 (16-bit), qkv, attention
+    # output, LSE (float per head), gate/up (reserved as float), SwiGLU output, and the LoRA
+    # down-projections of the four groups (float + 16-bit, 64 wide), each 1024-byte aligned
+    cfg = synth.LLAMA8B
+    B, S = 1, 512
+    M, H, I = B * S, cfg.hidden, cfg.inter
+    qd, kvd = cfg.n_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim
+    al = lambda n: -(-n // 1024) * 1024
+    one = (al(4 * M * H) + 2 * al(2 * M * H) + al(2 * M * (qd + 2 * kvd)) + al(2 * M * qd)
+           + al(4 * M * cfg.n_heads) + al(4 * M * I) + al(2 * M * I)
+           + 4 * (al(4 * M * 64) + al(2 * M * 64)))
+    base = api.workspace_bytes(cfg, B, S, n_slots=2)
+    keep = api.workspace_bytes(cfg, B, S, n_slots=2, keep_activations=True)
+    assert keep - base == (cfg.n_layers - 1) * one
+    both = api.workspace_bytes(cfg, B, S, resident=True, keep_activations=True)
+    assert both - api.workspace_bytes(cfg, B, S, resident=True) == (cfg.n_layers - 1) * one
+    tot, ws = api.peak_bytes(cfg, B, S, n_slots=2, keep_activations=True)
+    assert ws == keep and tot - ws == sizes.resident_bytes(cfg)
+    out = api.C.c_uint64()
+    assert api.lib.soup_workspace_bytes(api.C.byref(api.make_cfg(cfg)), B, S, 2, 4,
+                                        api.C.byref(out)) == api.EINVAL
