@@ -460,12 +460,14 @@ int attn_bwd_impl(const uint16_t *qkv, int ld, const uint16_t *o, const uint16_t
   dim3 grid((S + 63) / 64, nh, B);
   constexpr int LDS = D + 8;
   const int smem = (2 * 64 + 3 * 32) * LDS * 2 + 2 * 32 * 4;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  {
+    static std::atomic<int> attr_set[MAX_DEVICES];  // per device, per head dim
+    int done = 0;
+    cudaError_t e = per_device_once(attr_set, &done, [&](int, int *v) {
+      *v = 1;
+      return cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    });
     if (e != cudaSuccess) return set_error(SOUP_ECUDA, "attn smem attribute: %s", cudaGetErrorString(e));
-    attr = true;
   }
   attn_bwd_dkdv_kernel<D><<<grid, 128, smem, st>>>(qkv, ld, dO, lse, dsum, S, nh, nkv, part_k,
                                                    part_v, scale_log2, scale);

@@ -25,7 +25,7 @@
 //   boundary leaves one partial per CTA, summed in CTA order by a fix-up kernel (no atomics,
 //   so every launch is bit-reproducible).
 #include <algorithm>
-#include <mutex>
+#include <atomic>
 
 #include "common.cuh"
 #include "gemm.h"
@@ -626,36 +626,27 @@ __global__ void __launch_bounds__(GV_THREADS) gemv_fixup_kernel(const GvParams p
 }
 
 // ------------------------------------------------------------------ host
-std::mutex g_gv_mu;
-int g_sms = 0;
-
 int sm_count() {
-  std::lock_guard<std::mutex> lk(g_gv_mu);
-  if (!g_sms) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-      (void)cudaGetLastError();
-      g_sms = 0;
-    }
+  static std::atomic<int> sms[MAX_DEVICES];
+  int n = 0;
+  if (per_device_once(sms, &n, [](int dev, int *v) {
+        return cudaDeviceGetAttribute(v, cudaDevAttrMultiProcessorCount, dev);
+      }) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
   }
-  return g_sms;
+  return n;
 }
 
 template <int MODE, int NT, typename K>
 int resident_ctas(K kern, int threads, int smem, int *out) {
-  static std::mutex mu;
-  static int cached = 0;  // per (MODE, NT) instantiation
-  std::lock_guard<std::mutex> lk(mu);
-  if (!cached) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cached, kern, threads, smem);
-    if (e != cudaSuccess) {
-      cached = 0;
-      return set_error(SOUP_ECUDA, "small-M GEMM setup: %s", cudaGetErrorString(e));
-    }
-  }
-  *out = cached;
+  static std::atomic<int> cached[MAX_DEVICES];  // per device, per (MODE, NT) instantiation
+  cudaError_t e = per_device_once(cached, out, [&](int, int *v) {
+    cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (r == cudaSuccess) r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(v, kern, threads, smem);
+    return r;
+  });
+  if (e != cudaSuccess) return set_error(SOUP_ECUDA, "small-M GEMM setup: %s", cudaGetErrorString(e));
   return 0;
 }
 
