@@ -92,6 +92,9 @@ def _args():
     p.add_argument("--seq", type=int, default=512)
     p.add_argument("--slots", type=int, default=2)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--pageable", action="store_true",
+                   help="stream from a pageable (not page-locked) copy of the store, to measure "
+                        "what the pageable fallback costs")
     p.add_argument("--no-overlap", action="store_true", help="skip the resident comparison run")
     p.add_argument("--no-variants", action="store_true",
                    help="skip the extra batch-4 / eight-slot measurements")
@@ -363,6 +366,12 @@ def run_ours(args, rank, world, local_rank, dist):
         idx = list(range(i0, min(cfg.n_layers, i0 + 8)))
         for i, src in zip(idx, synth.layer_sources(cfg, idx)):
             store.put_layer(i, [src[t] for t in synth.LAYER_TENSORS])
+    if args.pageable:
+        paged = api.Store(cfg, force_pageable=True)
+        for i in range(cfg.n_layers):
+            paged.put_shard(i, store.shard_bytes(i))
+        store.free()
+        store = paged
     t_build = time.perf_counter() - t_build
     _, store_bytes, pinned = store.info()
 
@@ -477,7 +486,7 @@ def run_ours(args, rank, world, local_rank, dist):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": _workload(cfg, args.slots),
+        "config": dict(_workload(cfg, args.slots), **({"store": "pageable"} if args.pageable else {})),
         "e2e": {"value": e2e_value, "unit": UNIT,
                 "h2d_bytes_per_step": tok_host.numel() * 4 + st_e2e["copy_bytes"] / args.steps,
                 "d2h_bytes_per_step": 4},

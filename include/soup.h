@@ -131,12 +131,19 @@ int soup_nf4_quantize_host(const uint16_t *src, int64_t n, uint8_t *codes, float
 /* Create an empty store of cfg.n_layers shards in ONE page-locked host arena (exact size,
  * no power-of-two rounding: the pages report rounding cost 1.73x at 14B).  If page-locking
  * fails and allow_pageable != 0, a pageable arena is used and SOUP_EPAGEABLE is returned
- * ("Measured numbers": pageable copies are synchronous and lose the overlap). */
+ * ("Measured numbers": pageable copies are synchronous and lose the overlap).
+ * allow_pageable == SOUP_STORE_PAGEABLE skips page-locking altogether (returns SOUP_OK), to
+ * measure what the pageable fallback costs. */
+enum { SOUP_STORE_PAGEABLE = 2 };
 int soup_store_create(const soup_cfg *cfg, int allow_pageable, soup_store **out);
 /* Quantise (NF4) or copy (bf16) one layer into its shard.  src: host pointers to the nine
  * bf16 tensors of the layer in order q,k,v,o,gate,up,down ([out,in] each), ln1, ln2 [hidden].
  * May be called from several host threads for different layers. */
 int soup_store_put_layer(soup_store *st, int layer, const uint16_t *const *src, int n_threads);
+/* Fill one shard from its bytes as laid out by soup_shard_layout_of (a shard read back from
+ * another store of the same cfg, or from a cache of built shards).  bytes must equal the
+ * layout's stride; the store keeps its own copy.  Thread-safe for different layers. */
+int soup_store_put_shard(soup_store *st, int layer, const void *shard, uint64_t bytes);
 /* soup_store_create + put_layer for every layer: src is [n_layers * 9] host pointers. */
 int soup_store_build(const soup_cfg *cfg, const uint16_t *const *src, int allow_pageable,
                      soup_store **out);

@@ -57,6 +57,7 @@ class soup_adamw(C.Structure):
 
 
 BWD_ACCUMULATE = 1
+STORE_PAGEABLE = 2
 MODE_RESIDENT, MODE_KEEP_ACTIVATIONS = 1, 2
 
 
@@ -79,6 +80,7 @@ def _load() -> C.CDLL:
         "soup_nf4_quantize_host": (I32, [P, C.c_int64, P, P, I32]),
         "soup_store_create": (I32, [C.POINTER(soup_cfg), I32, C.POINTER(VP)]),
         "soup_store_put_layer": (I32, [VP, I32, C.POINTER(P), I32]),
+        "soup_store_put_shard": (I32, [VP, I32, P, U64]),
         "soup_store_build": (I32, [C.POINTER(soup_cfg), C.POINTER(P), I32, C.POINTER(VP)]),
         "soup_store_info": (I32, [VP, C.POINTER(P), C.POINTER(U64), C.POINTER(I32)]),
         "soup_store_free": (None, [VP]),
@@ -203,10 +205,12 @@ def peak_bytes(cfg, batch, seq, n_slots=2, resident=False, keep_activations=Fals
 class Store:
     """One page-locked host arena holding every layer's shard (soup_store_*)."""
 
-    def __init__(self, cfg, allow_pageable: bool = True):
+    def __init__(self, cfg, allow_pageable: bool = True, force_pageable: bool = False):
+        """force_pageable: skip page-locking (to measure the pageable fallback)."""
         self.cfg = make_cfg(cfg)
         h = C.c_void_p()
-        rc = lib.soup_store_create(C.byref(self.cfg), int(allow_pageable), C.byref(h))
+        rc = lib.soup_store_create(C.byref(self.cfg), STORE_PAGEABLE if force_pageable else int(allow_pageable),
+                                   C.byref(h))
         self.pageable_warning = rc == EPAGEABLE
         _check(rc, allow=(EPAGEABLE,))
         self.handle = h
@@ -216,6 +220,11 @@ class Store:
         arrs = [np.ascontiguousarray(t, np.uint16) for t in tensors]
         ptrs = (C.c_void_p * 9)(*[a.ctypes.data for a in arrs])
         _check(lib.soup_store_put_layer(self.handle, layer, ptrs, n_threads))
+
+    def put_shard(self, layer: int, shard: np.ndarray):
+        """Fill a shard from its bytes (e.g. another store's ``shard_bytes``)."""
+        b = np.ascontiguousarray(shard, np.uint8)
+        _check(lib.soup_store_put_shard(self.handle, layer, b.ctypes.data, b.nbytes))
 
     def info(self):
         base, nb, pinned = C.c_void_p(), C.c_uint64(), C.c_int()

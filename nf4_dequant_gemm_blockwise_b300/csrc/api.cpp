@@ -68,6 +68,9 @@ int soup_store_create(const soup_cfg *cfg, int allow_pageable, soup_store **out)
 int soup_store_put_layer(soup_store *st, int layer, const uint16_t *const *src, int n_threads) {
   return store_put_layer(st, layer, src, n_threads);
 }
+int soup_store_put_shard(soup_store *st, int layer, const void *shard, uint64_t bytes) {
+  return store_put_shard(st, layer, shard, bytes);
+}
 int soup_store_build(const soup_cfg *cfg, const uint16_t *const *src, int allow_pageable,
                      soup_store **out) {
   if (!src) return set_error(SOUP_EINVAL, "src is NULL");

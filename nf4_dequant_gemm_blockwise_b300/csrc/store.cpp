@@ -202,7 +202,8 @@ int store_create(const soup_cfg *c, int allow_pageable, soup_store **out) {
   st->lay = L;
   st->bytes = L.stride * (uint64_t)c->n_layers;
   void *p = nullptr;
-  cudaError_t e = cudaHostAlloc(&p, st->bytes, cudaHostAllocDefault);
+  const bool force_pageable = allow_pageable == SOUP_STORE_PAGEABLE;
+  cudaError_t e = force_pageable ? cudaErrorNotPermitted : cudaHostAlloc(&p, st->bytes, cudaHostAllocDefault);
   int rc = 0;
   if (e == cudaSuccess) {
     st->pinned = 1;
@@ -221,13 +222,25 @@ int store_create(const soup_cfg *c, int allow_pageable, soup_store **out) {
                        (unsigned long long)(L.stride * (uint64_t)c->n_layers));
     }
     st->pinned = 0;
-    rc = set_error(SOUP_EPAGEABLE, "store: page-locking failed (%s); using pageable memory",
-                   cudaGetErrorString(e));
+    if (!force_pageable)
+      rc = set_error(SOUP_EPAGEABLE, "store: page-locking failed (%s); using pageable memory",
+                     cudaGetErrorString(e));
   }
   st->base = static_cast<uint8_t *>(p);
   st->filled.assign(c->n_layers, 0);
   *out = st;
   return rc;
+}
+
+int store_put_shard(soup_store *st, int layer, const void *shard, uint64_t bytes) {
+  if (!st || !shard) return set_error(SOUP_EINVAL, "store_put_shard: NULL argument");
+  if (layer < 0 || layer >= st->cfg.n_layers) return set_error(SOUP_EINVAL, "layer %d out of range", layer);
+  if (bytes != st->lay.stride)
+    return set_error(SOUP_EINVAL, "store_put_shard: %llu bytes, the shard stride is %llu",
+                     (unsigned long long)bytes, (unsigned long long)st->lay.stride);
+  std::memcpy(st->base + (uint64_t)layer * st->lay.stride, shard, bytes);
+  st->filled[layer] = 1;
+  return 0;
 }
 
 int store_put_layer(soup_store *st, int layer, const uint16_t *const *src, int n_threads) {

@@ -21,6 +21,7 @@ void group_shapes(const soup_cfg *c, int n_out[4], int n_in[4]);
 int shard_layout(const soup_cfg *c, soup_shard_layout *L);
 int store_create(const soup_cfg *c, int allow_pageable, soup_store **out);
 int store_put_layer(soup_store *st, int layer, const uint16_t *const *src, int n_threads);
+int store_put_shard(soup_store *st, int layer, const void *shard, uint64_t bytes);
 void store_free(soup_store *st);
 void nf4_quantize_host(const uint16_t *src, int64_t n, uint8_t *codes, float *absmax, int n_threads);
 const float *nf4_midpoints();

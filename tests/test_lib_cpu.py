@@ -156,3 +156,25 @@ def test_keep_activations_plan_adds_one_activation_set_per_layer():
     out = api.C.c_uint64()
     assert api.lib.soup_workspace_bytes(api.C.byref(api.make_cfg(cfg)), B, S, 2, 4,
                                         api.C.byref(out)) == api.EINVAL
+
+
+def test_forced_pageable_store_and_raw_shard_copy():
+    # a store filled shard by shard from another store's bytes is byte-identical, and a store
+    # created with page-locking skipped reports itself pageable without a warning
+    cfg = synth.TINY
+    a = api.Store(cfg)
+    for i in range(cfg.n_layers):
+        src = synth.layer_source(cfg, i)
+        a.put_layer(i, [src[t] for t in synth.LAYER_TENSORS])
+    b = api.Store(cfg, force_pageable=True)
+    assert not b.pageable_warning and b.info()[2] is False
+    for i in range(cfg.n_layers):
+        b.put_shard(i, a.shard_bytes(i))
+    for i in range(cfg.n_layers):
+        assert np.array_equal(a.shard_bytes(i), b.shard_bytes(i))
+    with pytest.raises(api.SoupError):
+        b.put_shard(0, a.shard_bytes(0)[:-16])
+    with pytest.raises(api.SoupError):
+        b.put_shard(cfg.n_layers, a.shard_bytes(0))
+    a.free()
+    b.free()
