@@ -199,7 +199,11 @@ int soup_stream_init(soup_store *st, const soup_cfg *cfg, int max_batch, int max
  *   tokens_dev: dev int32 [B, S], ids in [0, vocab) (ids out of range are clamped).
  *   lora_A: host array [n_layers * 7] of dev float [r, in_p]; lora_B: [n_layers * 7] of dev
  *   float [out_p, r]; p in SOUP_Q..SOUP_DOWN order.  They must stay valid until the matching
- *   soup_step_bwd has been enqueued.
+ *   soup_step_bwd has been enqueued.  Both NULL switches the adapters off: the frozen base
+ *   alone over the same stream, the reference model of preference losses ("Layer streaming:
+ *   fine-tune a model that does not fit in your card", opening version notes: DPO's
+ *   reference model is the streamed base with its adapters switched off); soup_step_bwd then
+ *   returns SOUP_ESTATE until a forward with adapters.  One NULL and one not: SOUP_EINVAL.
  *   loss_dev: dev float [1], mean next-token cross-entropy over B*(S-1) positions.
  *   logits_dev (optional, NULL in timed runs): dev float [B*S, vocab].
  *   layer_out_dev (optional): dev float [(n_layers + 1), B*S, hidden] — the residual stream

@@ -276,9 +276,13 @@ class Stream:
         self.handle = h
 
     def fwd(self, tokens, B, S, lora_A, lora_B, loss, logits=None, layer_out=None):
-        n = len(lora_A)
-        a = (C.c_void_p * n)(*[_ptr(t) for t in lora_A])
-        b = (C.c_void_p * n)(*[_ptr(t) for t in lora_B])
+        """lora_A = lora_B = None: adapters switched off (the base alone)."""
+        if lora_A is None and lora_B is None:
+            a = b = None
+        else:
+            n = len(lora_A)
+            a = (C.c_void_p * n)(*[_ptr(t) for t in lora_A])
+            b = (C.c_void_p * n)(*[_ptr(t) for t in lora_B])
         self._lora = (a, b, lora_A, lora_B)
         _check(lib.soup_step_fwd(self.handle, _ptr(tokens), B, S, a, b, _ptr(loss), _ptr(logits),
                                  _ptr(layer_out)))

@@ -214,8 +214,10 @@ LoraSeg make_seg(soup_stream *h, int layer, int g, bool grads) {
     L.off[p] = off;
     L.n[p] = sizes[proj];
     off += sizes[proj];
-    L.A[p] = h->lora_A[idx];
-    L.B[p] = h->lora_B[idx];
+    if (!h->adapters_off) {
+      L.A[p] = h->lora_A[idx];
+      L.B[p] = h->lora_B[idx];
+    }
     if (grads) {
       L.dA[p] = h->grad_A[idx];
       L.dB[p] = h->grad_B[idx];
@@ -346,13 +348,18 @@ int layer_forward(soup_stream *h, int li, const uint8_t *shard, bool recompute) 
 
   float *part = F(h, P.lora_part);
   // the forward's tensor-core operands are IEEE half (x1, qkv, att, x2, gu, act, LoRA packs)
+  // adapters switched off (the reference forward of preference losses): no LoRA kernels and
+  // no LoRA extension tiles, the plain dequant GEMMs
+  const bool ad = !h->adapters_off;
   k_rmsnorm_fwd(hin, ln1, c.rms_eps, M, H, B16(h, Lb.x1), true, st);
-  k_lora_down(B16(h, Lb.x1), H, M, H, Lq, F(h, Lb.u_f32[0]), B16(h, Lb.u_b[0]), true, true, part, st);
+  if (ad) k_lora_down(B16(h, Lb.x1), H, M, H, Lq, F(h, Lb.u_f32[0]), B16(h, Lb.u_b[0]), true, true, part, st);
   {
     GemmArgs g = weight_args(h, shard, SOUP_G_QKV, GEMM_FWD);
     g.op_f16 = 1; g.M = M; g.a = B16(h, Lb.x1); g.lda = H;
-    g.ul = B16(h, Lb.u_b[0]); g.vl = B16(h, P.vl[(size_t)li * 4 + 0]); g.R = Lq.Rpad();
-    g.lora_u = F(h, Lb.u_f32[0]); g.lseg = Lq; g.after_lora = 1;
+    if (ad) {
+      g.ul = B16(h, Lb.u_b[0]); g.vl = B16(h, P.vl[(size_t)li * 4 + 0]); g.R = Lq.Rpad();
+      g.lora_u = F(h, Lb.u_f32[0]); g.lseg = Lq; g.after_lora = 1;
+    }
     g.epi = EPI_16; g.out = B16(h, Lb.qkv); g.ldo = nqkv;
     SOUP_TRY(timed_gemm(h, g));
   }
@@ -360,32 +367,38 @@ int layer_forward(soup_stream *h, int li, const uint8_t *shard, bool recompute) 
              c.n_kv_heads, c.head_dim, true, st);
   SOUP_TRY(k_attn_fwd(B16(h, Lb.qkv), nqkv, B, S, c.n_heads, c.n_kv_heads, c.head_dim,
                       B16(h, Lb.att), F(h, Lb.lse), st));
-  k_lora_down(B16(h, Lb.att), qd, M, qd, Lo, F(h, Lb.u_f32[1]), B16(h, Lb.u_b[1]), true, true, part, st);
+  if (ad) k_lora_down(B16(h, Lb.att), qd, M, qd, Lo, F(h, Lb.u_f32[1]), B16(h, Lb.u_b[1]), true, true, part, st);
   {
     GemmArgs g = weight_args(h, shard, SOUP_G_O, GEMM_FWD);
     g.op_f16 = 1; g.M = M; g.a = B16(h, Lb.att); g.lda = qd;
-    g.ul = B16(h, Lb.u_b[1]); g.vl = B16(h, P.vl[(size_t)li * 4 + 1]); g.R = Lo.Rpad();
-    g.lora_u = F(h, Lb.u_f32[1]); g.lseg = Lo; g.after_lora = 1;
+    if (ad) {
+      g.ul = B16(h, Lb.u_b[1]); g.vl = B16(h, P.vl[(size_t)li * 4 + 1]); g.R = Lo.Rpad();
+      g.lora_u = F(h, Lb.u_f32[1]); g.lseg = Lo; g.after_lora = 1;
+    }
     g.epi = EPI_F32_ADD; g.add_src = hin; g.ld_add = H; g.out = F(h, Lb.hm); g.ldo = H;
     SOUP_TRY(timed_gemm(h, g));
   }
   k_rmsnorm_fwd(F(h, Lb.hm), ln2, c.rms_eps, M, H, B16(h, Lb.x2), true, st);
-  k_lora_down(B16(h, Lb.x2), H, M, H, Lg, F(h, Lb.u_f32[2]), B16(h, Lb.u_b[2]), true, true, part, st);
+  if (ad) k_lora_down(B16(h, Lb.x2), H, M, H, Lg, F(h, Lb.u_f32[2]), B16(h, Lb.u_b[2]), true, true, part, st);
   {
     GemmArgs g = weight_args(h, shard, SOUP_G_GU, GEMM_FWD);
     g.op_f16 = 1; g.M = M; g.a = B16(h, Lb.x2); g.lda = H;
-    g.ul = B16(h, Lb.u_b[2]); g.vl = B16(h, P.vl[(size_t)li * 4 + 2]); g.R = Lg.Rpad();
-    g.lora_u = F(h, Lb.u_f32[2]); g.lseg = Lg; g.after_lora = 1;
+    if (ad) {
+      g.ul = B16(h, Lb.u_b[2]); g.vl = B16(h, P.vl[(size_t)li * 4 + 2]); g.R = Lg.Rpad();
+      g.lora_u = F(h, Lb.u_f32[2]); g.lseg = Lg; g.after_lora = 1;
+    }
     g.epi = EPI_16; g.out = B16(h, Lb.gu); g.ldo = 2 * I;
     SOUP_TRY(timed_gemm(h, g));
   }
   k_swiglu_fwd(B16(h, Lb.gu), M, I, B16(h, Lb.act), true, st);
-  k_lora_down(B16(h, Lb.act), I, M, I, Ld, F(h, Lb.u_f32[3]), B16(h, Lb.u_b[3]), true, true, part, st);
+  if (ad) k_lora_down(B16(h, Lb.act), I, M, I, Ld, F(h, Lb.u_f32[3]), B16(h, Lb.u_b[3]), true, true, part, st);
   if (!recompute) {
     GemmArgs g = weight_args(h, shard, SOUP_G_DOWN, GEMM_FWD);
     g.op_f16 = 1; g.M = M; g.a = B16(h, Lb.act); g.lda = I;
-    g.ul = B16(h, Lb.u_b[3]); g.vl = B16(h, P.vl[(size_t)li * 4 + 3]); g.R = Ld.Rpad();
-    g.lora_u = F(h, Lb.u_f32[3]); g.lseg = Ld; g.after_lora = 1;
+    if (ad) {
+      g.ul = B16(h, Lb.u_b[3]); g.vl = B16(h, P.vl[(size_t)li * 4 + 3]); g.R = Ld.Rpad();
+      g.lora_u = F(h, Lb.u_f32[3]); g.lseg = Ld; g.after_lora = 1;
+    }
     g.epi = EPI_F32_ADD; g.add_src = F(h, Lb.hm); g.ld_add = H;
     g.out = F(h, P.h_all) + (size_t)(li + 1) * M * H; g.ldo = H;
     SOUP_TRY(timed_gemm(h, g));
@@ -533,19 +546,27 @@ int stream_init(soup_store *st, const soup_cfg *c, int maxB, int maxS, void *ws,
 
 int step_fwd(soup_stream *h, const int32_t *tokens, int B, int S, const float *const *lA,
              const float *const *lB, float *loss, float *logits, float *layer_out) {
-  if (!h || !tokens || !lA || !lB || !loss) return set_error(SOUP_EINVAL, "step_fwd: NULL argument");
+  if (!h || !tokens || !loss) return set_error(SOUP_EINVAL, "step_fwd: NULL argument");
+  if (!lA != !lB) return set_error(SOUP_EINVAL, "step_fwd: lora_A and lora_B must both be given or both NULL");
+  const bool adapters_off = !lA;
   const soup_cfg &c = h->cfg;
   if (B < 1 || S < 2 || S > h->maxS || (int64_t)B * S > (int64_t)h->maxB * h->maxS)
     return set_error(SOUP_EINVAL, "step_fwd: B=%d S=%d outside the workspace (max %d x %d)", B, S,
                      h->maxB, h->maxS);
   const int L = c.n_layers;
-  for (int i = 0; i < L * 7; ++i)
+  for (int i = 0; i < L * 7 && !adapters_off; ++i)
     if (!lA[i] || !lB[i]) return set_error(SOUP_EINVAL, "step_fwd: LoRA pointer %d is NULL", i);
   h->B = B;
   h->S = S;
   h->tokens = tokens;
-  h->lora_A.assign(lA, lA + (size_t)L * 7);
-  h->lora_B.assign(lB, lB + (size_t)L * 7);
+  h->adapters_off = adapters_off ? 1 : 0;
+  if (adapters_off) {
+    h->lora_A.clear();
+    h->lora_B.clear();
+  } else {
+    h->lora_A.assign(lA, lA + (size_t)L * 7);
+    h->lora_B.assign(lB, lB + (size_t)L * 7);
+  }
   h->in_bwd = 0;
   harvest(h, false);
   const Plan &P = h->plan;
@@ -561,7 +582,7 @@ int step_fwd(soup_stream *h, const int32_t *tokens, int B, int S, const float *c
     // 16-bit LoRA operands of this layer's tensor-core GEMMs (forward: half B rows; dX:
     // bf16 A rows), packed just before first use so that the first layer's kernels, and so
     // the first slot release, are not queued behind every layer's packing
-    for (int g = 0; g < 4; ++g) {
+    for (int g = 0; g < 4 && !adapters_off; ++g) {
       LoraSeg Lg = make_seg(h, i, g, false);
       k_pack_fwd(Lg, h->lay.n_out[g], B16(h, P.vl[(size_t)i * 4 + g]), true, st);
       k_pack_bwd(Lg, h->lay.n_in[g], B16(h, P.ac[(size_t)i * 4 + g]), false, st);
@@ -590,7 +611,8 @@ int step_fwd(soup_stream *h, const int32_t *tokens, int B, int S, const float *c
     SOUP_CUDA_TRY(cudaMemcpyAsync(layer_out, F(h, P.h_all), 4ull * (L + 1) * M * H,
                                   cudaMemcpyDeviceToDevice, st));
   SOUP_CUDA_TRY(cudaEventRecord(h->done, st));
-  h->fwd_ready = 1;
+  // a backward follows a forward with adapters only; an adapters-off forward leaves none
+  h->fwd_ready = adapters_off ? 0 : 1;
   h->last_layer_fresh = 1;  // the last layer's activations are still in the scratch buffers
   h->stats.steps_fwd += 1;
   return check_cuda("step_fwd");
@@ -599,7 +621,9 @@ int step_fwd(soup_stream *h, const int32_t *tokens, int B, int S, const float *c
 int step_bwd(soup_stream *h, float *const *dA, float *const *dB, float *dh_out, int flags) {
   if (!h || !dA || !dB) return set_error(SOUP_EINVAL, "step_bwd: NULL argument");
   if (flags & ~SOUP_BWD_ACCUMULATE) return set_error(SOUP_EINVAL, "step_bwd: unknown flags 0x%x", flags);
-  if (!h->fwd_ready) return set_error(SOUP_ESTATE, "step_bwd without a preceding step_fwd");
+  if (!h->fwd_ready)
+    return set_error(SOUP_ESTATE, h->adapters_off ? "step_bwd after an adapters-off forward"
+                                                  : "step_bwd without a preceding step_fwd");
   const soup_cfg &c = h->cfg;
   const int L = c.n_layers;
   for (int i = 0; i < L * 7; ++i)

@@ -66,6 +66,7 @@ struct soup_stream {
   std::vector<const float *> lora_A, lora_B;
   std::vector<float *> grad_A, grad_B;
   int grad_accumulate = 0;  // this backward adds to grad_A/grad_B (SOUP_BWD_ACCUMULATE)
+  int adapters_off = 0;     // the last forward ran without adapters (lora_A = lora_B = NULL)
   // measurement
   soup_stats stats{};
   std::vector<soup::TimedEv> copy_ev, gemm_ev;

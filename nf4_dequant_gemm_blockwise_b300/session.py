@@ -78,6 +78,13 @@ class StreamedLoRA:
         self.compute.wait_stream(torch.cuda.current_stream())
         self.stream.fwd(tokens, B, S, self.lora_A, self.lora_B, self.loss, logits, layer_out)
 
+    def reference_fwd(self, tokens: torch.Tensor, loss: torch.Tensor, logits=None, layer_out=None):
+        """Forward of the frozen base with the adapters switched off, over the same stream (the
+        reference model of preference losses); no backward may follow it."""
+        B, S = tokens.shape
+        self.compute.wait_stream(torch.cuda.current_stream())
+        self.stream.fwd(tokens, B, S, None, None, loss, logits, layer_out)
+
     def bwd(self, dh_out=None, accumulate=False):
         """accumulate: add this backward's LoRA gradients to the ones held (micro-batches)."""
         self.stream.bwd(self.dA, self.dB, dh_out, accumulate=accumulate)

@@ -149,6 +149,42 @@ def test_tiny_stale_slot_control_is_caught(tiny):
     _assert_bit_equal(clean, tiny["resident"])
 
 
+def test_tiny_adapters_off_forward_is_the_base(tiny):
+    """The reference forward of preference losses: the streamed base with the adapters
+    switched off.  Streamed == resident bitwise; against the oracle with no LoRA at the forward
+    bars; no backward may follow it; the next step with adapters is unaffected."""
+    from nf4_dequant_gemm_blockwise_b300 import api
+    cfg = tiny["cfg"]
+    M = cfg.batch * cfg.seq
+    tok = torch.from_numpy(synth.tokens(cfg)).cuda()
+    outs = []
+    for sess in (tiny["s"], tiny["r"]):
+        logits = torch.empty((M, cfg.vocab), dtype=torch.float32, device="cuda")
+        lay = torch.empty((cfg.n_layers + 1, M, cfg.hidden), dtype=torch.float32, device="cuda")
+        loss = torch.zeros(1, dtype=torch.float32, device="cuda")
+        sess.reference_fwd(tok, loss, logits=logits, layer_out=lay)
+        sess.sync()
+        outs.append((float(loss.item()), logits.cpu().numpy(), lay.cpu().numpy()))
+        with pytest.raises(api.SoupError) as e:
+            sess.bwd()
+        assert e.value.code == api.ESTATE
+    (ls, zs, hs), (lr_, zr, hr) = outs
+    assert ls == lr_
+    assert np.array_equal(zs.view(np.uint32), zr.view(np.uint32))
+    assert np.array_equal(hs.view(np.uint32), hr.view(np.uint32))
+    W = model.weights_from_source(cfg, [synth.layer_source(cfg, i) for i in range(cfg.n_layers)],
+                                  synth.embedding(cfg), synth.lm_head(cfg), synth.final_norm(cfg))
+    o = model.forward(cfg, W, synth.tokens(cfg), None, keep_cache=False)
+    for i in range(cfg.n_layers + 1):
+        assert rel_l2(hs[i], o["hs"][i].reshape(M, -1)) <= TOL_FWD_REL, i
+    lo = o["logits"].reshape(M, -1)
+    assert rel_l2(zs, lo) <= TOL_FWD_REL
+    assert np.abs(zs - lo).max() <= TOL_LOGIT_ABS
+    assert abs(ls - o["loss"]) <= 1e-3 * o["loss"]
+    assert not np.array_equal(zs, tiny["stream"]["logits"])  # the adapters do change the output
+    _assert_bit_equal(tiny["stream"], _run(tiny["s"], cfg))
+
+
 @pytest.mark.parametrize("resident", [False, True])
 def test_tiny_kept_activations_equal_recompute_bitwise(tiny, resident):
     """"How it works": with stream_recompute off the backward uses the forward's activations
