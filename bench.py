@@ -323,7 +323,38 @@ def run_micro(args):
                 out[name] = {"us": t * 1e6, "tflops": flops / t / 1e12, "gbs": byts / t / 1e9,
                              "bound": bound, "frac": max(t_hbm, t_tc) / t}
             out["peak_source"] = f"{peaks['src']}: hbm {peaks['hbm']} GB/s, bf16 burst {peaks['bf16']} TFLOP/s"
+            if not args.no_cpu_baseline:
+                out["cpu_baseline"] = run_micro_oracle(N, K, M, r, s, codes, absmax, A, B)
             print(json.dumps(out), flush=True)
+
+
+def run_micro_oracle(N, K, M, r, s, codes, absmax, A, B, cap_rows=512):
+    """The CPU oracle on one microbench projection: forward (dequantise + x W^T + LoRA) and
+    backward (dequantise + dX + dA/dB), float32 NumPy.  Above cap_rows rows the products of a
+    cap_rows-row slice are timed and scaled by M / cap_rows (they are linear in M); the
+    dequantisation is timed once and counted in both."""
+    import numpy as np
+
+    import synth
+    from oracle import model, nf4
+
+    rows = min(M, cap_rows)
+    x = synth.bf16_bits_to_f32(synth.activations_bf16(M, K, key=1))[:rows]
+    x = x.astype(np.float16).astype(np.float32)
+    dy = synth.bf16_bits_to_f32(synth.activations_bf16(M, N, key=2))[:rows]
+    t0 = time.perf_counter()
+    W = nf4.dequantize_tensor(codes, absmax, (N, K))
+    t1 = time.perf_counter()
+    _, u = model.lora_linear(x, W, A, B, s)
+    t2 = time.perf_counter()
+    model.lora_linear_backward(dy, x, u, W, A, B, s)
+    t3 = time.perf_counter()
+    scale = M / rows
+    deq = t1 - t0  # once per call, like the kernels' dequantisation
+    return {"fwd_us": (deq + (t2 - t1) * scale) * 1e6, "bwd_us": (deq + (t3 - t2) * scale) * 1e6,
+            "cores": _threads(), "kind": "oracle",
+            "sample": f"products on {rows} of {M} rows, scaled by {scale:g}; one dequantisation "
+                      f"per call"}
 
 
 # ------------------------------------------------------------------------------ our arm
