@@ -212,6 +212,32 @@ def run_oracle_timed(cfg):
     return one
 
 
+def oracle_tiny_step_s():
+    """Wall time of the oracle's whole tiny-stack step (2 layers, S=64: forward, loss, backward,
+    AdamW on every adapter), best of 3."""
+    import numpy as np
+
+    import synth
+    from oracle import model, optim
+
+    cfg = synth.TINY
+    W = model.weights_from_source(cfg, [synth.layer_source(cfg, i) for i in range(cfg.n_layers)],
+                                  synth.embedding(cfg), synth.lm_head(cfg), synth.final_norm(cfg))
+    tok = synth.tokens(cfg)
+    lora = synth.lora_params(cfg)
+    best = float("inf")
+    for _ in range(3):
+        t0 = time.perf_counter()
+        fwd = model.forward(cfg, W, tok, lora)
+        grads, _ = model.backward(cfg, W, tok, lora, fwd)
+        for layer_g, layer_p in zip(grads, lora):
+            for (dA, dB), (A, B) in zip(layer_g, layer_p):
+                optim.adamw_step(A, dA, np.zeros_like(dA), np.zeros_like(dA), 1, LR)
+                optim.adamw_step(B, dB, np.zeros_like(dB), np.zeros_like(dB), 1, LR)
+        best = min(best, time.perf_counter() - t0)
+    return best
+
+
 def _threads():
     try:
         from threadpoolctl import threadpool_info
@@ -580,7 +606,8 @@ def run_ours(args, rank, world, local_rank, dist):
         line["cpu_baseline"] = {"value": tokens / step_s, "unit": UNIT, "cores": _threads(), "kind": "oracle",
                                 "sample": f"one decoder layer fwd+bwd+AdamW and the output head fwd+bwd of this "
                                           f"workload on the CPU oracle (float32 NumPy), step time = "
-                                          f"{cfg.n_layers} x layer + head; best of 2"}
+                                          f"{cfg.n_layers} x layer + head; best of 2",
+                                "tiny_step_s": oracle_tiny_step_s()}
     sess.close()
     store.free()
     if rank == 0:
