@@ -13,9 +13,12 @@
 // slot's `freed`, and no kernel keeps a weight pointer beyond its own launch.
 #include "step.h"
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <algorithm>
 #include <chrono>
 #include <cmath>
+#include <cstdio>
 #include <cstring>
 #include <thread>
 
@@ -27,6 +30,19 @@
 namespace soup {
 
 static uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
+
+// A named host-side range on a profiler's timeline (NVTX); costs nothing without a profiler.
+struct TraceRange {
+  explicit TraceRange(const char *name, int index = -1) {
+    char buf[48];
+    if (index >= 0) std::snprintf(buf, sizeof buf, "%s %d", name, index);
+    else std::snprintf(buf, sizeof buf, "%s", name);
+    nvtxRangePushA(buf);
+  }
+  ~TraceRange() { nvtxRangePop(); }
+  TraceRange(const TraceRange &) = delete;
+  TraceRange &operator=(const TraceRange &) = delete;
+};
 
 int ce_chunk_cols(int M, int V) {
   int vc = (int)((1ull << 24) / (uint64_t)std::max(M, 1) / 256ull) * 256;
@@ -587,12 +603,14 @@ int step_fwd(soup_stream *h, const int32_t *tokens, int B, int S, const float *c
       k_pack_fwd(Lg, h->lay.n_out[g], B16(h, P.vl[(size_t)i * 4 + g]), true, st);
       k_pack_bwd(Lg, h->lay.n_in[g], B16(h, P.ac[(size_t)i * 4 + g]), false, st);
     }
+    TraceRange tr("fwd layer", i);
     SOUP_TRY(acquire(h, seq, (size_t)i, &shard, &s));
     SOUP_TRY(layer_forward(h, i, shard, false));
     SOUP_TRY(release(h, s));
     if (!h->resident) SOUP_TRY(prefetch(h, seq, (size_t)i + 1, look - 1));
   }
   // final norm + vocabulary-chunked loss
+  TraceRange tr_head("loss head fwd");
   k_rmsnorm_fwd(F(h, P.h_all) + (size_t)L * M * H, h->final_norm, c.rms_eps, M, H, B16(h, P.hn), false, st);
   const int vc = P.vc;
   for (int v0 = 0, ci = 0; v0 < c.vocab; v0 += vc, ++ci) {
@@ -639,23 +657,26 @@ int step_bwd(soup_stream *h, float *const *dA, float *const *dB, float *dh_out, 
   // loss backward, chunk by chunk: recompute logits, dz = (softmax - onehot) / N, dhn += dz W
   const int vc = P.vc;
   const float inv_n = 1.0f / (float)((int64_t)B * (S - 1));
-  for (int v0 = 0, ci = 0; v0 < c.vocab; v0 += vc, ++ci) {
-    const int n = std::min(vc, c.vocab - v0);
-    const uint16_t *w = lm_weight(h) + (size_t)v0 * H;
-    GemmArgs g;
-    g.mode = GEMM_FWD; g.wfmt = W_BF16; g.w = w; g.Nw = n; g.Kw = H;
-    g.M = M; g.a = B16(h, P.hn); g.lda = H; g.epi = EPI_F32; g.out = F(h, P.z); g.ldo = vc;
-    g.err = h->err_dev;
-    SOUP_TRY(gemm_launch(g, st));
-    k_ce_chunk_bwd(F(h, P.z), vc, v0, n, F(h, P.ce_lse), h->tokens, M, S, inv_n, B16(h, P.dz), st);
-    GemmArgs d;
-    d.mode = GEMM_DX; d.wfmt = W_BF16; d.w = w; d.Nw = n; d.Kw = H;
-    d.M = M; d.a = B16(h, P.dz); d.lda = vc; d.epi = ci == 0 ? EPI_F32 : EPI_F32_ACC;
-    d.out = F(h, P.dhn); d.ldo = H; d.err = h->err_dev;
-    SOUP_TRY(gemm_launch(d, st));
+  {
+    TraceRange tr_head("loss head bwd");
+    for (int v0 = 0, ci = 0; v0 < c.vocab; v0 += vc, ++ci) {
+      const int n = std::min(vc, c.vocab - v0);
+      const uint16_t *w = lm_weight(h) + (size_t)v0 * H;
+      GemmArgs g;
+      g.mode = GEMM_FWD; g.wfmt = W_BF16; g.w = w; g.Nw = n; g.Kw = H;
+      g.M = M; g.a = B16(h, P.hn); g.lda = H; g.epi = EPI_F32; g.out = F(h, P.z); g.ldo = vc;
+      g.err = h->err_dev;
+      SOUP_TRY(gemm_launch(g, st));
+      k_ce_chunk_bwd(F(h, P.z), vc, v0, n, F(h, P.ce_lse), h->tokens, M, S, inv_n, B16(h, P.dz), st);
+      GemmArgs d;
+      d.mode = GEMM_DX; d.wfmt = W_BF16; d.w = w; d.Nw = n; d.Kw = H;
+      d.M = M; d.a = B16(h, P.dz); d.lda = vc; d.epi = ci == 0 ? EPI_F32 : EPI_F32_ACC;
+      d.out = F(h, P.dhn); d.ldo = H; d.err = h->err_dev;
+      SOUP_TRY(gemm_launch(d, st));
+    }
+    k_rmsnorm_bwd(F(h, P.dhn), F(h, P.h_all) + (size_t)L * M * H, h->final_norm, c.rms_eps, M, H,
+                  nullptr, F(h, P.dh), B16(h, P.dh_b), st);
   }
-  k_rmsnorm_bwd(F(h, P.dhn), F(h, P.h_all) + (size_t)L * M * H, h->final_norm, c.rms_eps, M, H,
-                nullptr, F(h, P.dh), B16(h, P.dh_b), st);
   if (dh_out)
     SOUP_CUDA_TRY(cudaMemcpyAsync(dh_out + (size_t)L * M * H, F(h, P.dh), 4ull * M * H,
                                   cudaMemcpyDeviceToDevice, st));
@@ -666,6 +687,7 @@ int step_bwd(soup_stream *h, float *const *dA, float *const *dB, float *dh_out, 
     const int li = seq[j];
     const uint8_t *shard;
     int s;
+    TraceRange tr("bwd layer", li);
     SOUP_TRY(acquire(h, seq, (size_t)j, &shard, &s));
     // the forward's last layer left its activations in the scratch buffers (the loss head
     // between uses separate ones): its backward reuses them instead of recomputing them, which
