@@ -184,3 +184,56 @@ def test_finite_difference_gradients_float64(seed):
     # ~1e-9 for the B entries (h = 1e-3 * rms(B) ~ 1e-6, loss ~ 7)
     assert np.all(err <= 1e-5 * np.abs(an) + 1e-9), (err.max(), np.abs(an).max())
     assert np.linalg.norm(fd - an) / np.linalg.norm(an) < 1e-6
+
+
+def test_silu_hand_values():
+    # silu(x) = x * sigmoid(x): values worked by hand from e^-1 = 0.36787944117144233
+    np.testing.assert_allclose(model.silu(np.array([0.0, 1.0, -1.0])),
+                               [0.0, 1.0 / 1.36787944117144233, -1.0 / (1.0 + math.e)], rtol=1e-15)
+    assert abs(model.silu(np.array([40.0]))[0] - 40.0) < 1e-12
+
+
+def test_rope_pairs_and_frequencies_hand_worked():
+    # head_dim 4, theta 1e4: pair (0, 2) turns by pos * 1, pair (1, 3) by pos * 1e4^(-1/2)
+    cos, sin = model.rope_tables(4, 4, 10000.0, np.float64)
+    pos = 3
+    for i, want in ((0, [math.cos(3), 0, math.sin(3), 0]),
+                    (1, [0, math.cos(0.03), 0, math.sin(0.03)]),
+                    (2, [-math.sin(3), 0, math.cos(3), 0]),
+                    (3, [0, -math.sin(0.03), 0, math.cos(0.03)])):
+        x = np.zeros((1, 4, 1, 4))
+        x[0, pos, 0, i] = 1.0
+        np.testing.assert_allclose(model.rope(x, cos, sin)[0, pos, 0], want, atol=1e-15)
+
+
+def test_rmsnorm_hand_worked():
+    # x = (3, 4): mean square 12.5; eps inside the root: 1 / sqrt(13)
+    y, r = model.rmsnorm(np.array([[3.0, 4.0]]), np.array([1.0, 2.0]), 0.5)
+    np.testing.assert_allclose(y, [[3 / math.sqrt(13), 8 / math.sqrt(13)]], rtol=1e-15)
+    np.testing.assert_allclose(r, [[1 / math.sqrt(13)]], rtol=1e-15)
+
+
+def test_identity_like_layer_reduces_to_closed_form():
+    """q = k = 0 makes every causal score equal, so attention is the running mean of v; with
+    v taking the first head_dim features, o = I, gate = 2 I, up = I and down = I the layer is
+        h' = h + [mean_{s<=t} n1[s, :4], same],   h'' = h' + silu(2 n2) * n2
+    with n1, n2 the RMS-normalised h, h'.  Checks which projection feeds which, the causal
+    mask, both residuals and the gate/up order."""
+    cfg = TINY.with_(hidden=8, inter=8, n_heads=2, n_kv_heads=1, head_dim=4, rms_eps=1e-5)
+    H, S = 8, 5
+    W = {"q": np.zeros((8, 8)), "k": np.zeros((4, 8)), "v": np.eye(4, 8), "o": np.eye(8),
+         "gate": 2 * np.eye(8), "up": np.eye(8), "down": np.eye(8),
+         "ln1": np.ones(8), "ln2": np.ones(8)}
+    rng = np.random.default_rng(11)
+    h = rng.standard_normal((1, S, H))
+    cos, sin = model.rope_tables(S, 4, cfg.rope_theta, np.float64)
+    out, _ = model.layer_forward(h, W, None, cfg, cos, sin)
+
+    def norm(x):
+        return x / np.sqrt((x * x).mean(-1, keepdims=True) + cfg.rms_eps)
+    n1 = norm(h[0])
+    run_mean = np.cumsum(n1[:, :4], axis=0) / np.arange(1, S + 1)[:, None]
+    h1 = h[0] + np.concatenate([run_mean, run_mean], axis=1)
+    n2 = norm(h1)
+    want = h1 + (2 * n2) / (1 + np.exp(-2 * n2)) * n2
+    np.testing.assert_allclose(out[0], want, rtol=1e-12, atol=1e-12)
