@@ -237,3 +237,38 @@ def test_identity_like_layer_reduces_to_closed_form():
     n2 = norm(h1)
     want = h1 + (2 * n2) / (1 + np.exp(-2 * n2)) * n2
     np.testing.assert_allclose(out[0], want, rtol=1e-12, atol=1e-12)
+
+
+def test_weights_from_source_maps_each_tensor():
+    """Every projection lands under its own name with its [out, in] shape: the NF4 base stays
+    within each 64-block's half-step of its own bf16 source (a swapped pair of equal-shape
+    projections breaks that), and a bf16 base is the source itself."""
+    cb = nf4.codebook().astype(np.float64)
+    half_gap = float(np.max(np.diff(cb))) / 2
+    for cfg in (TINY, TINY.with_(base_fmt="bf16")):
+        W = _tiny_weights(np.float64, cfg)
+        for i in range(cfg.n_layers):
+            src = synth.layer_source(cfg, i)
+            for p in model.PROJ:
+                ref = nf4.bf16_to_f32(src[p]).astype(np.float64)
+                got = W.layers[i][p]
+                assert got.shape == cfg.proj_shape(p), (p, got.shape)
+                if cfg.base_fmt == "bf16":
+                    assert np.array_equal(got, ref), p
+                else:
+                    blocks = np.abs(ref.reshape(-1, 64)).max(axis=1, keepdims=True)
+                    err = np.abs(got.reshape(-1, 64) - ref.reshape(-1, 64))
+                    assert np.all(err <= blocks * half_gap * (1 + 1e-6)), (i, p)
+            for n in ("ln1", "ln2"):
+                assert np.array_equal(W.layers[i][n], nf4.bf16_to_f32(src[n]))
+        assert np.array_equal(W.embed, nf4.bf16_to_f32(synth.embedding(cfg)))
+        assert np.array_equal(W.lm_head, nf4.bf16_to_f32(synth.lm_head(cfg)))
+
+
+def test_logits_of_identity_head_is_the_normalised_state():
+    rng = np.random.default_rng(12)
+    hL = rng.standard_normal((3, 4))
+    w_f = np.array([1.0, 2.0, 0.5, 1.0])
+    z, _ = model.logits_of(hL, w_f, 3.0 * np.eye(4), 1e-6)
+    want = 3.0 * hL / np.sqrt((hL * hL).mean(-1, keepdims=True) + 1e-6) * w_f
+    np.testing.assert_allclose(z, want, rtol=1e-13)
