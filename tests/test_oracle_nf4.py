@@ -5,7 +5,6 @@ printed on the pages."""
 import os
 
 import numpy as np
-import pytest
 from scipy.special import ndtr
 
 from oracle import nf4, sizes
