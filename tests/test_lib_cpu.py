@@ -178,3 +178,44 @@ def test_forced_pageable_store_and_raw_shard_copy():
         b.put_shard(cfg.n_layers, a.shard_bytes(0))
     a.free()
     b.free()
+
+
+def test_c_abi_from_plain_c(tmp_path):
+    """The library used from C99 through include/soup.h alone (gcc, no Python in between):
+    the codebook and the host quantiser agree bit for bit with the oracle, the layout and
+    memory plan with the binding's, and argument errors come back as SOUP_EINVAL."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    pkg = os.path.join(root, "nf4_dequant_gemm_blockwise_b300")
+    exe = str(tmp_path / "abi_smoke")
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(root, "include"),
+                    os.path.join(root, "tests", "c", "abi_smoke.c"), "-L", pkg, "-lsoup",
+                    f"-Wl,-rpath,{pkg}", "-o", exe], check=True)
+    # the header is also valid C++ (the library's own translation units include it too)
+    subprocess.run(["g++", "-std=c++17", "-fsyntax-only", "-x", "c++",
+                    os.path.join(root, "include", "soup.h")], check=True)
+    out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout
+    kv = {ln.split(" ", 1)[0]: ln.split(" ", 1)[1] for ln in out.strip().splitlines()}
+    cb = np.array([int(h, 16) for h in kv["codebook"].split()], np.uint32)
+    assert np.array_equal(cb, nf4.codebook().astype(np.float32).view(np.uint32))
+    # the program's input: k / 17 in float32 for k = (37 i mod 101) - 50, rounded to bf16
+    k = (np.arange(130) * 37 % 101 - 50).astype(np.float32)
+    bits = (k / np.float32(17)).view(np.uint32)
+    bits = ((bits + 0x7FFF + ((bits >> 16) & 1)) >> 16).astype(np.uint16)
+    packed, absmax = nf4.quantize_tensor(bits)
+    assert np.array_equal(np.array([int(h, 16) for h in kv["codes"].split()], np.uint8), packed)
+    assert np.array_equal(np.array([int(h, 16) for h in kv["absmax"].split()], np.uint32),
+                          absmax.astype(np.float32).view(np.uint32))
+    cfg = synth.TINY
+    assert int(kv["stride"]) == api.shard_layout_of(cfg).stride
+    ws0, ws2 = (int(v) for v in kv["workspace"].split())
+    assert ws0 == api.workspace_bytes(cfg, 1, 64) and ws2 == api.workspace_bytes(cfg, 1, 64, keep_activations=True)
+    assert int(kv["peak"]) == api.peak_bytes(cfg, 1, 64)[0]
+    assert int(kv["bad_mode"]) == api.EINVAL and int(kv["short_shard"]) == api.EINVAL
+    nbytes, pinned, first = kv["store"].split()
+    assert int(nbytes) == cfg.n_layers * api.shard_layout_of(cfg).stride and pinned == "0" and first == "5a"
+    assert int(kv["adamw_step0"]) == api.EINVAL and "step numbers start at 1" in kv["last_error"]
