@@ -219,3 +219,20 @@ def test_c_abi_from_plain_c(tmp_path):
     nbytes, pinned, first = kv["store"].split()
     assert int(nbytes) == cfg.n_layers * api.shard_layout_of(cfg).stride and pinned == "0" and first == "5a"
     assert int(kv["adamw_step0"]) == api.EINVAL and "step numbers start at 1" in kv["last_error"]
+
+
+@pytest.mark.parametrize("n_threads", [1, 3, 16])
+def test_host_packer_special_values_and_threads(n_threads):
+    # bf16 subnormals, negative zeros, an all-negative block, a block whose absmax is a
+    # subnormal, and a ragged tail: same bits as the oracle at any thread count
+    rng = np.random.default_rng(7)
+    x = (rng.standard_normal(64 * 9 + 5) * 0.02).astype(np.float32)
+    x[0:64] = -np.abs(x[0:64])                              # all negative
+    x[64:128] = rng.standard_normal(64).astype(np.float32) * np.float32(1e-39)  # subnormals
+    x[128:192:3] = np.float32(-0.0)                          # negative zeros
+    x[192] = np.float32(3e-39)
+    bits = synth.to_bf16_bits(x)
+    codes, absmax = api.nf4_quantize_host(bits, n_threads=n_threads)
+    oc, oa = nf4.quantize(nf4.bf16_to_f32(bits))
+    assert np.array_equal(absmax.view(np.uint32), oa.view(np.uint32))
+    assert np.array_equal(codes, nf4.pack(oc[: x.size + (x.size % 2)]))
