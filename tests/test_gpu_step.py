@@ -185,6 +185,25 @@ def test_tiny_adapters_off_forward_is_the_base(tiny):
     _assert_bit_equal(tiny["stream"], _run(tiny["s"], cfg))
 
 
+def test_tiny_pageable_store_stays_exact(tiny):
+    """The fallback when page-locking fails ("Layer streaming: fine-tune a model that does not
+    fit in your card", "Measured numbers": pageable copies lose the overlap): the same shard
+    bytes in a pageable arena stream to the same results, bit for bit."""
+    from nf4_dequant_gemm_blockwise_b300 import api
+    cfg = tiny["cfg"]
+    paged = api.Store(cfg, force_pageable=True)
+    for i in range(cfg.n_layers):
+        paged.put_shard(i, tiny["s"].store.shard_bytes(i))
+    assert paged.info()[2] is False
+    s = _session(cfg, resident=False, store=paged)
+    try:
+        out = _run(s, cfg)
+    finally:
+        s.close()
+        paged.free()
+    _assert_bit_equal(tiny["resident"], out)
+
+
 @pytest.mark.parametrize("resident", [False, True])
 def test_tiny_kept_activations_equal_recompute_bitwise(tiny, resident):
     """"How it works": with stream_recompute off the backward uses the forward's activations
