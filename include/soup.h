@@ -47,7 +47,9 @@ enum {
   SOUP_ECUDA = -3,      /* a CUDA runtime call failed (message names it)                */
   SOUP_ESTATE = -4,     /* call out of order (e.g. backward without a forward)          */
   SOUP_ETIMEDOUT = -5,  /* soup_sync gave up, or a kernel's bounded wait ran out        */
-  SOUP_EPAGEABLE = -6   /* warning: page-locking failed, the store is pageable          */
+  SOUP_EPAGEABLE = -6,  /* warning: page-locking failed, the store is pageable          */
+  SOUP_ERANGE = -7      /* a forward value stored as an IEEE-half operand was NaN or
+                           beyond +-65504 (the half range); the results are unusable     */
 };
 
 enum { SOUP_FMT_BF16 = 0, SOUP_FMT_NF4 = 1 };
@@ -232,13 +234,29 @@ int soup_step_bwd_ex(soup_stream *h, float *const *dA, float *const *dB, float *
                      int flags);
 
 /* Host-side bounded wait for all work enqueued on the handle: polls, never spins on the
- * device.  Returns SOUP_ETIMEDOUT after timeout_ms, or the error a kernel reported. */
+ * device.  Returns SOUP_ETIMEDOUT after timeout_ms (timeout_ms = 0: only asks whether the work
+ * is done; < 0: no limit), or the error the kernels reported since the last soup_sync that
+ * returned: SOUP_ETIMEDOUT if a kernel's bounded wait gave up, SOUP_ERANGE if a forward
+ * operand left the half range ("Layer streaming: fine-tune a model that does not fit in
+ * your card", "Troubleshooting": a read that wedges is given up after a bounded wait and
+ * reported, not waited on forever).  Reading the kernels' error flag clears it. */
 int soup_sync(soup_stream *h, int timeout_ms);
 int soup_stream_stats(soup_stream *h, soup_stats *out, int reset);
-/* Debug switches: what = SOUP_DBG_PROFILE (time every base GEMM with events),
- * SOUP_DBG_STALE_SLOT (backward reads the slot of a neighbouring layer: a deliberately
- * broken control that the exactness tests must catch; reads valid memory only). */
-enum { SOUP_DBG_PROFILE = 1, SOUP_DBG_STALE_SLOT = 2 };
+/* Debug switches: what =
+ *   SOUP_DBG_PROFILE        time every base GEMM with events (value 0/1);
+ *   SOUP_DBG_STALE_SLOT     backward reads the slot of a neighbouring layer: a deliberately
+ *                           broken control that the exactness tests must catch; reads valid
+ *                           memory only (value 0/1);
+ *   SOUP_DBG_COPY_DELAY_US  the host sleeps `value` microseconds (0..1e6) before enqueueing
+ *                           each shard copy: changes timing only, never results;
+ *   SOUP_DBG_WAIT_PROBE     enqueues, on the compute stream, one kernel whose bounded wait
+ *                           on a barrier that nothing signals gives up after about `value`
+ *                           microseconds (1..1e6) and raises the kernels' error flag, so the
+ *                           next soup_sync returns SOUP_ETIMEDOUT — the failure path of
+ *                           "Troubleshooting" (a wedged read is given up and reported),
+ *                           exercised without a real stall; the stream stays usable. */
+enum { SOUP_DBG_PROFILE = 1, SOUP_DBG_STALE_SLOT = 2, SOUP_DBG_COPY_DELAY_US = 3,
+       SOUP_DBG_WAIT_PROBE = 4 };
 int soup_stream_debug(soup_stream *h, int what, int value);
 void soup_stream_free(soup_stream *h);
 
@@ -276,10 +294,11 @@ int soup_proj_lora_grad(const uint16_t *x, const uint16_t *dy, int M, int N, int
                         float *dB, void *scratch, uint64_t scratch_bytes, uintptr_t stream);
 
 /* Status of the projections that used `scratch` (same M, N, K as those calls): waits for
- * `stream`, reads the scratch's device error flag, clears it, and returns SOUP_OK, or
- * SOUP_ETIMEDOUT if a kernel's bounded wait gave up (its outputs are then unusable).  The flag
- * lives in the scratch: zero-fill a new scratch buffer (or pass it here once) before relying
- * on the result. */
+ * `stream`, reads the scratch's device error flag, clears it, and returns SOUP_OK,
+ * SOUP_ETIMEDOUT if a kernel's bounded wait gave up, or SOUP_ERANGE if a half-precision
+ * forward value overflowed (the outputs are unusable in both cases).  The flag lives in the
+ * scratch: zero-fill a new scratch buffer (or pass it here once) before relying on the
+ * result. */
 int soup_proj_status(void *scratch, int M, int N, int K, uintptr_t stream);
 
 /* soup_proj_fwd without caller-provided scratch, for callers that cannot allocate device
@@ -299,6 +318,14 @@ int soup_proj_fwd_noalloc(const uint16_t *x, int M, int N, int K, const uint8_t 
                           const float *absmax, const uint16_t *w_bf16, const float *A,
                           const float *B, int r, float s, int x_f16, uint16_t *y,
                           uintptr_t stream);
+/* Status of the soup_proj_fwd_noalloc calls on the current device: waits for `stream`, reads
+ * the error flag those calls share (it sits at a fixed place in the static array and collects
+ * the error bits of every call since it was last read), clears it, and returns SOUP_OK,
+ * SOUP_ETIMEDOUT (a kernel's bounded wait gave up) or SOUP_ERANGE (a half-precision value
+ * overflowed); the outputs of the calls since the last read are then unusable.  Call it on
+ * the stream the calls ran on, after them.  The pages have no counterpart.  Allocates
+ * nothing; like the first call, its first use on a device looks up the array's address. */
+int soup_proj_noalloc_status(uintptr_t stream);
 
 /* ------------------------------------------------------------------ optimizer */
 

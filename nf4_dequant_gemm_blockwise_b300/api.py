@@ -13,9 +13,9 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libsoup.so")
 
-OK, EINVAL, ENOMEM, ECUDA, ESTATE, ETIMEDOUT, EPAGEABLE = 0, -1, -2, -3, -4, -5, -6
+OK, EINVAL, ENOMEM, ECUDA, ESTATE, ETIMEDOUT, EPAGEABLE, ERANGE = 0, -1, -2, -3, -4, -5, -6, -7
 FMT_BF16, FMT_NF4 = 0, 1
-DBG_PROFILE, DBG_STALE_SLOT = 1, 2
+DBG_PROFILE, DBG_STALE_SLOT, DBG_COPY_DELAY_US, DBG_WAIT_PROBE = 1, 2, 3, 4
 PROJ = ("q", "k", "v", "o", "gate", "up", "down")
 
 
@@ -104,6 +104,7 @@ def _load() -> C.CDLL:
         "soup_nf4_dequant": (I32, [P, P, C.c_int64, P, P, C.c_size_t]),
         "soup_proj_fwd_noalloc": (I32, [P, I32, I32, I32, P, P, P, P, P, I32, F32, I32, P, C.c_size_t]),
         "soup_proj_status": (I32, [P, I32, I32, I32, C.c_size_t]),
+        "soup_proj_noalloc_status": (I32, [C.c_size_t]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -335,6 +336,12 @@ def proj_fwd_noalloc(x, M, N, K, codes, absmax, w_bf16, A, B, r, s, y, stream=0,
     """soup_proj_fwd with the library's static device scratch (no allocation by anyone)."""
     _check(lib.soup_proj_fwd_noalloc(_ptr(x), M, N, K, _ptr(codes), _ptr(absmax), _ptr(w_bf16),
                                      _ptr(A), _ptr(B), r, s, int(x_f16), _ptr(y), _stream(stream)))
+
+
+def proj_noalloc_status(stream=0):
+    """Wait for `stream` and raise if a proj_fwd_noalloc call since the last check reported a
+    kernel error (bounded wait given up, half-precision overflow); clears the shared flag."""
+    _check(lib.soup_proj_noalloc_status(_stream(stream)))
 
 
 def proj_dx(dy, M, N, K, codes, absmax, w_bf16, A, B, r, s, dx, scratch, stream=0):

@@ -28,6 +28,17 @@ int set_error(int code, const char *fmt, ...) {
   return code;
 }
 void clear_error() { g_err.clear(); }
+int kernel_flags_status(int flags, const char *who) {
+  if (!flags) return 0;
+  if (flags & 1)  // SOUP_KERR_WAIT_TIMEOUT
+    return set_error(SOUP_ETIMEDOUT, "%s: a kernel's bounded wait gave up (flags 0x%x); its outputs are unusable",
+                     who, flags);
+  if (flags & 4)  // SOUP_KERR_RANGE
+    return set_error(SOUP_ERANGE,
+                     "%s: a value left the range of IEEE half (|x| > 65504 or NaN) where the forward stores "
+                     "its 16-bit operands (flags 0x%x)", who, flags);
+  return set_error(SOUP_ECUDA, "%s: kernel error flags 0x%x", who, flags);
+}
 namespace {
 std::atomic<uint64_t> g_launches{0};
 }
@@ -148,7 +159,16 @@ int soup_stream_debug(soup_stream *h, int what, int value) {
   if (!h) return set_error(SOUP_EINVAL, "handle is NULL");
   if (what == SOUP_DBG_PROFILE) h->dbg_profile = value;
   else if (what == SOUP_DBG_STALE_SLOT) h->dbg_stale = value;
-  else return set_error(SOUP_EINVAL, "unknown debug switch %d", what);
+  else if (what == SOUP_DBG_COPY_DELAY_US) {
+    if (value < 0 || value > 1000000) return set_error(SOUP_EINVAL, "copy delay %d us outside [0, 1 s]", value);
+    h->dbg_copy_delay_us = value;
+  } else if (what == SOUP_DBG_WAIT_PROBE) {
+    if (value < 1 || value > 1000000) return set_error(SOUP_EINVAL, "probe limit %d us outside [1, 1 s]", value);
+    k_wait_probe(h->err_dev, 2000ll * value, h->cs);  // ~2000 SM cycles per microsecond
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(SOUP_ECUDA, "wait probe launch: %s", cudaGetErrorString(e));
+    SOUP_CUDA_TRY(cudaEventRecord(h->done, h->cs));
+  } else return set_error(SOUP_EINVAL, "unknown debug switch %d", what);
   return 0;
 }
 void soup_stream_free(soup_stream *h) { soup_stream_free_impl(h); }
@@ -252,7 +272,7 @@ int soup_proj_fwd(const uint16_t *x, int M, int N, int K, const uint8_t *codes, 
   if (r > 0) {
     k_lora_down(x, K, M, K, L, reinterpret_cast<float *>(base + P.u_f32),
                 reinterpret_cast<uint16_t *>(base + P.ul), f16, f16,
-                reinterpret_cast<float *>(base + P.part), st);
+                reinterpret_cast<float *>(base + P.part), reinterpret_cast<int *>(base + P.err), st);
     g.lora_u = reinterpret_cast<float *>(base + P.u_f32);
     g.lseg = L;
     g.after_lora = 1;
@@ -313,7 +333,8 @@ int soup_proj_lora_grad(const uint16_t *x, const uint16_t *dy, int M, int N, int
   float *part = reinterpret_cast<float *>(base + P.part);
   const bool f16 = x_f16 != 0;
   k_lora_down(x, K, M, K, L, reinterpret_cast<float *>(base + P.u_f32),
-              reinterpret_cast<uint16_t *>(base + P.ul), f16, f16, part, st);
+              reinterpret_cast<uint16_t *>(base + P.ul), f16, f16, part,
+              reinterpret_cast<int *>(base + P.err), st);
   k_lora_du(dy, N, M, L, reinterpret_cast<float *>(base + P.du_f32),
             reinterpret_cast<uint16_t *>(base + P.dul), false, false, part, st);
   k_lora_dB(dy, N, M, reinterpret_cast<float *>(base + P.u_f32), L, false, part, st);
@@ -331,8 +352,7 @@ int soup_proj_status(void *scratch, int M, int N, int K, uintptr_t stream) {
   SOUP_CUDA_TRY(cudaMemcpyAsync(&flags, err, sizeof(int), cudaMemcpyDeviceToHost, st));
   SOUP_CUDA_TRY(cudaStreamSynchronize(st));
   SOUP_CUDA_TRY(cudaMemsetAsync(err, 0, sizeof(int), st));
-  if (flags) return set_error(SOUP_ETIMEDOUT, "a kernel's bounded wait gave up (flags 0x%x)", flags);
-  return 0;
+  return kernel_flags_status(flags, "soup_proj_status");
 }
 
 int soup_nf4_dequant(const uint8_t *codes, const float *absmax, int64_t n, float *out_f32,

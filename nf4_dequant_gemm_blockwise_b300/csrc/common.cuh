@@ -14,7 +14,8 @@
 #define SOUP_DEV __device__ __forceinline__
 
 // Error flags written by kernels into a device int (bitwise OR).
-enum : int { SOUP_KERR_WAIT_TIMEOUT = 1, SOUP_KERR_BAD_ARG = 2 };
+// RANGE: a value stored as an IEEE-half operand was NaN or beyond +-65504.
+enum : int { SOUP_KERR_WAIT_TIMEOUT = 1, SOUP_KERR_BAD_ARG = 2, SOUP_KERR_RANGE = 4 };
 
 // ~0.2 s at 2 GHz: far beyond any legitimate wait in these kernels (the longest, a CTA's
 // whole main loop before its epilogue, is well under a millisecond).
@@ -45,6 +46,14 @@ SOUP_DEV uint32_t pack_h2(float lo, float hi) {
 }
 SOUP_DEV float h16_to_f(uint16_t v) { return __half2float(__ushort_as_half(v)); }
 SOUP_DEV uint16_t f_to_h16(float f) { return __half_as_ushort(__float2half_rn(f)); }
+
+// True when v does not survive a store as IEEE half: NaN, or |v| >= 65520 (which rounds to
+// infinity).  Kernels that store the forward's half operands OR SOUP_KERR_RANGE into their
+// error flag when any value fails; the compare is one instruction, the atomic runs only then.
+SOUP_DEV bool half_out_of_range(float v) { return !(fabsf(v) < 65520.f); }
+SOUP_DEV void flag_range(bool bad, int *err) {
+  if (bad && err) atomicOr(err, SOUP_KERR_RANGE);
+}
 
 // 16-bit operand format chosen at compile time: F16 = IEEE half, else bf16.
 template <bool F16>
@@ -90,16 +99,17 @@ SOUP_DEV bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait: returns false (and sets *err) if the phase did not complete in time, or if
-// another role already gave up (*abort != 0).
-SOUP_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, int *err, volatile int *abort) {
+// Bounded wait: returns false (and sets *err) if the phase did not complete within `limit`
+// cycles, or if another role already gave up (*abort != 0).
+SOUP_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, int *err, volatile int *abort,
+                        long long limit = SOUP_WAIT_CYCLES) {
   if (mbar_try_wait(bar, parity)) return true;
   long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (*abort) return false;
-      if (clock64() - t0 > SOUP_WAIT_CYCLES) {
+      if (clock64() - t0 > limit) {
         *abort = 1;
         if (err) atomicOr(err, SOUP_KERR_WAIT_TIMEOUT);
         return false;

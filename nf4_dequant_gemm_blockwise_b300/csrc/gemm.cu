@@ -387,6 +387,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         } else if (EPI == EPI_16) {
           uint16_t *o = reinterpret_cast<uint16_t *>(p.out) + (size_t)m * p.ldo + n;
+          if (F16) {  // half outputs: flag values beyond the half range (or NaN)
+            bool bad = false;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) bad |= half_out_of_range(__uint_as_float(r[j])) && (n + j < p.Ng);
+            flag_range(bad, p.err);
+          }
           if (full_row) {
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
@@ -446,6 +452,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 struct FbParams {
   Codebook cb;
   int f16;
+  int *err;
   int mode, M, Ng, Kg, wfmt, Nw, Kw, ldw, lda, R, epi, ldo, ld_add;
   const uint16_t *a;
   const uint8_t *codes;
@@ -526,6 +533,7 @@ __global__ void __launch_bounds__(256) fallback_gemm_kernel(const FbParams p) {
       if (n >= p.Ng) continue;
       const float v = acc[i][j];
       if (p.epi == EPI_16) {
+        if (p.f16) flag_range(half_out_of_range(v), p.err);
         reinterpret_cast<uint16_t *>(p.out)[(int64_t)m * p.ldo + n] = p.f16 ? f_to_h16(v) : f_to_bf16(v);
       } else {
         float *o = reinterpret_cast<float *>(p.out) + (int64_t)m * p.ldo + n;
@@ -544,6 +552,7 @@ struct RedParams {
   int splits, M, Ng, epi, f16, ldo, ld_add;
   void *out;
   const float *add_src;
+  int *err;
 };
 // Sum of the split partial planes in split order, then the epilogue.  Launched as a
 // programmatic dependent of the GEMM: waits for it before reading the partials.  V = 4: four
@@ -572,6 +581,12 @@ __global__ void splitk_reduce_kernel(const RedParams p) {
     }
     if (p.epi == EPI_16) {
       uint16_t *o = reinterpret_cast<uint16_t *>(p.out) + (size_t)m * p.ldo + n;
+      if (p.f16) {
+        bool bad = false;
+#pragma unroll
+        for (int j = 0; j < V; ++j) bad |= half_out_of_range(v[j]);
+        flag_range(bad, p.err);
+      }
 #pragma unroll
       for (int j = 0; j < V; ++j) o[j] = p.f16 ? f_to_h16(v[j]) : f_to_bf16(v[j]);
     } else {
@@ -657,6 +672,7 @@ int launch_tc(const GemmArgs &g, const CUtensorMap *maps, cudaStream_t st) {
     RedParams rp;
     rp.part = g.part; rp.splits = p.splits; rp.M = g.M; rp.Ng = p.Ng; rp.epi = g.epi;
     rp.f16 = g.op_f16; rp.ldo = g.ldo; rp.ld_add = g.ld_add; rp.out = g.out; rp.add_src = g.add_src;
+    rp.err = g.err;
     const bool vec = p.Ng % 4 == 0 && g.ldo % 4 == 0 && (g.epi != EPI_F32_ADD || g.ld_add % 4 == 0) &&
                      (reinterpret_cast<uintptr_t>(g.part) & 15) == 0;
     const int64_t n = (int64_t)g.M * p.Ng / (vec ? 4 : 1);
@@ -790,6 +806,7 @@ int gemm_launch(const GemmArgs &g, cudaStream_t st) {
     FbParams p;
     p.cb = nf4_codebook_param();
     p.f16 = g.op_f16;
+    p.err = g.err;
     p.mode = g.mode; p.M = g.M; p.Ng = g.Ng(); p.Kg = g.Kg(); p.wfmt = g.wfmt;
     p.Nw = g.Nw; p.Kw = g.Kw; p.ldw = g.ldw ? g.ldw : g.Kw; p.lda = g.lda; p.R = g.R;
     p.epi = g.epi; p.ldo = g.ldo; p.ld_add = g.ld_add; p.a = g.a; p.codes = g.codes;

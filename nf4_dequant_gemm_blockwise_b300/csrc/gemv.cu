@@ -173,6 +173,7 @@ SOUP_DEV void gv_emit(const GvParams &p, int m, int col, float v) {
   const size_t o = (size_t)m * p.ldo + col;
   switch (p.epi) {
     case EPI_16:
+      if (MODE == GEMM_FWD) flag_range(half_out_of_range(v), p.err);
       reinterpret_cast<uint16_t *>(p.out)[o] = MODE == GEMM_FWD ? f_to_h16(v) : f_to_bf16(v);
       break;
     case EPI_F32: reinterpret_cast<float *>(p.out)[o] = v; break;

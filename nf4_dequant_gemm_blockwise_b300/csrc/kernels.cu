@@ -66,7 +66,7 @@ SOUP_DEV float block_sum256(float v, float *sh) {
 
 template <bool F16>
 __global__ void __launch_bounds__(RMS_T) rmsnorm_fwd_kernel(const float *h, const uint16_t *w, float eps,
-                                                            int M, int H, uint16_t *out) {
+                                                            int M, int H, uint16_t *out, int *err) {
   __shared__ float sh[RMS_T / 32];
   const int row = blockIdx.x;
   const float *x = h + (size_t)row * H;
@@ -81,16 +81,21 @@ __global__ void __launch_bounds__(RMS_T) rmsnorm_fwd_kernel(const float *h, cons
   ss = block_sum256(ss, sh);
   const float r = 1.0f / sqrtf(ss / (float)H + eps);
   uint16_t *o = out + (size_t)row * H;
+  bool bad = false;
 #pragma unroll
   for (int it = 0; it < RMS_V; ++it) {
     const int i = (threadIdx.x + it * RMS_T) * 4;
     if (i >= H) break;
     const uint2 wv = *reinterpret_cast<const uint2 *>(w + i);
+    const float y0 = v[it].x * r * bf16_lo(wv.x), y1 = v[it].y * r * bf16_hi(wv.x);
+    const float y2 = v[it].z * r * bf16_lo(wv.y), y3 = v[it].w * r * bf16_hi(wv.y);
+    if (F16) bad |= half_out_of_range(y0) | half_out_of_range(y1) | half_out_of_range(y2) | half_out_of_range(y3);
     uint2 res;
-    res.x = pack16x2<F16>(v[it].x * r * bf16_lo(wv.x), v[it].y * r * bf16_hi(wv.x));
-    res.y = pack16x2<F16>(v[it].z * r * bf16_lo(wv.y), v[it].w * r * bf16_hi(wv.y));
+    res.x = pack16x2<F16>(y0, y1);
+    res.y = pack16x2<F16>(y2, y3);
     *reinterpret_cast<uint2 *>(o + i) = res;
   }
+  flag_range(bad, err);
 }
 
 __global__ void __launch_bounds__(RMS_T) rmsnorm_bwd_kernel(const float *dy, const float *h, const uint16_t *w,
@@ -146,8 +151,9 @@ __global__ void __launch_bounds__(RMS_T) rmsnorm_bwd_kernel(const float *dy, con
 // ------------------------------------------------------------------ RoPE (rotate-half)
 template <bool F16>
 __global__ void rope_fwd_kernel(uint16_t *qkv, int ld, const float *cs, const float *sn, int M,
-                                int S, int nheads_rot, int d) {
+                                int S, int nheads_rot, int d, int *err) {
   const int half = d >> 1;
+  bool bad = false;
   const int64_t total = (int64_t)M * nheads_rot * half;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
        idx += (int64_t)gridDim.x * blockDim.x) {
@@ -159,9 +165,12 @@ __global__ void rope_fwd_kernel(uint16_t *qkv, int ld, const float *cs, const fl
     uint16_t *p = qkv + (size_t)m * ld + (size_t)head * d;
     const float x1 = ld16<F16>(p[i]), x2 = ld16<F16>(p[i + half]);
     const float c = cs[pos * half + i], s = sn[pos * half + i];
-    p[i] = st16<F16>(x1 * c - x2 * s);
-    p[i + half] = st16<F16>(x2 * c + x1 * s);
+    const float y1 = x1 * c - x2 * s, y2 = x2 * c + x1 * s;
+    if (F16) bad |= half_out_of_range(y1) | half_out_of_range(y2);
+    p[i] = st16<F16>(y1);
+    p[i + half] = st16<F16>(y2);
   }
+  flag_range(bad, err);
 }
 
 __global__ void rope_bwd_kernel(const float *dqkv, uint16_t *out, int ld, const float *cs,
@@ -194,9 +203,10 @@ __global__ void rope_bwd_kernel(const float *dqkv, uint16_t *out, int ld, const 
 SOUP_DEV float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
 
 template <bool F16>
-__global__ void swiglu_fwd_kernel(const uint16_t *gu, int M, int I, uint16_t *act) {
+__global__ void swiglu_fwd_kernel(const uint16_t *gu, int M, int I, uint16_t *act, int *err) {
   // 8 consecutive outputs per item when I % 8 == 0 (16-byte loads of gate and up)
   const int I8 = I / 8;
+  bool bad = false;
   const int64_t total = (int64_t)M * I8;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
        idx += (int64_t)gridDim.x * blockDim.x) {
@@ -209,22 +219,29 @@ __global__ void swiglu_fwd_kernel(const uint16_t *gu, int M, int I, uint16_t *ac
     for (int e = 0; e < 4; ++e) {
       const float g0 = lo16<F16>(gw[e]), g1 = hi16<F16>(gw[e]);
       const float u0 = lo16<F16>(uw[e]), u1 = hi16<F16>(uw[e]);
-      o[e] = pack16x2<F16>(g0 * sigmoidf_(g0) * u0, g1 * sigmoidf_(g1) * u1);
+      const float y0 = g0 * sigmoidf_(g0) * u0, y1 = g1 * sigmoidf_(g1) * u1;
+      if (F16) bad |= half_out_of_range(y0) | half_out_of_range(y1);
+      o[e] = pack16x2<F16>(y0, y1);
     }
     *reinterpret_cast<uint4 *>(act + m * I + j) = make_uint4(o[0], o[1], o[2], o[3]);
   }
+  flag_range(bad, err);
 }
 
 template <bool F16>
-__global__ void swiglu_fwd_scalar_kernel(const uint16_t *gu, int M, int I, uint16_t *act) {
+__global__ void swiglu_fwd_scalar_kernel(const uint16_t *gu, int M, int I, uint16_t *act, int *err) {
   const int64_t total = (int64_t)M * I;
+  bool bad = false;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
        idx += (int64_t)gridDim.x * blockDim.x) {
     const int64_t m = idx / I, j = idx % I;
     const float g = ld16<F16>(gu[m * 2 * I + j]);
     const float u = ld16<F16>(gu[m * 2 * I + I + j]);
-    act[idx] = st16<F16>(g * sigmoidf_(g) * u);
+    const float y = g * sigmoidf_(g) * u;
+    if (F16) bad |= half_out_of_range(y);
+    act[idx] = st16<F16>(y);
   }
+  flag_range(bad, err);
 }
 
 // 8 consecutive columns per item (inter % 8 == 0): 32-byte dact loads, 16-byte gate / up loads
@@ -421,7 +438,7 @@ __global__ void __launch_bounds__(128) lora_part_kernel(const uint16_t *X, int l
 // out_f32[m, o] = (DU ? s : 1) * sum_split part; out16[m, o] = 16-bit(s * sum), zero padded.
 template <bool DU, bool OF16>
 __global__ void lora_reduce_kernel(const float *part, int nsplit, int M, const LoraSeg L,
-                                   float *out_f32, uint16_t *out16) {
+                                   float *out_f32, uint16_t *out16, int *err) {
   pdl_trigger();
   pdl_wait();  // launched as a dependent of the partial kernel
   // one warp per output: lanes take the splits lane, lane + 32, ... and the lane sums are
@@ -442,6 +459,7 @@ __global__ void lora_reduce_kernel(const float *part, int nsplit, int M, const L
     acc = warp_sum(acc);
     if (lane == 0) {
       out_f32[(size_t)m * nout + o] = DU ? L.s * acc : acc;
+      if (OF16) flag_range(half_out_of_range(L.s * acc), err);
       out16[idx] = st16<OF16>(L.s * acc);
     }
   }
@@ -811,10 +829,10 @@ void k_embed(const int32_t *tok, const uint16_t *E, int V, int H, int M, float *
   }
 }
 void k_rmsnorm_fwd(const float *h, const uint16_t *w, float eps, int M, int H, uint16_t *out,
-                   bool out_f16, cudaStream_t st) {
+                   bool out_f16, int *err, cudaStream_t st) {
   if (M <= 0) return;
-  if (out_f16) rmsnorm_fwd_kernel<true><<<M, RMS_T, 0, st>>>(h, w, eps, M, H, out);
-  else rmsnorm_fwd_kernel<false><<<M, RMS_T, 0, st>>>(h, w, eps, M, H, out);
+  if (out_f16) rmsnorm_fwd_kernel<true><<<M, RMS_T, 0, st>>>(h, w, eps, M, H, out, err);
+  else rmsnorm_fwd_kernel<false><<<M, RMS_T, 0, st>>>(h, w, eps, M, H, out, err);
   count_launches(1);
 }
 void k_rmsnorm_bwd(const float *dy, const float *h, const uint16_t *w, float eps, int M, int H,
@@ -824,11 +842,11 @@ void k_rmsnorm_bwd(const float *dy, const float *h, const uint16_t *w, float eps
   count_launches(1);
 }
 void k_rope_fwd(uint16_t *qkv, int ld, const float *cos, const float *sin, int M, int S, int nh,
-                int nkv, int d, bool f16, cudaStream_t st) {
+                int nkv, int d, bool f16, int *err, cudaStream_t st) {
   const int64_t n = (int64_t)M * (nh + nkv) * (d / 2);
   if (n <= 0) return;
-  if (f16) rope_fwd_kernel<true><<<grid_for(n, 256), 256, 0, st>>>(qkv, ld, cos, sin, M, S, nh + nkv, d);
-  else rope_fwd_kernel<false><<<grid_for(n, 256), 256, 0, st>>>(qkv, ld, cos, sin, M, S, nh + nkv, d);
+  if (f16) rope_fwd_kernel<true><<<grid_for(n, 256), 256, 0, st>>>(qkv, ld, cos, sin, M, S, nh + nkv, d, err);
+  else rope_fwd_kernel<false><<<grid_for(n, 256), 256, 0, st>>>(qkv, ld, cos, sin, M, S, nh + nkv, d, err);
   count_launches(1);
 }
 void k_rope_bwd(const float *dqkv, uint16_t *out, int ld, const float *cos, const float *sin,
@@ -839,16 +857,16 @@ void k_rope_bwd(const float *dqkv, uint16_t *out, int ld, const float *cos, cons
                                                     nh + 2 * nkv, d);
   count_launches(1);
 }
-void k_swiglu_fwd(const uint16_t *gu, int M, int I, uint16_t *act, bool f16, cudaStream_t st) {
+void k_swiglu_fwd(const uint16_t *gu, int M, int I, uint16_t *act, bool f16, int *err, cudaStream_t st) {
   const int64_t n = (int64_t)M * I;
   if (n <= 0) return;
   if (I % 8 == 0) {
     const int64_t n8 = n / 8;
-    if (f16) swiglu_fwd_kernel<true><<<grid_for(n8, 256), 256, 0, st>>>(gu, M, I, act);
-    else swiglu_fwd_kernel<false><<<grid_for(n8, 256), 256, 0, st>>>(gu, M, I, act);
+    if (f16) swiglu_fwd_kernel<true><<<grid_for(n8, 256), 256, 0, st>>>(gu, M, I, act, err);
+    else swiglu_fwd_kernel<false><<<grid_for(n8, 256), 256, 0, st>>>(gu, M, I, act, err);
   } else {
-    if (f16) swiglu_fwd_scalar_kernel<true><<<grid_for(n, 256), 256, 0, st>>>(gu, M, I, act);
-    else swiglu_fwd_scalar_kernel<false><<<grid_for(n, 256), 256, 0, st>>>(gu, M, I, act);
+    if (f16) swiglu_fwd_scalar_kernel<true><<<grid_for(n, 256), 256, 0, st>>>(gu, M, I, act, err);
+    else swiglu_fwd_scalar_kernel<false><<<grid_for(n, 256), 256, 0, st>>>(gu, M, I, act, err);
   }
   count_launches(1);
 }
@@ -893,7 +911,7 @@ size_t lora_scratch_floats(int M, int dim, int nout) {
 
 template <bool DU>
 static void lora_proj(const uint16_t *X, int ldx, int M, int K, const LoraSeg &L, float *out_f32,
-                      uint16_t *out16, bool x_f16, bool o_f16, float *part, cudaStream_t st) {
+                      uint16_t *out16, bool x_f16, bool o_f16, float *part, int *err, cudaStream_t st) {
   if (M <= 0) return;
   int KS;
   const int ns = lora_splits(M, K, &KS);
@@ -901,8 +919,8 @@ static void lora_proj(const uint16_t *X, int ldx, int M, int K, const LoraSeg &L
   if (x_f16) lora_part_kernel<DU, true><<<grid, 128, 0, st>>>(X, ldx, M, K, KS, L, part);
   else lora_part_kernel<DU, false><<<grid, 128, 0, st>>>(X, ldx, M, K, KS, L, part);
   const int64_t n = (int64_t)M * L.Rpad() * 32;  // one warp per output
-  if (o_f16) launch_pdl(lora_reduce_kernel<DU, true>, dim3(grid_for(n, 256)), dim3(256), 0, st, part, ns, M, L, out_f32, out16);
-  else launch_pdl(lora_reduce_kernel<DU, false>, dim3(grid_for(n, 256)), dim3(256), 0, st, part, ns, M, L, out_f32, out16);
+  if (o_f16) launch_pdl(lora_reduce_kernel<DU, true>, dim3(grid_for(n, 256)), dim3(256), 0, st, part, ns, M, L, out_f32, out16, err);
+  else launch_pdl(lora_reduce_kernel<DU, false>, dim3(grid_for(n, 256)), dim3(256), 0, st, part, ns, M, L, out_f32, out16, err);
   count_launches(2);
 }
 static int seg_cols(const LoraSeg &L) {
@@ -911,12 +929,12 @@ static int seg_cols(const LoraSeg &L) {
   return Ng;
 }
 void k_lora_down(const uint16_t *x, int lda, int M, int K, const LoraSeg &L, float *u_f32,
-                 uint16_t *ul, bool x_f16, bool ul_f16, float *part, cudaStream_t st) {
-  lora_proj<false>(x, lda, M, K, L, u_f32, ul, x_f16, ul_f16, part, st);
+                 uint16_t *ul, bool x_f16, bool ul_f16, float *part, int *err, cudaStream_t st) {
+  lora_proj<false>(x, lda, M, K, L, u_f32, ul, x_f16, ul_f16, part, err, st);
 }
 void k_lora_du(const uint16_t *dy, int ldy, int M, const LoraSeg &L, float *du_f32, uint16_t *dul,
                bool dy_f16, bool dul_f16, float *part, cudaStream_t st) {
-  lora_proj<true>(dy, ldy, M, seg_cols(L), L, du_f32, dul, dy_f16, dul_f16, part, st);
+  lora_proj<true>(dy, ldy, M, seg_cols(L), L, du_f32, dul, dy_f16, dul_f16, part, nullptr, st);
 }
 void k_lora_dB(const uint16_t *dy, int ldy, int M, const float *u_f32, const LoraSeg &L, bool dy_f16,
                float *part, cudaStream_t st) {
@@ -990,6 +1008,24 @@ void k_cast_bf16(const float *in, uint16_t *out, int64_t n, cudaStream_t st) {
     cast_bf16_kernel<<<grid_for(n, 256), 256, 0, st>>>(in, out, n);
     count_launches(1);
   }
+}
+// Waits on an mbarrier that nothing ever arrives on, through the same bounded wait every
+// pipelined kernel uses, with a limit of `limit` cycles: the wait gives up, raises
+// SOUP_KERR_WAIT_TIMEOUT in *err and the kernel returns.  Exercises the error path (flag set
+// on the device, read by the host) without a real stall.
+__global__ void wait_probe_kernel(int *err, long long limit) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  soupk::mbar_init(&bar, 1);
+  soupk::fence_mbar_init();
+  abort_flag = 0;
+  volatile int *ab = &abort_flag;
+  soupk::mbar_wait(&bar, 0, err, ab, limit);
+}
+void k_wait_probe(int *err, long long limit_cycles, cudaStream_t st) {
+  wait_probe_kernel<<<1, 32, 0, st>>>(err, limit_cycles);
+  count_launches(1);
 }
 void k_nf4_dequant(const uint8_t *codes, const float *absmax, int64_t n, float *out_f32,
                    uint16_t *out_bf16, cudaStream_t st) {

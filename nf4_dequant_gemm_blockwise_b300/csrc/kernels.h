@@ -34,17 +34,19 @@ void k_embed(const int32_t *tok, const uint16_t *E, int V, int H, int M, float *
 // Tensors in 16-bit are either IEEE half (the forward's tensor-core operands: normalised
 // inputs, qkv, attention output, gate/up, SwiGLU output, the forward LoRA packs) or bf16
 // (gradients, the loss head); each launcher takes a flag saying which.
+// Forward kernels that store half operands take `err`: a device int into which they OR
+// SOUP_KERR_RANGE if a stored value was NaN or beyond the half range (may be null).
 void k_rmsnorm_fwd(const float *h, const uint16_t *w, float eps, int M, int H, uint16_t *out,
-                   bool out_f16, cudaStream_t st);
+                   bool out_f16, int *err, cudaStream_t st);
 // out = dres + rmsnorm_backward(dy); dres may be null (treated as 0) or alias out.
 void k_rmsnorm_bwd(const float *dy, const float *h, const uint16_t *w, float eps, int M, int H,
                    const float *dres, float *out, uint16_t *out_bf16, cudaStream_t st);
 void k_rope_fwd(uint16_t *qkv, int ld, const float *cos, const float *sin, int M, int S, int nh,
-                int nkv, int d, bool f16, cudaStream_t st);
+                int nkv, int d, bool f16, int *err, cudaStream_t st);
 // in: dqkv float [M, ld]; out bf16 [M, ld]: q/k heads rotated back, v heads cast.
 void k_rope_bwd(const float *dqkv, uint16_t *out, int ld, const float *cos, const float *sin,
                 int M, int S, int nh, int nkv, int d, cudaStream_t st);
-void k_swiglu_fwd(const uint16_t *gu, int M, int I, uint16_t *act, bool f16, cudaStream_t st);
+void k_swiglu_fwd(const uint16_t *gu, int M, int I, uint16_t *act, bool f16, int *err, cudaStream_t st);
 void k_swiglu_bwd(const float *dact, const uint16_t *gu, int M, int I, uint16_t *dgu, bool gu_f16,
                   cudaStream_t st);
 
@@ -55,7 +57,7 @@ int lora_splits(int M, int K, int *KS);
 size_t lora_scratch_floats(int M, int dim, int nout);
 // u = x A^T per segment -> u_f32 [M, nseg*r]; ul = 16-bit(s * u) [M, Rpad] (zero padded)
 void k_lora_down(const uint16_t *x, int lda, int M, int K, const LoraSeg &L, float *u_f32,
-                 uint16_t *ul, bool x_f16, bool ul_f16, float *part, cudaStream_t st);
+                 uint16_t *ul, bool x_f16, bool ul_f16, float *part, int *err, cudaStream_t st);
 // du_p = s dY_p B_p -> du_f32 [M, nseg*r]; dul = 16-bit(du) [M, Rpad]
 void k_lora_du(const uint16_t *dy, int ldy, int M, const LoraSeg &L, float *du_f32, uint16_t *dul,
                bool dy_f16, bool dul_f16, float *part, cudaStream_t st);
@@ -84,6 +86,9 @@ void k_cast_bf16(const float *in, uint16_t *out, int64_t n, cudaStream_t st);
 void k_adamw(float *p, const float *g, float *m, float *v, int64_t n, float lr, float beta1,
              float beta2, float eps, float weight_decay, float grad_scale, int64_t step,
              cudaStream_t st);
+// One block that waits on an mbarrier nothing arrives on, bounded by limit_cycles, and raises
+// the wait-timeout bit in *err (a test of the error path).
+void k_wait_probe(int *err, long long limit_cycles, cudaStream_t st);
 void k_nf4_dequant(const uint8_t *codes, const float *absmax, int64_t n, float *out_f32,
                    uint16_t *out_bf16, cudaStream_t st);
 

@@ -17,6 +17,10 @@
 //     on one stream or synchronise between them.
 //   - A call whose working memory would exceed the array is rejected with SOUP_EINVAL before
 //     anything is enqueued.
+//   - Kernels OR their error bits (a bounded wait that gave up, a half-precision overflow) into
+//     a flag at the start of the array.  The flag is zero when the library loads and is read
+//     and cleared only by soup_proj_noalloc_status, so it collects every call's errors since
+//     the last read.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -55,12 +59,15 @@ int scratch_address(void **out) {
   return 0;
 }
 
+// The error flag sits at a fixed place (the first 256 bytes) so that soup_proj_noalloc_status
+// can find it without knowing the calls' shapes; the working buffers follow it.
+constexpr uint64_t kErrOffset = 0;
 struct Layout {
-  uint64_t u_f32, ul, vl, part, gpart, gpart_floats, err, total;
+  uint64_t u_f32, ul, vl, part, gpart, gpart_floats, total;
 };
 Layout layout(int M, int N, int K) {
   Layout s;
-  uint64_t off = 0;
+  uint64_t off = 256;  // past the error flag
   auto take = [&](uint64_t b) {
     const uint64_t o = off;
     off = (off + b + 255) / 256 * 256;
@@ -73,7 +80,6 @@ Layout layout(int M, int N, int K) {
   // small-M path: per-CTA partial strips (no split-K buffer for the tensor-core path)
   s.gpart_floats = M <= 16 ? gemv_part_floats(GEMM_FWD) : 0;
   s.gpart = take(4 * s.gpart_floats);
-  s.err = take(64);
   s.total = off;
   return s;
 }
@@ -104,8 +110,6 @@ extern "C" int soup_proj_fwd_noalloc(const uint16_t *x, int M, int N, int K, con
   SOUP_TRY(scratch_address(&base_v));
   uint8_t *base = static_cast<uint8_t *>(base_v);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  // the error flag is OR-ed into by kernels, so it must start at zero on every call
-  SOUP_CUDA_TRY(cudaMemsetAsync(base + L.err, 0, 64, st));
   const bool f16 = x_f16 != 0;
   LoraSeg seg;
   seg.nseg = 1;
@@ -134,7 +138,7 @@ extern "C" int soup_proj_fwd_noalloc(const uint16_t *x, int M, int N, int K, con
   g.epi = EPI_16;
   g.out = y;
   g.ldo = N;
-  g.err = reinterpret_cast<int *>(base + L.err);
+  g.err = reinterpret_cast<int *>(base + kErrOffset);
   // partial strips of the small-M path only; the tensor-core path runs without split-K here
   g.part = L.gpart_floats ? reinterpret_cast<float *>(base + L.gpart) : nullptr;
   g.part_floats = L.gpart_floats;
@@ -142,7 +146,7 @@ extern "C" int soup_proj_fwd_noalloc(const uint16_t *x, int M, int N, int K, con
   if (r > 0) {
     k_lora_down(x, K, M, K, seg, reinterpret_cast<float *>(base + L.u_f32),
                 reinterpret_cast<uint16_t *>(base + L.ul), f16, f16,
-                reinterpret_cast<float *>(base + L.part), st);
+                reinterpret_cast<float *>(base + L.part), g.err, st);
     g.lora_u = reinterpret_cast<float *>(base + L.u_f32);
     g.lseg = seg;
     g.after_lora = 1;
@@ -154,4 +158,16 @@ extern "C" int soup_proj_fwd_noalloc(const uint16_t *x, int M, int N, int K, con
     }
   }
   return gemm_launch(g, st);
+}
+
+extern "C" int soup_proj_noalloc_status(uintptr_t stream) {
+  void *base_v = nullptr;
+  SOUP_TRY(scratch_address(&base_v));
+  int *err = reinterpret_cast<int *>(static_cast<uint8_t *>(base_v) + kErrOffset);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int flags = 0;
+  SOUP_CUDA_TRY(cudaMemcpyAsync(&flags, err, sizeof(int), cudaMemcpyDeviceToHost, st));
+  SOUP_CUDA_TRY(cudaStreamSynchronize(st));
+  if (flags) SOUP_CUDA_TRY(cudaMemsetAsync(err, 0, sizeof(int), st));
+  return kernel_flags_status(flags, "soup_proj_fwd_noalloc");
 }

@@ -164,8 +164,8 @@ void harvest(soup_stream *h, bool block) {
         if (count) ++*count;
         if (flops) *flops += e.flops;
         if (bytes) *bytes += e.bytes;
-        cudaEventDestroy(e.start);
-        cudaEventDestroy(e.end);
+        h->ev_pool.push_back(e.start);  // reused by the next timed launch or copy
+        h->ev_pool.push_back(e.end);
       } else {
         if (q != cudaErrorNotReady) (void)cudaGetLastError();
         v[keep++] = e;
@@ -178,6 +178,20 @@ void harvest(soup_stream *h, bool block) {
       &h->stats.gemm_bytes);
 }
 
+// A pair of timing events for one launch or copy: from the pool of harvested ones when it has
+// any (no event creation on the hot path after the first step), else new ones.
+int take_events(soup_stream *h, TimedEv *e) {
+  for (cudaEvent_t *ev : {&e->start, &e->end}) {
+    if (!h->ev_pool.empty()) {
+      *ev = h->ev_pool.back();
+      h->ev_pool.pop_back();
+    } else {
+      SOUP_CUDA_TRY(cudaEventCreate(ev));
+    }
+  }
+  return 0;
+}
+
 int timed_gemm(soup_stream *h, GemmArgs &g) {
   g.err = h->err_dev;
   g.part = F(h, h->plan.gemm_part);
@@ -186,8 +200,7 @@ int timed_gemm(soup_stream *h, GemmArgs &g) {
   TimedEv e;
   e.flops = gemm_flops(g);
   e.bytes = gemm_bytes(g);
-  SOUP_CUDA_TRY(cudaEventCreate(&e.start));
-  SOUP_CUDA_TRY(cudaEventCreate(&e.end));
+  SOUP_TRY(take_events(h, &e));
   SOUP_CUDA_TRY(cudaEventRecord(e.start, h->cs));
   int rc = gemm_launch(g, h->cs);
   SOUP_CUDA_TRY(cudaEventRecord(e.end, h->cs));
@@ -253,11 +266,12 @@ int next_use(const std::vector<int> &seq, size_t from, int layer) {
 
 int issue_copy(soup_stream *h, int slot, int layer) {
   Slot &s = h->slot[slot];
+  // an injected host-side delay before the copy is enqueued may change timing, never results
+  if (h->dbg_copy_delay_us) std::this_thread::sleep_for(std::chrono::microseconds(h->dbg_copy_delay_us));
   SOUP_CUDA_TRY(cudaStreamWaitEvent(h->xs, s.freed, 0));  // WAR: last reader of the slot done
   TimedEv e;
   e.bytes = (double)h->lay.stride;
-  SOUP_CUDA_TRY(cudaEventCreate(&e.start));
-  SOUP_CUDA_TRY(cudaEventCreate(&e.end));
+  SOUP_TRY(take_events(h, &e));
   SOUP_CUDA_TRY(cudaEventRecord(e.start, h->xs));
   SOUP_CUDA_TRY(cudaMemcpyAsync(s.dev, h->store->base + (uint64_t)layer * h->lay.stride, h->lay.stride,
                                 cudaMemcpyHostToDevice, h->xs));
@@ -367,8 +381,8 @@ int layer_forward(soup_stream *h, int li, const uint8_t *shard, bool recompute) 
   // adapters switched off (the reference forward of preference losses): no LoRA kernels and
   // no LoRA extension tiles, the plain dequant GEMMs
   const bool ad = !h->adapters_off;
-  k_rmsnorm_fwd(hin, ln1, c.rms_eps, M, H, B16(h, Lb.x1), true, st);
-  if (ad) k_lora_down(B16(h, Lb.x1), H, M, H, Lq, F(h, Lb.u_f32[0]), B16(h, Lb.u_b[0]), true, true, part, st);
+  k_rmsnorm_fwd(hin, ln1, c.rms_eps, M, H, B16(h, Lb.x1), true, h->err_dev, st);
+  if (ad) k_lora_down(B16(h, Lb.x1), H, M, H, Lq, F(h, Lb.u_f32[0]), B16(h, Lb.u_b[0]), true, true, part, h->err_dev, st);
   {
     GemmArgs g = weight_args(h, shard, SOUP_G_QKV, GEMM_FWD);
     g.op_f16 = 1; g.M = M; g.a = B16(h, Lb.x1); g.lda = H;
@@ -380,10 +394,10 @@ int layer_forward(soup_stream *h, int li, const uint8_t *shard, bool recompute) 
     SOUP_TRY(timed_gemm(h, g));
   }
   k_rope_fwd(B16(h, Lb.qkv), nqkv, F(h, P.rope_cos), F(h, P.rope_sin), M, S, c.n_heads,
-             c.n_kv_heads, c.head_dim, true, st);
+             c.n_kv_heads, c.head_dim, true, h->err_dev, st);
   SOUP_TRY(k_attn_fwd(B16(h, Lb.qkv), nqkv, B, S, c.n_heads, c.n_kv_heads, c.head_dim,
                       B16(h, Lb.att), F(h, Lb.lse), st));
-  if (ad) k_lora_down(B16(h, Lb.att), qd, M, qd, Lo, F(h, Lb.u_f32[1]), B16(h, Lb.u_b[1]), true, true, part, st);
+  if (ad) k_lora_down(B16(h, Lb.att), qd, M, qd, Lo, F(h, Lb.u_f32[1]), B16(h, Lb.u_b[1]), true, true, part, h->err_dev, st);
   {
     GemmArgs g = weight_args(h, shard, SOUP_G_O, GEMM_FWD);
     g.op_f16 = 1; g.M = M; g.a = B16(h, Lb.att); g.lda = qd;
@@ -394,8 +408,8 @@ int layer_forward(soup_stream *h, int li, const uint8_t *shard, bool recompute) 
     g.epi = EPI_F32_ADD; g.add_src = hin; g.ld_add = H; g.out = F(h, Lb.hm); g.ldo = H;
     SOUP_TRY(timed_gemm(h, g));
   }
-  k_rmsnorm_fwd(F(h, Lb.hm), ln2, c.rms_eps, M, H, B16(h, Lb.x2), true, st);
-  if (ad) k_lora_down(B16(h, Lb.x2), H, M, H, Lg, F(h, Lb.u_f32[2]), B16(h, Lb.u_b[2]), true, true, part, st);
+  k_rmsnorm_fwd(F(h, Lb.hm), ln2, c.rms_eps, M, H, B16(h, Lb.x2), true, h->err_dev, st);
+  if (ad) k_lora_down(B16(h, Lb.x2), H, M, H, Lg, F(h, Lb.u_f32[2]), B16(h, Lb.u_b[2]), true, true, part, h->err_dev, st);
   {
     GemmArgs g = weight_args(h, shard, SOUP_G_GU, GEMM_FWD);
     g.op_f16 = 1; g.M = M; g.a = B16(h, Lb.x2); g.lda = H;
@@ -406,8 +420,8 @@ int layer_forward(soup_stream *h, int li, const uint8_t *shard, bool recompute) 
     g.epi = EPI_16; g.out = B16(h, Lb.gu); g.ldo = 2 * I;
     SOUP_TRY(timed_gemm(h, g));
   }
-  k_swiglu_fwd(B16(h, Lb.gu), M, I, B16(h, Lb.act), true, st);
-  if (ad) k_lora_down(B16(h, Lb.act), I, M, I, Ld, F(h, Lb.u_f32[3]), B16(h, Lb.u_b[3]), true, true, part, st);
+  k_swiglu_fwd(B16(h, Lb.gu), M, I, B16(h, Lb.act), true, h->err_dev, st);
+  if (ad) k_lora_down(B16(h, Lb.act), I, M, I, Ld, F(h, Lb.u_f32[3]), B16(h, Lb.u_b[3]), true, true, part, h->err_dev, st);
   if (!recompute) {
     GemmArgs g = weight_args(h, shard, SOUP_G_DOWN, GEMM_FWD);
     g.op_f16 = 1; g.M = M; g.a = B16(h, Lb.act); g.lda = I;
@@ -611,7 +625,7 @@ int step_fwd(soup_stream *h, const int32_t *tokens, int B, int S, const float *c
   }
   // final norm + vocabulary-chunked loss
   TraceRange tr_head("loss head fwd");
-  k_rmsnorm_fwd(F(h, P.h_all) + (size_t)L * M * H, h->final_norm, c.rms_eps, M, H, B16(h, P.hn), false, st);
+  k_rmsnorm_fwd(F(h, P.h_all) + (size_t)L * M * H, h->final_norm, c.rms_eps, M, H, B16(h, P.hn), false, nullptr, st);
   const int vc = P.vc;
   for (int v0 = 0, ci = 0; v0 < c.vocab; v0 += vc, ++ci) {
     const int n = std::min(vc, c.vocab - v0);
@@ -722,8 +736,11 @@ int stream_sync(soup_stream *h, int timeout_ms) {
   }
   int err = 0;
   SOUP_CUDA_TRY(cudaMemcpy(&err, h->err_dev, sizeof(int), cudaMemcpyDeviceToHost));
-  if (err) return set_error(SOUP_ETIMEDOUT, "a kernel's bounded wait gave up (flags 0x%x)", err);
   harvest(h, false);
+  if (err) {  // reported once: the next step starts with a clear flag
+    SOUP_CUDA_TRY(cudaMemset(h->err_dev, 0, sizeof(int)));
+    return kernel_flags_status(err, "soup_sync");
+  }
   return 0;
 }
 
@@ -745,6 +762,7 @@ void soup_stream_free_impl(soup_stream *h) {
       cudaEventDestroy(s.ready);
       cudaEventDestroy(s.freed);
     }
+  for (cudaEvent_t e : h->ev_pool) cudaEventDestroy(e);
   if (h->done) cudaEventDestroy(h->done);
   delete h;
 }

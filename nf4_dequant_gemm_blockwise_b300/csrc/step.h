@@ -70,7 +70,9 @@ struct soup_stream {
   // measurement
   soup_stats stats{};
   std::vector<soup::TimedEv> copy_ev, gemm_ev;
+  std::vector<cudaEvent_t> ev_pool;  // timing events whose measurement was harvested, for reuse
   int dbg_profile = 0, dbg_stale = 0;
+  int dbg_copy_delay_us = 0;  // host sleep before each shard copy is enqueued (timing only)
 };
 
 namespace soup {

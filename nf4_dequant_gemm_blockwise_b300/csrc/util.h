@@ -32,6 +32,10 @@ cudaError_t per_device_once(std::atomic<int> (&slot)[MAX_DEVICES], int *out, Fn 
 
 // Record a formatted message as this thread's last error and return `code`.
 int set_error(int code, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+// Status of the error bits kernels OR into a device flag (SOUP_KERR_* in common.cuh):
+// 0 when no bit is set, else SOUP_ETIMEDOUT (a bounded wait gave up) or SOUP_ERANGE (a value
+// left the 16-bit operand range), with the message set.  `who` names the flag's owner.
+int kernel_flags_status(int flags, const char *who);
 void clear_error();
 // Process-wide count of kernels this library has launched (for launch accounting).
 void count_launches(int n);

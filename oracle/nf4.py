@@ -64,8 +64,13 @@ def quantize(x: np.ndarray):
     nz = absmax > 0
     with np.errstate(divide="ignore", invalid="ignore"):
         q = (blocks[nz] / absmax[nz, None]).astype(np.float32)   # IEEE float32 divide
-    # count of midpoints strictly below q (searchsorted 'left' stops before an equal one)
-    codes[nz] = np.searchsorted(m, q, side="left").astype(np.uint8)
+    # the code is the count of midpoints strictly below q, counted one midpoint at a time
+    count = np.zeros(q.shape, np.uint8)
+    below = np.empty(q.shape, bool)
+    for mk in m:
+        np.greater(q, mk, out=below)
+        count += below.view(np.uint8)
+    codes[nz] = count
     codes = codes.reshape(-1)
     codes[n:] = 7
     return codes, absmax

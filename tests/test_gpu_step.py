@@ -8,8 +8,8 @@ two claims, not one"; "Read this first"):
   abs error <= 5e-2, LoRA gradients relative L2 <= 2e-2 and cosine >= 0.999 per tensor;
 * a deliberately stale slot (the pages' control) must break the gradients.
 The tiny stack is compared end to end with the oracle; the 8B-, 32B- and 3B-shaped stacks
-(full sizes) layer by layer: the oracle recomputes sampled layers from the GPU's own layer
-inputs and upstream gradients.
+(full sizes) layer by layer: the oracle recomputes every layer from the GPU's own layer inputs
+and upstream gradients (tests/layer_oracle.py runs the layers on the host cores in parallel).
 """
 import numpy as np
 import pytest
@@ -289,51 +289,65 @@ def test_errors_are_reported():
 
 
 # ----------------------------------------------------------------------------- full sizes
-def _oracle_layer_check(cfg, g, li, M):
-    """Recompute layer li in float32 from the GPU's own input h_li and upstream gradient."""
-    src = synth.layer_source(cfg, li)
-    W = model.weights_from_source(cfg, [src], synth.embedding(cfg.with_(vocab=2)),
-                                  synth.embedding(cfg.with_(vocab=2)), synth.final_norm(cfg)).layers[0]
-    lora = model.lora_dict(synth.lora_params(cfg.with_(n_layers=li + 1))[li], np.float32)
-    cos, sin = model.rope_tables(cfg.seq, cfg.head_dim, cfg.rope_theta, np.float32)
-    h_in = g["layers"][li].reshape(cfg.batch, cfg.seq, cfg.hidden)
-    out, cache = model.layer_forward(h_in, W, lora, cfg, cos, sin)
-    assert rel_l2(g["layers"][li + 1], out.reshape(M, -1)) <= TOL_FWD_REL, li
-    dh_out = g["dh"][li + 1].reshape(cfg.batch, cfg.seq, cfg.hidden)
-    dh_in, grads = model.layer_backward(dh_out, cache, W, lora, cfg, cos, sin)
-    assert rel_l2(g["dh"][li], dh_in.reshape(M, -1)) <= TOL_GRAD_REL, li
-    for p, name in enumerate(model.PROJ):
-        for w in range(2):
-            got, want = g["grads"][li][p][w], grads[name][w]
-            assert rel_l2(got, want) <= TOL_GRAD_REL, (li, name, w, rel_l2(got, want))
-            assert cosine(got, want) >= TOL_GRAD_COS, (li, name, w)
+def _assert_layer_figures(figs):
+    """The oracle bars on every checked layer: output and dL/dh within the forward / gradient
+    relative L2, every LoRA gradient within relative L2 2e-2 and cosine 0.999."""
+    n = 0
+    for per_layer in figs:
+        for f in per_layer:
+            assert f["out_rel"] <= TOL_FWD_REL, f
+            assert f["dh_rel"] <= TOL_GRAD_REL, f
+            for name, w, rel, cos in f["grads"]:
+                assert rel <= TOL_GRAD_REL, (f["layer"], f["batch"], name, w, rel)
+                assert cos >= TOL_GRAD_COS, (f["layer"], f["batch"], name, w, cos)
+                n += 1
+    return n
 
 
-def _full_size(cfg, check_layers, logit_rows=64):
-    M = cfg.batch * cfg.seq
+def _cases(cfg, runs, li):
+    """The GPU's figures of layer li in each run, as the oracle's layer check takes them."""
+    out = []
+    for c, g in runs:
+        B, S, H = c.batch, c.seq, c.hidden
+        out.append({"h_in": g["layers"][li].reshape(B, S, H), "h_out": g["layers"][li + 1],
+                    "dh_out": g["dh"][li + 1].reshape(B, S, H), "dh_in": g["dh"][li],
+                    "grads": g["grads"][li]})
+    return out
+
+
+def _oracle_every_layer(cfg, runs):
+    """Every layer of every run against the oracle, on the host cores in parallel."""
+    import layer_oracle
+    figs = layer_oracle.check_layers(cfg, range(cfg.n_layers), lambda li: _cases(cfg, runs, li))
+    n = _assert_layer_figures(figs)
+    assert n == 14 * cfg.n_layers * len(runs)
+
+
+def _build_store(cfg):
     from nf4_dequant_gemm_blockwise_b300 import api
-    from nf4_dequant_gemm_blockwise_b300.session import StreamedLoRA
     store = api.Store(cfg, allow_pageable=True)
-    srcs = synth.layer_sources
     for i0 in range(0, cfg.n_layers, 8):
-        for i, src in zip(range(i0, min(cfg.n_layers, i0 + 8)), srcs(cfg, range(i0, min(cfg.n_layers, i0 + 8)))):
+        idx = list(range(i0, min(cfg.n_layers, i0 + 8)))
+        for i, src in zip(idx, synth.layer_sources(cfg, idx)):
             store.put_layer(i, [src[t] for t in synth.LAYER_TENSORS])
-    lora = synth.lora_params(cfg)
-    mk = lambda res: StreamedLoRA(cfg, None, synth.embedding(cfg), synth.lm_head(cfg), synth.final_norm(cfg),
-                                  lora, cfg.batch, cfg.seq, n_slots=2, resident=res, store=store)
-    s = mk(False)
-    g = _run(s, cfg)
-    s.close()
-    torch.cuda.empty_cache()
-    r = mk(True)
-    gr = _run(r, cfg)
-    r.close()
-    n = _assert_bit_equal(g, gr)
-    assert n == 14 * cfg.n_layers
-    del gr
-    for li in check_layers:
-        _oracle_layer_check(cfg, g, li, M)
-    # logits on sampled rows, loss from the full logits
+    return store
+
+
+def _full_run(cfg, store, lora, resident=False, n_slots=2, keep_activations=False):
+    from nf4_dequant_gemm_blockwise_b300.session import StreamedLoRA
+    s = StreamedLoRA(cfg, None, synth.embedding(cfg), synth.lm_head(cfg), synth.final_norm(cfg), lora,
+                     cfg.batch, cfg.seq, n_slots=n_slots, resident=resident, store=store,
+                     keep_activations=keep_activations)
+    try:
+        return _run(s, cfg)
+    finally:
+        s.close()
+        torch.cuda.empty_cache()
+
+
+def _head_checks(cfg, g, logit_rows=64):
+    """Logits on sampled rows against the oracle's head, the loss from the full logits."""
+    M = cfg.batch * cfg.seq
     rows = np.linspace(0, M - 1, logit_rows).astype(int)
     w_lm = nf4.bf16_to_f32(synth.lm_head(cfg))
     lo, _ = model.logits_of(g["layers"][-1][rows], nf4.bf16_to_f32(synth.final_norm(cfg)), w_lm, cfg.rms_eps)
@@ -341,19 +355,65 @@ def _full_size(cfg, check_layers, logit_rows=64):
     assert np.abs(g["logits"][rows] - lo).max() <= TOL_LOGIT_ABS
     loss, _ = model.loss_of(g["logits"].reshape(cfg.batch, cfg.seq, -1), synth.tokens(cfg))
     assert abs(g["loss"] - loss) <= 1e-4 * loss
-    store.free()
 
 
-def test_llama8b_b1_full_size():
-    cfg = synth.LLAMA8B
-    _full_size(cfg, [0, 1, 15, 30, 31])
+def _full_size(cfg):
+    """Streamed == resident bit for bit on everything, then every layer against the oracle."""
+    store = _build_store(cfg)
+    lora = synth.lora_params(cfg)
+    try:
+        g = _full_run(cfg, store, lora)
+        n = _assert_bit_equal(g, _full_run(cfg, store, lora, resident=True))
+        assert n == 14 * cfg.n_layers
+        _head_checks(cfg, g)
+        g.pop("logits")
+        _oracle_every_layer(cfg, [(cfg, g)])
+    finally:
+        store.free()
+
+
+def test_llama8b_full_size():
+    """The 8B-shaped stack at both of its batch sizes (B=1 and B=4, S=512): streamed == resident
+    bit for bit with two slots, with eight slots (B=1) and with kept activations (B=4, the
+    backward re-runs no layer); then every layer of both batch sizes against the oracle."""
+    cfg1 = synth.LLAMA8B
+    cfg4 = synth.LLAMA8B.with_(batch=4)
+    store = _build_store(cfg1)
+    lora = synth.lora_params(cfg1)
+    try:
+        g1 = _full_run(cfg1, store, lora)
+        assert _assert_bit_equal(g1, _full_run(cfg1, store, lora, resident=True)) == 14 * cfg1.n_layers
+        _assert_bit_equal(g1, _full_run(cfg1, store, lora, n_slots=8))
+        _head_checks(cfg1, g1)
+        g1.pop("logits")
+        g4 = _full_run(cfg4, store, lora)
+        assert _assert_bit_equal(g4, _full_run(cfg4, store, lora, resident=True)) == 14 * cfg4.n_layers
+        _assert_bit_equal(g4, _full_run(cfg4, store, lora, keep_activations=True))
+        _head_checks(cfg4, g4)
+        g4.pop("logits")
+        _oracle_every_layer(cfg1, [(cfg1, g1), (cfg4, g4)])
+    finally:
+        store.free()
 
 
 def test_qwen32b_large_layers_full_size():
-    cfg = synth.QWEN32B
-    _full_size(cfg, [0, 31, 63])
+    """64 layers of 261.6 MiB each (every layer above the pages' ~165 MiB threshold)."""
+    _full_size(synth.QWEN32B)
 
 
 def test_qwen3b_bf16_full_size():
-    cfg = synth.QWEN3B_BF16
-    _full_size(cfg, [0, 35])
+    _full_size(synth.QWEN3B_BF16)
+
+
+@pytest.mark.parametrize("keep", [False, True])
+def test_tiny_eight_slots_equal_resident_bitwise(tiny, keep):
+    """stream_buffers' upper bound: eight device slots (more slots than the stack has layers
+    here, so the slot choice keeps every layer after its first copy), recomputing and with
+    kept activations, two steps in a row."""
+    s = _session(tiny["cfg"], resident=False, store=tiny["s"].store, n_slots=8, keep_activations=keep)
+    try:
+        a, b = _run(s, tiny["cfg"]), _run(s, tiny["cfg"])
+    finally:
+        s.close()
+    _assert_bit_equal(tiny["resident"], a)
+    _assert_bit_equal(tiny["resident"], b)
