@@ -89,8 +89,11 @@ def _args():
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--batch", type=int, default=1)
-    p.add_argument("--seq", type=int, default=512)
+    p.add_argument("--seq", type=int, default=None)
     p.add_argument("--slots", type=int, default=2)
+    p.add_argument("--config", default="llama8b", choices=["llama8b", "qwen3b", "qwen32b"],
+                   help="stack shape: the 8B NF4 stack (default, the headline workload), the 3B stack "
+                        "with a bf16 base (S=512), or the 32B NF4 stack of large layers (S=1024)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--pageable", action="store_true",
                    help="stream from a pageable (not page-locked) copy of the store, to measure "
@@ -115,10 +118,20 @@ def _peaks():
     return {"hbm": 6400.0, "bf16": 1800.0, "bf16_sus": 1400.0, "src": "fallback"}
 
 
+def _stack(args):
+    """The stack the step runs on: --config picks the shape; --batch / --seq override the
+    8B stack's (the 3B and 32B stacks keep their own sequence length unless --seq is given)."""
+    import synth
+    base = {"llama8b": synth.LLAMA8B, "qwen3b": synth.QWEN3B_BF16, "qwen32b": synth.QWEN32B}[args.config]
+    seq = args.seq if (args.seq is not None) else base.seq
+    return base.with_(batch=args.batch, seq=seq)
+
+
 def _workload(cfg, slots):
     return {"workload": f"{cfg.name}: streamed LoRA training step (fwd+bwd+AdamW), {cfg.n_layers} layers, hidden "
                         f"{cfg.hidden}, inter {cfg.inter}, {cfg.n_heads}/{cfg.n_kv_heads} heads, vocab "
-                        f"{cfg.vocab}, NF4 base, r={cfg.lora_r}, {slots} device slots, AdamW lr {LR}",
+                        f"{cfg.vocab}, {cfg.base_fmt.upper()} base{', tied head' if cfg.tied else ''}, "
+                        f"r={cfg.lora_r}, {slots} device slots, AdamW lr {LR}",
             "global_batch": cfg.batch, "seq_len": cfg.seq, "tokens_per_step": cfg.batch * cfg.seq,
             "parallelism": "replicas", "l2": "inputs larger than L2 (whole store re-streamed each step)"}
 
@@ -254,7 +267,7 @@ def _threads():
 # ------------------------------------------------------------------------------ reference arm
 def run_reference(args, rank):
     import synth
-    cfg = synth.LLAMA8B.with_(batch=args.batch, seq=args.seq)
+    cfg = _stack(args)
     if rank != 0:
         return
     one = run_oracle_timed(cfg)
@@ -422,7 +435,7 @@ def run_ours(args, rank, world, local_rank, dist):
     from nf4_dequant_gemm_blockwise_b300.session import StreamedLoRA
 
     torch.cuda.set_device(local_rank)
-    cfg = synth.LLAMA8B.with_(batch=args.batch, seq=args.seq)
+    cfg = _stack(args)
     B, S = cfg.batch, cfg.seq
     peaks = _peaks()
     h2d_peak = h2d_peak_gbs(torch)
@@ -538,6 +551,30 @@ def run_ours(args, rank, world, local_rank, dist):
         ms_res = g0.elapsed_time(g1) / args.steps
         sess_r.close()
 
+    # ---- every kernel family of the step, event-timed per launch group over a few extra steps
+    # (not the timed run: the events themselves cost a little)
+    prof_steps = 3
+    sess.stream.debug(api.DBG_PROFILE, 2)
+    sess.stream.kernel_stats(reset=True)
+    for _ in range(prof_steps):
+        _train_step(sess, tok_dev)
+    sess.sync()
+    fams = sess.stream.kernel_stats(reset=True)
+    sess.stream.debug(api.DBG_PROFILE, 0)
+    kernels = []
+    for f in fams:
+        if f["ms"] <= 0:
+            continue
+        if f["tensor_bound"]:
+            ach, peak, unit = f["flops"] / (f["ms"] * 1e-3) / 1e12, peaks["bf16_sus"], "TFLOP/s"
+        else:
+            ach, peak, unit = f["bytes"] / (f["ms"] * 1e-3) / 1e9, peaks["hbm"], "GB/s"
+        kernels.append({"family": f["name"], "bound": "tensor" if f["tensor_bound"] else "hbm",
+                        "launch_groups_per_step": f["launches"] / prof_steps,
+                        "ms_per_step": f["ms"] / prof_steps, "flops_per_step": f["flops"] / prof_steps,
+                        "bytes_per_step": f["bytes"] / prof_steps, "achieved": ach, "unit": unit,
+                        "peak": peak, "frac": ach / peak})
+
     # ---- max over ranks
     ms_step, ms_e2e_step = max_over_ranks(dist, [ms_total / args.steps, ms_e2e / args.steps], "cuda")
     tokens = B * S
@@ -574,6 +611,10 @@ def run_ours(args, rank, world, local_rank, dist):
                 "frac": h2d_gbs / h2d_peak if h2d_gbs else None, "bytes_per_step": st["copy_bytes"] / args.steps,
                 "copies_per_step": st["copies"] / args.steps, "store_bytes": store_bytes, "pinned": pinned},
         "overlap": overlap,
+        "kernels": {"method": f"CUDA events around every launch group on the compute stream over {prof_steps} "
+                              "extra steps (profiling mode 2, outside the timed run); algorithmic flops or "
+                              f"bytes per family; peaks: {peaks['src']} bf16 sustained / HBM copy",
+                    "families": kernels},
         "optimizer": {"kernel": "adamw (float32 state, one launch over all adapters)",
                       "params": sess.n_params, "ms": opt_ms, "bound": "hbm", "achieved_gbs": opt_gbs,
                       "frac": opt_gbs / peaks["hbm"], "bytes_per_param": 28},
@@ -583,16 +624,23 @@ def run_ours(args, rank, world, local_rank, dist):
         "loss": loss_val,
         "clocks": clk,
     }
+    sess.close()
+    del sess
+    torch.cuda.empty_cache()
     # ---- extra configurations of the same store: batch 4 (the pages' other 8B batch), eight
     # device slots (stream_buffers' upper bound) and kept activations (stream_recompute: off);
     # same timing method, fewer steps
-    if not args.no_variants:
+    if not args.no_variants and args.config == "llama8b":
         variants = []
-        for vb, vslots, keep in ((4, args.slots, False), (1, 8, False), (4, 8, False),
-                                 (1, args.slots, True), (4, args.slots, True)):
+        for vb, vslots, keep, shead in ((4, args.slots, False, False), (1, 8, False, False),
+                                        (4, 8, False, False), (1, args.slots, True, False),
+                                        (4, args.slots, True, False), (1, args.slots, False, True)):
             vcfg = cfg.with_(batch=vb)
+            torch.cuda.synchronize()
+            torch.cuda.reset_peak_memory_stats()
             vs = StreamedLoRA(vcfg, None, synth.embedding(cfg), synth.lm_head(cfg), synth.final_norm(cfg),
-                              lora, vb, S, n_slots=vslots, store=store, keep_activations=keep)
+                              lora, vb, S, n_slots=vslots, store=store, keep_activations=keep,
+                              stream_head=shead)
             vtok = torch.from_numpy(synth.tokens(vcfg)).cuda()
             for _ in range(args.warmup):
                 _train_step(vs, vtok)
@@ -609,9 +657,14 @@ def run_ours(args, rank, world, local_rank, dist):
             torch.cuda.synchronize()
             vms = v0.elapsed_time(v1) / nsteps
             vst = vs.stream.stats(reset=True)
-            variants.append({"batch": vb, "slots": vslots, "keep_activations": keep, "tokens_per_step": vb * S,
+            variants.append({"batch": vb, "slots": vslots, "keep_activations": keep, "stream_head": shead,
+                             "tokens_per_step": vb * S,
                              "value": world * vb * S / (vms * 1e-3), "ms_per_step": vms,
-                             "copies_per_step": vst["copies"] / nsteps, "steps": nsteps})
+                             "copies_per_step": vst["copies"] / nsteps, "steps": nsteps,
+                             "peak_vram_bytes": torch.cuda.max_memory_allocated(),
+                             "peak_vram_predicted_bytes": api.peak_bytes(vcfg, vb, S, n_slots=vslots,
+                                                                         keep_activations=keep,
+                                                                         stream_head=shead)[0]})
             vs.close()
         line["variants"] = variants
     if rank == 0 and not args.no_cpu_baseline:
@@ -623,7 +676,6 @@ def run_ours(args, rank, world, local_rank, dist):
                                           f"workload on the CPU oracle (float32 NumPy), step time = "
                                           f"{cfg.n_layers} x layer + head; best of 2",
                                 "tiny_step_s": oracle_tiny_step_s()}
-    sess.close()
     store.free()
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -146,6 +146,13 @@ int soup_store_put_layer(soup_store *st, int layer, const uint16_t *const *src, 
  * another store of the same cfg, or from a cache of built shards).  bytes must equal the
  * layout's stride; the store keeps its own copy.  Thread-safe for different layers. */
 int soup_store_put_shard(soup_store *st, int layer, const void *shard, uint64_t bytes);
+/* Put the embedding and the output head into the store, for streams in SOUP_MODE_STREAM_HEAD
+ * ("Layer streaming: fine-tune a model that does not fit in your card", "Measured numbers":
+ * the untied embed_tokens and lm_head move into the store and reuse one device buffer).
+ *   embed: host bf16 [vocab, hidden]; lm_head: host bf16 [vocab, hidden], NULL when cfg.tied
+ *   (the embedding is then the head).  The store keeps its own page-locked, device-mapped copy
+ *   (SOUP_ENOMEM if page-locking fails).  May be called again to replace the tables. */
+int soup_store_put_head(soup_store *st, const uint16_t *embed, const uint16_t *lm_head);
 /* soup_store_create + put_layer for every layer: src is [n_layers * 9] host pointers. */
 int soup_store_build(const soup_cfg *cfg, const uint16_t *const *src, int allow_pageable,
                      soup_store **out);
@@ -162,8 +169,16 @@ void soup_store_free(soup_store *st);
  *     which then skips re-running each layer's forward but still reads every layer's weights
  *     again ("Layer streaming: fine-tune a model that does not fit in your card", "How it
  *     works": training.stream_recompute: off).  Costs one activation set per layer.
+ *   SOUP_MODE_STREAM_HEAD: the embedding and the untied output head live in the store
+ *     (soup_store_put_head), not in caller memory.  The device holds one vocabulary-sized
+ *     buffer [vocab, hidden] bf16 inside the workspace, which the output head occupies (copied
+ *     from the store at soup_stream_init); the embedding gather reads each step's rows straight
+ *     from the page-locked store, so only B*S rows cross the bus ("Layer streaming: fine-tune a
+ *     model that does not fit in your card", "Measured numbers": embed_tokens and lm_head move
+ *     into the store and reuse one device buffer).  Results are bitwise those of a stream with
+ *     resident tables (same kernels on the same bytes).
  * Other bits: SOUP_EINVAL. */
-enum { SOUP_MODE_RESIDENT = 1, SOUP_MODE_KEEP_ACTIVATIONS = 2 };
+enum { SOUP_MODE_RESIDENT = 1, SOUP_MODE_KEEP_ACTIVATIONS = 2, SOUP_MODE_STREAM_HEAD = 4 };
 
 /* Device bytes of the workspace a stream handle needs for batches up to max_batch x max_seq:
  * n_slots shard slots (or every layer in SOUP_MODE_RESIDENT), saved activations (one layer's
@@ -172,7 +187,8 @@ enum { SOUP_MODE_RESIDENT = 1, SOUP_MODE_KEEP_ACTIVATIONS = 2 };
 int soup_workspace_bytes(const soup_cfg *cfg, int max_batch, int max_seq, int n_slots,
                          int mode, uint64_t *ws_bytes);
 /* Device bytes of a whole training run: workspace + caller-side resident tensors (embedding,
- * untied head, final norm, float32 LoRA A/B, their gradients and the two AdamW moments).
+ * untied head — neither in SOUP_MODE_STREAM_HEAD, where the workspace holds the one vocabulary
+ * buffer — final norm, float32 LoRA A/B, their gradients and the two AdamW moments).
  * The pages bound peak VRAM by a single layer plus the resident parts ("About Soup"); this
  * is that bound made exact.  Returns 0 for an invalid cfg or mode.  workspace_bytes
  * (optional) receives the workspace part. */
@@ -184,7 +200,8 @@ uint64_t soup_peak_bytes(const soup_cfg *cfg, int batch, int seq, int n_slots, i
 /* Bind a store to a device workspace.
  *   dev_ws / ws_bytes: caller device buffer, >= soup_workspace_bytes(), 256-B aligned.
  *   embed: dev bf16 [vocab, hidden]; lm_head: dev bf16 [vocab, hidden] or NULL when tied;
- *   final_norm: dev bf16 [hidden].
+ *   both ignored (may be NULL) in SOUP_MODE_STREAM_HEAD, where the store's tables are used
+ *   (SOUP_ESTATE if soup_store_put_head was never called);  final_norm: dev bf16 [hidden].
  *   compute_stream / copy_stream: distinct streams ("How it works": a dedicated copy stream).
  *   n_slots in [2, 8] ("Turn it on": stream_buffers).
  *   mode (bits above): SOUP_MODE_RESIDENT copies every shard to the workspace once here
@@ -242,8 +259,25 @@ int soup_step_bwd_ex(soup_stream *h, float *const *dA, float *const *dB, float *
  * reported, not waited on forever).  Reading the kernels' error flag clears it. */
 int soup_sync(soup_stream *h, int timeout_ms);
 int soup_stream_stats(soup_stream *h, soup_stats *out, int reset);
+
+/* Time spent per kernel family of the step, measured with CUDA events around each group of
+ * launches on the compute stream while SOUP_DBG_PROFILE is 2 (events add a little overhead, so
+ * time a run with it off for throughput).  flops / bytes: the family's algorithmic work over
+ * those launches (the operands and results each kernel must read and write once, not the
+ * traffic it causes); tensor_bound: 1 where the family is a tensor-core contraction (its
+ * roofline is the tensor pipe), 0 where it is bound by memory bandwidth. */
+typedef struct soup_kernel_stat {
+  char name[32];
+  int32_t tensor_bound;
+  uint64_t launches;   /* launch groups timed (one event pair each) */
+  double ms, flops, bytes;
+} soup_kernel_stat;
+/* Writes up to `max` families that ran since the last reset (in a fixed order) and sets *n to
+ * how many there are; reset != 0 clears the counters.  Waits for the timed work. */
+int soup_stream_kernel_stats(soup_stream *h, soup_kernel_stat *out, int max, int *n, int reset);
 /* Debug switches: what =
- *   SOUP_DBG_PROFILE        time every base GEMM with events (value 0/1);
+ *   SOUP_DBG_PROFILE        1: time every base GEMM with events (soup_stream_stats);
+ *                           2: also time every kernel family (soup_stream_kernel_stats); 0: off;
  *   SOUP_DBG_STALE_SLOT     backward reads the slot of a neighbouring layer: a deliberately
  *                           broken control that the exactness tests must catch; reads valid
  *                           memory only (value 0/1);

@@ -51,6 +51,11 @@ class soup_stats(C.Structure):
         return {f: getattr(self, f) for f, _ in self._fields_}
 
 
+class soup_kernel_stat(C.Structure):
+    _fields_ = [("name", C.c_char * 32), ("tensor_bound", C.c_int32), ("launches", C.c_uint64),
+                ("ms", C.c_double), ("flops", C.c_double), ("bytes", C.c_double)]
+
+
 class soup_adamw(C.Structure):
     _fields_ = [("lr", C.c_float), ("beta1", C.c_float), ("beta2", C.c_float),
                 ("eps", C.c_float), ("weight_decay", C.c_float), ("grad_scale", C.c_float)]
@@ -58,11 +63,12 @@ class soup_adamw(C.Structure):
 
 BWD_ACCUMULATE = 1
 STORE_PAGEABLE = 2
-MODE_RESIDENT, MODE_KEEP_ACTIVATIONS = 1, 2
+MODE_RESIDENT, MODE_KEEP_ACTIVATIONS, MODE_STREAM_HEAD = 1, 2, 4
 
 
-def _mode(resident, keep_activations) -> int:
-    return (MODE_RESIDENT if resident else 0) | (MODE_KEEP_ACTIVATIONS if keep_activations else 0)
+def _mode(resident, keep_activations, stream_head=False) -> int:
+    return ((MODE_RESIDENT if resident else 0) | (MODE_KEEP_ACTIVATIONS if keep_activations else 0)
+            | (MODE_STREAM_HEAD if stream_head else 0))
 
 
 def _load() -> C.CDLL:
@@ -81,6 +87,7 @@ def _load() -> C.CDLL:
         "soup_store_create": (I32, [C.POINTER(soup_cfg), I32, C.POINTER(VP)]),
         "soup_store_put_layer": (I32, [VP, I32, C.POINTER(P), I32]),
         "soup_store_put_shard": (I32, [VP, I32, P, U64]),
+        "soup_store_put_head": (I32, [VP, P, P]),
         "soup_store_build": (I32, [C.POINTER(soup_cfg), C.POINTER(P), I32, C.POINTER(VP)]),
         "soup_store_info": (I32, [VP, C.POINTER(P), C.POINTER(U64), C.POINTER(I32)]),
         "soup_store_free": (None, [VP]),
@@ -95,6 +102,7 @@ def _load() -> C.CDLL:
                                   C.c_size_t]),
         "soup_sync": (I32, [VP, I32]),
         "soup_stream_stats": (I32, [VP, C.POINTER(soup_stats), I32]),
+        "soup_stream_kernel_stats": (I32, [VP, C.POINTER(soup_kernel_stat), I32, C.POINTER(I32), I32]),
         "soup_stream_debug": (I32, [VP, I32, I32]),
         "soup_stream_free": (None, [VP]),
         "soup_proj_scratch_bytes": (I32, [I32, I32, I32, I32, C.POINTER(U64)]),
@@ -184,20 +192,21 @@ def nf4_quantize_host(src_bf16_bits: np.ndarray, n_threads: int = 0):
     return codes, absmax
 
 
-def workspace_bytes(cfg, max_batch, max_seq, n_slots=2, resident=False, keep_activations=False) -> int:
+def workspace_bytes(cfg, max_batch, max_seq, n_slots=2, resident=False, keep_activations=False,
+                    stream_head=False) -> int:
     c = make_cfg(cfg)
     out = C.c_uint64()
     _check(lib.soup_workspace_bytes(C.byref(c), max_batch, max_seq, n_slots,
-                                    _mode(resident, keep_activations), C.byref(out)))
+                                    _mode(resident, keep_activations, stream_head), C.byref(out)))
     return out.value
 
 
-def peak_bytes(cfg, batch, seq, n_slots=2, resident=False, keep_activations=False):
+def peak_bytes(cfg, batch, seq, n_slots=2, resident=False, keep_activations=False, stream_head=False):
     """(total device bytes of a run, workspace part)."""
     c = make_cfg(cfg)
     ws = C.c_uint64()
-    tot = lib.soup_peak_bytes(C.byref(c), batch, seq, n_slots, _mode(resident, keep_activations),
-                              C.byref(ws))
+    tot = lib.soup_peak_bytes(C.byref(c), batch, seq, n_slots,
+                              _mode(resident, keep_activations, stream_head), C.byref(ws))
     if tot == 0:
         raise SoupError(EINVAL, last_error())
     return tot, ws.value
@@ -226,6 +235,13 @@ class Store:
         """Fill a shard from its bytes (e.g. another store's ``shard_bytes``)."""
         b = np.ascontiguousarray(shard, np.uint8)
         _check(lib.soup_store_put_shard(self.handle, layer, b.ctypes.data, b.nbytes))
+
+    def put_head(self, embed: np.ndarray, lm_head: np.ndarray | None):
+        """The embedding and the untied output head (None when tied), bf16 bits [vocab,
+        hidden], for streams with stream_head=True."""
+        e = np.ascontiguousarray(embed, np.uint16)
+        h = None if lm_head is None else np.ascontiguousarray(lm_head, np.uint16)
+        _check(lib.soup_store_put_head(self.handle, e.ctypes.data, None if h is None else h.ctypes.data))
 
     def info(self):
         base, nb, pinned = C.c_void_p(), C.c_uint64(), C.c_int()
@@ -261,11 +277,12 @@ class Stream:
     """A stream handle: a store bound to a device workspace and two CUDA streams."""
 
     def __init__(self, store: Store, max_batch, max_seq, workspace, embed, lm_head, final_norm,
-                 compute_stream, copy_stream, n_slots=2, resident=False, keep_activations=False):
+                 compute_stream, copy_stream, n_slots=2, resident=False, keep_activations=False,
+                 stream_head=False):
         self.store = store
         self.cfg = store.cfg
         ws_need = C.c_uint64()
-        mode = _mode(resident, keep_activations)
+        mode = _mode(resident, keep_activations, stream_head)
         _check(lib.soup_workspace_bytes(C.byref(self.cfg), max_batch, max_seq, n_slots, mode,
                                         C.byref(ws_need)))
         self.keep = (workspace, embed, lm_head, final_norm)
@@ -304,6 +321,15 @@ class Stream:
         s = soup_stats()
         _check(lib.soup_stream_stats(self.handle, C.byref(s), int(reset)))
         return s.as_dict()
+
+    def kernel_stats(self, reset: bool = False) -> list:
+        """Per kernel family (profiling mode 2): name, tensor_bound, launches, ms, flops, bytes."""
+        n = C.c_int()
+        _check(lib.soup_stream_kernel_stats(self.handle, None, 0, C.byref(n), 0))
+        arr = (soup_kernel_stat * max(n.value, 1))()
+        _check(lib.soup_stream_kernel_stats(self.handle, arr, n.value, C.byref(n), int(reset)))
+        return [{"name": a.name.decode(), "tensor_bound": bool(a.tensor_bound), "launches": a.launches,
+                 "ms": a.ms, "flops": a.flops, "bytes": a.bytes} for a in arr[:n.value]]
 
     def debug(self, what: int, value: int):
         _check(lib.soup_stream_debug(self.handle, what, value))

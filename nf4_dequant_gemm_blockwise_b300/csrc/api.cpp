@@ -82,6 +82,9 @@ int soup_store_put_layer(soup_store *st, int layer, const uint16_t *const *src, 
 int soup_store_put_shard(soup_store *st, int layer, const void *shard, uint64_t bytes) {
   return store_put_shard(st, layer, shard, bytes);
 }
+int soup_store_put_head(soup_store *st, const uint16_t *embed, const uint16_t *lm_head) {
+  return store_put_head(st, embed, lm_head);
+}
 int soup_store_build(const soup_cfg *cfg, const uint16_t *const *src, int allow_pageable,
                      soup_store **out) {
   if (!src) return set_error(SOUP_EINVAL, "src is NULL");
@@ -131,7 +134,8 @@ uint64_t soup_peak_bytes(const soup_cfg *cfg, int batch, int seq, int n_slots, i
   for (int p = 0; p < 7; ++p) lora += r * (outs[p] + ins[p]);
   lora *= (uint64_t)cfg->n_layers;
   // float32 adapters, their gradients and the two AdamW moments
-  const uint64_t resident_t = 2 * V * H + (cfg->tied ? 0 : 2 * V * H) + 2 * H + 4 * 4 * lora;
+  const uint64_t tables = (mode & SOUP_MODE_STREAM_HEAD) ? 0 : 2 * V * H + (cfg->tied ? 0 : 2 * V * H);
+  const uint64_t resident_t = tables + 2 * H + 4 * 4 * lora;
   return P.total + resident_t;
 }
 
@@ -172,11 +176,14 @@ int soup_stream_debug(soup_stream *h, int what, int value) {
   return 0;
 }
 void soup_stream_free(soup_stream *h) { soup_stream_free_impl(h); }
+int soup_stream_kernel_stats(soup_stream *h, soup_kernel_stat *out, int max, int *n, int reset) {
+  return stream_kernel_stats(h, out, max, n, reset);
+}
 
 // ------------------------------------------------------------------ single projection
 namespace {
 struct ProjScratch {
-  uint64_t u_f32, ul, vl, ac, du_f32, dul, part, gpart, gpart_floats, err, total;
+  uint64_t u_f32, ul, vl, ac, du_f32, dul, part, gpart, gpart_floats, cnt, cnt_ints, err, total;
 };
 ProjScratch proj_plan(int M, int N, int K) {
   ProjScratch s;
@@ -194,14 +201,23 @@ ProjScratch proj_plan(int M, int N, int K) {
   s.dul = take(2ull * M * 64);
   s.part = take(4ull * std::max(lora_scratch_floats(std::max(M, 1), K, 64),
                                  lora_scratch_floats(std::max(M, 1), N, 64)));
-  s.gpart_floats = std::min<uint64_t>(4ull * M * std::max(N, K), 1ull << 26);
-  if (M <= 16)  // the small-M path's per-CTA partial strips
-    s.gpart_floats = std::max<uint64_t>(s.gpart_floats, std::max(gemv_part_floats(GEMM_FWD),
-                                                                 gemv_part_floats(GEMM_DX)));
+  // partial tiles of the tensor-core path's stream-K schedule, or the small-M path's strips
+  s.gpart_floats = M <= 16 ? std::max(gemv_part_floats(GEMM_FWD), gemv_part_floats(GEMM_DX))
+                           : SK_PART_FLOATS;
   s.gpart = take(4 * s.gpart_floats);
+  s.cnt_ints = sk_counter_ints(std::max(M, 1), std::max(N, K));
+  s.cnt = take(4 * s.cnt_ints);
   s.err = take(64);
   s.total = off;
   return s;
+}
+// The stream-K tile counters live in the caller's scratch, whose contents are unknown: they
+// are zeroed on the stream before every call (a few kilobytes).
+int proj_counters(GemmArgs &g, uint8_t *base, const ProjScratch &P, cudaStream_t st) {
+  g.counters = reinterpret_cast<int *>(base + P.cnt);
+  g.counter_ints = P.cnt_ints;
+  SOUP_CUDA_TRY(cudaMemsetAsync(g.counters, 0, 4 * P.cnt_ints, st));
+  return 0;
 }
 int proj_check(int M, int N, int K, const uint8_t *codes, const float *absmax, const uint16_t *w,
                const float *A, const float *B, int r, void *scratch, uint64_t bytes) {
@@ -269,6 +285,7 @@ int soup_proj_fwd(const uint16_t *x, int M, int N, int K, const uint8_t *codes, 
   g.err = reinterpret_cast<int *>(base + P.err);
   g.part = reinterpret_cast<float *>(base + P.gpart);
   g.part_floats = P.gpart_floats;
+  SOUP_TRY(proj_counters(g, base, P, st));
   if (r > 0) {
     k_lora_down(x, K, M, K, L, reinterpret_cast<float *>(base + P.u_f32),
                 reinterpret_cast<uint16_t *>(base + P.ul), f16, f16,
@@ -302,6 +319,7 @@ int soup_proj_dx(const uint16_t *dy, int M, int N, int K, const uint8_t *codes, 
   g.err = reinterpret_cast<int *>(base + P.err);
   g.part = reinterpret_cast<float *>(base + P.gpart);
   g.part_floats = P.gpart_floats;
+  SOUP_TRY(proj_counters(g, base, P, st));
   if (r > 0) {
     k_lora_du(dy, N, M, L, reinterpret_cast<float *>(base + P.du_f32),
               reinterpret_cast<uint16_t *>(base + P.dul), false, false,

@@ -714,6 +714,44 @@ __global__ void pack_bwd_kernel(const LoraSeg L, int K, uint16_t *acat) {
   }
 }
 
+// All eight LoRA operand packs of one layer in one launch: blockIdx.y = 2 g + (0: the
+// forward's half Vl [n_out, Rpad] of group g, 1: the dX GEMM's bf16 Acat [Rpad, n_in]); the
+// same element rule as pack_fwd_kernel / pack_bwd_kernel.
+struct PackJobs {
+  LoraSeg L[4];
+  int n_out[4], n_in[4];
+  uint16_t *vl[4], *ac[4];
+};
+__global__ void pack_layer_kernel(const PackJobs J) {
+  const int g = blockIdx.y >> 1;
+  const LoraSeg &L = J.L[g];
+  const int Rp = L.Rpad();
+  if ((blockIdx.y & 1) == 0) {
+    const int64_t total = (int64_t)J.n_out[g] * Rp;
+    uint16_t *vl = J.vl[g];
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+      const int n = (int)(idx / Rp), c = (int)(idx % Rp);
+      float v = 0.f;
+      const int seg = c / L.r;
+      if (seg < L.nseg && n >= L.off[seg] && n < L.off[seg] + L.n[seg])
+        v = L.B[seg][(size_t)(n - L.off[seg]) * L.r + (c % L.r)];
+      vl[idx] = st16<true>(v);
+    }
+  } else {
+    const int K = J.n_in[g];
+    const int64_t total = (int64_t)Rp * K;
+    uint16_t *acat = J.ac[g];
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+      const int row = (int)(idx / K), k = (int)(idx % K);
+      float v = 0.f;
+      if (row < L.nseg * L.r) v = L.A[row / L.r][(size_t)(row % L.r) * K + k];
+      acat[idx] = st16<false>(v);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ cross-entropy
 template <int NT>
 SOUP_DEV float block_reduce(float v, float *sh, bool is_max) {
@@ -979,6 +1017,23 @@ void k_pack_bwd(const LoraSeg &L, int K, uint16_t *acat, bool f16, cudaStream_t 
   const int64_t n = (int64_t)L.Rpad() * K;
   if (f16) pack_bwd_kernel<true><<<grid_for(n, 256), 256, 0, st>>>(L, K, acat);
   else pack_bwd_kernel<false><<<grid_for(n, 256), 256, 0, st>>>(L, K, acat);
+  count_launches(1);
+}
+void k_pack_layer(const LoraSeg (&L)[4], const int n_out[4], const int n_in[4], uint16_t *const vl[4],
+                  uint16_t *const ac[4], cudaStream_t st) {
+  PackJobs J;
+  int64_t most = 1;
+  for (int g = 0; g < 4; ++g) {
+    J.L[g] = L[g];
+    J.n_out[g] = n_out[g];
+    J.n_in[g] = n_in[g];
+    J.vl[g] = vl[g];
+    J.ac[g] = ac[g];
+    most = std::max(most, (int64_t)L[g].Rpad() * std::max(n_out[g], n_in[g]));
+  }
+  // enough blocks for the largest pack, at most two waves per job
+  const int bx = std::min(grid_for(most, 256), 148 * 2);
+  pack_layer_kernel<<<dim3(bx, 8), 256, 0, st>>>(J);
   count_launches(1);
 }
 void k_ce_chunk_fwd(const float *z, int ldz, int v0, int vc, const int32_t *tok, int M, int S,

@@ -71,6 +71,9 @@ void k_lora_dA(const float *du_f32, const uint16_t *x, int lda, int M, int K, co
 void k_pack_fwd(const LoraSeg &L, int Ng, uint16_t *vl, bool f16, cudaStream_t st);
 // Acat [Rpad, K]: row p*r + j holds 16-bit(A_p[j, :]); rows past nseg*r are zero
 void k_pack_bwd(const LoraSeg &L, int K, uint16_t *acat, bool f16, cudaStream_t st);
+// One launch for a layer's four groups: vl[g] as k_pack_fwd in half, ac[g] as k_pack_bwd in bf16.
+void k_pack_layer(const LoraSeg (&L)[4], const int n_out[4], const int n_in[4], uint16_t *const vl[4],
+                  uint16_t *const ac[4], cudaStream_t st);
 
 // Vocabulary-chunked cross-entropy.  Rows are tokens b*S + t; row t has label tok[b*S+t+1]
 // for t < S-1 and none for t = S-1.

@@ -29,6 +29,14 @@
 
 namespace soup {
 
+const char *const kFamName[FAM_COUNT] = {
+    "embed", "rmsnorm_fwd", "rmsnorm_bwd", "rope_fwd", "rope_bwd", "swiglu_fwd", "swiglu_bwd",
+    "attn_fwd", "attn_bwd", "cast_bf16", "lora_pack", "lora_down", "lora_du", "lora_dB", "lora_dA",
+    "gemm_fwd_qkv", "gemm_fwd_o", "gemm_fwd_gate_up", "gemm_fwd_down", "gemm_dx_qkv", "gemm_dx_o",
+    "gemm_dx_gate_up", "gemm_dx_down", "head_gemm", "head_dx", "ce_fwd", "ce_bwd"};
+const int kFamTensor[FAM_COUNT] = {0, 0, 0, 0, 0, 0, 0, 1, 1, 0, 0, 0, 0, 0, 0,
+                                   1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 0, 0};
+
 static uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 
 // A named host-side range on a profiler's timeline (NVTX); costs nothing without a profiler.
@@ -53,7 +61,7 @@ int ce_chunk_cols(int M, int V) {
 
 int make_plan(const soup_cfg *c, int maxB, int maxS, int n_slots, int mode, Plan *P) {
   SOUP_TRY(validate_cfg(c));
-  if (mode & ~(SOUP_MODE_RESIDENT | SOUP_MODE_KEEP_ACTIVATIONS))
+  if (mode & ~(SOUP_MODE_RESIDENT | SOUP_MODE_KEEP_ACTIVATIONS | SOUP_MODE_STREAM_HEAD))
     return set_error(SOUP_EINVAL, "unknown stream mode bits 0x%x", mode);
   const bool resident = (mode & SOUP_MODE_RESIDENT) != 0;
   if (maxB < 1 || maxS < 2) return set_error(SOUP_EINVAL, "max_batch >= 1 and max_seq >= 2 required");
@@ -109,9 +117,17 @@ int make_plan(const soup_cfg *c, int maxB, int maxS, int n_slots, int mode, Plan
     for (int k : dims) mx = std::max(mx, lora_scratch_floats((int)M, k, 3 * c->lora_r));
     P->lora_part = take(4 * mx);
   }
-  // split-K partial tiles for the base GEMMs whose output grid under-fills the GPU
-  P->gemm_part_floats = 4ull * M * std::max<uint64_t>(std::max(nqkv, H), std::max(qd, (uint64_t)I));
+  // partial tiles of the tensor-core GEMMs' stream-K schedule (and the small-M path's partial
+  // strips), and the per-tile counters, sized for the widest output of the step
+  P->gemm_part_floats = std::max<uint64_t>(SK_PART_FLOATS, std::max(gemv_part_floats(GEMM_FWD),
+                                                                    gemv_part_floats(GEMM_DX)));
   P->gemm_part = take(4 * P->gemm_part_floats);
+  {
+    const uint64_t widest = std::max<uint64_t>(std::max<uint64_t>(nqkv, 2 * I),
+                                               std::max<uint64_t>(H, (uint64_t)ce_chunk_cols((int)M, c->vocab)));
+    P->gemm_cnt_ints = sk_counter_ints((int)M, (int)widest);
+    P->gemm_cnt = take(4 * P->gemm_cnt_ints);
+  }
   P->hn = take(2 * M * H);
   P->vc = ce_chunk_cols((int)M, c->vocab);
   P->z = take(4 * M * (uint64_t)P->vc);
@@ -134,6 +150,7 @@ int make_plan(const soup_cfg *c, int maxB, int maxS, int n_slots, int mode, Plan
   P->rope_cos = take(4ull * maxS * (c->head_dim / 2));
   P->rope_sin = take(4ull * maxS * (c->head_dim / 2));
   P->err = take(64);
+  if (mode & SOUP_MODE_STREAM_HEAD) P->vocab_buf = take(2ull * c->vocab * H);
   P->total = off;
   return 0;
 }
@@ -151,7 +168,7 @@ int check_cuda(const char *what) {
 }
 
 void harvest(soup_stream *h, bool block) {
-  auto run = [&](std::vector<TimedEv> &v, double &ms_sum, uint64_t *count, double *flops,
+  auto run = [&](std::vector<TimedEv> &v, double *ms_sum, uint64_t *count, double *flops,
                  double *bytes) {
     size_t keep = 0;
     for (size_t i = 0; i < v.size(); ++i) {
@@ -160,10 +177,17 @@ void harvest(soup_stream *h, bool block) {
       if (q == cudaSuccess) {
         float ms = 0.f;
         cudaEventElapsedTime(&ms, e.start, e.end);
-        ms_sum += ms;
+        if (ms_sum) *ms_sum += ms;
         if (count) ++*count;
         if (flops) *flops += e.flops;
         if (bytes) *bytes += e.bytes;
+        if (e.fam >= 0) {
+          FamStat &f = h->fam[e.fam];
+          f.launches += 1;
+          f.ms += ms;
+          f.flops += e.flops;
+          f.bytes += e.bytes;
+        }
         h->ev_pool.push_back(e.start);  // reused by the next timed launch or copy
         h->ev_pool.push_back(e.end);
       } else {
@@ -173,9 +197,10 @@ void harvest(soup_stream *h, bool block) {
     }
     v.resize(keep);
   };
-  run(h->copy_ev, h->stats.copy_ms, nullptr, nullptr, nullptr);
-  run(h->gemm_ev, h->stats.gemm_ms, &h->stats.gemm_launches, &h->stats.gemm_flops,
+  run(h->copy_ev, &h->stats.copy_ms, nullptr, nullptr, nullptr);
+  run(h->gemm_ev, &h->stats.gemm_ms, &h->stats.gemm_launches, &h->stats.gemm_flops,
       &h->stats.gemm_bytes);
+  run(h->fam_ev, nullptr, nullptr, nullptr, nullptr);
 }
 
 // A pair of timing events for one launch or copy: from the pool of harvested ones when it has
@@ -192,14 +217,43 @@ int take_events(soup_stream *h, TimedEv *e) {
   return 0;
 }
 
-int timed_gemm(soup_stream *h, GemmArgs &g) {
+// Profiling mode 2: one event pair around a group of launches of one kernel family, with the
+// group's algorithmic flops and bytes.  Costs nothing when profiling is off.
+template <class Fn>
+int prof(soup_stream *h, int fam, double flops, double bytes, Fn &&fn) {
+  if (h->dbg_profile < 2) {
+    fn();
+    return 0;
+  }
+  TimedEv e;
+  e.flops = flops;
+  e.bytes = bytes;
+  e.fam = fam;
+  SOUP_TRY(take_events(h, &e));
+  SOUP_CUDA_TRY(cudaEventRecord(e.start, h->cs));
+  fn();
+  SOUP_CUDA_TRY(cudaEventRecord(e.end, h->cs));
+  h->fam_ev.push_back(e);
+  return 0;
+}
+
+// A base-weight GEMM of group `grp` (forward or dX), timed in profiling modes 1 and 2.
+// The step's split-work scratch for a GEMM (partial tiles, counters) and its error flag.
+void gemm_scratch(soup_stream *h, GemmArgs &g) {
   g.err = h->err_dev;
   g.part = F(h, h->plan.gemm_part);
   g.part_floats = h->plan.gemm_part_floats;
+  g.counters = reinterpret_cast<int *>(h->ws + h->plan.gemm_cnt);
+  g.counter_ints = h->plan.gemm_cnt_ints;
+}
+
+int timed_gemm(soup_stream *h, GemmArgs &g, int grp) {
+  gemm_scratch(h, g);
   if (!h->dbg_profile) return gemm_launch(g, h->cs);
   TimedEv e;
   e.flops = gemm_flops(g);
   e.bytes = gemm_bytes(g);
+  e.fam = (g.mode == GEMM_FWD ? FAM_GEMM_FWD_QKV : FAM_GEMM_DX_QKV) + grp;
   SOUP_TRY(take_events(h, &e));
   SOUP_CUDA_TRY(cudaEventRecord(e.start, h->cs));
   int rc = gemm_launch(g, h->cs);
@@ -264,24 +318,45 @@ int next_use(const std::vector<int> &seq, size_t from, int layer) {
   return INT32_MAX;
 }
 
+// Byte ranges of chunk g inside a shard: the group's weight section (codes and absmax are
+// adjacent) and, for q|k|v and gate|up, the norm vector the layer reads just before that GEMM.
+int chunk_ranges(const soup_shard_layout &L, int hidden, int g, uint64_t off[2], uint64_t len[2]) {
+  const uint64_t end = L.a_bytes[g] ? L.a_off[g] + L.a_bytes[g] : L.w_off[g] + L.w_bytes[g];
+  off[0] = L.w_off[g];
+  len[0] = end - L.w_off[g];
+  if (g == SOUP_G_QKV || g == SOUP_G_GU) {
+    off[1] = g == SOUP_G_QKV ? L.ln1_off : L.ln2_off;
+    len[1] = 2ull * hidden;
+    return 2;
+  }
+  return 1;
+}
+
+// Copy `layer` into `slot`, chunk by chunk in the order the layer reads them (q|k|v, o,
+// gate|up, down: the forward's order, and the backward's recompute's).
 int issue_copy(soup_stream *h, int slot, int layer) {
   Slot &s = h->slot[slot];
   // an injected host-side delay before the copy is enqueued may change timing, never results
   if (h->dbg_copy_delay_us) std::this_thread::sleep_for(std::chrono::microseconds(h->dbg_copy_delay_us));
-  SOUP_CUDA_TRY(cudaStreamWaitEvent(h->xs, s.freed, 0));  // WAR: last reader of the slot done
-  TimedEv e;
-  e.bytes = (double)h->lay.stride;
-  SOUP_TRY(take_events(h, &e));
-  SOUP_CUDA_TRY(cudaEventRecord(e.start, h->xs));
-  SOUP_CUDA_TRY(cudaMemcpyAsync(s.dev, h->store->base + (uint64_t)layer * h->lay.stride, h->lay.stride,
-                                cudaMemcpyHostToDevice, h->xs));
-  SOUP_CUDA_TRY(cudaEventRecord(e.end, h->xs));
-  SOUP_CUDA_TRY(cudaEventRecord(s.ready, h->xs));         // RAW: the copy landed
-  h->copy_ev.push_back(e);
+  const uint8_t *src = h->store->base + (uint64_t)layer * h->lay.stride;
+  for (int g = 0; g < NCHUNK; ++g) {
+    uint64_t off[2], len[2];
+    const int n = chunk_ranges(h->lay, h->cfg.hidden, g, off, len);
+    SOUP_CUDA_TRY(cudaStreamWaitEvent(h->xs, s.freed[g], 0));  // WAR: last reader of the chunk done
+    TimedEv e;
+    for (int k = 0; k < n; ++k) e.bytes += (double)len[k];
+    SOUP_TRY(take_events(h, &e));
+    SOUP_CUDA_TRY(cudaEventRecord(e.start, h->xs));
+    for (int k = 0; k < n; ++k)
+      SOUP_CUDA_TRY(cudaMemcpyAsync(s.dev + off[k], src + off[k], len[k], cudaMemcpyHostToDevice, h->xs));
+    SOUP_CUDA_TRY(cudaEventRecord(e.end, h->xs));
+    SOUP_CUDA_TRY(cudaEventRecord(s.ready[g], h->xs));         // RAW: the chunk landed
+    h->copy_ev.push_back(e);
+    s.pending[g] = 1;
+    h->stats.copy_bytes += (uint64_t)e.bytes;
+  }
   s.layer = layer;
-  s.pending = 1;
   h->stats.copies += 1;
-  h->stats.copy_bytes += h->lay.stride;
   return 0;
 }
 
@@ -311,7 +386,8 @@ int prefetch(soup_stream *h, const std::vector<int> &seq, size_t pos, int look) 
   return 0;
 }
 
-// Device pointer of `layer`'s shard for the use at position pos; waits for its copy.
+// The slot holding `layer` for the use at position pos (a copy is issued if none does).  No
+// wait here: each kernel group waits for its own chunk (use_chunk).
 int acquire(soup_stream *h, const std::vector<int> &seq, size_t pos, const uint8_t **shard,
             int *slot_out) {
   const int layer = seq[pos];
@@ -325,10 +401,6 @@ int acquire(soup_stream *h, const std::vector<int> &seq, size_t pos, const uint8
   for (int k = 0; k < (int)h->slot.size(); ++k)
     if (h->slot[k].layer == layer) s = k;
   if (s < 0) return set_error(SOUP_ESTATE, "internal: layer %d has no slot", layer);
-  if (h->slot[s].pending) {
-    SOUP_CUDA_TRY(cudaStreamWaitEvent(h->cs, h->slot[s].ready, 0));
-    h->slot[s].pending = 0;
-  }
   int use = s;
   if (h->dbg_stale && h->in_bwd) use = (s + 1) % (int)h->slot.size();  // deliberately wrong
   *shard = h->slot[use].dev;
@@ -336,9 +408,21 @@ int acquire(soup_stream *h, const std::vector<int> &seq, size_t pos, const uint8
   return 0;
 }
 
-int release(soup_stream *h, int slot) {
+// Before the first kernel that reads chunk g of the slot: wait for its copy (RAW).
+int use_chunk(soup_stream *h, int slot, int g) {
   if (slot < 0) return 0;
-  SOUP_CUDA_TRY(cudaEventRecord(h->slot[slot].freed, h->cs));
+  Slot &s = h->slot[slot];
+  if (s.pending[g]) {
+    SOUP_CUDA_TRY(cudaStreamWaitEvent(h->cs, s.ready[g], 0));
+    s.pending[g] = 0;
+  }
+  return 0;
+}
+
+// After the last kernel of this use that reads chunk g: a later copy into it may start (WAR).
+int release_chunk(soup_stream *h, int slot, int g) {
+  if (slot < 0) return 0;
+  SOUP_CUDA_TRY(cudaEventRecord(h->slot[slot].freed[g], h->cs));
   h->slot[slot].tick = ++h->tick;
   return 0;
 }
@@ -362,7 +446,23 @@ LayerBufs bufs_of(const soup_stream *h, int li) {
   return b;
 }
 
-int layer_forward(soup_stream *h, int li, const uint8_t *shard, bool recompute) {
+// Algorithmic work of the LoRA down-projection u = x A^T (x [M, K] 16-bit, nseg * r outputs):
+// flops of the product; bytes of x, A, u (float) and its 16-bit pack.
+double lora_down_flops(const LoraSeg &L, int M, int K) { return 2.0 * M * K * L.nseg * L.r; }
+double lora_down_bytes(const LoraSeg &L, int M, int K) {
+  const double nr = (double)L.nseg * L.r;
+  return 2.0 * M * K + 4.0 * nr * K + 4.0 * M * nr + 2.0 * M * L.Rpad();
+}
+// Causal attention products: `mats` S x S x d products per head (2 forward: q k^T and p v; 5
+// backward: the score recompute, dP, dV, dQ, dK), each over the S (S + 1) / 2 causal pairs.
+double attn_flops(const soup_cfg &c, int B, int S, int mats) {
+  return (double)mats * B * c.n_heads * (double)S * (S + 1) * c.head_dim;
+}
+
+// Forward of layer li on its shard (held in `slot`, -1 when resident).  In the forward proper
+// each chunk is released after its GEMM; the backward's recompute (recompute = true) releases
+// nothing, since the backward reads every chunk again.
+int layer_forward(soup_stream *h, int li, const uint8_t *shard, int slot, bool recompute) {
   const soup_cfg &c = h->cfg;
   const Plan &P = h->plan;
   const LayerBufs Lb = bufs_of(h, li);
@@ -381,8 +481,15 @@ int layer_forward(soup_stream *h, int li, const uint8_t *shard, bool recompute) 
   // adapters switched off (the reference forward of preference losses): no LoRA kernels and
   // no LoRA extension tiles, the plain dequant GEMMs
   const bool ad = !h->adapters_off;
-  k_rmsnorm_fwd(hin, ln1, c.rms_eps, M, H, B16(h, Lb.x1), true, h->err_dev, st);
-  if (ad) k_lora_down(B16(h, Lb.x1), H, M, H, Lq, F(h, Lb.u_f32[0]), B16(h, Lb.u_b[0]), true, true, part, h->err_dev, st);
+  const bool rel = !recompute;
+  SOUP_TRY(use_chunk(h, slot, SOUP_G_QKV));  // ln1 travels with the q|k|v chunk
+  const double dM = M, dH = H, dI = I;
+  SOUP_TRY(prof(h, FAM_RMSNORM_FWD, 0, 6.0 * dM * dH + 2.0 * dH,
+                [&] { k_rmsnorm_fwd(hin, ln1, c.rms_eps, M, H, B16(h, Lb.x1), true, h->err_dev, st); }));
+  if (ad)
+    SOUP_TRY(prof(h, FAM_LORA_DOWN, lora_down_flops(Lq, M, H), lora_down_bytes(Lq, M, H), [&] {
+      k_lora_down(B16(h, Lb.x1), H, M, H, Lq, F(h, Lb.u_f32[0]), B16(h, Lb.u_b[0]), true, true, part, h->err_dev, st);
+    }));
   {
     GemmArgs g = weight_args(h, shard, SOUP_G_QKV, GEMM_FWD);
     g.op_f16 = 1; g.M = M; g.a = B16(h, Lb.x1); g.lda = H;
@@ -391,13 +498,25 @@ int layer_forward(soup_stream *h, int li, const uint8_t *shard, bool recompute) 
       g.lora_u = F(h, Lb.u_f32[0]); g.lseg = Lq; g.after_lora = 1;
     }
     g.epi = EPI_16; g.out = B16(h, Lb.qkv); g.ldo = nqkv;
-    SOUP_TRY(timed_gemm(h, g));
+    SOUP_TRY(timed_gemm(h, g, SOUP_G_QKV));
   }
-  k_rope_fwd(B16(h, Lb.qkv), nqkv, F(h, P.rope_cos), F(h, P.rope_sin), M, S, c.n_heads,
-             c.n_kv_heads, c.head_dim, true, h->err_dev, st);
-  SOUP_TRY(k_attn_fwd(B16(h, Lb.qkv), nqkv, B, S, c.n_heads, c.n_kv_heads, c.head_dim,
-                      B16(h, Lb.att), F(h, Lb.lse), st));
-  if (ad) k_lora_down(B16(h, Lb.att), qd, M, qd, Lo, F(h, Lb.u_f32[1]), B16(h, Lb.u_b[1]), true, true, part, h->err_dev, st);
+  if (rel) SOUP_TRY(release_chunk(h, slot, SOUP_G_QKV));
+  const double rot = (double)(c.n_heads + c.n_kv_heads) * c.head_dim;
+  SOUP_TRY(prof(h, FAM_ROPE_FWD, 0, 4.0 * dM * rot, [&] {
+    k_rope_fwd(B16(h, Lb.qkv), nqkv, F(h, P.rope_cos), F(h, P.rope_sin), M, S, c.n_heads,
+               c.n_kv_heads, c.head_dim, true, h->err_dev, st);
+  }));
+  int arc = 0;
+  SOUP_TRY(prof(h, FAM_ATTN_FWD, attn_flops(c, B, S, 2), 2.0 * dM * (nqkv + qd) + 4.0 * dM * c.n_heads, [&] {
+    arc = k_attn_fwd(B16(h, Lb.qkv), nqkv, B, S, c.n_heads, c.n_kv_heads, c.head_dim, B16(h, Lb.att),
+                     F(h, Lb.lse), st);
+  }));
+  SOUP_TRY(arc);
+  if (ad)
+    SOUP_TRY(prof(h, FAM_LORA_DOWN, lora_down_flops(Lo, M, qd), lora_down_bytes(Lo, M, qd), [&] {
+      k_lora_down(B16(h, Lb.att), qd, M, qd, Lo, F(h, Lb.u_f32[1]), B16(h, Lb.u_b[1]), true, true, part, h->err_dev, st);
+    }));
+  SOUP_TRY(use_chunk(h, slot, SOUP_G_O));
   {
     GemmArgs g = weight_args(h, shard, SOUP_G_O, GEMM_FWD);
     g.op_f16 = 1; g.M = M; g.a = B16(h, Lb.att); g.lda = qd;
@@ -406,10 +525,16 @@ int layer_forward(soup_stream *h, int li, const uint8_t *shard, bool recompute) 
       g.lora_u = F(h, Lb.u_f32[1]); g.lseg = Lo; g.after_lora = 1;
     }
     g.epi = EPI_F32_ADD; g.add_src = hin; g.ld_add = H; g.out = F(h, Lb.hm); g.ldo = H;
-    SOUP_TRY(timed_gemm(h, g));
+    SOUP_TRY(timed_gemm(h, g, SOUP_G_O));
   }
-  k_rmsnorm_fwd(F(h, Lb.hm), ln2, c.rms_eps, M, H, B16(h, Lb.x2), true, h->err_dev, st);
-  if (ad) k_lora_down(B16(h, Lb.x2), H, M, H, Lg, F(h, Lb.u_f32[2]), B16(h, Lb.u_b[2]), true, true, part, h->err_dev, st);
+  if (rel) SOUP_TRY(release_chunk(h, slot, SOUP_G_O));
+  SOUP_TRY(use_chunk(h, slot, SOUP_G_GU));  // ln2 travels with the gate|up chunk
+  SOUP_TRY(prof(h, FAM_RMSNORM_FWD, 0, 6.0 * dM * dH + 2.0 * dH,
+                [&] { k_rmsnorm_fwd(F(h, Lb.hm), ln2, c.rms_eps, M, H, B16(h, Lb.x2), true, h->err_dev, st); }));
+  if (ad)
+    SOUP_TRY(prof(h, FAM_LORA_DOWN, lora_down_flops(Lg, M, H), lora_down_bytes(Lg, M, H), [&] {
+      k_lora_down(B16(h, Lb.x2), H, M, H, Lg, F(h, Lb.u_f32[2]), B16(h, Lb.u_b[2]), true, true, part, h->err_dev, st);
+    }));
   {
     GemmArgs g = weight_args(h, shard, SOUP_G_GU, GEMM_FWD);
     g.op_f16 = 1; g.M = M; g.a = B16(h, Lb.x2); g.lda = H;
@@ -418,11 +543,17 @@ int layer_forward(soup_stream *h, int li, const uint8_t *shard, bool recompute) 
       g.lora_u = F(h, Lb.u_f32[2]); g.lseg = Lg; g.after_lora = 1;
     }
     g.epi = EPI_16; g.out = B16(h, Lb.gu); g.ldo = 2 * I;
-    SOUP_TRY(timed_gemm(h, g));
+    SOUP_TRY(timed_gemm(h, g, SOUP_G_GU));
   }
-  k_swiglu_fwd(B16(h, Lb.gu), M, I, B16(h, Lb.act), true, h->err_dev, st);
-  if (ad) k_lora_down(B16(h, Lb.act), I, M, I, Ld, F(h, Lb.u_f32[3]), B16(h, Lb.u_b[3]), true, true, part, h->err_dev, st);
+  if (rel) SOUP_TRY(release_chunk(h, slot, SOUP_G_GU));
+  SOUP_TRY(prof(h, FAM_SWIGLU_FWD, 0, 6.0 * dM * dI,
+                [&] { k_swiglu_fwd(B16(h, Lb.gu), M, I, B16(h, Lb.act), true, h->err_dev, st); }));
+  if (ad)
+    SOUP_TRY(prof(h, FAM_LORA_DOWN, lora_down_flops(Ld, M, I), lora_down_bytes(Ld, M, I), [&] {
+      k_lora_down(B16(h, Lb.act), I, M, I, Ld, F(h, Lb.u_f32[3]), B16(h, Lb.u_b[3]), true, true, part, h->err_dev, st);
+    }));
   if (!recompute) {
+    SOUP_TRY(use_chunk(h, slot, SOUP_G_DOWN));
     GemmArgs g = weight_args(h, shard, SOUP_G_DOWN, GEMM_FWD);
     g.op_f16 = 1; g.M = M; g.a = B16(h, Lb.act); g.lda = I;
     if (ad) {
@@ -431,7 +562,8 @@ int layer_forward(soup_stream *h, int li, const uint8_t *shard, bool recompute) 
     }
     g.epi = EPI_F32_ADD; g.add_src = F(h, Lb.hm); g.ld_add = H;
     g.out = F(h, P.h_all) + (size_t)(li + 1) * M * H; g.ldo = H;
-    SOUP_TRY(timed_gemm(h, g));
+    SOUP_TRY(timed_gemm(h, g, SOUP_G_DOWN));
+    SOUP_TRY(release_chunk(h, slot, SOUP_G_DOWN));
   }
   return check_cuda("layer forward");
 }
@@ -446,19 +578,28 @@ int group_backward(soup_stream *h, int li, const uint8_t *shard, int grp, const 
   LoraSeg L = make_seg(h, li, grp, true);
   const int K = h->lay.n_in[grp];
   // gradients travel in bf16; the layer inputs x are the forward's half tensors
-  k_lora_du(dy, ldy, M, L, F(h, P.du_f32), B16(h, P.du_b), false, false, F(h, P.lora_part), st);
+  const int Ng = h->lay.n_out[grp];
+  const double nr = (double)L.nseg * L.r, dM = M;
+  SOUP_TRY(prof(h, FAM_LORA_DU, 2.0 * dM * Ng * L.r,
+                2.0 * dM * Ng + 4.0 * Ng * L.r + 4.0 * dM * nr + 2.0 * dM * L.Rpad(), [&] {
+                  k_lora_du(dy, ldy, M, L, F(h, P.du_f32), B16(h, P.du_b), false, false, F(h, P.lora_part), st);
+                }));
   GemmArgs g = weight_args(h, shard, grp, GEMM_DX);
   g.M = M; g.a = dy; g.lda = ldy;
   g.ul = B16(h, P.du_b); g.vl = B16(h, P.ac[(size_t)li * 4 + grp]); g.R = L.Rpad();
   g.lora_u = F(h, P.du_f32); g.lseg = L; g.after_lora = 1;
   g.epi = EPI_F32; g.out = dx_out; g.ldo = K;
-  SOUP_TRY(timed_gemm(h, g));
-  k_lora_dB(dy, ldy, M, F(h, Lb.u_f32[grp]), L, false, F(h, P.lora_part), st);
-  k_lora_dA(F(h, P.du_f32), x, ldx, M, K, L, true, F(h, P.lora_part), st);
+  SOUP_TRY(timed_gemm(h, g, grp));
+  SOUP_TRY(prof(h, FAM_LORA_DB, 2.0 * dM * Ng * L.r, 2.0 * dM * Ng + 4.0 * dM * nr + 4.0 * Ng * L.r,
+                [&] { k_lora_dB(dy, ldy, M, F(h, Lb.u_f32[grp]), L, false, F(h, P.lora_part), st); }));
+  SOUP_TRY(prof(h, FAM_LORA_DA, 2.0 * dM * K * nr, 4.0 * dM * nr + 2.0 * dM * K + 4.0 * nr * K,
+                [&] { k_lora_dA(F(h, P.du_f32), x, ldx, M, K, L, true, F(h, P.lora_part), st); }));
   return 0;
 }
 
-int layer_backward(soup_stream *h, int li, const uint8_t *shard) {
+// Backward of layer li; releases each chunk after its last reader (the dX GEMM of its group,
+// and for q|k|v and gate|up the RMSNorm backward that reads the chunk's norm vector).
+int layer_backward(soup_stream *h, int li, const uint8_t *shard, int slot) {
   const soup_cfg &c = h->cfg;
   const Plan &P = h->plan;
   const LayerBufs Lb = bufs_of(h, li);
@@ -471,18 +612,40 @@ int layer_backward(soup_stream *h, int li, const uint8_t *shard) {
   const uint16_t *ln2 = reinterpret_cast<const uint16_t *>(shard + SL.ln2_off);
 
   // dh / dh_b hold dL/dh_{li+1}
+  SOUP_TRY(use_chunk(h, slot, SOUP_G_DOWN));
   SOUP_TRY(group_backward(h, li, shard, SOUP_G_DOWN, B16(h, P.dh_b), H, B16(h, Lb.act), I, F(h, P.dact)));
-  k_swiglu_bwd(F(h, P.dact), B16(h, Lb.gu), M, I, B16(h, P.dgu), true, st);
+  SOUP_TRY(release_chunk(h, slot, SOUP_G_DOWN));
+  const double dM = M, dH = H, dI = I;
+  SOUP_TRY(prof(h, FAM_SWIGLU_BWD, 0, 12.0 * dM * dI,
+                [&] { k_swiglu_bwd(F(h, P.dact), B16(h, Lb.gu), M, I, B16(h, P.dgu), true, st); }));
+  SOUP_TRY(use_chunk(h, slot, SOUP_G_GU));
   SOUP_TRY(group_backward(h, li, shard, SOUP_G_GU, B16(h, P.dgu), 2 * I, B16(h, Lb.x2), H, F(h, P.dx)));
-  k_rmsnorm_bwd(F(h, P.dx), F(h, Lb.hm), ln2, c.rms_eps, M, H, F(h, P.dh), F(h, P.dhm), B16(h, P.dhm_b), st);
+  SOUP_TRY(prof(h, FAM_RMSNORM_BWD, 0, 18.0 * dM * dH + 2.0 * dH, [&] {
+    k_rmsnorm_bwd(F(h, P.dx), F(h, Lb.hm), ln2, c.rms_eps, M, H, F(h, P.dh), F(h, P.dhm), B16(h, P.dhm_b), st);
+  }));
+  SOUP_TRY(release_chunk(h, slot, SOUP_G_GU));
+  SOUP_TRY(use_chunk(h, slot, SOUP_G_O));
   SOUP_TRY(group_backward(h, li, shard, SOUP_G_O, B16(h, P.dhm_b), H, B16(h, Lb.att), qd, F(h, P.datt)));
-  k_cast_bf16(F(h, P.datt), B16(h, P.datt_b), (int64_t)M * qd, st);
-  SOUP_TRY(k_attn_bwd(B16(h, Lb.qkv), nqkv, B16(h, Lb.att), B16(h, P.datt_b), F(h, Lb.lse), B, S,
-                      c.n_heads, c.n_kv_heads, c.head_dim, F(h, P.attn_scratch), F(h, P.dqkv), st));
-  k_rope_bwd(F(h, P.dqkv), B16(h, P.dqkv_b), nqkv, F(h, P.rope_cos), F(h, P.rope_sin), M, S,
-             c.n_heads, c.n_kv_heads, c.head_dim, st);
+  SOUP_TRY(release_chunk(h, slot, SOUP_G_O));
+  SOUP_TRY(prof(h, FAM_CAST, 0, 6.0 * dM * qd,
+                [&] { k_cast_bf16(F(h, P.datt), B16(h, P.datt_b), (int64_t)M * qd, st); }));
+  int arc = 0;
+  SOUP_TRY(prof(h, FAM_ATTN_BWD, attn_flops(c, B, S, 5),
+                2.0 * dM * nqkv + 4.0 * dM * qd + 4.0 * dM * c.n_heads + 4.0 * dM * nqkv, [&] {
+                  arc = k_attn_bwd(B16(h, Lb.qkv), nqkv, B16(h, Lb.att), B16(h, P.datt_b), F(h, Lb.lse), B, S,
+                                   c.n_heads, c.n_kv_heads, c.head_dim, F(h, P.attn_scratch), F(h, P.dqkv), st);
+                }));
+  SOUP_TRY(arc);
+  SOUP_TRY(prof(h, FAM_ROPE_BWD, 0, 6.0 * dM * nqkv, [&] {
+    k_rope_bwd(F(h, P.dqkv), B16(h, P.dqkv_b), nqkv, F(h, P.rope_cos), F(h, P.rope_sin), M, S,
+               c.n_heads, c.n_kv_heads, c.head_dim, st);
+  }));
+  SOUP_TRY(use_chunk(h, slot, SOUP_G_QKV));
   SOUP_TRY(group_backward(h, li, shard, SOUP_G_QKV, B16(h, P.dqkv_b), nqkv, B16(h, Lb.x1), H, F(h, P.dx)));
-  k_rmsnorm_bwd(F(h, P.dx), hin, ln1, c.rms_eps, M, H, F(h, P.dhm), F(h, P.dh), B16(h, P.dh_b), st);
+  SOUP_TRY(prof(h, FAM_RMSNORM_BWD, 0, 18.0 * dM * dH + 2.0 * dH, [&] {
+    k_rmsnorm_bwd(F(h, P.dx), hin, ln1, c.rms_eps, M, H, F(h, P.dhm), F(h, P.dh), B16(h, P.dh_b), st);
+  }));
+  SOUP_TRY(release_chunk(h, slot, SOUP_G_QKV));
   return check_cuda("layer backward");
 }
 
@@ -496,9 +659,12 @@ int stream_init(soup_store *st, const soup_cfg *c, int maxB, int maxS, void *ws,
                 uintptr_t xs, int n_slots, int mode, soup_stream **out) {
   if (!out) return set_error(SOUP_EINVAL, "out is NULL");
   *out = nullptr;
-  if (!st || !c || !ws || !embed || !final_norm)
+  const bool stream_head = (mode & SOUP_MODE_STREAM_HEAD) != 0;
+  if (!st || !c || !ws || (!embed && !stream_head) || !final_norm)
     return set_error(SOUP_EINVAL, "stream_init: NULL argument");
-  if (!c->tied && !lm_head) return set_error(SOUP_EINVAL, "untied config needs lm_head");
+  if (!c->tied && !lm_head && !stream_head) return set_error(SOUP_EINVAL, "untied config needs lm_head");
+  if (stream_head && !st->head)
+    return set_error(SOUP_ESTATE, "stream_init: SOUP_MODE_STREAM_HEAD needs soup_store_put_head first");
   if (std::memcmp(&st->cfg, c, sizeof(soup_cfg)) != 0)
     return set_error(SOUP_EINVAL, "stream_init: cfg differs from the store's");
   for (int l = 0; l < c->n_layers; ++l)
@@ -524,15 +690,24 @@ int stream_init(soup_store *st, const soup_cfg *c, int maxB, int maxS, void *ws,
   h->cs = reinterpret_cast<cudaStream_t>(cs);
   h->xs = reinterpret_cast<cudaStream_t>(xs);
   h->ws = static_cast<uint8_t *>(ws);
-  h->embed = static_cast<const uint16_t *>(embed);
-  h->lm_head = c->tied ? nullptr : static_cast<const uint16_t *>(lm_head);
+  h->stream_head = stream_head ? 1 : 0;
+  if (stream_head) {
+    // the gather reads the embedding rows from the mapped page-locked store; the head table
+    // (the embedding itself when tied) occupies the workspace's vocabulary buffer
+    h->embed = reinterpret_cast<const uint16_t *>(st->head_dev);
+    h->lm_head = reinterpret_cast<const uint16_t *>(h->ws + P.vocab_buf);
+  } else {
+    h->embed = static_cast<const uint16_t *>(embed);
+    h->lm_head = c->tied ? nullptr : static_cast<const uint16_t *>(lm_head);
+  }
   h->final_norm = static_cast<const uint16_t *>(final_norm);
   h->err_dev = reinterpret_cast<int *>(h->ws + P.err);
   auto fail = [&](int rc) {
     soup_stream_free_impl(h);
     return rc;
   };
-  if (cudaMemsetAsync(h->err_dev, 0, 64, h->cs) != cudaSuccess)
+  if (cudaMemsetAsync(h->err_dev, 0, 64, h->cs) != cudaSuccess ||
+      cudaMemsetAsync(h->ws + P.gemm_cnt, 0, 4 * P.gemm_cnt_ints, h->cs) != cudaSuccess)
     return fail(set_error(SOUP_ECUDA, "workspace memset failed"));
   // RoPE tables: angle pos * theta^(-2i/d) formed in double, cos/sin rounded to float.
   {
@@ -549,6 +724,12 @@ int stream_init(soup_store *st, const soup_cfg *c, int maxB, int maxS, void *ws,
         cudaMemcpy(h->ws + P.rope_sin, sn_h.data(), sn_h.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess)
       return fail(set_error(SOUP_ECUDA, "rope table upload failed"));
   }
+  if (stream_head) {
+    const uint64_t table = 2ull * c->vocab * c->hidden;
+    if (cudaMemcpy(h->ws + P.vocab_buf, st->head + (c->tied ? 0 : table), table, cudaMemcpyHostToDevice) !=
+        cudaSuccess)
+      return fail(set_error(SOUP_ECUDA, "head table upload failed"));
+  }
   if (h->resident) {
     for (int l = 0; l < c->n_layers; ++l) {
       if (cudaMemcpy(h->ws + P.slots + (uint64_t)l * h->lay.stride, st->base + (uint64_t)l * h->lay.stride,
@@ -560,10 +741,11 @@ int stream_init(soup_store *st, const soup_cfg *c, int maxB, int maxS, void *ws,
     for (int k = 0; k < n_slots; ++k) {
       Slot &s = h->slot[k];
       s.dev = h->ws + P.slots + (uint64_t)k * h->lay.stride;
-      if (cudaEventCreateWithFlags(&s.ready, cudaEventDisableTiming) != cudaSuccess ||
-          cudaEventCreateWithFlags(&s.freed, cudaEventDisableTiming) != cudaSuccess)
-        return fail(set_error(SOUP_ECUDA, "event creation failed"));
       s.has_events = 1;
+      for (int g = 0; g < NCHUNK; ++g)
+        if (cudaEventCreateWithFlags(&s.ready[g], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&s.freed[g], cudaEventDisableTiming) != cudaSuccess)
+          return fail(set_error(SOUP_ECUDA, "event creation failed"));
       // an unrecorded event counts as complete for cudaStreamWaitEvent
     }
   }
@@ -602,7 +784,7 @@ int step_fwd(soup_stream *h, const int32_t *tokens, int B, int S, const float *c
   const Plan &P = h->plan;
   cudaStream_t st = h->cs;
   const int M = B * S, H = c.hidden;
-  k_embed(tokens, h->embed, c.vocab, H, M, F(h, P.h_all), st);
+  SOUP_TRY(prof(h, FAM_EMBED, 0, 6.0 * M * H, [&] { k_embed(tokens, h->embed, c.vocab, H, M, F(h, P.h_all), st); }));
   std::vector<int> seq(L);
   for (int i = 0; i < L; ++i) seq[i] = i;
   const int look = std::max(0, (int)h->slot.size() - 1);
@@ -612,15 +794,23 @@ int step_fwd(soup_stream *h, const int32_t *tokens, int B, int S, const float *c
     // 16-bit LoRA operands of this layer's tensor-core GEMMs (forward: half B rows; dX:
     // bf16 A rows), packed just before first use so that the first layer's kernels, and so
     // the first slot release, are not queued behind every layer's packing
-    for (int g = 0; g < 4 && !adapters_off; ++g) {
-      LoraSeg Lg = make_seg(h, i, g, false);
-      k_pack_fwd(Lg, h->lay.n_out[g], B16(h, P.vl[(size_t)i * 4 + g]), true, st);
-      k_pack_bwd(Lg, h->lay.n_in[g], B16(h, P.ac[(size_t)i * 4 + g]), false, st);
+    if (!adapters_off) {  // one launch packs the layer's four groups, both directions
+      LoraSeg Ls[4];
+      uint16_t *vl[4], *ac[4];
+      for (int g = 0; g < 4; ++g) {
+        Ls[g] = make_seg(h, i, g, false);
+        vl[g] = B16(h, P.vl[(size_t)i * 4 + g]);
+        ac[g] = B16(h, P.ac[(size_t)i * 4 + g]);
+      }
+      double pb = 0;
+      for (int g = 0; g < 4; ++g)
+        pb += 4.0 * Ls[g].r * (h->lay.n_out[g] + (double)Ls[g].nseg * h->lay.n_in[g]) +
+              2.0 * Ls[g].Rpad() * ((double)h->lay.n_out[g] + h->lay.n_in[g]);
+      SOUP_TRY(prof(h, FAM_LORA_PACK, 0, pb, [&] { k_pack_layer(Ls, h->lay.n_out, h->lay.n_in, vl, ac, st); }));
     }
     TraceRange tr("fwd layer", i);
     SOUP_TRY(acquire(h, seq, (size_t)i, &shard, &s));
-    SOUP_TRY(layer_forward(h, i, shard, false));
-    SOUP_TRY(release(h, s));
+    SOUP_TRY(layer_forward(h, i, shard, s, false));
     if (!h->resident) SOUP_TRY(prefetch(h, seq, (size_t)i + 1, look - 1));
   }
   // final norm + vocabulary-chunked loss
@@ -634,9 +824,14 @@ int step_fwd(soup_stream *h, const int32_t *tokens, int B, int S, const float *c
     g.M = M; g.a = B16(h, P.hn); g.lda = H; g.epi = EPI_F32;
     float *z = logits ? logits + v0 : F(h, P.z);
     const int ldz = logits ? c.vocab : vc;
-    g.out = z; g.ldo = ldz; g.err = h->err_dev;
-    SOUP_TRY(gemm_launch(g, st));
-    k_ce_chunk_fwd(z, ldz, v0, n, tokens, M, S, ci == 0, F(h, P.ce_max), F(h, P.ce_sum), F(h, P.ce_lab), st);
+    g.out = z; g.ldo = ldz;
+    gemm_scratch(h, g);
+    int grc = 0;
+    SOUP_TRY(prof(h, FAM_HEAD_GEMM, gemm_flops(g), gemm_bytes(g), [&] { grc = gemm_launch(g, st); }));
+    SOUP_TRY(grc);
+    SOUP_TRY(prof(h, FAM_CE_FWD, 0, 4.0 * M * n, [&] {
+      k_ce_chunk_fwd(z, ldz, v0, n, tokens, M, S, ci == 0, F(h, P.ce_max), F(h, P.ce_sum), F(h, P.ce_lab), st);
+    }));
   }
   k_ce_finalize(F(h, P.ce_max), F(h, P.ce_sum), F(h, P.ce_lab), M, S, F(h, P.ce_lse), loss, st);
   if (layer_out)
@@ -679,14 +874,20 @@ int step_bwd(soup_stream *h, float *const *dA, float *const *dB, float *dh_out, 
       GemmArgs g;
       g.mode = GEMM_FWD; g.wfmt = W_BF16; g.w = w; g.Nw = n; g.Kw = H;
       g.M = M; g.a = B16(h, P.hn); g.lda = H; g.epi = EPI_F32; g.out = F(h, P.z); g.ldo = vc;
-      g.err = h->err_dev;
-      SOUP_TRY(gemm_launch(g, st));
-      k_ce_chunk_bwd(F(h, P.z), vc, v0, n, F(h, P.ce_lse), h->tokens, M, S, inv_n, B16(h, P.dz), st);
+      gemm_scratch(h, g);
+      int grc = 0;
+      SOUP_TRY(prof(h, FAM_HEAD_GEMM, gemm_flops(g), gemm_bytes(g), [&] { grc = gemm_launch(g, st); }));
+      SOUP_TRY(grc);
+      SOUP_TRY(prof(h, FAM_CE_BWD, 0, 6.0 * M * n, [&] {
+        k_ce_chunk_bwd(F(h, P.z), vc, v0, n, F(h, P.ce_lse), h->tokens, M, S, inv_n, B16(h, P.dz), st);
+      }));
       GemmArgs d;
       d.mode = GEMM_DX; d.wfmt = W_BF16; d.w = w; d.Nw = n; d.Kw = H;
       d.M = M; d.a = B16(h, P.dz); d.lda = vc; d.epi = ci == 0 ? EPI_F32 : EPI_F32_ACC;
-      d.out = F(h, P.dhn); d.ldo = H; d.err = h->err_dev;
-      SOUP_TRY(gemm_launch(d, st));
+      d.out = F(h, P.dhn); d.ldo = H;
+      gemm_scratch(h, d);
+      SOUP_TRY(prof(h, FAM_HEAD_DX, gemm_flops(d), gemm_bytes(d), [&] { grc = gemm_launch(d, st); }));
+      SOUP_TRY(grc);
     }
     k_rmsnorm_bwd(F(h, P.dhn), F(h, P.h_all) + (size_t)L * M * H, h->final_norm, c.rms_eps, M, H,
                   nullptr, F(h, P.dh), B16(h, P.dh_b), st);
@@ -707,10 +908,9 @@ int step_bwd(soup_stream *h, float *const *dA, float *const *dB, float *dh_out, 
     // between uses separate ones): its backward reuses them instead of recomputing them, which
     // would reproduce the same values with the same kernels.  With kept activations every
     // layer's are still there ("stream_recompute: off"); only the weights are read again.
-    if (!h->keep_act && !(j == 0 && h->last_layer_fresh)) SOUP_TRY(layer_forward(h, li, shard, true));
+    if (!h->keep_act && !(j == 0 && h->last_layer_fresh)) SOUP_TRY(layer_forward(h, li, shard, s, true));
     h->last_layer_fresh = 0;
-    SOUP_TRY(layer_backward(h, li, shard));
-    SOUP_TRY(release(h, s));
+    SOUP_TRY(layer_backward(h, li, shard, s));
     if (!h->resident) SOUP_TRY(prefetch(h, seq, (size_t)j + 1, look - 1));
     if (dh_out)
       SOUP_CUDA_TRY(cudaMemcpyAsync(dh_out + (size_t)li * M * H, F(h, P.dh), 4ull * M * H,
@@ -739,8 +939,34 @@ int stream_sync(soup_stream *h, int timeout_ms) {
   harvest(h, false);
   if (err) {  // reported once: the next step starts with a clear flag
     SOUP_CUDA_TRY(cudaMemset(h->err_dev, 0, sizeof(int)));
+    // a kernel that gave up may have left tile counters counted in: start them afresh
+    SOUP_CUDA_TRY(cudaMemset(h->ws + h->plan.gemm_cnt, 0, 4 * h->plan.gemm_cnt_ints));
     return kernel_flags_status(err, "soup_sync");
   }
+  return 0;
+}
+
+int stream_kernel_stats(soup_stream *h, soup_kernel_stat *out, int max, int *n, int reset) {
+  if (!h || !n || (max > 0 && !out)) return set_error(SOUP_EINVAL, "NULL argument");
+  harvest(h, true);
+  int k = 0;
+  for (int f = 0; f < FAM_COUNT; ++f) {
+    if (!h->fam[f].launches) continue;
+    if (k < max) {
+      soup_kernel_stat &o = out[k];
+      std::memset(&o, 0, sizeof(o));
+      std::snprintf(o.name, sizeof(o.name), "%s", kFamName[f]);
+      o.tensor_bound = kFamTensor[f];
+      o.launches = h->fam[f].launches;
+      o.ms = h->fam[f].ms;
+      o.flops = h->fam[f].flops;
+      o.bytes = h->fam[f].bytes;
+    }
+    ++k;
+  }
+  *n = k;
+  if (reset)
+    for (auto &f : h->fam) f = FamStat();
   return 0;
 }
 
@@ -758,10 +984,11 @@ void soup_stream_free_impl(soup_stream *h) {
   if (h->xs) cudaStreamSynchronize(h->xs);
   harvest(h, true);
   for (auto &s : h->slot)
-    if (s.has_events) {
-      cudaEventDestroy(s.ready);
-      cudaEventDestroy(s.freed);
-    }
+    if (s.has_events)
+      for (int g = 0; g < NCHUNK; ++g) {
+        if (s.ready[g]) cudaEventDestroy(s.ready[g]);
+        if (s.freed[g]) cudaEventDestroy(s.freed[g]);
+      }
   for (cudaEvent_t e : h->ev_pool) cudaEventDestroy(e);
   if (h->done) cudaEventDestroy(h->done);
   delete h;

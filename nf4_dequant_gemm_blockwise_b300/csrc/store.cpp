@@ -274,8 +274,43 @@ int store_put_layer(soup_store *st, int layer, const uint16_t *const *src, int n
   return 0;
 }
 
+// The head tables go into one mapped page-locked allocation: the embedding gather reads its
+// rows straight from it, and the output head is copied from it into the device buffer.
+int store_put_head(soup_store *st, const uint16_t *embed, const uint16_t *lm_head) {
+  if (!st || !embed) return set_error(SOUP_EINVAL, "store_put_head: NULL argument");
+  const soup_cfg &c = st->cfg;
+  if (c.tied && lm_head) return set_error(SOUP_EINVAL, "store_put_head: a tied stack has no separate head");
+  if (!c.tied && !lm_head) return set_error(SOUP_EINVAL, "store_put_head: an untied stack needs lm_head");
+  const uint64_t table = 2ull * c.vocab * c.hidden;
+  const uint64_t bytes = c.tied ? table : 2 * table;
+  if (!st->head) {
+    void *p = nullptr;
+    cudaError_t e = cudaHostAlloc(&p, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();
+      return set_error(SOUP_ENOMEM, "store_put_head: page-locking %llu bytes failed (%s); the streamed "
+                       "head needs page-locked memory", (unsigned long long)bytes, cudaGetErrorString(e));
+    }
+    void *d = nullptr;
+    e = cudaHostGetDevicePointer(&d, p, 0);
+    if (e != cudaSuccess || !d) {
+      (void)cudaGetLastError();
+      cudaFreeHost(p);
+      return set_error(SOUP_ECUDA, "store_put_head: no device address for the head tables (%s)",
+                       cudaGetErrorString(e));
+    }
+    st->head = static_cast<uint8_t *>(p);
+    st->head_dev = static_cast<uint8_t *>(d);
+    st->head_bytes = bytes;
+  }
+  std::memcpy(st->head, embed, table);
+  if (!c.tied) std::memcpy(st->head + table, lm_head, table);
+  return 0;
+}
+
 void store_free(soup_store *st) {
   if (!st) return;
+  if (st->head) cudaFreeHost(st->head);
   if (st->base) {
     if (st->pinned) cudaFreeHost(st->base);
     else std::free(st->base);

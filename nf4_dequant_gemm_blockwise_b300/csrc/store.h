@@ -13,6 +13,11 @@ struct soup_store {
   uint64_t bytes = 0;
   int pinned = 0;
   std::vector<char> filled;
+  // the embedding and (untied) output head, bf16 [vocab, hidden] each, in their own
+  // page-locked allocation (soup_store_put_head); head_dev is its device-side address
+  uint8_t *head = nullptr;
+  uint8_t *head_dev = nullptr;
+  uint64_t head_bytes = 0;
 };
 
 namespace soup {
@@ -22,6 +27,7 @@ int shard_layout(const soup_cfg *c, soup_shard_layout *L);
 int store_create(const soup_cfg *c, int allow_pageable, soup_store **out);
 int store_put_layer(soup_store *st, int layer, const uint16_t *const *src, int n_threads);
 int store_put_shard(soup_store *st, int layer, const void *shard, uint64_t bytes);
+int store_put_head(soup_store *st, const uint16_t *embed, const uint16_t *lm_head);
 void store_free(soup_store *st);
 void nf4_quantize_host(const uint16_t *src, int64_t n, uint8_t *codes, float *absmax, int n_threads);
 const float *nf4_midpoints();

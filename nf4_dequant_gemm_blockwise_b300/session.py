@@ -25,10 +25,14 @@ class StreamedLoRA:
     layer_source(i) -> dict of the nine bf16-bit host arrays of layer i.
     lora: list over layers of 7 (A [r, in], B [out, r]) float32 host arrays.
     keep_activations: keep every layer's activations for the backward instead of re-running
-    each layer's forward ("How it works": stream_recompute: off); weights are still re-read."""
+    each layer's forward ("How it works": stream_recompute: off); weights are still re-read.
+    stream_head: the embedding and the untied head go into the store instead of device memory
+    ("Measured numbers": they move into the store and reuse one device buffer); the embedding
+    rows are gathered straight from the page-locked store."""
 
     def __init__(self, cfg, layer_source, embed_bits, lm_head_bits, final_bits, lora, max_batch,
-                 max_seq, n_slots=2, resident=False, store=None, threads=0, keep_activations=False):
+                 max_seq, n_slots=2, resident=False, store=None, threads=0, keep_activations=False,
+                 stream_head=False):
         self.cfg = cfg
         self.own_store = store is None
         if store is None:
@@ -37,8 +41,12 @@ class StreamedLoRA:
                 src = layer_source(i)
                 store.put_layer(i, [src[t] for t in LAYER_TENSORS], n_threads=threads)
         self.store = store
-        self.embed = _bits_to_dev(embed_bits)
-        self.lm_head = None if cfg.tied else _bits_to_dev(lm_head_bits)
+        if stream_head:
+            store.put_head(embed_bits, None if cfg.tied else lm_head_bits)
+            self.embed = self.lm_head = None
+        else:
+            self.embed = _bits_to_dev(embed_bits)
+            self.lm_head = None if cfg.tied else _bits_to_dev(lm_head_bits)
         self.final = _bits_to_dev(final_bits)
         # adapters, gradients and AdamW moments each live in one flat float buffer (tensors
         # at 256-byte aligned offsets), so the optimizer is a single launch over all of them
@@ -63,14 +71,16 @@ class StreamedLoRA:
         pv, gv = views(self.params), views(self.grad_flat)
         self.lora_A, self.lora_B = pv[0::2], pv[1::2]
         self.dA, self.dB = gv[0::2], gv[1::2]
-        nbytes = api.workspace_bytes(cfg, max_batch, max_seq, n_slots, resident, keep_activations)
+        nbytes = api.workspace_bytes(cfg, max_batch, max_seq, n_slots, resident, keep_activations,
+                                     stream_head)
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
         self.compute = torch.cuda.Stream()
         self.copy = torch.cuda.Stream()
         self.loss = torch.zeros(1, dtype=torch.float32, device="cuda")
         self.stream = api.Stream(store, max_batch, max_seq, self.workspace, self.embed, self.lm_head,
                                  self.final, self.compute, self.copy, n_slots=n_slots,
-                                 resident=resident, keep_activations=keep_activations)
+                                 resident=resident, keep_activations=keep_activations,
+                                 stream_head=stream_head)
         torch.cuda.synchronize()
 
     def fwd(self, tokens: torch.Tensor, logits=None, layer_out=None):

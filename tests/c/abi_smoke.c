@@ -54,7 +54,7 @@ int main(void) {
   if (soup_workspace_bytes(&cfg, 1, 64, 2, 0, &ws0) != SOUP_OK) return 4;
   if (soup_workspace_bytes(&cfg, 1, 64, 2, SOUP_MODE_KEEP_ACTIVATIONS, &ws2) != SOUP_OK) return 5;
   printf("workspace %llu %llu\n", (unsigned long long)ws0, (unsigned long long)ws2);
-  printf("bad_mode %d\n", soup_workspace_bytes(&cfg, 1, 64, 2, 4, &ws_bad));
+  printf("bad_mode %d\n", soup_workspace_bytes(&cfg, 1, 64, 2, 8, &ws_bad));
   uint64_t ws_part = 0;
   printf("peak %llu\n", (unsigned long long)soup_peak_bytes(&cfg, 1, 64, 2, 0, &ws_part));
 

@@ -38,13 +38,14 @@ def cosine(a, b):
     return float(a @ b / max(np.linalg.norm(a) * np.linalg.norm(b), 1e-300))
 
 
-def _session(cfg, resident, store=None, n_slots=2, lora=None, keep_activations=False):
+def _session(cfg, resident, store=None, n_slots=2, lora=None, keep_activations=False,
+             stream_head=False):
     from nf4_dequant_gemm_blockwise_b300.session import StreamedLoRA
     return StreamedLoRA(cfg, lambda i: synth.layer_source(cfg, i), synth.embedding(cfg),
                         synth.lm_head(cfg), synth.final_norm(cfg),
                         lora if lora is not None else synth.lora_params(cfg),
                         cfg.batch, cfg.seq, n_slots=n_slots, resident=resident, store=store,
-                        keep_activations=keep_activations)
+                        keep_activations=keep_activations, stream_head=stream_head)
 
 
 def _run(sess, cfg, want_logits=True):
@@ -333,11 +334,11 @@ def _build_store(cfg):
     return store
 
 
-def _full_run(cfg, store, lora, resident=False, n_slots=2, keep_activations=False):
+def _full_run(cfg, store, lora, resident=False, n_slots=2, keep_activations=False, stream_head=False):
     from nf4_dequant_gemm_blockwise_b300.session import StreamedLoRA
     s = StreamedLoRA(cfg, None, synth.embedding(cfg), synth.lm_head(cfg), synth.final_norm(cfg), lora,
                      cfg.batch, cfg.seq, n_slots=n_slots, resident=resident, store=store,
-                     keep_activations=keep_activations)
+                     keep_activations=keep_activations, stream_head=stream_head)
     try:
         return _run(s, cfg)
     finally:
@@ -374,8 +375,9 @@ def _full_size(cfg):
 
 def test_llama8b_full_size():
     """The 8B-shaped stack at both of its batch sizes (B=1 and B=4, S=512): streamed == resident
-    bit for bit with two slots, with eight slots (B=1) and with kept activations (B=4, the
-    backward re-runs no layer); then every layer of both batch sizes against the oracle."""
+    bit for bit with two slots, with eight slots and with the streamed head (B=1), and with kept
+    activations (B=4, the backward re-runs no layer); then every layer of both batch sizes
+    against the oracle."""
     cfg1 = synth.LLAMA8B
     cfg4 = synth.LLAMA8B.with_(batch=4)
     store = _build_store(cfg1)
@@ -384,6 +386,7 @@ def test_llama8b_full_size():
         g1 = _full_run(cfg1, store, lora)
         assert _assert_bit_equal(g1, _full_run(cfg1, store, lora, resident=True)) == 14 * cfg1.n_layers
         _assert_bit_equal(g1, _full_run(cfg1, store, lora, n_slots=8))
+        _assert_bit_equal(g1, _full_run(cfg1, store, lora, stream_head=True))
         _head_checks(cfg1, g1)
         g1.pop("logits")
         g4 = _full_run(cfg4, store, lora)
@@ -417,3 +420,29 @@ def test_tiny_eight_slots_equal_resident_bitwise(tiny, keep):
         s.close()
     _assert_bit_equal(tiny["resident"], a)
     _assert_bit_equal(tiny["resident"], b)
+
+
+@pytest.mark.parametrize("tied", [False, True])
+def test_tiny_stream_head_equals_resident_tables_bitwise(tiny, tied):
+    """"Measured numbers": the embedding and the head move into the store and reuse one device
+    buffer.  The gather reads the rows from the page-locked store and the head GEMMs read the
+    buffer: every output and gradient is bitwise that of resident tables, two steps in a row,
+    untied and tied (the embedding is the head), and the device total drops by the tables."""
+    from nf4_dequant_gemm_blockwise_b300 import api
+    cfg = tiny["cfg"].with_(tied=tied)
+    if tied:
+        ref = _session(cfg, resident=True)
+        want = _run(ref, cfg)
+        store = ref.store
+    else:
+        ref, want, store = None, tiny["resident"], tiny["s"].store
+    s = _session(cfg, resident=False, store=store, stream_head=True)
+    try:
+        a, b = _run(s, cfg), _run(s, cfg)
+    finally:
+        s.close()
+        if ref is not None:
+            ref.close()
+    _assert_bit_equal(want, a)
+    _assert_bit_equal(want, b)
+    assert api.peak_bytes(cfg, cfg.batch, cfg.seq, stream_head=True)[0] < api.peak_bytes(cfg, cfg.batch, cfg.seq)[0]

@@ -154,8 +154,40 @@ def test_keep_activations_plan_adds_one_activation_set_per_layer():
     tot, ws = api.peak_bytes(cfg, B, S, n_slots=2, keep_activations=True)
     assert ws == keep and tot - ws == sizes.resident_bytes(cfg)
     out = api.C.c_uint64()
-    assert api.lib.soup_workspace_bytes(api.C.byref(api.make_cfg(cfg)), B, S, 2, 4,
+    assert api.lib.soup_workspace_bytes(api.C.byref(api.make_cfg(cfg)), B, S, 2, 8,
                                         api.C.byref(out)) == api.EINVAL
+
+
+@pytest.mark.parametrize("cfg", [synth.LLAMA8B, synth.QWEN3B_BF16])
+def test_stream_head_plan_trades_the_tables_for_one_vocabulary_buffer(cfg):
+    # "Measured numbers": the embedding and the untied head move into the store and reuse one
+    # device buffer.  The workspace grows by one [vocab, hidden] bf16 table (1024-byte aligned)
+    # and the resident tables (two untied, one tied) leave the run's device total.
+    B, S = 1, 512
+    table = 2 * cfg.vocab * cfg.hidden
+    base = api.workspace_bytes(cfg, B, S, n_slots=2)
+    sh = api.workspace_bytes(cfg, B, S, n_slots=2, stream_head=True)
+    assert sh - base == -(-table // 1024) * 1024
+    tot, ws = api.peak_bytes(cfg, B, S, n_slots=2, stream_head=True)
+    assert ws == sh
+    assert tot - ws == sizes.resident_bytes(cfg) - table * (1 if cfg.tied else 2)
+    tot0, _ = api.peak_bytes(cfg, B, S, n_slots=2)
+    assert tot0 - tot == table * (1 if cfg.tied else 2) - (-(-table // 1024) * 1024)
+
+
+def test_put_head_checks_its_arguments():
+    cfg = synth.TINY
+    st = api.Store(cfg)
+    e = synth.embedding(cfg)
+    with pytest.raises(api.SoupError) as ex:
+        st.put_head(e, None)                      # untied: the head is required
+    assert ex.value.code == api.EINVAL
+    tied = api.Store(cfg.with_(tied=True))
+    with pytest.raises(api.SoupError) as ex:
+        tied.put_head(e, e)                       # tied: no separate head
+    assert ex.value.code == api.EINVAL
+    st.free()
+    tied.free()
 
 
 def test_forced_pageable_store_and_raw_shard_copy():
