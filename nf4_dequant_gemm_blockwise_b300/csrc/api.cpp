@@ -183,7 +183,7 @@ int soup_stream_kernel_stats(soup_stream *h, soup_kernel_stat *out, int max, int
 // ------------------------------------------------------------------ single projection
 namespace {
 struct ProjScratch {
-  uint64_t u_f32, ul, vl, ac, du_f32, dul, part, gpart, gpart_floats, cnt, cnt_ints, err, total;
+  uint64_t u_f32, ul, vl, ac, du_f32, dul, part, gpart, gpart_floats, err, total;
 };
 ProjScratch proj_plan(int M, int N, int K) {
   ProjScratch s;
@@ -201,23 +201,14 @@ ProjScratch proj_plan(int M, int N, int K) {
   s.dul = take(2ull * M * 64);
   s.part = take(4ull * std::max(lora_scratch_floats(std::max(M, 1), K, 64),
                                  lora_scratch_floats(std::max(M, 1), N, 64)));
-  // partial tiles of the tensor-core path's stream-K schedule, or the small-M path's strips
-  s.gpart_floats = M <= 16 ? std::max(gemv_part_floats(GEMM_FWD), gemv_part_floats(GEMM_DX))
-                           : SK_PART_FLOATS;
+  s.gpart_floats = std::min<uint64_t>(4ull * M * std::max(N, K), 1ull << 26);
+  if (M <= 16)  // the small-M path's per-CTA partial strips
+    s.gpart_floats = std::max<uint64_t>(s.gpart_floats, std::max(gemv_part_floats(GEMM_FWD),
+                                                                 gemv_part_floats(GEMM_DX)));
   s.gpart = take(4 * s.gpart_floats);
-  s.cnt_ints = sk_counter_ints(std::max(M, 1), std::max(N, K));
-  s.cnt = take(4 * s.cnt_ints);
   s.err = take(64);
   s.total = off;
   return s;
-}
-// The stream-K tile counters live in the caller's scratch, whose contents are unknown: they
-// are zeroed on the stream before every call (a few kilobytes).
-int proj_counters(GemmArgs &g, uint8_t *base, const ProjScratch &P, cudaStream_t st) {
-  g.counters = reinterpret_cast<int *>(base + P.cnt);
-  g.counter_ints = P.cnt_ints;
-  SOUP_CUDA_TRY(cudaMemsetAsync(g.counters, 0, 4 * P.cnt_ints, st));
-  return 0;
 }
 int proj_check(int M, int N, int K, const uint8_t *codes, const float *absmax, const uint16_t *w,
                const float *A, const float *B, int r, void *scratch, uint64_t bytes) {
@@ -285,7 +276,6 @@ int soup_proj_fwd(const uint16_t *x, int M, int N, int K, const uint8_t *codes, 
   g.err = reinterpret_cast<int *>(base + P.err);
   g.part = reinterpret_cast<float *>(base + P.gpart);
   g.part_floats = P.gpart_floats;
-  SOUP_TRY(proj_counters(g, base, P, st));
   if (r > 0) {
     k_lora_down(x, K, M, K, L, reinterpret_cast<float *>(base + P.u_f32),
                 reinterpret_cast<uint16_t *>(base + P.ul), f16, f16,
@@ -319,7 +309,6 @@ int soup_proj_dx(const uint16_t *dy, int M, int N, int K, const uint8_t *codes, 
   g.err = reinterpret_cast<int *>(base + P.err);
   g.part = reinterpret_cast<float *>(base + P.gpart);
   g.part_floats = P.gpart_floats;
-  SOUP_TRY(proj_counters(g, base, P, st));
   if (r > 0) {
     k_lora_du(dy, N, M, L, reinterpret_cast<float *>(base + P.du_f32),
               reinterpret_cast<uint16_t *>(base + P.dul), false, false,

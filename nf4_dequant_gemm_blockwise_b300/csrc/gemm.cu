@@ -27,7 +27,6 @@
 
 #include <algorithm>
 #include <cstdio>
-#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -83,11 +82,8 @@ struct TcParams {
   const float *absmax;  // NF4 block scales of W [Nw, Kw]: absmax[row * kblocks + col / 64]
   int kblocks, Nw;
   int M, Ng, n_main, n_ext;
-  int n_mt;       // tiles per column of tiles (m-tiles of MT * 128 rows)
-  int KT;         // units per tile: n_main main k-tiles, then n_ext LoRA extension k-tiles
-  int U;          // units of the whole launch: tiles * KT
-  float *part;    // partial-tile slots (2 per CTA) for tiles cut between CTAs
-  int *counters;  // per (tile, worker warp): contributions counted in; zero between launches
+  int splits, per_split;  // split-K: blockIdx.z takes k-tiles [z * per_split, ...); >1 -> partials
+  float *part;            // split-K partial tiles [splits, M, Ng] (float)
   void *out;
   int ldo;
   const float *add_src;
@@ -136,165 +132,6 @@ SOUP_DEV uint32_t sw128(int r, int c) {
   return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
-// Stream-K schedule: the tiles (MT*128 rows x BN columns, m-tiles varying fastest, so the CTAs
-// that share a weight tile work at the same time) are cut into KT units each (the main k-tiles,
-// then the LoRA extension k-tiles), and CTA c of the C in the grid takes the contiguous units
-// [c U / C, (c + 1) U / C) of the U = tiles * KT.  Every CTA gets the same work to one unit,
-// whatever the tile count.  A tile cut between CTAs is finished by the last of them to arrive:
-// the others leave their float partial tile in a slot and count in on the tile's counter; the
-// last adds the contributions in CTA order (a fixed order, so the result does not depend on
-// which CTA arrives last) and runs the epilogue.  Counters return to zero after each launch.
-SOUP_DEV int sk_first_unit(int c, int U, int C) { return (int)((long long)c * U / C); }
-SOUP_DEV int sk_cta_of(int u, int U, int C) {  // the CTA whose range holds unit u
-  return (int)(((long long)(u + 1) * C + U - 1) / U - 1);
-}
-
-// Epilogue of one output value block held by this worker warp: 32 rows (its TMEM lane
-// quarter) of each m-tile times BN / 4 columns, from the accumulator in TMEM.
-//   store(mt, m, n, r): writes the 32 values r[0..31] of row m, columns n .. n + 31.
-template <int BN, int EPI, bool F16>
-SOUP_DEV void store_out(const TcParams &p, int m, int n, const float (&v)[32]) {
-  if (m >= p.M || n >= p.Ng) return;
-  const bool full_row = (n + 32 <= p.Ng);
-  if (EPI == EPI_16) {
-    uint16_t *o = reinterpret_cast<uint16_t *>(p.out) + (size_t)m * p.ldo + n;
-    if (F16) {  // half outputs: flag values beyond the half range (or NaN)
-      bool bad = false;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) bad |= half_out_of_range(v[j]) && (n + j < p.Ng);
-      flag_range(bad, p.err);
-    }
-    if (full_row) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint4 w;
-        w.x = pack16x2<F16>(v[8 * c + 0], v[8 * c + 1]);
-        w.y = pack16x2<F16>(v[8 * c + 2], v[8 * c + 3]);
-        w.z = pack16x2<F16>(v[8 * c + 4], v[8 * c + 5]);
-        w.w = pack16x2<F16>(v[8 * c + 6], v[8 * c + 7]);
-        *reinterpret_cast<uint4 *>(o + 8 * c) = w;
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (n + j < p.Ng) o[j] = st16<F16>(v[j]);
-    }
-  } else {
-    float *o = reinterpret_cast<float *>(p.out) + (size_t)m * p.ldo + n;
-    const float *src = (EPI == EPI_F32_ADD) ? p.add_src + (size_t)m * p.ld_add + n
-                                            : (EPI == EPI_F32_ACC ? o : nullptr);
-    if (full_row) {
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        float4 w = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-        if (src) {
-          const float4 b = *reinterpret_cast<const float4 *>(src + 4 * c);
-          w.x = b.x + w.x; w.y = b.y + w.y; w.z = b.z + w.z; w.w = b.w + w.w;
-        }
-        *reinterpret_cast<float4 *>(o + 4 * c) = w;
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        if (n + j < p.Ng) {
-          float w = v[j];
-          if (src) w = src[j] + w;
-          o[j] = w;
-        }
-      }
-    }
-  }
-}
-
-// The epilogue of one segment (tile `tile`, this CTA's units of it), run by each worker warp
-// on its own part of the tile: a segment that covers the whole tile is stored directly; a cut
-// tile leaves this warp's part in the CTA's partial slot and counts in on the per-(tile, warp)
-// counter, and the warp that counts in last adds every contribution in CTA order and stores
-// the result.  No barrier spans warps, so a warp that gave up a wait cannot stall the others.
-template <int BN, int EPI, bool F16, int MT>
-__device__ __noinline__ void tile_epilogue(const TcParams &p, uint32_t tmem, int tile, bool whole, int m0, int n0,
-                                           int cta, int ub, int U, int CT) {
-  constexpr int TILE_FLOATS = MT * BM * BN;
-  constexpr int COLS = BN / (WORKERS / 4);  // columns per warp
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int q = warp & 3;
-  auto load = [&](int it, float (&v)[32], int &row, int &col) {
-    const int mt = it / (COLS / 32), cc = it % (COLS / 32);
-    row = mt * BM + q * 32 + lane;           // row inside the tile
-    col = (warp >> 2) * COLS + cc * 32;      // first column inside the tile
-    uint32_t r[32];
-    tc_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + mt * BN + col, r);
-    tc_wait_ld();
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-  };
-  constexpr int ITS = MT * (COLS / 32);
-  if (whole) {
-    for (int it = 0; it < ITS; ++it) {
-      float v[32];
-      int row, col;
-      load(it, v, row, col);
-      store_out<BN, EPI, F16>(p, m0 + row, n0 + col, v);
-    }
-    return;
-  }
-  const int KT = p.KT;
-  const int first_tile = ub / KT;
-  float *mine = p.part + (size_t)(2 * cta + (tile == first_tile ? 0 : 1)) * TILE_FLOATS;
-  for (int it = 0; it < ITS; ++it) {
-    float v[32];
-    int row, col;
-    load(it, v, row, col);
-    float *d = mine + (size_t)row * BN + col;
-#pragma unroll
-    for (int c = 0; c < 8; ++c)
-      *reinterpret_cast<float4 *>(d + 4 * c) = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-  }
-  __threadfence();  // this warp's partial is visible before it counts in
-  __syncwarp();
-  const int c_lo = sk_cta_of(tile * KT, U, CT);
-  const int c_hi = sk_cta_of((tile + 1) * KT - 1, U, CT);
-  int *counter = p.counters + (size_t)tile * WORKERS + warp;
-  int last = 0;
-  if (lane == 0) last = atomicAdd(counter, 1) == c_hi - c_lo;
-  last = __shfl_sync(0xffffffffu, last, 0);
-  if (!last) return;
-  __threadfence();  // the other contributions are read only after their counts were seen
-  for (int it = 0; it < ITS; ++it) {
-    const int mt = it / (COLS / 32), cc = it % (COLS / 32);
-    const int row = mt * BM + q * 32 + lane;
-    const int col = (warp >> 2) * COLS + cc * 32;
-    float acc[32];
-    // eight columns at a time: the own contribution comes from TMEM, the others' from their
-    // slots, added in CTA order
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      for (int j = c_lo; j <= c_hi; ++j) {
-        float w[8];
-        if (j == cta) {
-          uint32_t r[8];
-          tc_ld_32x32b_x8(tmem + ((uint32_t)(q * 32) << 16) + mt * BN + col + 8 * h, r);
-          tc_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 8; ++e) w[e] = __uint_as_float(r[e]);
-        } else {
-          const int jt = sk_first_unit(j, U, CT) / KT;
-          const float *src = p.part + (size_t)(2 * j + (tile == jt ? 0 : 1)) * TILE_FLOATS +
-                             (size_t)row * BN + col + 8 * h;
-          const float4 w0 = __ldcg(reinterpret_cast<const float4 *>(src));
-          const float4 w1 = __ldcg(reinterpret_cast<const float4 *>(src + 4));
-          w[0] = w0.x; w[1] = w0.y; w[2] = w0.z; w[3] = w0.w;
-          w[4] = w1.x; w[5] = w1.y; w[6] = w1.z; w[7] = w1.w;
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[8 * h + e] = (j == c_lo) ? w[e] : acc[8 * h + e] + w[e];
-      }
-    }
-    store_out<BN, EPI, F16>(p, m0 + row, n0 + col, acc);
-  }
-  if (lane == 0) *counter = 0;  // ready for the next launch
-}
-
 template <int BN, int BMODE, int EPI, bool F16, int MT>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
@@ -314,26 +151,24 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t *lempty = bar + NL;        // MMAs done with the load stage
   uint64_t *bready = bar + 2 * NL;    // B stage written (dequantised / converted)
   uint64_t *bempty = bar + 2 * NL + NB;  // MMAs done with the B stage
-  uint64_t *accf = bar + 2 * NL + 2 * NB;  // a segment's accumulator complete
-  uint64_t *tfree = accf + 1;              // the epilogue has read the accumulator out of TMEM
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tfree + 1);
+  uint64_t *accf = bar + 2 * NL + 2 * NB;  // accumulator complete
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accf + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
+  pdl_trigger();  // a dependent split-K reduction may be scheduled now; it waits for this grid
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int U = p.U, CT = gridDim.x, cta = blockIdx.x;
-  const int ub = sk_first_unit(cta, U, CT), ue = sk_first_unit(cta + 1, U, CT);
-  const int KT = p.KT;
-  // Walks this CTA's segments (one tile each): fn(t, k0, k1, m0, n0) for units [k0, k1) of
-  // tile t, whose output block starts at row m0, column n0.
-  auto for_segments = [&](auto &&fn) {
-    for (int u = ub; u < ue;) {
-      const int t = u / KT, k0 = u % KT;
-      const int k1 = min(KT, k0 + (ue - u));
-      if (!fn(t, k0, k1, (t % p.n_mt) * BM * MT, (t / p.n_mt) * BN)) return;
-      u += k1 - k0;
-    }
-  };
+  // m-tiles vary fastest in the launch order, so the CTAs that share a weight tile run
+  // together and the tile is read from DRAM once (the others hit L2)
+  const int n0 = blockIdx.y * BN;
+  const int m0 = blockIdx.x * BM * MT;
+  // this split's k-tiles, renumbered from 0: main tiles [kb, ke), then the LoRA extension
+  // tiles on the last split only
+  const int z = blockIdx.z;
+  const int kb = z * p.per_split;
+  const int ke = min(p.n_main, kb + p.per_split);
+  const int n_my_main = max(0, ke - kb);
+  const int n_total = n_my_main + (z == p.splits - 1 ? p.n_ext : 0);
 
   auto A_s = [&](int s) { return lring + s * C::LSTAGE; };
   auto R_s = [&](int s) { return lring + s * C::LSTAGE + MT * C::A_BYTES; };
@@ -357,7 +192,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&bempty[s], 1);
     }
     mbar_init(accf, 1);
-    mbar_init(tfree, WORKERS);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -375,187 +209,235 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       tma_prefetch_desc(&map_a);
       tma_prefetch_desc(&map_b0);
-      int kt = 0;  // k-tiles issued by this CTA (ring position)
-      for_segments([&](int t, int k0, int k1, int m0, int n0) {
-        for (int k = k0; k < k1; ++k, ++kt) {
-          const int sl = kt % NL, sb = kt % NB;
-          if (kt >= NL && !mbar_wait(&lempty[sl], ((kt / NL) - 1) & 1, p.err, abort_flag)) return false;
-          const bool b_direct = !C::NF4 || k >= p.n_main;  // B arrives by TMA into the B ring
-          if (b_direct && kt >= NB && !mbar_wait(&bempty[sb], ((kt / NB) - 1) & 1, p.err, abort_flag))
-            return false;
-          if (k < p.n_main) {
-            mbar_arrive_expect_tx(&lfull[sl], C::TX_MAIN);
+      int issued = 0;
+      for (int kt = 0; kt < n_total; ++kt) {
+        const int sl = kt % NL, sb = kt % NB;
+        if (kt >= NL && !mbar_wait(&lempty[sl], ((kt / NL) - 1) & 1, p.err, abort_flag)) break;
+        const bool b_direct = !C::NF4 || kt >= n_my_main;  // B arrives by TMA into the B ring
+        if (b_direct && kt >= NB && !mbar_wait(&bempty[sb], ((kt / NB) - 1) & 1, p.err, abort_flag)) break;
+        if (kt < n_my_main) {
+          const int g = kb + kt;  // global k-tile
+          mbar_arrive_expect_tx(&lfull[sl], C::TX_MAIN);
 #pragma unroll
-            for (int i = 0; i < MT; ++i)
-              tma_load_2d(A_s(sl) + i * C::A_BYTES, &map_a, k * BK, m0 + i * BM, &lfull[sl]);
-            if (BMODE == B_NF4_K) {
-              tma_load_2d(R_s(sl), &map_b0, k * (BK / 2), n0, &lfull[sl]);
-            } else if (BMODE == B_NF4_MN) {
-              tma_load_2d(R_s(sl), &map_b0, n0 / 2, k * BK, &lfull[sl]);
-            } else if (BMODE == B_BF16_K) {
-              tma_load_2d(B_s(sb), &map_b0, k * BK, n0, &lfull[sl]);
-            } else {
-#pragma unroll
-              for (int c = 0; c < BN / 64; ++c)
-                tma_load_2d(B_s(sb) + c * 8192, &map_b0, n0 + 64 * c, k * BK, &lfull[sl]);
-            }
+          for (int i = 0; i < MT; ++i)
+            tma_load_2d(A_s(sl) + i * C::A_BYTES, &map_a, g * BK, m0 + i * BM, &lfull[sl]);
+          if (BMODE == B_NF4_K) {
+            tma_load_2d(R_s(sl), &map_b0, g * (BK / 2), n0, &lfull[sl]);
+          } else if (BMODE == B_NF4_MN) {
+            tma_load_2d(R_s(sl), &map_b0, n0 / 2, g * BK, &lfull[sl]);
+          } else if (BMODE == B_BF16_K) {
+            tma_load_2d(B_s(sb), &map_b0, g * BK, n0, &lfull[sl]);
           } else {
-            const int e = k - p.n_main;
-            mbar_arrive_expect_tx(&lfull[sl], C::TX_EXT);
 #pragma unroll
-            for (int i = 0; i < MT; ++i)
-              tma_load_2d(A_s(sl) + i * C::A_BYTES, &map_ul, e * BK, m0 + i * BM, &lfull[sl]);
-            if (!C::MN) {
-              tma_load_2d(B_s(sb), &map_vl, e * BK, n0, &lfull[sl]);
-            } else {
+            for (int c = 0; c < BN / 64; ++c)
+              tma_load_2d(B_s(sb) + c * 8192, &map_b0, n0 + 64 * c, g * BK, &lfull[sl]);
+          }
+        } else {
+          const int e = kt - n_my_main;
+          mbar_arrive_expect_tx(&lfull[sl], C::TX_EXT);
 #pragma unroll
-              for (int c = 0; c < BN / 64; ++c)
-                tma_load_2d(B_s(sb) + c * 8192, &map_vl, n0 + 64 * c, e * BK, &lfull[sl]);
-            }
+          for (int i = 0; i < MT; ++i)
+            tma_load_2d(A_s(sl) + i * C::A_BYTES, &map_ul, e * BK, m0 + i * BM, &lfull[sl]);
+          if (!C::MN) {
+            tma_load_2d(B_s(sb), &map_vl, e * BK, n0, &lfull[sl]);
+          } else {
+#pragma unroll
+            for (int c = 0; c < BN / 64; ++c)
+              tma_load_2d(B_s(sb) + c * 8192, &map_vl, n0 + 64 * c, e * BK, &lfull[sl]);
           }
         }
-        return true;
-      });
+        ++issued;
+      }
       // never leave the CTA with copies still landing in its shared memory
-      for (int j = (kt > NL ? kt - NL : 0); j < kt; ++j) {
+      for (int kt = (issued > NL ? issued - NL : 0); kt < issued; ++kt) {
         volatile int no_abort = 0;
-        mbar_wait(&lfull[j % NL], (j / NL) & 1, p.err, &no_abort);
+        mbar_wait(&lfull[kt % NL], (kt / NL) & 1, p.err, &no_abort);
       }
     }
   } else if (warp == WORKERS + 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_16(BM, BN, 0, C::MN ? 1 : 0, F16 ? 1 : 0);
-      int kt = 0, seg = 0;
-      bool gave_up = false;
-      for_segments([&](int, int k0, int k1, int, int) {
-        // the previous segment's epilogue must have read its accumulator out of TMEM
-        if (seg > 0 && !mbar_wait(tfree, (seg - 1) & 1, p.err, abort_flag)) return !(gave_up = true);
+      for (int kt = 0; kt < n_total; ++kt) {
+        const int sl = kt % NL, sb = kt % NB;
+        // produce modes: the workers waited for the load stage before marking the B stage
+        // ready; direct modes: the load-stage barrier also counts the B tile's bytes
+        const bool ok = C::PRODUCE ? mbar_wait(&bready[sb], (kt / NB) & 1, p.err, abort_flag)
+                                   : mbar_wait(&lfull[sl], (kt / NL) & 1, p.err, abort_flag);
+        if (!ok) break;
         tc_fence_after();
-        for (int k = k0; k < k1; ++k, ++kt) {
-          const int sl = kt % NL, sb = kt % NB;
-          // produce modes: the workers waited for the load stage before marking the B stage
-          // ready; direct modes: the load-stage barrier also counts the B tile's bytes
-          const bool ok = C::PRODUCE ? mbar_wait(&bready[sb], (kt / NB) & 1, p.err, abort_flag)
-                                     : mbar_wait(&lfull[sl], (kt / NL) & 1, p.err, abort_flag);
-          if (!ok) return !(gave_up = true);
-          tc_fence_after();
-          const uint32_t a_addr = smem_u32(A_s(sl));
-          const uint32_t b_addr = smem_u32(B_s(sb));
+        const uint32_t a_addr = smem_u32(A_s(sl));
+        const uint32_t b_addr = smem_u32(B_s(sb));
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t bd = C::MN ? smem_desc(b_addr + kk * 2048, 8192, 1024)
-                                      : smem_desc(b_addr + kk * 32, 16, 1024);
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint64_t bd = C::MN ? smem_desc(b_addr + kk * 2048, 8192, 1024)
+                                    : smem_desc(b_addr + kk * 32, 16, 1024);
 #pragma unroll
-            for (int i = 0; i < MT; ++i) {
-              const uint64_t ad = smem_desc(a_addr + i * C::A_BYTES + kk * 32, 16, 1024);
-              tc_mma_bf16(tmem + i * BN, ad, bd, idesc, (k != k0 || kk != 0) ? 1u : 0u);
-            }
+          for (int i = 0; i < MT; ++i) {
+            const uint64_t ad = smem_desc(a_addr + i * C::A_BYTES + kk * 32, 16, 1024);
+            tc_mma_bf16(tmem + i * BN, ad, bd, idesc, (kt | kk) != 0);
           }
-          tc_commit(&lempty[sl]);
-          tc_commit(&bempty[sb]);
         }
-        tc_commit(accf);  // this segment's accumulator is complete once its MMAs retire
-        ++seg;
-        return true;
-      });
-      // every MMA retired before TMEM is freed.  Normally that is the last segment's commit; a
-      // segment abandoned half way gets its commit here (the workers may be waiting on it), so
-      // the barrier never runs two phases ahead of a waiter
-      volatile int no_abort = 0;
-      if (gave_up || seg == 0) {
-        tc_commit(accf);
-        mbar_wait(accf, seg & 1, p.err, &no_abort);
-      } else {
-        mbar_wait(accf, (seg - 1) & 1, p.err, &no_abort);
+        tc_commit(&lempty[sl]);
+        tc_commit(&bempty[sb]);
       }
+      tc_commit(accf);
+      volatile int no_abort = 0;
+      mbar_wait(accf, 0, p.err, &no_abort);  // every MMA retired before TMEM is freed
     }
   } else {
     // ---------------------------------------------------------------- worker warps
     const int grp = warp / DQ_WARPS;
     const int t = threadIdx.x - grp * DQ_WARPS * 32;  // 0 .. 255 within the group
-    // the codebook is read from shared memory (broadcast loads) where a block's table is
-    // formed, which keeps sixteen registers free for the dequantisation
-    const float *cbr = s_cb;
-    int kt = 0, seg = 0;
-    for_segments([&](int tile, int k0, int k1, int m0, int n0) {
-      // this thread's block scale for main k-tile k: forward = (row n0 + t, block k); dX =
-      // (row k * 64 + (t & 63), block n0 / 64 + (t >> 6)); rows past the weight read as 0
-      auto absmax_of = [&](int k) -> float {
-        if (!C::NF4 || k >= p.n_main || k >= k1) return 0.f;
-        const int row = (BMODE == B_NF4_K) ? n0 + t : k * BK + (t & 63);
-        const int col = (BMODE == B_NF4_K) ? k : n0 / 64 + (t >> 6);
-        if (row >= p.Nw || col >= p.kblocks) return 0.f;
-        return __ldg(p.absmax + (size_t)row * p.kblocks + col);
-      };
-      // this group's k-tiles of the segment are those with (kt + k - k0) % NGROUPS == grp
-      const int first = k0 + ((grp - kt) % NGROUPS + NGROUPS) % NGROUPS;
-      float a_next = absmax_of(first);
-      for (int k = first; C::PRODUCE && k < k1; k += NGROUPS) {
-        const int q = kt + (k - k0);  // this k-tile's ring position
-        const int sl = q % NL, sb = q % NB;
-        const float a = a_next;
-        a_next = absmax_of(k + NGROUPS);  // in flight while this tile is waited for and dequantised
-        if (!mbar_wait(&lfull[sl], (q / NL) & 1, p.err, abort_flag)) return false;
-        if (C::NF4 && k < p.n_main) {
-          // dequantise into registers first, then wait for the B stage (the MMAs of this
-          // group's previous tile in it) and store
-          uint8_t *Bs = B_s(sb);
-          const uint8_t *Rs = R_s(sl);
-          uint4 o[8];
-          if (BMODE == B_NF4_K) {
-            // BN == 256 rows: one row-block per thread
-            const uint4 c0 = *reinterpret_cast<const uint4 *>(Rs + t * 32);
-            const uint4 c1 = *reinterpret_cast<const uint4 *>(Rs + t * 32 + 16);
-            const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-            dq_block64<F16>(cbr, cw, a, o);
-          } else {
-            // 64 reduction rows x (BN / 64) column segments: one row-block per thread
-            const int n = t & 63, sg = t >> 6;
-            const uint4 c0 = *reinterpret_cast<const uint4 *>(Rs + sw128(n, 2 * sg));
-            const uint4 c1 = *reinterpret_cast<const uint4 *>(Rs + sw128(n, 2 * sg + 1));
-            const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-            dq_block64<F16>(cbr, cw, a, o);
-          }
-          if (q >= NB && !mbar_wait(&bempty[sb], ((q / NB) - 1) & 1, p.err, abort_flag)) return false;
-          if (BMODE == B_NF4_K) {
+    float cbr[16];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(Bs + sw128(t, c)) = o[c];
-          } else {
-            const int n = t & 63, sg = t >> 6;
+    for (int i = 0; i < 16; ++i) cbr[i] = s_cb[i];
+    // this thread's block scale for k-tile kt: forward = (row n0 + t, block kt); dX = (row
+    // kt * 64 + (t & 63), block n0 / 64 + (t >> 6)); rows past the weight read as 0
+    auto absmax_of = [&](int kt) -> float {
+      if (!C::NF4 || kt >= n_my_main) return 0.f;
+      const int g = kb + kt;
+      const int row = (BMODE == B_NF4_K) ? n0 + t : g * BK + (t & 63);
+      const int col = (BMODE == B_NF4_K) ? g : n0 / 64 + (t >> 6);
+      if (row >= p.Nw || col >= p.kblocks) return 0.f;
+      return __ldg(p.absmax + (size_t)row * p.kblocks + col);
+    };
+    float a_next = absmax_of(grp);
+    for (int kt = grp; C::PRODUCE && kt < n_total; kt += NGROUPS) {
+      const int sl = kt % NL, sb = kt % NB;
+      const float a = a_next;
+      a_next = absmax_of(kt + NGROUPS);  // in flight while this tile is waited for and dequantised
+      if (!mbar_wait(&lfull[sl], (kt / NL) & 1, p.err, abort_flag)) break;
+      if (C::NF4 && kt < n_my_main) {
+        // dequantise into registers first, then wait for the B stage (the MMAs of this
+        // group's previous tile in it) and store
+        uint8_t *Bs = B_s(sb);
+        const uint8_t *Rs = R_s(sl);
+        uint4 o[8];
+        if (BMODE == B_NF4_K) {
+          // BN == 256 rows: one row-block per thread
+          const int n = t;
+          const uint4 c0 = *reinterpret_cast<const uint4 *>(Rs + n * 32);
+          const uint4 c1 = *reinterpret_cast<const uint4 *>(Rs + n * 32 + 16);
+          const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          dq_block64<F16>(cbr, cw, a, o);
+        } else {
+          // 64 reduction rows x (BN / 64) column segments: one row-block per thread
+          const int n = t & 63, seg = t >> 6;
+          const uint4 c0 = *reinterpret_cast<const uint4 *>(Rs + sw128(n, 2 * seg));
+          const uint4 c1 = *reinterpret_cast<const uint4 *>(Rs + sw128(n, 2 * seg + 1));
+          const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          dq_block64<F16>(cbr, cw, a, o);
+        }
+        if (kt >= NB && !mbar_wait(&bempty[sb], ((kt / NB) - 1) & 1, p.err, abort_flag)) break;
+        if (BMODE == B_NF4_K) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-              *reinterpret_cast<uint4 *>(Bs + sg * 8192 + sw128(n, c)) = o[c];
-          }
-          fence_async_smem();
-        } else if (C::CONV && k < p.n_main) {
-          // bf16 -> half, element by element; the byte layout (and so the swizzle) is unchanged
-          uint4 *Bs = reinterpret_cast<uint4 *>(B_s(sb));
-          for (int i = t; i < C::B_BYTES / 16; i += DQ_WARPS * 32) {
-            uint4 v = Bs[i];
-            v.x = pack_h2(bf16_lo(v.x), bf16_hi(v.x));
-            v.y = pack_h2(bf16_lo(v.y), bf16_hi(v.y));
-            v.z = pack_h2(bf16_lo(v.z), bf16_hi(v.z));
-            v.w = pack_h2(bf16_lo(v.w), bf16_hi(v.w));
-            Bs[i] = v;
-          }
-          fence_async_smem();
+          for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(Bs + sw128(t, c)) = o[c];
+        } else {
+          const int n = t & 63, seg = t >> 6;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4 *>(Bs + seg * 8192 + sw128(n, c)) = o[c];
+        }
+        fence_async_smem();
+      } else if (C::CONV && kt < n_my_main) {
+        // bf16 -> half, element by element; the byte layout (and so the swizzle) is unchanged
+        uint4 *Bs = reinterpret_cast<uint4 *>(B_s(sb));
+        for (int i = t; i < C::B_BYTES / 16; i += DQ_WARPS * 32) {
+          uint4 v = Bs[i];
+          v.x = pack_h2(bf16_lo(v.x), bf16_hi(v.x));
+          v.y = pack_h2(bf16_lo(v.y), bf16_hi(v.y));
+          v.z = pack_h2(bf16_lo(v.z), bf16_hi(v.z));
+          v.w = pack_h2(bf16_lo(v.w), bf16_hi(v.w));
+          Bs[i] = v;
+        }
+        fence_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bready[sb]);
+    }
+    // ---------------------------------------------------------------- epilogue
+    volatile int no_abort = 0;
+    const bool ok = !*abort_flag && mbar_wait(accf, 0, p.err, &no_abort) && !*abort_flag;
+    tc_fence_after();
+    if (ok) {
+      // Each warp owns 32 rows (its TMEM lane quarter) x COLS columns of every m-tile.  The
+      // block goes through shared memory — the rings are idle now: every MMA has retired and
+      // every TMA copy has landed — so that the global stores cover whole row segments: lane l
+      // takes columns 2l, 2l + 1 of one row per store, 128 or 256 contiguous bytes per
+      // instruction instead of 32 scattered rows.
+      const int q = warp & 3;
+      constexpr int COLS = BN / (WORKERS / 4);  // columns per warp
+      constexpr int LDSW = COLS + 4;            // staged row stride in floats (conflict-free)
+      static_assert(WORKERS * 32 * LDSW * 4 <= NL * C::LSTAGE + NB * C::B_BYTES, "staging space");
+      float *stage = reinterpret_cast<float *>(smem) + (size_t)warp * 32 * LDSW;
+      const int c0 = (warp >> 2) * COLS;         // first column of this warp inside the tile
+      const int ncol = n0 + c0 + 2 * lane;       // this lane's first output column
+      const bool pair_ok = ((p.splits > 1 ? p.Ng : p.ldo) & 1) == 0 &&
+                           (EPI != EPI_F32_ADD || p.splits > 1 || (p.ld_add & 1) == 0);
+      for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+        for (int cc = 0; cc < COLS / 32; ++cc) {
+          uint32_t r[32];
+          tc_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + mt * BN + c0 + cc * 32, r);
+          tc_wait_ld();
+          float *row = stage + lane * LDSW + cc * 32;
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            *reinterpret_cast<float4 *>(row + 4 * v) =
+                make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                            __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bready[sb]);
+        bool bad = false;
+        const int mrow0 = m0 + mt * BM + q * 32;
+        for (int rr = 0; rr < 32; ++rr) {
+          const int m = mrow0 + rr;
+          if (m >= p.M) break;
+          const float2 v = *reinterpret_cast<const float2 *>(stage + rr * LDSW + 2 * lane);
+          const bool in0 = ncol < p.Ng, in1 = ncol + 1 < p.Ng;
+          if (!in0) continue;
+          if (p.splits > 1) {
+            float *o = p.part + ((size_t)z * p.M + m) * p.Ng + ncol;
+            if (in1 && pair_ok) *reinterpret_cast<float2 *>(o) = v;
+            else {
+              o[0] = v.x;
+              if (in1) o[1] = v.y;
+            }
+          } else if (EPI == EPI_16) {
+            if (F16) bad |= half_out_of_range(v.x) || (in1 && half_out_of_range(v.y));
+            uint16_t *o = reinterpret_cast<uint16_t *>(p.out) + (size_t)m * p.ldo + ncol;
+            if (in1 && pair_ok) *reinterpret_cast<uint32_t *>(o) = pack16x2<F16>(v.x, v.y);
+            else {
+              o[0] = st16<F16>(v.x);
+              if (in1) o[1] = st16<F16>(v.y);
+            }
+          } else {
+            float *o = reinterpret_cast<float *>(p.out) + (size_t)m * p.ldo + ncol;
+            float2 w = v;
+            if (EPI == EPI_F32_ADD || EPI == EPI_F32_ACC) {
+              const float *src = EPI == EPI_F32_ADD ? p.add_src + (size_t)m * p.ld_add + ncol : o;
+              if (in1 && pair_ok) {
+                const float2 b = *reinterpret_cast<const float2 *>(src);
+                w.x = b.x + w.x;
+                w.y = b.y + w.y;
+              } else {
+                w.x = src[0] + w.x;
+                if (in1) w.y = src[1] + w.y;
+              }
+            }
+            if (in1 && pair_ok) *reinterpret_cast<float2 *>(o) = w;
+            else {
+              o[0] = w.x;
+              if (in1) o[1] = w.y;
+            }
+          }
+        }
+        if (F16 && EPI == EPI_16) flag_range(bad, p.err);
+        __syncwarp();  // the staged block is read before the next m-tile overwrites it
       }
-      kt += k1 - k0;
-      // ------------------------------------------------------------ this segment's epilogue
-      volatile int no_abort = 0;
-      const bool ok = !*abort_flag && mbar_wait(accf, seg & 1, p.err, &no_abort) && !*abort_flag;
-      tc_fence_after();
-      if (ok) tile_epilogue<BN, EPI, F16, MT>(p, tmem, tile, k0 == 0 && k1 == KT, m0, n0, cta, ub, U, CT);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tfree);
-      ++seg;
-      return ok;
-    });
+    }
+    tc_fence_before();
   }
   __syncthreads();
   if (warp == WORKERS + 1) {
@@ -665,6 +547,62 @@ __global__ void __launch_bounds__(256) fallback_gemm_kernel(const FbParams p) {
 }
 
 // ---------------------------------------------------------------------------------------
+// Split-K reduction: out = epilogue(sum over splits, in split order) — deterministic.
+struct RedParams {
+  const float *part;
+  int splits, M, Ng, epi, f16, ldo, ld_add;
+  void *out;
+  const float *add_src;
+  int *err;
+};
+// Sum of the split partial planes in split order, then the epilogue.  Launched as a
+// programmatic dependent of the GEMM: waits for it before reading the partials.  V = 4: four
+// consecutive columns per item (Ng, ldo, ld_add multiples of 4, 16-byte aligned buffers).
+template <int V>
+__global__ void splitk_reduce_kernel(const RedParams p) {
+  pdl_wait();
+  const int nv = p.Ng / V;
+  const int64_t total = (int64_t)p.M * nv;
+  const int64_t plane = (int64_t)p.M * p.Ng;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int m = (int)(idx / nv), n = (int)(idx - (int64_t)m * nv) * V;
+    const size_t e = (size_t)m * p.Ng + n;
+    float v[V];
+    if constexpr (V == 4) {
+      float4 a = *reinterpret_cast<const float4 *>(p.part + e);
+      for (int z = 1; z < p.splits; ++z) {
+        const float4 b = *reinterpret_cast<const float4 *>(p.part + (size_t)z * plane + e);
+        a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+      }
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    } else {
+      v[0] = p.part[e];
+      for (int z = 1; z < p.splits; ++z) v[0] += p.part[(size_t)z * plane + e];
+    }
+    if (p.epi == EPI_16) {
+      uint16_t *o = reinterpret_cast<uint16_t *>(p.out) + (size_t)m * p.ldo + n;
+      if (p.f16) {
+        bool bad = false;
+#pragma unroll
+        for (int j = 0; j < V; ++j) bad |= half_out_of_range(v[j]);
+        flag_range(bad, p.err);
+      }
+#pragma unroll
+      for (int j = 0; j < V; ++j) o[j] = p.f16 ? f_to_h16(v[j]) : f_to_bf16(v[j]);
+    } else {
+      float *o = reinterpret_cast<float *>(p.out) + (size_t)m * p.ldo + n;
+#pragma unroll
+      for (int j = 0; j < V; ++j) {
+        if (p.epi == EPI_F32) o[j] = v[j];
+        else if (p.epi == EPI_F32_ADD) o[j] = p.add_src[(size_t)m * p.ld_add + n + j] + v[j];
+        else o[j] = o[j] + v[j];
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------
 // host side
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::mutex g_mu;
@@ -720,18 +658,31 @@ int launch_tc(const GemmArgs &g, const CUtensorMap *maps, cudaStream_t st) {
   p.Ng = g.Ng();
   p.n_main = (g.Kg() + BK - 1) / BK;
   p.n_ext = g.R / BK;
-  p.n_mt = (g.M + BM * MT - 1) / (BM * MT);
-  p.KT = p.n_main + p.n_ext;
-  p.U = (int)((long long)p.n_mt * ((p.Ng + BN - 1) / BN) * p.KT);
+  p.splits = g.splits > 1 ? g.splits : 1;
+  p.per_split = (p.n_main + p.splits - 1) / p.splits;
   p.part = g.part;
-  p.counters = g.counters;
   p.out = g.out;
   p.ldo = g.ldo;
   p.add_src = g.add_src;
   p.ld_add = g.ld_add;
   p.err = g.err;
-  kern<<<dim3(g.ctas), THREADS, C::SMEM, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
+  dim3 grid((g.M + BM * MT - 1) / (BM * MT), (p.Ng + BN - 1) / BN, p.splits);
+  kern<<<grid, THREADS, C::SMEM, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
   count_launches(1);
+  if (p.splits > 1) {
+    RedParams rp;
+    rp.part = g.part; rp.splits = p.splits; rp.M = g.M; rp.Ng = p.Ng; rp.epi = g.epi;
+    rp.f16 = g.op_f16; rp.ldo = g.ldo; rp.ld_add = g.ld_add; rp.out = g.out; rp.add_src = g.add_src;
+    rp.err = g.err;
+    const bool vec = p.Ng % 4 == 0 && g.ldo % 4 == 0 && (g.epi != EPI_F32_ADD || g.ld_add % 4 == 0) &&
+                     (reinterpret_cast<uintptr_t>(g.part) & 15) == 0;
+    const int64_t n = (int64_t)g.M * p.Ng / (vec ? 4 : 1);
+    const int blocks = (int)std::min<int64_t>((n + 255) / 256, 148 * 16);
+    cudaError_t le = vec ? launch_pdl(splitk_reduce_kernel<4>, dim3(blocks), dim3(256), 0, st, rp)
+                         : launch_pdl(splitk_reduce_kernel<1>, dim3(blocks), dim3(256), 0, st, rp);
+    if (le != cudaSuccess) return set_error(SOUP_ECUDA, "split-K reduce launch: %s", cudaGetErrorString(le));
+    count_launches(1);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(SOUP_ECUDA, "tc_gemm launch: %s", cudaGetErrorString(e));
   return 0;
@@ -766,44 +717,42 @@ int tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t i
   return make_map(m, dt, base, inner, outer, row_bytes, box_inner, box_outer, sw, what);
 }
 
+// Tiling of one call: m-tiles per CTA (1 or 2) and split-K factor (1..4), minimising a model
+// of waves x k-tiles per CTA x time per k-tile, plus the cost of writing and re-reading the
+// float partial planes.  Two m-tiles halve the dequantisation per flop: an NF4 k-tile costs
+// max(512 x MT tensor cycles, ~900 cycles of byte-permute work for the 256 x 64 B tile);
+// bf16 weights have no dequantisation.  Split-K needs the caller's partial buffer.
 struct Tiling {
-  int mt = 1;    // 128-row m-tiles per CTA
-  int ctas = 1;  // grid size
+  int mt, s;
 };
-// SMs of the current device (looked up once per device).
-int sm_count() {
-  static std::atomic<int> slot[MAX_DEVICES];
-  int v = 0;
-  if (per_device_once(slot, &v, [](int dev, int *out) {
-        return cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev);
-      }) != cudaSuccess || v < 1)
-    return 148;
-  return v;
-}
-
-// Tiling of one call.  Two 128-row m-tiles per CTA whenever there are more than 128 rows:
-// each dequantised weight tile then feeds 256 rows, which halves the dequantisation per flop.
-// Grid: one CTA per SM, each taking an equal run of the launch's units (stream-K), when the
-// caller's buffers hold the partial tiles and the counters; otherwise one CTA per whole tile.
 Tiling choose_tiling(const GemmArgs &g, int bn) {
-  Tiling tl;
-  tl.mt = g.M > 128 ? 2 : 1;
-  const long long tiles = (long long)((g.M + 128 * tl.mt - 1) / (128 * tl.mt)) * ((g.Ng() + bn - 1) / bn);
-  const long long kt = (g.Kg() + 63) / 64 + g.R / 64;
-  const long long units = tiles * kt;
-  const size_t tile_floats = (size_t)tl.mt * 128 * bn;
-  const int sms = sm_count();
-  long long ctas = std::min<long long>(sms, std::max<long long>(1, units / SK_MIN_UNITS));
-  const bool can_cut = g.cut_allowed && g.part && g.counters &&
-                       (size_t)tiles * SK_WARPS <= g.counter_ints &&
-                       2 * (size_t)ctas * tile_floats <= g.part_floats;
-  if (!can_cut || ctas >= tiles * kt) ctas = tiles;  // whole tiles only
-  tl.ctas = (int)ctas;
-  return tl;
+  const int64_t ntile = (g.Ng() + bn - 1) / bn;
+  const int kt = (g.Kg() + 63) / 64;
+  const bool nf4 = g.wfmt == W_NF4;
+  const bool can_split = g.part && g.part_floats > 0 && g.splits_allowed;
+  const double cyc_per_s = 1.9e9, bw = 6.0e12;  // partial traffic (mostly L2-resident), bytes / s
+  Tiling best{1, 1};
+  double best_t = 1e300;
+  for (int mt = 1; mt <= 2; ++mt) {
+    if (mt == 2 && g.M <= 128) break;
+    const double per_ktile = nf4 ? std::max(512.0 * mt, 900.0) : 512.0 * mt;
+    const int64_t tiles = (int64_t)((g.M + 128 * mt - 1) / (128 * mt)) * ntile;
+    for (int s = 1; s <= 4; ++s) {
+      if (s > 1 && (!can_split || kt / s < 4 || (double)s * g.M * g.Ng() > (double)g.part_floats)) break;
+      const int64_t waves = (tiles * s + 147) / 148;
+      const double t = (double)waves * ((kt + s - 1) / s) * per_ktile +
+                       (s > 1 ? 2.0 * s * g.M * (double)g.Ng() * 4.0 / bw * cyc_per_s : 0.0);
+      if (t < best_t * 0.97) {  // a clear gain only: fewer CTAs, fewer partial planes first
+        best_t = t;
+        best = {mt, s};
+      }
+    }
+  }
+  return best;
 }
 
+int choose_splits(const GemmArgs &g, int bn) { return choose_tiling(g, bn).s; }
 int choose_mtiles(const GemmArgs &g, int bn) { return choose_tiling(g, bn).mt; }
-int choose_ctas(const GemmArgs &g, int bn) { return choose_tiling(g, bn).ctas; }
 
 int gemm_uses_tc(const GemmArgs &g) {
   if (g_force_fallback) return 0;
@@ -877,7 +826,7 @@ int gemm_launch(const GemmArgs &g, cudaStream_t st) {
   GemmArgs g2 = g;
   const Tiling tl = choose_tiling(g, BN);
   g2.mtiles = tl.mt;
-  g2.ctas = tl.ctas;
+  g2.splits = tl.s;
   return gemm_launch_tc(g2, st);
 }
 

@@ -43,18 +43,13 @@ struct GemmArgs {
   const float *add_src = nullptr;
   int ld_add = 0;
   int *err = nullptr;              // device int: kernels OR error bits into it
-  // Scratch for work split between CTAs (optional): `part` holds the tensor-core path's
-  // partial tiles (2 per CTA; SK_PART_FLOATS) and the small-M path's partial strips;
-  // `counters` (counter_ints >= SK_WARPS per tile) must be zero before the first call and is
-  // left zero by every call.  Without them (or with cut_allowed = 0) each CTA takes whole
-  // tiles.
+  // split-K scratch (optional): float buffer the kernel may use for partial tiles when the
+  // output grid under-fills the GPU; splits is chosen by gemm_launch
   float *part = nullptr;
   size_t part_floats = 0;
-  int *counters = nullptr;
-  size_t counter_ints = 0;
-  int cut_allowed = 1;
+  int splits_allowed = 1;
+  int splits = 1;
   int mtiles = 1;                  // 128-row m-tiles per CTA (1 or 2), chosen by gemm_launch
-  int ctas = 1;                    // grid size, chosen by gemm_launch
   // LoRA term in float for the small-M path (which ignores ul / vl / R):
   //   FWD y[m, n]  += s * sum_j lora_u[m, p r + j] * B_p[n - off_p, j]   (lora_u = x A^T)
   //   DX  dx[m, k] += sum_p sum_j lora_u[m, p r + j] * A_p[j, k]          (lora_u = s dY B)
@@ -78,20 +73,10 @@ double gemm_bytes(const GemmArgs &g);
 int gemm_launch(const GemmArgs &g, cudaStream_t stream);
 // 1 if gemm_launch would take the tensor-core path for this shape.
 int gemm_uses_tc(const GemmArgs &g);
-// 128-row m-tiles per CTA (1 or 2) and grid size gemm_launch picks for this call.
+// Split-K factor gemm_launch picks for this call (1 = none).
+int choose_splits(const GemmArgs &g, int bn);
+// 128-row m-tiles per CTA (1 or 2) gemm_launch picks for this call.
 int choose_mtiles(const GemmArgs &g, int bn);
-int choose_ctas(const GemmArgs &g, int bn);
-// Stream-K scratch bounds: at most SK_MAX_CTAS CTAs (one per SM), each with two partial tiles
-// of up to 2 x 128 x 256 floats; SK_WARPS counters per tile; a CTA takes at least SK_MIN_UNITS
-// k-tiles.
-constexpr int SK_MAX_CTAS = 160;
-constexpr int SK_WARPS = 16;
-constexpr int SK_MIN_UNITS = 4;
-constexpr size_t SK_PART_FLOATS = 2ull * SK_MAX_CTAS * 2 * 128 * 256;
-// Counters a call on an [M, Ng] output needs (an upper bound over the tilings).
-inline size_t sk_counter_ints(int M, int Ng) {
-  return (size_t)SK_WARPS * ((M + 127) / 128) * ((Ng + 255) / 256);
-}
 int gemm_launch_tc(const GemmArgs &g, cudaStream_t stream);
 // Force the fallback path (tests compare the two).
 void gemm_force_fallback(int on);

@@ -139,10 +139,10 @@ extern "C" int soup_proj_fwd_noalloc(const uint16_t *x, int M, int N, int K, con
   g.out = y;
   g.ldo = N;
   g.err = reinterpret_cast<int *>(base + kErrOffset);
-  // partial strips of the small-M path only; the tensor-core path cuts no tile here
+  // partial strips of the small-M path only; the tensor-core path runs without split-K here
   g.part = L.gpart_floats ? reinterpret_cast<float *>(base + L.gpart) : nullptr;
   g.part_floats = L.gpart_floats;
-  g.cut_allowed = 0;  // whole tiles per CTA: no partial tiles or counters needed
+  g.splits_allowed = 0;
   if (r > 0) {
     k_lora_down(x, K, M, K, seg, reinterpret_cast<float *>(base + L.u_f32),
                 reinterpret_cast<uint16_t *>(base + L.ul), f16, f16,

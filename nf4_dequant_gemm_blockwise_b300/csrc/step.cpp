@@ -117,17 +117,10 @@ int make_plan(const soup_cfg *c, int maxB, int maxS, int n_slots, int mode, Plan
     for (int k : dims) mx = std::max(mx, lora_scratch_floats((int)M, k, 3 * c->lora_r));
     P->lora_part = take(4 * mx);
   }
-  // partial tiles of the tensor-core GEMMs' stream-K schedule (and the small-M path's partial
-  // strips), and the per-tile counters, sized for the widest output of the step
-  P->gemm_part_floats = std::max<uint64_t>(SK_PART_FLOATS, std::max(gemv_part_floats(GEMM_FWD),
-                                                                    gemv_part_floats(GEMM_DX)));
+  // split-K partial tiles for the base GEMMs whose output grid under-fills the GPU (and the
+  // small-M path's partial strips)
+  P->gemm_part_floats = 4ull * M * std::max<uint64_t>(std::max(nqkv, H), std::max(qd, (uint64_t)I));
   P->gemm_part = take(4 * P->gemm_part_floats);
-  {
-    const uint64_t widest = std::max<uint64_t>(std::max<uint64_t>(nqkv, 2 * I),
-                                               std::max<uint64_t>(H, (uint64_t)ce_chunk_cols((int)M, c->vocab)));
-    P->gemm_cnt_ints = sk_counter_ints((int)M, (int)widest);
-    P->gemm_cnt = take(4 * P->gemm_cnt_ints);
-  }
   P->hn = take(2 * M * H);
   P->vc = ce_chunk_cols((int)M, c->vocab);
   P->z = take(4 * M * (uint64_t)P->vc);
@@ -237,16 +230,14 @@ int prof(soup_stream *h, int fam, double flops, double bytes, Fn &&fn) {
   return 0;
 }
 
-// A base-weight GEMM of group `grp` (forward or dX), timed in profiling modes 1 and 2.
-// The step's split-work scratch for a GEMM (partial tiles, counters) and its error flag.
+// The step's split-K scratch for a GEMM (partial tiles) and its error flag.
 void gemm_scratch(soup_stream *h, GemmArgs &g) {
   g.err = h->err_dev;
   g.part = F(h, h->plan.gemm_part);
   g.part_floats = h->plan.gemm_part_floats;
-  g.counters = reinterpret_cast<int *>(h->ws + h->plan.gemm_cnt);
-  g.counter_ints = h->plan.gemm_cnt_ints;
 }
 
+// A base-weight GEMM of group `grp` (forward or dX), timed in profiling modes 1 and 2.
 int timed_gemm(soup_stream *h, GemmArgs &g, int grp) {
   gemm_scratch(h, g);
   if (!h->dbg_profile) return gemm_launch(g, h->cs);
@@ -706,8 +697,7 @@ int stream_init(soup_store *st, const soup_cfg *c, int maxB, int maxS, void *ws,
     soup_stream_free_impl(h);
     return rc;
   };
-  if (cudaMemsetAsync(h->err_dev, 0, 64, h->cs) != cudaSuccess ||
-      cudaMemsetAsync(h->ws + P.gemm_cnt, 0, 4 * P.gemm_cnt_ints, h->cs) != cudaSuccess)
+  if (cudaMemsetAsync(h->err_dev, 0, 64, h->cs) != cudaSuccess)
     return fail(set_error(SOUP_ECUDA, "workspace memset failed"));
   // RoPE tables: angle pos * theta^(-2i/d) formed in double, cos/sin rounded to float.
   {
@@ -939,8 +929,6 @@ int stream_sync(soup_stream *h, int timeout_ms) {
   harvest(h, false);
   if (err) {  // reported once: the next step starts with a clear flag
     SOUP_CUDA_TRY(cudaMemset(h->err_dev, 0, sizeof(int)));
-    // a kernel that gave up may have left tile counters counted in: start them afresh
-    SOUP_CUDA_TRY(cudaMemset(h->ws + h->plan.gemm_cnt, 0, 4 * h->plan.gemm_cnt_ints));
     return kernel_flags_status(err, "soup_sync");
   }
   return 0;

@@ -22,7 +22,6 @@ struct Plan {
   uint64_t rope_cos = 0, rope_sin = 0, err = 0;
   uint64_t vocab_buf = 0;  // SOUP_MODE_STREAM_HEAD: the one vocabulary-sized table buffer
   uint64_t gemm_part = 0, gemm_part_floats = 0;
-  uint64_t gemm_cnt = 0, gemm_cnt_ints = 0;  // stream-K tile counters (zero between launches)
   // keep-activations mode: hm .. u_b[3] repeat once per layer at this stride (0 otherwise)
   uint64_t act_stride = 0;
 };

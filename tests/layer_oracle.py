@@ -79,28 +79,38 @@ def _workers(n_layers, gb_per_worker):
     return max(1, min(cores, n_layers, int(avail_gb // gb_per_worker)))
 
 
+class LayerChecks:
+    """A pool of worker processes checking layers while the caller goes on (with the GPU).
+    submit(cfg, layers, cases_of) queues layer checks (cases_of(li) builds that layer's cases
+    from the GPU results, called here, in the parent); results() waits for all of them and
+    returns {layer: figures} in submission order per layer."""
+
+    def __init__(self, n_layers, gb_per_worker=8.0):
+        self.n = _workers(n_layers, gb_per_worker)
+        threads = max(1, (os.cpu_count() or 1) // self.n)
+        root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+        self.ex = cf.ProcessPoolExecutor(max_workers=self.n, mp_context=mp.get_context("spawn"),
+                                         initializer=_init_worker, initargs=(root, threads))
+        self.futures = []
+
+    def submit(self, cfg, layers, cases_of):
+        for li in layers:
+            self.futures.append((li, self.ex.submit(check_layer, cfg, li, cases_of(li))))
+
+    def results(self):
+        out = {}
+        try:
+            for li, f in self.futures:
+                out.setdefault(li, []).extend(f.result())
+        finally:
+            self.ex.shutdown()
+        return out
+
+
 def check_layers(cfg, layers, cases_of, gb_per_worker=8.0):
-    """Run check_layer for every layer in `layers` on worker processes; cases_of(li) builds
-    that layer's cases from the GPU results.  Returns the figures in layer order."""
+    """Run check_layer for every layer in `layers` and wait: the figures in layer order."""
     layers = list(layers)
-    n = _workers(len(layers), gb_per_worker)
-    threads = max(1, (os.cpu_count() or 1) // n)
-    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    ctx = mp.get_context("spawn")
-    figs = {}
-    with cf.ProcessPoolExecutor(max_workers=n, mp_context=ctx, initializer=_init_worker,
-                                initargs=(root, threads)) as ex:
-        # at most 2n layers in flight, so the pickled GPU results do not pile up
-        pending, it = {}, iter(layers)
-        for li in it:
-            pending[ex.submit(check_layer, cfg, li, cases_of(li))] = li
-            if len(pending) >= 2 * n:
-                break
-        while pending:
-            done, _ = cf.wait(pending, return_when=cf.FIRST_COMPLETED)
-            for f in done:
-                figs[pending.pop(f)] = f.result()
-                nxt = next(it, None)
-                if nxt is not None:
-                    pending[ex.submit(check_layer, cfg, nxt, cases_of(nxt))] = nxt
-    return [figs[li] for li in layers]
+    lc = LayerChecks(len(layers), gb_per_worker)
+    lc.submit(cfg, layers, cases_of)
+    res = lc.results()
+    return [res[li] for li in layers]
