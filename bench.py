@@ -657,15 +657,18 @@ def run_ours(args, rank, world, local_rank, dist):
             torch.cuda.synchronize()
             vms = v0.elapsed_time(v1) / nsteps
             vst = vs.stream.stats(reset=True)
+            v_peak = torch.cuda.max_memory_allocated()
             variants.append({"batch": vb, "slots": vslots, "keep_activations": keep, "stream_head": shead,
                              "tokens_per_step": vb * S,
                              "value": world * vb * S / (vms * 1e-3), "ms_per_step": vms,
                              "copies_per_step": vst["copies"] / nsteps, "steps": nsteps,
-                             "peak_vram_bytes": torch.cuda.max_memory_allocated(),
+                             "peak_vram_bytes": v_peak,
                              "peak_vram_predicted_bytes": api.peak_bytes(vcfg, vb, S, n_slots=vslots,
                                                                          keep_activations=keep,
                                                                          stream_head=shead)[0]})
             vs.close()
+            del vs  # free its device buffers before the next variant's peak is measured
+            torch.cuda.empty_cache()
         line["variants"] = variants
     if rank == 0 and not args.no_cpu_baseline:
         one = run_oracle_timed(cfg)
