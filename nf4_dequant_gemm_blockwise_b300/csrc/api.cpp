@@ -344,8 +344,17 @@ int soup_proj_lora_grad(const uint16_t *x, const uint16_t *dy, int M, int N, int
               reinterpret_cast<int *>(base + P.err), st);
   k_lora_du(dy, N, M, L, reinterpret_cast<float *>(base + P.du_f32),
             reinterpret_cast<uint16_t *>(base + P.dul), false, false, part, st);
-  k_lora_dB(dy, N, M, reinterpret_cast<float *>(base + P.u_f32), L, false, part, st);
-  k_lora_dA(reinterpret_cast<float *>(base + P.du_f32), x, K, M, K, L, f16, part, st);
+  LoraGradGroup G;
+  G.L = L;
+  G.dy = dy;
+  G.ldy = N;
+  G.Ng = N;
+  G.u = reinterpret_cast<float *>(base + P.u_f32);
+  G.du = reinterpret_cast<float *>(base + P.du_f32);
+  G.x = x;
+  G.ldx = K;
+  G.K = K;
+  k_lora_grads(&G, 1, M, f16, st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(SOUP_ECUDA, "lora grad launch: %s", cudaGetErrorString(e));
   return 0;

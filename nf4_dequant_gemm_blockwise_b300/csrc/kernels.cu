@@ -436,253 +436,39 @@ __global__ void __launch_bounds__(128) lora_part_kernel(const uint16_t *X, int l
 }
 
 // out_f32[m, o] = (DU ? s : 1) * sum_split part; out16[m, o] = 16-bit(s * sum), zero padded.
+// One thread per output (m, o): consecutive threads take consecutive o, so every split's loads
+// are contiguous; the splits are added in split order.
 template <bool DU, bool OF16>
 __global__ void lora_reduce_kernel(const float *part, int nsplit, int M, const LoraSeg L,
                                    float *out_f32, uint16_t *out16, int *err) {
   pdl_trigger();
   pdl_wait();  // launched as a dependent of the partial kernel
-  // one warp per output: lanes take the splits lane, lane + 32, ... and the lane sums are
-  // combined by a fixed butterfly, so the order of additions never changes
   const int nout = L.nseg * L.r;
   const int Rp = L.Rpad();
   const int64_t total = (int64_t)M * Rp;
-  const int lane = threadIdx.x & 31;
-  const int64_t wpb = blockDim.x >> 5;
-  for (int64_t idx = blockIdx.x * wpb + (threadIdx.x >> 5); idx < total; idx += (int64_t)gridDim.x * wpb) {
+  const size_t plane = (size_t)M * 64;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
     const int m = (int)(idx / Rp), o = (int)(idx % Rp);
     if (o >= nout) {
-      if (lane == 0) out16[idx] = 0;
+      out16[idx] = 0;
       continue;
     }
-    float acc = 0.f;
-    for (int ks = lane; ks < nsplit; ks += 32) acc += part[((size_t)ks * M + m) * 64 + o];
-    acc = warp_sum(acc);
-    if (lane == 0) {
-      out_f32[(size_t)m * nout + o] = DU ? L.s * acc : acc;
-      if (OF16) flag_range(half_out_of_range(L.s * acc), err);
-      out16[idx] = st16<OF16>(L.s * acc);
+    const float *src = part + (size_t)m * 64 + o;
+    float acc = src[0];
+    int ks = 1;
+    for (; ks + 4 <= nsplit; ks += 4) {  // four loads in flight, added in order
+      const float a0 = src[(size_t)ks * plane], a1 = src[(size_t)(ks + 1) * plane];
+      const float a2 = src[(size_t)(ks + 2) * plane], a3 = src[(size_t)(ks + 3) * plane];
+      acc += a0;
+      acc += a1;
+      acc += a2;
+      acc += a3;
     }
-  }
-}
-
-// dB partials: part[ms][n][j] = sum over the block's rows m of dY[m, n] u[m, seg(n) r + j].
-// D[n, j] = sum_m dY^T[n, m] u[m, j]: tile 64 n x r per 128-thread block (warp w: n rows
-// 16w..16w+15), rows m in chunks of 32 staged in shared memory.  A tile that straddles a
-// segment boundary runs once per segment with the other segment's rows masked.
-template <bool F16>
-__global__ void __launch_bounds__(128) lora_dB_part_kernel(const uint16_t *dy, int ldy, int M,
-                                                           int Ng, int MC, const float *u,
-                                                           const LoraSeg L, float *part) {
-  __shared__ uint32_t ds[32][72];  // [m][n]
-  __shared__ uint32_t us[32][72];  // [m][o], o < nout
-  const int t = threadIdx.x, w = t >> 5, lane = t & 31, g = lane >> 2, q = lane & 3;
-  const int n0 = blockIdx.x * 64;
-  const int mb = blockIdx.y * MC, me = min(M, mb + MC);
-  const int nout = L.nseg * L.r;
-  const int JT = (L.r + 7) / 8;
-  const int s_lo = seg_of(L, n0), s_hi = seg_of(L, min(n0 + 63, Ng - 1));
-  const int na = n0 + 16 * w + g, nb = na + 8;  // this lane's two rows
-  // the next chunk's operands are fetched into registers while the current one is computed
-  uint4 dr[2];
-  float ur[16];
-  auto load = [&](int m0) {
-#pragma unroll
-    for (int it = 0; it < 2; ++it) {  // dY: 32 m x 64 n, 8 elements per item
-      const int i = t + 128 * it, rr = i >> 3, c8 = (i & 7) * 8;
-      const int m = m0 + rr, n = n0 + c8;
-      if (m < me && n + 8 <= Ng && ((ldy | n) & 7) == 0) {
-        dr[it] = *reinterpret_cast<const uint4 *>(dy + (size_t)m * ldy + n);
-      } else {
-        uint32_t h[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) h[e] = (m < me && n + e < Ng) ? dy[(size_t)m * ldy + n + e] : 0u;
-        dr[it] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
-      }
-    }
-#pragma unroll
-    for (int it = 0; it < 16; ++it) {  // u: 32 m x 64 o
-      const int i = t + 128 * it, rr = i >> 6, o = i & 63;
-      const int m = m0 + rr;
-      ur[it] = (m < me && o < nout) ? u[(size_t)m * nout + o] : 0.f;
-    }
-  };
-  float acc[3][4];
-#pragma unroll
-  for (int i = 0; i < 3; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-  if (mb < me) load(mb);
-  for (int m0 = mb; m0 < me; m0 += 32) {
-#pragma unroll
-    for (int it = 0; it < 2; ++it) {
-      const int i = t + 128 * it, rr = i >> 3, c8 = (i & 7) * 8;
-      const uint32_t wv[4] = {dr[it].x, dr[it].y, dr[it].z, dr[it].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        ds[rr][c8 + 2 * e] = __float_as_uint(lo16<F16>(wv[e]));
-        ds[rr][c8 + 2 * e + 1] = __float_as_uint(hi16<F16>(wv[e]));
-      }
-    }
-#pragma unroll
-    for (int it = 0; it < 16; ++it) {
-      const int i = t + 128 * it;
-      us[i >> 6][i & 63] = to_tf32(ur[it]);
-    }
-    __syncthreads();
-    if (m0 + 32 < me) load(m0 + 32);
-    for (int sg = s_lo; sg <= s_hi; ++sg) {
-      const bool ina = na < Ng && seg_of(L, na) == sg, inb = nb < Ng && seg_of(L, nb) == sg;
-#pragma unroll
-      for (int k8 = 0; k8 < 32; k8 += 8) {
-        const uint32_t a[4] = {ina ? ds[k8 + q][na - n0] : 0u, inb ? ds[k8 + q][nb - n0] : 0u,
-                               ina ? ds[k8 + q + 4][na - n0] : 0u, inb ? ds[k8 + q + 4][nb - n0] : 0u};
-#pragma unroll
-        for (int jt = 0; jt < 3; ++jt) {
-          if (jt >= JT) break;
-          const int j = 8 * jt + g;
-          const uint32_t b0 = j < L.r ? us[k8 + q][sg * L.r + j] : 0u;
-          const uint32_t b1 = j < L.r ? us[k8 + q + 4][sg * L.r + j] : 0u;
-          mma_tf32(acc[jt], a, b0, b1);
-        }
-      }
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int jt = 0; jt < 3; ++jt) {
-    if (jt >= JT) break;
-    const int j = 8 * jt + 2 * q;
-    if (na < Ng) {
-      float *d = part + ((size_t)blockIdx.y * Ng + na) * L.r;
-      if (j < L.r) d[j] = acc[jt][0];
-      if (j + 1 < L.r) d[j + 1] = acc[jt][1];
-    }
-    if (nb < Ng) {
-      float *d = part + ((size_t)blockIdx.y * Ng + nb) * L.r;
-      if (j < L.r) d[j] = acc[jt][2];
-      if (j + 1 < L.r) d[j + 1] = acc[jt][3];
-    }
-  }
-}
-
-__global__ void lora_dB_reduce_kernel(const float *part, int msplit, int Ng, const LoraSeg L) {
-  pdl_wait();  // launched as a dependent of the partial kernel
-  const int64_t total = (int64_t)Ng * L.r;
-  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
-       idx += (int64_t)gridDim.x * blockDim.x) {
-    const int n = (int)(idx / L.r), j = (int)(idx % L.r);
-    float acc = 0.f;
-    for (int ms = 0; ms < msplit; ++ms) acc += part[(size_t)ms * total + idx];
-    int seg = 0;
-    for (int p = 0; p < L.nseg; ++p)
-      if (n >= L.off[p] && n < L.off[p] + L.n[p]) seg = p;
-    float *dst = L.dB[seg] + (size_t)(n - L.off[seg]) * L.r + j;
-    const float g = L.s * acc;
-    *dst = L.accumulate ? *dst + g : g;
-  }
-}
-
-// dA partials: part[ms][o][k] = sum over the block's rows m of du[m, o] x[m, k].
-// D[o, k] = sum_m du^T[o, m] x[m, k]: OT 16-row output tiles (OT = ceil(nout / 16)) x KW
-// features per 128-thread block (warp w: output tile w % OT, features (w / OT) * 64 .. + 64),
-// rows m in chunks of 32 staged in shared memory.
-template <bool F16, int OT>
-__global__ void __launch_bounds__(128) lora_dA_part_kernel(const float *du, const uint16_t *x, int ldx,
-                                                           int M, int K, int MC, int nout,
-                                                           float *part) {
-  constexpr int KW = (4 / OT) * 64;
-  constexpr int DN = OT * 16 * 32 / 128;  // du values per thread and chunk
-  constexpr int XN = KW / 32;             // 8-element x items per thread and chunk
-  __shared__ uint32_t dus[32][OT * 16 + 8];  // [m][o]
-  __shared__ uint32_t xs[32][KW + 8];        // [m][k]
-  const int t = threadIdx.x, w = t >> 5, lane = t & 31, g = lane >> 2, q = lane & 3;
-  const int ot = w % OT, kg = w / OT;
-  const int k0 = blockIdx.x * KW;
-  const int mb = blockIdx.y * MC, me = min(M, mb + MC);
-  // the next chunk's operands are fetched into registers while the current one is computed
-  float dr[DN];
-  uint4 xr[XN];
-  auto load = [&](int m0) {
-#pragma unroll
-    for (int it = 0; it < DN; ++it) {
-      const int i = t + 128 * it, rr = i / (OT * 16), o = i % (OT * 16);
-      const int m = m0 + rr;
-      dr[it] = (m < me && o < nout) ? du[(size_t)m * nout + o] : 0.f;
-    }
-#pragma unroll
-    for (int it = 0; it < XN; ++it) {  // x: 32 m x KW k, 8 elements per item
-      const int i = t + 128 * it, rr = i / (KW / 8), c8 = (i % (KW / 8)) * 8;
-      const int m = m0 + rr, k = k0 + c8;
-      if (m < me && k + 8 <= K && ((ldx | k) & 7) == 0) {
-        xr[it] = *reinterpret_cast<const uint4 *>(x + (size_t)m * ldx + k);
-      } else {
-        uint32_t h[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) h[e] = (m < me && k + e < K) ? x[(size_t)m * ldx + k + e] : 0u;
-        xr[it] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
-      }
-    }
-  };
-  float acc[8][4];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-  if (mb < me) load(mb);
-  for (int m0 = mb; m0 < me; m0 += 32) {
-#pragma unroll
-    for (int it = 0; it < DN; ++it) {
-      const int i = t + 128 * it;
-      dus[i / (OT * 16)][i % (OT * 16)] = to_tf32(dr[it]);
-    }
-#pragma unroll
-    for (int it = 0; it < XN; ++it) {
-      const int i = t + 128 * it, rr = i / (KW / 8), c8 = (i % (KW / 8)) * 8;
-      const uint32_t wv[4] = {xr[it].x, xr[it].y, xr[it].z, xr[it].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        xs[rr][c8 + 2 * e] = __float_as_uint(lo16<F16>(wv[e]));
-        xs[rr][c8 + 2 * e + 1] = __float_as_uint(hi16<F16>(wv[e]));
-      }
-    }
-    __syncthreads();
-    if (m0 + 32 < me) load(m0 + 32);
-#pragma unroll
-    for (int k8 = 0; k8 < 32; k8 += 8) {
-      const int oa = 16 * ot + g;
-      const uint32_t a[4] = {dus[k8 + q][oa], dus[k8 + q][oa + 8], dus[k8 + q + 4][oa], dus[k8 + q + 4][oa + 8]};
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        const int kc = kg * 64 + 8 * nt + g;
-        mma_tf32(acc[nt], a, xs[k8 + q][kc], xs[k8 + q + 4][kc]);
-      }
-    }
-    __syncthreads();
-  }
-  const int oa = 16 * ot + g;
-#pragma unroll
-  for (int nt = 0; nt < 8; ++nt) {
-    const int k = k0 + kg * 64 + 8 * nt + 2 * q;
-    if (oa < nout) {
-      float *d = part + ((size_t)blockIdx.y * nout + oa) * K;
-      if (k < K) d[k] = acc[nt][0];
-      if (k + 1 < K) d[k + 1] = acc[nt][1];
-    }
-    if (oa + 8 < nout) {
-      float *d = part + ((size_t)blockIdx.y * nout + oa + 8) * K;
-      if (k < K) d[k] = acc[nt][2];
-      if (k + 1 < K) d[k + 1] = acc[nt][3];
-    }
-  }
-}
-
-__global__ void lora_dA_reduce_kernel(const float *part, int msplit, int K, const LoraSeg L) {
-  pdl_wait();  // launched as a dependent of the partial kernel
-  const int nout = L.nseg * L.r;
-  const int64_t total = (int64_t)nout * K;
-  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
-       idx += (int64_t)gridDim.x * blockDim.x) {
-    const int o = (int)(idx / K), k = (int)(idx % K);
-    float acc = 0.f;
-    for (int ms = 0; ms < msplit; ++ms) acc += part[(size_t)ms * total + idx];
-    float *dst = L.dA[o / L.r] + (size_t)(o % L.r) * K + k;
-    *dst = L.accumulate ? *dst + acc : acc;
+    for (; ks < nsplit; ++ks) acc += src[(size_t)ks * plane];
+    out_f32[(size_t)m * nout + o] = DU ? L.s * acc : acc;
+    if (OF16) flag_range(half_out_of_range(L.s * acc), err);
+    out16[idx] = st16<OF16>(L.s * acc);
   }
 }
 
@@ -928,23 +714,9 @@ int lora_splits(int M, int K, int *KS) {
   if (KS) *KS = ks;
   return cdiv(K, ks);
 }
-// Row split of the gradient reductions: several blocks per SM; at most one split per 128 rows
-// so that the float partials stay below the 16-bit operand traffic.
-static int lora_msplit(int M, int col_blocks, int *MC) {
-  int ms = std::max(1, std::min(cdiv(148 * 8, col_blocks), cdiv(M, 128)));
-  int mc = cdiv(cdiv(M, ms), 32) * 32;
-  if (MC) *MC = mc;
-  return cdiv(M, mc);
-}
-static int da_ot(int nout) { return nout <= 16 ? 1 : nout <= 32 ? 2 : 4; }
-static int da_kw(int nout) { return (4 / da_ot(nout)) * 64; }
 size_t lora_scratch_floats(int M, int dim, int nout) {
-  const size_t proj = (size_t)lora_splits(M, dim, nullptr) * M * 64;
-  const size_t db = (size_t)lora_msplit(M, cdiv(dim, 64), nullptr) * dim * nout;
-  size_t da = 0;
-  for (int n = 16; n <= 64; n += 16)  // any output count up to nout
-    if (n - 16 < nout) da = std::max(da, (size_t)lora_msplit(M, cdiv(dim, da_kw(n)), nullptr) * dim * nout);
-  return std::max(proj, std::max(db, da));
+  (void)nout;
+  return (size_t)lora_splits(M, dim, nullptr) * M * 64;
 }
 
 template <bool DU>
@@ -956,7 +728,7 @@ static void lora_proj(const uint16_t *X, int ldx, int M, int K, const LoraSeg &L
   dim3 grid(cdiv(M, 64), ns);
   if (x_f16) lora_part_kernel<DU, true><<<grid, 128, 0, st>>>(X, ldx, M, K, KS, L, part);
   else lora_part_kernel<DU, false><<<grid, 128, 0, st>>>(X, ldx, M, K, KS, L, part);
-  const int64_t n = (int64_t)M * L.Rpad() * 32;  // one warp per output
+  const int64_t n = (int64_t)M * L.Rpad();  // one thread per output
   if (o_f16) launch_pdl(lora_reduce_kernel<DU, true>, dim3(grid_for(n, 256)), dim3(256), 0, st, part, ns, M, L, out_f32, out16, err);
   else launch_pdl(lora_reduce_kernel<DU, false>, dim3(grid_for(n, 256)), dim3(256), 0, st, part, ns, M, L, out_f32, out16, err);
   count_launches(2);
@@ -973,39 +745,6 @@ void k_lora_down(const uint16_t *x, int lda, int M, int K, const LoraSeg &L, flo
 void k_lora_du(const uint16_t *dy, int ldy, int M, const LoraSeg &L, float *du_f32, uint16_t *dul,
                bool dy_f16, bool dul_f16, float *part, cudaStream_t st) {
   lora_proj<true>(dy, ldy, M, seg_cols(L), L, du_f32, dul, dy_f16, dul_f16, part, nullptr, st);
-}
-void k_lora_dB(const uint16_t *dy, int ldy, int M, const float *u_f32, const LoraSeg &L, bool dy_f16,
-               float *part, cudaStream_t st) {
-  if (M <= 0) return;
-  const int Ng = seg_cols(L);
-  int MC;
-  const int ms = lora_msplit(M, cdiv(Ng, 64), &MC);
-  dim3 grid(cdiv(Ng, 64), ms);
-  if (dy_f16) lora_dB_part_kernel<true><<<grid, 128, 0, st>>>(dy, ldy, M, Ng, MC, u_f32, L, part);
-  else lora_dB_part_kernel<false><<<grid, 128, 0, st>>>(dy, ldy, M, Ng, MC, u_f32, L, part);
-  launch_pdl(lora_dB_reduce_kernel, dim3(grid_for((int64_t)Ng * L.r, 256)), dim3(256), 0, st, part, ms, Ng, L);
-  count_launches(2);
-}
-template <int OT>
-static void dA_launch(const float *du, const uint16_t *x, int lda, int M, int K, int MC, int ms,
-                      int nout, bool x_f16, float *part, cudaStream_t st) {
-  dim3 grid(cdiv(K, (4 / OT) * 64), ms);
-  if (x_f16) lora_dA_part_kernel<true, OT><<<grid, 128, 0, st>>>(du, x, lda, M, K, MC, nout, part);
-  else lora_dA_part_kernel<false, OT><<<grid, 128, 0, st>>>(du, x, lda, M, K, MC, nout, part);
-}
-void k_lora_dA(const float *du_f32, const uint16_t *x, int lda, int M, int K, const LoraSeg &L,
-               bool x_f16, float *part, cudaStream_t st) {
-  if (M <= 0) return;
-  const int nout = L.nseg * L.r;
-  int MC;
-  const int ms = lora_msplit(M, cdiv(K, da_kw(nout)), &MC);
-  switch (da_ot(nout)) {
-    case 1: dA_launch<1>(du_f32, x, lda, M, K, MC, ms, nout, x_f16, part, st); break;
-    case 2: dA_launch<2>(du_f32, x, lda, M, K, MC, ms, nout, x_f16, part, st); break;
-    default: dA_launch<4>(du_f32, x, lda, M, K, MC, ms, nout, x_f16, part, st); break;
-  }
-  launch_pdl(lora_dA_reduce_kernel, dim3(grid_for((int64_t)nout * K, 256)), dim3(256), 0, st, part, ms, K, L);
-  count_launches(2);
 }
 void k_pack_fwd(const LoraSeg &L, int Ng, uint16_t *vl, bool f16, cudaStream_t st) {
   const int64_t n = (int64_t)Ng * L.Rpad();

@@ -50,9 +50,9 @@ void k_swiglu_fwd(const uint16_t *gu, int M, int I, uint16_t *act, bool f16, int
 void k_swiglu_bwd(const float *dact, const uint16_t *gu, int M, int I, uint16_t *dgu, bool gu_f16,
                   cudaStream_t st);
 
-// LoRA reductions are split (over K for the projections, over M for the gradients) and the
-// partial sums are added in a fixed order by a second kernel.  Scratch they need, in floats,
-// for M rows, a reduction/output width `dim` and nout = segments * r outputs:
+// The LoRA projections are split over K and the partial sums are added in a fixed order by a
+// second kernel.  Scratch they need, in floats, for M rows, a reduction width `dim` and
+// nout = segments * r outputs:
 int lora_splits(int M, int K, int *KS);
 size_t lora_scratch_floats(int M, int dim, int nout);
 // u = x A^T per segment -> u_f32 [M, nseg*r]; ul = 16-bit(s * u) [M, Rpad] (zero padded)
@@ -61,12 +61,21 @@ void k_lora_down(const uint16_t *x, int lda, int M, int K, const LoraSeg &L, flo
 // du_p = s dY_p B_p -> du_f32 [M, nseg*r]; dul = 16-bit(du) [M, Rpad]
 void k_lora_du(const uint16_t *dy, int ldy, int M, const LoraSeg &L, float *du_f32, uint16_t *dul,
                bool dy_f16, bool dul_f16, float *part, cudaStream_t st);
-// dB_p = s dY_p^T u_p   (written into L.dB)
-void k_lora_dB(const uint16_t *dy, int ldy, int M, const float *u_f32, const LoraSeg &L, bool dy_f16,
-               float *part, cudaStream_t st);
-// dA_p = du_p^T x       (written into L.dA)
-void k_lora_dA(const float *du_f32, const uint16_t *x, int lda, int M, int K, const LoraSeg &L,
-               bool x_f16, float *part, cudaStream_t st);
+// The LoRA gradients of one fused group: dB_p = s dY_p^T u_p and dA_p = du_p^T x for its
+// segments, written into (or, with L.accumulate, added to) L.dB / L.dA.
+struct LoraGradGroup {
+  LoraSeg L;
+  const uint16_t *dy = nullptr;  // bf16 dY [M, Ng], row stride ldy
+  int ldy = 0, Ng = 0;
+  const float *u = nullptr;      // [M, nseg r]: x A^T
+  const float *du = nullptr;     // [M, nseg r]: s dY B
+  const uint16_t *x = nullptr;   // 16-bit x [M, K] (half if x_f16), row stride ldx
+  int ldx = 0, K = 0;
+};
+// Gradients of up to four groups in one launch (lora_grad.cu): per 64-column tile of each
+// product a cluster of 8 CTAs splits the tokens and sums its partial tiles in rank order
+// through distributed shared memory (no global scratch, fixed summation order).
+void k_lora_grads(const LoraGradGroup *groups, int ngroups, int M, bool x_f16, cudaStream_t st);
 // Vl [Ng, Rpad]: row n of segment p holds 16-bit(B_p[n - off_p, :]) at columns p*r .. p*r+r-1
 void k_pack_fwd(const LoraSeg &L, int Ng, uint16_t *vl, bool f16, cudaStream_t st);
 // Acat [Rpad, K]: row p*r + j holds 16-bit(A_p[j, :]); rows past nseg*r are zero

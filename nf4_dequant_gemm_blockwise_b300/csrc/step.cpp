@@ -31,10 +31,10 @@ namespace soup {
 
 const char *const kFamName[FAM_COUNT] = {
     "embed", "rmsnorm_fwd", "rmsnorm_bwd", "rope_fwd", "rope_bwd", "swiglu_fwd", "swiglu_bwd",
-    "attn_fwd", "attn_bwd", "cast_bf16", "lora_pack", "lora_down", "lora_du", "lora_dB", "lora_dA",
+    "attn_fwd", "attn_bwd", "cast_bf16", "lora_pack", "lora_down", "lora_du", "lora_grad",
     "gemm_fwd_qkv", "gemm_fwd_o", "gemm_fwd_gate_up", "gemm_fwd_down", "gemm_dx_qkv", "gemm_dx_o",
     "gemm_dx_gate_up", "gemm_dx_down", "head_gemm", "head_dx", "ce_fwd", "ce_bwd"};
-const int kFamTensor[FAM_COUNT] = {0, 0, 0, 0, 0, 0, 0, 1, 1, 0, 0, 0, 0, 0, 0,
+const int kFamTensor[FAM_COUNT] = {0, 0, 0, 0, 0, 0, 0, 1, 1, 0, 0, 0, 0, 0,
                                    1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 0, 0};
 
 static uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
@@ -109,7 +109,7 @@ int make_plan(const soup_cfg *c, int maxB, int maxS, int n_slots, int mode, Plan
   P->dqkv = take(4 * M * nqkv);
   P->dqkv_b = take(2 * M * nqkv);
   P->attn_scratch = take(4 * attn_bwd_scratch_floats(maxB, maxS, c->n_heads, c->head_dim));
-  P->du_f32 = take(4 * M * 64);
+  for (int g = 0; g < 4; ++g) P->du_f32[g] = take(4 * M * 64);
   P->du_b = take(2 * M * 64);
   {
     const int dims[5] = {(int)H, (int)qd, (int)I, (int)nqkv, (int)(2 * I)};
@@ -559,33 +559,61 @@ int layer_forward(soup_stream *h, int li, const uint8_t *shard, int slot, bool r
   return check_cuda("layer forward");
 }
 
-// Backward of one projection group: LoRA gradients and dX (= dY W + s (dY B) A, float out).
+// Backward of one projection group: du = s dY B (kept per group for the layer's gradient
+// launch) and dX = dY W + s (dY B) A (float out).
 int group_backward(soup_stream *h, int li, const uint8_t *shard, int grp, const uint16_t *dy,
-                   int ldy, const uint16_t *x, int ldx, float *dx_out) {
+                   int ldy, float *dx_out) {
   const Plan &P = h->plan;
-  const LayerBufs Lb = bufs_of(h, li);
   cudaStream_t st = h->cs;
   const int M = h->B * h->S;
   LoraSeg L = make_seg(h, li, grp, true);
   const int K = h->lay.n_in[grp];
-  // gradients travel in bf16; the layer inputs x are the forward's half tensors
+  // gradients travel in bf16
   const int Ng = h->lay.n_out[grp];
   const double nr = (double)L.nseg * L.r, dM = M;
   SOUP_TRY(prof(h, FAM_LORA_DU, 2.0 * dM * Ng * L.r,
                 2.0 * dM * Ng + 4.0 * Ng * L.r + 4.0 * dM * nr + 2.0 * dM * L.Rpad(), [&] {
-                  k_lora_du(dy, ldy, M, L, F(h, P.du_f32), B16(h, P.du_b), false, false, F(h, P.lora_part), st);
+                  k_lora_du(dy, ldy, M, L, F(h, P.du_f32[grp]), B16(h, P.du_b), false, false, F(h, P.lora_part), st);
                 }));
   GemmArgs g = weight_args(h, shard, grp, GEMM_DX);
   g.M = M; g.a = dy; g.lda = ldy;
   g.ul = B16(h, P.du_b); g.vl = B16(h, P.ac[(size_t)li * 4 + grp]); g.R = L.Rpad();
-  g.lora_u = F(h, P.du_f32); g.lseg = L; g.after_lora = 1;
+  g.lora_u = F(h, P.du_f32[grp]); g.lseg = L; g.after_lora = 1;
   g.epi = EPI_F32; g.out = dx_out; g.ldo = K;
   SOUP_TRY(timed_gemm(h, g, grp));
-  SOUP_TRY(prof(h, FAM_LORA_DB, 2.0 * dM * Ng * L.r, 2.0 * dM * Ng + 4.0 * dM * nr + 4.0 * Ng * L.r,
-                [&] { k_lora_dB(dy, ldy, M, F(h, Lb.u_f32[grp]), L, false, F(h, P.lora_part), st); }));
-  SOUP_TRY(prof(h, FAM_LORA_DA, 2.0 * dM * K * nr, 4.0 * dM * nr + 2.0 * dM * K + 4.0 * nr * K,
-                [&] { k_lora_dA(F(h, P.du_f32), x, ldx, M, K, L, true, F(h, P.lora_part), st); }));
   return 0;
+}
+
+// The LoRA gradients (dB and dA) of all four groups of layer li in one launch, from the
+// groups' upstream gradients, inputs, u and du, all still intact at the end of the layer.
+int layer_lora_grads(soup_stream *h, int li) {
+  const Plan &P = h->plan;
+  const LayerBufs Lb = bufs_of(h, li);
+  const soup_cfg &c = h->cfg;
+  const int M = h->B * h->S, H = c.hidden, I = c.inter, qd = c.n_heads * c.head_dim;
+  const int nqkv = h->lay.n_out[SOUP_G_QKV];
+  const uint16_t *dy[4] = {B16(h, P.dqkv_b), B16(h, P.dhm_b), B16(h, P.dgu), B16(h, P.dh_b)};
+  const int ldy[4] = {nqkv, H, 2 * I, H};
+  const uint16_t *x[4] = {B16(h, Lb.x1), B16(h, Lb.att), B16(h, Lb.x2), B16(h, Lb.act)};
+  const int ldx[4] = {H, qd, H, I};
+  LoraGradGroup G[4];
+  double flops = 0, bytes = 0;
+  for (int g = 0; g < 4; ++g) {
+    G[g].L = make_seg(h, li, g, true);
+    G[g].dy = dy[g];
+    G[g].ldy = ldy[g];
+    G[g].Ng = h->lay.n_out[g];
+    G[g].u = F(h, Lb.u_f32[g]);
+    G[g].du = F(h, P.du_f32[g]);
+    G[g].x = x[g];
+    G[g].ldx = ldx[g];
+    G[g].K = h->lay.n_in[g];
+    const double nr = (double)G[g].L.nseg * G[g].L.r;
+    flops += 2.0 * M * G[g].Ng * G[g].L.r + 2.0 * M * G[g].K * nr;
+    bytes += 2.0 * M * G[g].Ng + 4.0 * M * nr + 4.0 * G[g].Ng * G[g].L.r +  // dB: dY, u, dB
+             4.0 * M * nr + 2.0 * M * G[g].K + 4.0 * nr * G[g].K;             // dA: du, x, dA
+  }
+  return prof(h, FAM_LORA_GRAD, flops, bytes, [&] { k_lora_grads(G, 4, M, true, h->cs); });
 }
 
 // Backward of layer li; releases each chunk after its last reader (the dX GEMM of its group,
@@ -604,19 +632,19 @@ int layer_backward(soup_stream *h, int li, const uint8_t *shard, int slot) {
 
   // dh / dh_b hold dL/dh_{li+1}
   SOUP_TRY(use_chunk(h, slot, SOUP_G_DOWN));
-  SOUP_TRY(group_backward(h, li, shard, SOUP_G_DOWN, B16(h, P.dh_b), H, B16(h, Lb.act), I, F(h, P.dact)));
+  SOUP_TRY(group_backward(h, li, shard, SOUP_G_DOWN, B16(h, P.dh_b), H, F(h, P.dact)));
   SOUP_TRY(release_chunk(h, slot, SOUP_G_DOWN));
   const double dM = M, dH = H, dI = I;
   SOUP_TRY(prof(h, FAM_SWIGLU_BWD, 0, 12.0 * dM * dI,
                 [&] { k_swiglu_bwd(F(h, P.dact), B16(h, Lb.gu), M, I, B16(h, P.dgu), true, st); }));
   SOUP_TRY(use_chunk(h, slot, SOUP_G_GU));
-  SOUP_TRY(group_backward(h, li, shard, SOUP_G_GU, B16(h, P.dgu), 2 * I, B16(h, Lb.x2), H, F(h, P.dx)));
+  SOUP_TRY(group_backward(h, li, shard, SOUP_G_GU, B16(h, P.dgu), 2 * I, F(h, P.dx)));
   SOUP_TRY(prof(h, FAM_RMSNORM_BWD, 0, 18.0 * dM * dH + 2.0 * dH, [&] {
     k_rmsnorm_bwd(F(h, P.dx), F(h, Lb.hm), ln2, c.rms_eps, M, H, F(h, P.dh), F(h, P.dhm), B16(h, P.dhm_b), st);
   }));
   SOUP_TRY(release_chunk(h, slot, SOUP_G_GU));
   SOUP_TRY(use_chunk(h, slot, SOUP_G_O));
-  SOUP_TRY(group_backward(h, li, shard, SOUP_G_O, B16(h, P.dhm_b), H, B16(h, Lb.att), qd, F(h, P.datt)));
+  SOUP_TRY(group_backward(h, li, shard, SOUP_G_O, B16(h, P.dhm_b), H, F(h, P.datt)));
   SOUP_TRY(release_chunk(h, slot, SOUP_G_O));
   SOUP_TRY(prof(h, FAM_CAST, 0, 6.0 * dM * qd,
                 [&] { k_cast_bf16(F(h, P.datt), B16(h, P.datt_b), (int64_t)M * qd, st); }));
@@ -632,7 +660,10 @@ int layer_backward(soup_stream *h, int li, const uint8_t *shard, int slot) {
                c.n_heads, c.n_kv_heads, c.head_dim, st);
   }));
   SOUP_TRY(use_chunk(h, slot, SOUP_G_QKV));
-  SOUP_TRY(group_backward(h, li, shard, SOUP_G_QKV, B16(h, P.dqkv_b), nqkv, B16(h, Lb.x1), H, F(h, P.dx)));
+  SOUP_TRY(group_backward(h, li, shard, SOUP_G_QKV, B16(h, P.dqkv_b), nqkv, F(h, P.dx)));
+  // every group's dY, x, u and du are still intact here (the RMSNorm backward below is the
+  // first to overwrite one: dh_b, the down projection's dY)
+  SOUP_TRY(layer_lora_grads(h, li));
   SOUP_TRY(prof(h, FAM_RMSNORM_BWD, 0, 18.0 * dM * dH + 2.0 * dH, [&] {
     k_rmsnorm_bwd(F(h, P.dx), hin, ln1, c.rms_eps, M, H, F(h, P.dhm), F(h, P.dh), B16(h, P.dh_b), st);
   }));

@@ -16,7 +16,8 @@ struct Plan {
   uint64_t slots = 0, h_all = 0, hm = 0, x1 = 0, x2 = 0, qkv = 0, att = 0, lse = 0, gu = 0, act = 0;
   uint64_t u_f32[4] = {0, 0, 0, 0}, u_b[4] = {0, 0, 0, 0};
   uint64_t dh = 0, dhm = 0, dh_b = 0, dhm_b = 0, dact = 0, dgu = 0, dx = 0, datt = 0, datt_b = 0;
-  uint64_t dqkv = 0, dqkv_b = 0, attn_scratch = 0, du_f32 = 0, du_b = 0, lora_part = 0;
+  uint64_t dqkv = 0, dqkv_b = 0, attn_scratch = 0, du_b = 0, lora_part = 0;
+  uint64_t du_f32[4] = {0, 0, 0, 0};  // s dY B per group, kept for the layer's gradient launch
   uint64_t hn = 0, z = 0, dz = 0, dhn = 0, ce_max = 0, ce_sum = 0, ce_lab = 0, ce_lse = 0;
   std::vector<uint64_t> vl, ac;  // per (layer, group) LoRA operand packs
   uint64_t rope_cos = 0, rope_sin = 0, err = 0;
@@ -46,7 +47,7 @@ struct Slot {
 enum Fam : int {
   FAM_EMBED, FAM_RMSNORM_FWD, FAM_RMSNORM_BWD, FAM_ROPE_FWD, FAM_ROPE_BWD, FAM_SWIGLU_FWD,
   FAM_SWIGLU_BWD, FAM_ATTN_FWD, FAM_ATTN_BWD, FAM_CAST, FAM_LORA_PACK, FAM_LORA_DOWN, FAM_LORA_DU,
-  FAM_LORA_DB, FAM_LORA_DA, FAM_GEMM_FWD_QKV, FAM_GEMM_FWD_O, FAM_GEMM_FWD_GU, FAM_GEMM_FWD_DOWN,
+  FAM_LORA_GRAD, FAM_GEMM_FWD_QKV, FAM_GEMM_FWD_O, FAM_GEMM_FWD_GU, FAM_GEMM_FWD_DOWN,
   FAM_GEMM_DX_QKV, FAM_GEMM_DX_O, FAM_GEMM_DX_GU, FAM_GEMM_DX_DOWN, FAM_HEAD_GEMM, FAM_HEAD_DX,
   FAM_CE_FWD, FAM_CE_BWD, FAM_COUNT
 };
