@@ -361,6 +361,39 @@ int soup_proj_fwd_noalloc(const uint16_t *x, int M, int N, int K, const uint8_t 
  * nothing; like the first call, its first use on a device looks up the array's address. */
 int soup_proj_noalloc_status(uintptr_t stream);
 
+/* ------------------------------------------------------------------ attention, on its own */
+
+/* Causal grouped-query attention of one decoder layer, the kernels the step runs ("Layer
+ * streaming: fine-tune a model that does not fit in your card", "How it works": the family's
+ * own decoder layer, run unchanged): query head h reads key/value head floor(h * n_kv / n_h),
+ *   o = softmax(q k^T / sqrt(d) + causal mask) v,
+ * per sequence b of B and head, over S positions.
+ *   qkv: dev IEEE half [B * S, (n_heads + 2 n_kv_heads) * head_dim], row b * S + t holds the
+ *        q heads, then the k heads, then the v heads of position t (rotary embedding already
+ *        applied), 16-byte aligned.
+ *   o:   dev half [B * S, n_heads * head_dim] (written);
+ *   lse: dev float [B, n_heads, S] (written): log2 of the row's sum of exp2(score * log2(e)
+ *        / sqrt(d) - max) plus the max, in base-2 units of the scaled score.
+ *   err: dev int the kernels OR error bits into (1: a bounded wait gave up; 4 is not used
+ *        here), or NULL.  head_dim 64 or 128; n_heads a multiple of n_kv_heads.  With
+ *        head_dim 64 or 128 and at most 8 query heads per key/value head the tcgen05 kernels
+ *        run; otherwise the warp-level MMA kernels.  B == 0 or S == 0 does nothing.
+ * Asynchronous on `stream`; SOUP_EINVAL for bad shapes or NULL buffers. */
+int soup_attn_fwd(const uint16_t *qkv, int B, int S, int n_heads, int n_kv_heads, int head_dim,
+                  uint16_t *o, float *lse, int *err, uintptr_t stream);
+/* Scratch soup_attn_bwd needs for this shape (0 for a bad shape). */
+uint64_t soup_attn_bwd_scratch_bytes(int B, int S, int n_heads, int n_kv_heads, int head_dim);
+/* Backward of soup_attn_fwd: dqkv (dev float [B * S, (n_heads + 2 n_kv_heads) * head_dim],
+ * written completely) = dL/dq, dL/dk, dL/dv in qkv's layout, from the forward's qkv, o and lse
+ * and dO = dL/do (dev bf16 [B * S, n_heads * head_dim]).  The probabilities are recomputed from
+ * half q, k and lse; every product with a gradient is formed from bf16 operands with float
+ * accumulation.  Deterministic: the key/value gradients of the query heads that share a
+ * key/value head are summed in head order.  scratch: dev, 256-byte aligned, at least
+ * soup_attn_bwd_scratch_bytes; err as for soup_attn_fwd.  Asynchronous on `stream`. */
+int soup_attn_bwd(const uint16_t *qkv, const uint16_t *o, const uint16_t *dO, const float *lse, int B,
+                  int S, int n_heads, int n_kv_heads, int head_dim, void *scratch,
+                  uint64_t scratch_bytes, float *dqkv, int *err, uintptr_t stream);
+
 /* ------------------------------------------------------------------ optimizer */
 
 /* AdamW hyper-parameters.  grad_scale multiplies the gradient before it enters the moments

@@ -113,6 +113,9 @@ def _load() -> C.CDLL:
         "soup_proj_fwd_noalloc": (I32, [P, I32, I32, I32, P, P, P, P, P, I32, F32, I32, P, C.c_size_t]),
         "soup_proj_status": (I32, [P, I32, I32, I32, C.c_size_t]),
         "soup_proj_noalloc_status": (I32, [C.c_size_t]),
+        "soup_attn_fwd": (I32, [P, I32, I32, I32, I32, I32, P, P, P, C.c_size_t]),
+        "soup_attn_bwd_scratch_bytes": (U64, [I32, I32, I32, I32, I32]),
+        "soup_attn_bwd": (I32, [P, P, P, P, I32, I32, I32, I32, I32, P, U64, P, P, C.c_size_t]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -368,6 +371,24 @@ def proj_noalloc_status(stream=0):
     """Wait for `stream` and raise if a proj_fwd_noalloc call since the last check reported a
     kernel error (bounded wait given up, half-precision overflow); clears the shared flag."""
     _check(lib.soup_proj_noalloc_status(_stream(stream)))
+
+
+def attn_fwd(qkv, B, S, n_heads, n_kv_heads, head_dim, o, lse, err=None, stream=0):
+    """Causal GQA attention of one layer (soup_attn_fwd): qkv half [B*S, (nh + 2 nkv) d] ->
+    o half [B*S, nh d], lse float [B, nh, S]; err: optional device int32 for error bits."""
+    _check(lib.soup_attn_fwd(_ptr(qkv), B, S, n_heads, n_kv_heads, head_dim, _ptr(o), _ptr(lse),
+                             _ptr(err), _stream(stream)))
+
+
+def attn_bwd_scratch_bytes(B, S, n_heads, n_kv_heads, head_dim) -> int:
+    return int(lib.soup_attn_bwd_scratch_bytes(B, S, n_heads, n_kv_heads, head_dim))
+
+
+def attn_bwd(qkv, o, dO, lse, B, S, n_heads, n_kv_heads, head_dim, scratch, dqkv, err=None, stream=0):
+    """Backward of attn_fwd (soup_attn_bwd): dO bf16 [B*S, nh d] -> dqkv float in qkv's layout."""
+    _check(lib.soup_attn_bwd(_ptr(qkv), _ptr(o), _ptr(dO), _ptr(lse), B, S, n_heads, n_kv_heads,
+                             head_dim, _ptr(scratch), scratch.numel() * scratch.element_size(),
+                             _ptr(dqkv), _ptr(err), _stream(stream)))
 
 
 def proj_dx(dy, M, N, K, codes, absmax, w_bf16, A, B, r, s, dx, scratch, stream=0):

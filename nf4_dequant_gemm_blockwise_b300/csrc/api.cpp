@@ -371,6 +371,46 @@ int soup_proj_status(void *scratch, int M, int N, int K, uintptr_t stream) {
   return kernel_flags_status(flags, "soup_proj_status");
 }
 
+namespace {
+int attn_check(int B, int S, int nh, int nkv, int d) {
+  if (B < 0 || S < 0 || nh < 1 || nkv < 1 || nh % nkv != 0)
+    return set_error(SOUP_EINVAL, "attention: bad shape (B %d, S %d, heads %d / %d)", B, S, nh, nkv);
+  if (d != 64 && d != 128) return set_error(SOUP_EINVAL, "attention: head_dim %d not supported (64 or 128)", d);
+  return 0;
+}
+}  // namespace
+
+uint64_t soup_attn_bwd_scratch_bytes(int B, int S, int n_heads, int n_kv_heads, int head_dim) {
+  if (attn_check(B, S, n_heads, n_kv_heads, head_dim) < 0) return 0;
+  return 4ull * attn_bwd_scratch_floats(B, S, n_heads, n_kv_heads, head_dim);
+}
+
+int soup_attn_fwd(const uint16_t *qkv, int B, int S, int n_heads, int n_kv_heads, int head_dim,
+                  uint16_t *o, float *lse, int *err, uintptr_t stream) {
+  SOUP_TRY(attn_check(B, S, n_heads, n_kv_heads, head_dim));
+  if (B == 0 || S == 0) return 0;
+  if (!qkv || !o || !lse) return set_error(SOUP_EINVAL, "attention: NULL buffer");
+  const int ld = (n_heads + 2 * n_kv_heads) * head_dim;
+  return k_attn_fwd(qkv, ld, B, S, n_heads, n_kv_heads, head_dim, o, lse, err,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+int soup_attn_bwd(const uint16_t *qkv, const uint16_t *o, const uint16_t *dO, const float *lse, int B,
+                  int S, int n_heads, int n_kv_heads, int head_dim, void *scratch,
+                  uint64_t scratch_bytes, float *dqkv, int *err, uintptr_t stream) {
+  SOUP_TRY(attn_check(B, S, n_heads, n_kv_heads, head_dim));
+  if (B == 0 || S == 0) return 0;
+  if (!qkv || !o || !dO || !lse || !dqkv || !scratch) return set_error(SOUP_EINVAL, "attention: NULL buffer");
+  if (reinterpret_cast<uintptr_t>(scratch) % 256) return set_error(SOUP_EINVAL, "attention: scratch must be 256-byte aligned");
+  const uint64_t need = 4ull * attn_bwd_scratch_floats(B, S, n_heads, n_kv_heads, head_dim);
+  if (scratch_bytes < need)
+    return set_error(SOUP_EINVAL, "attention: scratch %llu bytes < %llu", (unsigned long long)scratch_bytes,
+                     (unsigned long long)need);
+  const int ld = (n_heads + 2 * n_kv_heads) * head_dim;
+  return k_attn_bwd(qkv, ld, o, dO, lse, B, S, n_heads, n_kv_heads, head_dim, static_cast<float *>(scratch),
+                    dqkv, err, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int soup_nf4_dequant(const uint8_t *codes, const float *absmax, int64_t n, float *out_f32,
                      uint16_t *out_bf16, uintptr_t stream) {
   if (n < 0 || (n > 0 && (!codes || !absmax))) return set_error(SOUP_EINVAL, "NULL argument");

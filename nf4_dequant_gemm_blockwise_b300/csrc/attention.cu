@@ -1,16 +1,19 @@
-// Causal grouped-query attention, forward and backward, for the decoder layer of the
-// streamed step ("Layer streaming: fine-tune a model that does not fit in your card",
-// "How it works": the family's own decoder layer; query head h reads key/value head
-// floor(h * n_kv / n_h); softmax(q k^T / sqrt(d) + causal mask) v).
+// Causal grouped-query attention, forward and backward, on the warp-level tensor-core MMA
+// (m16n8k16): the path for the shapes the tcgen05 kernels (attention_tc.cu) do not take, a
+// head dimension other than 64 or 128 or more than 8 query heads per key/value head
+// ("Layer streaming: fine-tune a model that does not fit in your card", "How it works": the
+// family's own decoder layer; query head h reads key/value head floor(h * n_kv / n_h);
+// softmax(q k^T / sqrt(d) + causal mask) v).
 //
 // Flash-style tiling: the S x S score matrix is never stored.  The forward keeps a running
 // row max and sum per query row and writes the base-2 log-sum-exp; the backward recomputes
-// the probabilities from it.  Tiles use the warp-level tensor-core MMA (m16n8k16, float
-// accumulation).  q, k, v and the output are IEEE half (the forward's operand format); the
-// backward recomputes the scores from the same half q and k, then forms every product with
-// a gradient in bf16 (v, k and q are converted to bf16 when they are staged).  Determinism: every output element is accumulated by one thread in a
-// fixed order; the key/value gradients of the heads that share a key/value head are summed
-// by a separate kernel in head order (no atomics).
+// the probabilities from it.  q, k, v and the output are IEEE half (the forward's operand
+// format); the backward recomputes the scores from the same half q and k, then forms every
+// product with a gradient in bf16 (v, k and q are converted to bf16 when they are staged).
+// Determinism: every output element is accumulated by one thread in a fixed order; the
+// key/value gradients of the heads that share a key/value head are summed by a separate
+// kernel in head order (no atomics).
+#include <algorithm>
 #include <cmath>
 
 #include "common.cuh"
@@ -483,12 +486,15 @@ int attn_bwd_impl(const uint16_t *qkv, int ld, const uint16_t *o, const uint16_t
 
 }  // namespace
 
-size_t attn_bwd_scratch_floats(int B, int S, int nh, int d) {
-  return (size_t)B * nh * S * (1 + 2 * (size_t)d);
+size_t attn_bwd_scratch_floats(int B, int S, int nh, int nkv, int d) {
+  const size_t mma = (size_t)B * nh * S * (1 + 2 * (size_t)d);
+  return std::max(mma, attn_tc_scratch_floats(B, S, nh, nkv, d));
 }
 
 int k_attn_fwd(const uint16_t *qkv, int ld, int B, int S, int nh, int nkv, int d, uint16_t *o,
-               float *lse, cudaStream_t st) {
+               float *lse, int *err, cudaStream_t st) {
+  if (B <= 0 || S <= 0) return 0;
+  if (attn_tc_eligible(d, nh, nkv)) return k_attn_fwd_tc(qkv, ld, B, S, nh, nkv, d, o, lse, err, st);
   const float scale_log2 = (1.0f / sqrtf((float)d)) * 1.4426950408889634f;
   dim3 grid((S + 63) / 64, nh, B);
   if (d == 128) attn_fwd_kernel<128, true><<<grid, 128, 0, st>>>(qkv, ld, S, nh, nkv, o, lse, scale_log2);
@@ -502,7 +508,10 @@ int k_attn_fwd(const uint16_t *qkv, int ld, int B, int S, int nh, int nkv, int d
 
 int k_attn_bwd(const uint16_t *qkv, int ld, const uint16_t *o, const uint16_t *dO,
                const float *lse, int B, int S, int nh, int nkv, int d, float *scratch, float *dqkv,
-               cudaStream_t st) {
+               int *err, cudaStream_t st) {
+  if (B <= 0 || S <= 0) return 0;
+  if (attn_tc_eligible(d, nh, nkv))
+    return k_attn_bwd_tc(qkv, ld, o, dO, lse, B, S, nh, nkv, d, scratch, dqkv, err, st);
   if (d == 128) return attn_bwd_impl<128>(qkv, ld, o, dO, lse, B, S, nh, nkv, scratch, dqkv, st);
   if (d == 64) return attn_bwd_impl<64>(qkv, ld, o, dO, lse, B, S, nh, nkv, scratch, dqkv, st);
   return set_error(SOUP_EINVAL, "attention: head_dim %d not supported (64 or 128)", d);

@@ -131,6 +131,15 @@ SOUP_DEV void tma_load_2d(void *smem_dst, const CUtensorMap *m, int c0, int c1, 
       : "memory");
 }
 
+// 3-D tiled load: c0 innermost (elements), c1 row, c2 outermost (e.g. the sequence of a batch).
+SOUP_DEV void tma_load_3d(void *smem_dst, const CUtensorMap *m, int c0, int c1, int c2, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // ------------------------------------------------------------------ tcgen05
 SOUP_DEV void tc_alloc(uint32_t *smem_slot, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -187,6 +196,13 @@ SOUP_DEV void tc_ld_32x32b_x8(uint32_t taddr, uint32_t (&r)[8]) {
                : "memory");
 }
 SOUP_DEV void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Offset of 16-byte chunk c of row r inside a 128-byte-swizzled tile (rows of 128 bytes,
+// 8-row atoms of 1024 bytes): the layout a SWIZZLE_128B TMA copy writes into a 1024-byte
+// aligned destination and the tensor core reads through smem_desc.
+SOUP_DEV uint32_t sw128(int r, int c) {
+  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
 
 // Shared-memory matrix descriptor (tcgen05): start address, leading/stride byte offsets,
 // fixed version field 1 at bit 46, swizzle mode in bits 61-63 (2 = 128-byte swizzle).

@@ -126,12 +126,6 @@ SOUP_DEV void dq_block64(const float *cb, const uint32_t (&cw)[8], float a, uint
   }
 }
 
-// Offset of 16-byte chunk c of row r inside a 128-byte-swizzled tile (rows of 128 bytes,
-// 8-row atoms of 1024 bytes).
-SOUP_DEV uint32_t sw128(int r, int c) {
-  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
-}
-
 template <int BN, int BMODE, int EPI, bool F16, int MT>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
@@ -715,6 +709,22 @@ int tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t i
             const char *what) {
   SOUP_TRY(get_encode());
   return make_map(m, dt, base, inner, outer, row_bytes, box_inner, box_outer, sw, what);
+}
+
+int tmap_3d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t d0, uint64_t d1,
+            uint64_t d2, uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1,
+            CUtensorMapSwizzle sw, const char *what) {
+  SOUP_TRY(get_encode());
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {stride1, stride2};
+  cuuint32_t box[3] = {box0, box1, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, dt, 3, const_cast<void *>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return set_error(SOUP_EINVAL, "tensor map for %s rejected (CUresult %d)", what, (int)r);
+  return 0;
 }
 
 // Tiling of one call: m-tiles per CTA (1 or 2) and split-K factor (1..4), minimising a model

@@ -87,6 +87,13 @@ int tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t i
             uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw,
             const char *what);
 
+// 3-D tiled TMA tensor map of a row-major [d2, d1, d0] array (rows of d0 elements stride1
+// bytes apart, d1 rows per outer index, outer indices stride2 bytes apart), box
+// [1, box1, box0]; rows past d1 read as zero.  0 or SOUP_E* with the message set.
+int tmap_3d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t d0, uint64_t d1,
+            uint64_t d2, uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1,
+            CUtensorMapSwizzle sw, const char *what);
+
 // Small-M path (1 <= M <= 16, NF4 weights; forward on half activations, dX on bf16
 // gradients): weight-stationary mma.sync kernels, stream-K over the weight.  gemm_launch takes
 // it whenever gemv_eligible() holds.

@@ -106,15 +106,24 @@ void k_nf4_dequant(const uint8_t *codes, const float *absmax, int64_t n, float *
 
 // Causal GQA attention on the fused half-precision qkv buffer [M, ld] (q heads, then k heads,
 // then v heads, each head_dim wide), rows b*S + t.  o: half [M, nh*d]; lse: float [B*nh*S]
-// (base-2 log-sum of exp2(scale*log2e*score)).  head_dim 64 or 128.
+// (base-2 log-sum of exp2(scale*log2e*score)).  head_dim 64 or 128.  The tcgen05 kernels
+// (attention_tc.cu) take head_dim 64 / 128 with at most 8 query heads per key/value head; other
+// shapes run the warp-level MMA kernels (attention.cu).  err: device int for error bits, or NULL.
 int k_attn_fwd(const uint16_t *qkv, int ld, int B, int S, int nh, int nkv, int d, uint16_t *o,
-               float *lse, cudaStream_t st);
+               float *lse, int *err, cudaStream_t st);
 // o: half [M, nh*d] (the forward output); dO: bf16 [M, nh*d]; dqkv: float [M, ld] written
-// completely (dq, dk, dv);
-// scratch: float [attn_bwd_scratch_floats()].
-size_t attn_bwd_scratch_floats(int B, int S, int nh, int d);
+// completely (dq, dk, dv); scratch: float [attn_bwd_scratch_floats()], 256-byte aligned.
+size_t attn_bwd_scratch_floats(int B, int S, int nh, int nkv, int d);
 int k_attn_bwd(const uint16_t *qkv, int ld, const uint16_t *o, const uint16_t *dO,
                const float *lse, int B, int S, int nh, int nkv, int d, float *scratch, float *dqkv,
-               cudaStream_t st);
+               int *err, cudaStream_t st);
+// the tcgen05 path (attention_tc.cu)
+int attn_tc_eligible(int d, int nh, int nkv);
+size_t attn_tc_scratch_floats(int B, int S, int nh, int nkv, int d);
+int k_attn_fwd_tc(const uint16_t *qkv, int ld, int B, int S, int nh, int nkv, int d, uint16_t *o,
+                  float *lse, int *err, cudaStream_t st);
+int k_attn_bwd_tc(const uint16_t *qkv, int ld, const uint16_t *o, const uint16_t *dO,
+                  const float *lse, int B, int S, int nh, int nkv, int d, float *scratch,
+                  float *dqkv, int *err, cudaStream_t st);
 
 }  // namespace soup

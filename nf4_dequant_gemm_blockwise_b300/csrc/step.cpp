@@ -108,7 +108,7 @@ int make_plan(const soup_cfg *c, int maxB, int maxS, int n_slots, int mode, Plan
   P->datt_b = take(2 * M * qd);
   P->dqkv = take(4 * M * nqkv);
   P->dqkv_b = take(2 * M * nqkv);
-  P->attn_scratch = take(4 * attn_bwd_scratch_floats(maxB, maxS, c->n_heads, c->head_dim));
+  P->attn_scratch = take(4 * attn_bwd_scratch_floats(maxB, maxS, c->n_heads, c->n_kv_heads, c->head_dim));
   for (int g = 0; g < 4; ++g) P->du_f32[g] = take(4 * M * 64);
   P->du_b = take(2 * M * 64);
   {
@@ -500,7 +500,7 @@ int layer_forward(soup_stream *h, int li, const uint8_t *shard, int slot, bool r
   int arc = 0;
   SOUP_TRY(prof(h, FAM_ATTN_FWD, attn_flops(c, B, S, 2), 2.0 * dM * (nqkv + qd) + 4.0 * dM * c.n_heads, [&] {
     arc = k_attn_fwd(B16(h, Lb.qkv), nqkv, B, S, c.n_heads, c.n_kv_heads, c.head_dim, B16(h, Lb.att),
-                     F(h, Lb.lse), st);
+                     F(h, Lb.lse), h->err_dev, st);
   }));
   SOUP_TRY(arc);
   if (ad)
@@ -652,7 +652,8 @@ int layer_backward(soup_stream *h, int li, const uint8_t *shard, int slot) {
   SOUP_TRY(prof(h, FAM_ATTN_BWD, attn_flops(c, B, S, 5),
                 2.0 * dM * nqkv + 4.0 * dM * qd + 4.0 * dM * c.n_heads + 4.0 * dM * nqkv, [&] {
                   arc = k_attn_bwd(B16(h, Lb.qkv), nqkv, B16(h, Lb.att), B16(h, P.datt_b), F(h, Lb.lse), B, S,
-                                   c.n_heads, c.n_kv_heads, c.head_dim, F(h, P.attn_scratch), F(h, P.dqkv), st);
+                                   c.n_heads, c.n_kv_heads, c.head_dim, F(h, P.attn_scratch), F(h, P.dqkv),
+                                   h->err_dev, st);
                 }));
   SOUP_TRY(arc);
   SOUP_TRY(prof(h, FAM_ROPE_BWD, 0, 6.0 * dM * nqkv, [&] {
