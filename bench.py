@@ -106,6 +106,9 @@ def _args():
     p.add_argument("--micro-shape", default="14336x4096,4096x14336", help="NxK list")
     p.add_argument("--micro-m", default="1,16,128,512,2048,8192")
     p.add_argument("--micro-iters", type=int, default=10)
+    p.add_argument("--micro-attn", default=None, metavar="BxSxHxKVxD,...",
+                   help="attention microbench instead of the step: forward and backward of causal GQA "
+                        "attention at each shape, e.g. 1x512x32x8x128 (the 8B layer at B=1, S=512)")
     return p.parse_args()
 
 
@@ -375,6 +378,56 @@ def run_micro(args):
             if not args.no_cpu_baseline:
                 out["cpu_baseline"] = run_micro_oracle(N, K, M, r, s, codes, absmax, A, B)
             print(json.dumps(out), flush=True)
+
+
+def run_micro_attn(args):
+    """Causal GQA attention alone (soup_attn_fwd / soup_attn_bwd), each call timed with CUDA
+    events after an L2 flush; flops count the causal half of every S x S x d product (2 in the
+    forward; 5 in the backward: score recompute, dP, dV, dQ, dK), as in the step's roofline."""
+    import torch
+
+    from nf4_dequant_gemm_blockwise_b300 import api
+
+    peaks = _peaks()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    st = torch.cuda.current_stream()
+    g = torch.Generator(device="cuda").manual_seed(0)
+    for shp in args.micro_attn.split(","):
+        B, S, nh, nkv, d = (int(v) for v in shp.lower().split("x"))
+        M, ld = B * S, (nh + 2 * nkv) * d
+        qkv = torch.randn((M, ld), generator=g, device="cuda").half().view(torch.int16)
+        o = torch.empty((M, nh * d), dtype=torch.int16, device="cuda")
+        lse = torch.empty((B, nh, S), dtype=torch.float32, device="cuda")
+        do = (torch.randn((M, nh * d), generator=g, device="cuda") * 0.05).bfloat16().view(torch.int16)
+        dqkv = torch.empty((M, ld), dtype=torch.float32, device="cuda")
+        scratch = torch.empty(api.attn_bwd_scratch_bytes(B, S, nh, nkv, d), dtype=torch.uint8, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        calls = {
+            "fwd": (2, lambda: api.attn_fwd(qkv, B, S, nh, nkv, d, o, lse, err, st)),
+            "bwd": (5, lambda: api.attn_bwd(qkv, o, do, lse, B, S, nh, nkv, d, scratch, dqkv, err, st)),
+        }
+        out = {"micro_attn": True, "B": B, "S": S, "n_heads": nh, "n_kv_heads": nkv, "head_dim": d,
+               "path": "tcgen05" if d in (64, 128) and nh % nkv == 0 and nh // nkv <= 8 else "mma.sync"}
+        for name, (mats, fn) in calls.items():
+            for _ in range(3):
+                fn()
+            ts = []
+            for _ in range(args.micro_iters):
+                flush.fill_(1)
+                torch.cuda._sleep(1_000_000)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                fn()
+                e1.record(st)
+                e1.synchronize()
+                ts.append(e0.elapsed_time(e1) * 1e-3)
+            t = statistics.median(ts)
+            flops = float(mats) * B * nh * S * (S + 1) * d
+            out[name] = {"us": t * 1e6, "tflops": flops / t / 1e12, "frac": flops / t / 1e12 / peaks["bf16"]}
+        torch.cuda.synchronize()
+        out["errors"] = int(err.item())
+        out["peak_source"] = f"{peaks['src']}: bf16 burst {peaks['bf16']} TFLOP/s"
+        print(json.dumps(out), flush=True)
 
 
 def run_micro_oracle(N, K, M, r, s, codes, absmax, A, B, cap_rows=512):
@@ -700,6 +753,9 @@ def main():
         dist = td
     if args.impl == "reference":
         run_reference(args, rank)
+    elif args.micro_attn:
+        if rank == 0:
+            run_micro_attn(args)
     elif args.micro:
         if rank == 0:
             run_micro(args)

@@ -24,7 +24,7 @@ LIB = os.path.join(PKG, "libsoup.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", f"-I{INCLUDE}", f"-I{CSRC}"]
-SOURCES = ["gemm.cu", "kernels.cu", "attention.cu", "store.cpp", "step.cpp", "api.cpp", "noalloc.cu", "gemv.cu", "optim.cu", "lora_grad.cu", "attention_tc.cu"]
+SOURCES = ["gemm.cu", "kernels.cu", "attention.cu", "store.cpp", "step.cpp", "api.cpp", "noalloc.cu", "gemv.cu", "optim.cu", "lora_grad.cu", "attention_tc.cu", "lora_proj.cu"]
 
 
 def nvcc() -> str:

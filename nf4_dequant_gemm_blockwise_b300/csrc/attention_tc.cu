@@ -16,10 +16,10 @@
 //   forward  one CTA per (128-query block, head, sequence); key/value blocks of 128 in a
 //            two-stage ring.  S = Q K^T goes to TMEM; each row thread takes its row's max,
 //            exponentials and sum and writes P (half) into shared memory in the swizzled
-//            K-major layout; P V goes to TMEM and is added into the row's output registers
-//            under the running rescale.
+//            K-major layout; P V accumulates into the output in TMEM, rescaled lazily.
 //   dQ       one CTA per (128-query block, head, sequence), key blocks of 64: S = Q K^T and
-//            dP = dO V^T, dS = P (dP - D) written as bf16, dQ += dS K (K read MN-major).
+//            dP = dO V^T (double-buffered in TMEM), dS = P (dP - D) written as bf16 into one of
+//            two shared buffers, dQ += dS K (K read MN-major).
 //   dK, dV   one CTA per (128-key block, query head, sequence), query blocks of 64:
 //            S^T = K Q^T, dP^T = V dO^T, P^T and dS^T written as bf16, dV += P^T dO and
 //            dK += dS^T Q (dO and Q read MN-major).  The query heads that share a key/value
@@ -71,12 +71,19 @@ SOUP_DEV uint4 u4(const uint32_t *p) { return make_uint4(p[0], p[1], p[2], p[3])
 SOUP_DEV bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
 
 // ---------------------------------------------------------------------------------- forward
+// The output accumulates in TMEM across the key blocks (P V with accumulate on).  A row's
+// reference max is raised lazily: only when a block's max exceeds it by more than 2^8 (log2
+// units) is the row's TMEM output rescaled, so P = exp2(s - ref) <= 256 stays exact in half and
+// the final O / l is the same whatever reference was used.  S is read out of TMEM in one batch,
+// which frees it for the next block's Q K^T while the exponentials run.
+constexpr float RESCALE_LOG2 = 8.0f;
+
 template <int D>
 struct Fwd {
   static constexpr int TILE = 128 * D * 2;      // a 128-row Q, K or V tile
   static constexpr int P_BYTES = 128 * 128 * 2;
   static constexpr int SMEM = 5 * TILE + P_BYTES + 1024 + 256;
-  static constexpr uint32_t TMEM_COLS = 256;    // S (128) + P V (D)
+  static constexpr uint32_t TMEM_COLS = 256;    // S (128) + O (D)
 };
 
 template <int D>
@@ -88,8 +95,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t *Qs = smem, *Ks = smem + C::TILE, *Vs = Ks + 2 * C::TILE, *Ps = Vs + 2 * C::TILE;
   uint64_t *bar = reinterpret_cast<uint64_t *>(Ps + C::P_BYTES);
   uint64_t *q_full = bar, *k_full = bar + 1, *v_full = bar + 3, *kv_empty = bar + 5;
-  uint64_t *s_full = bar + 7, *p_full = bar + 8, *pv_full = bar + 9, *mma_done = bar + 10;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 11);
+  uint64_t *s_full = bar + 7, *s_free = bar + 8, *p_full = bar + 9, *pv_done = bar + 10;
+  uint64_t *mma_done = bar + 11;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 12);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -107,8 +115,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&kv_empty[s], 1);
     }
     mbar_init(s_full, 1);
+    mbar_init(s_free, ROWS);
     mbar_init(p_full, ROWS);
-    mbar_init(pv_full, 1);
+    mbar_init(pv_done, 1);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -121,7 +130,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t t_s = tmem, t_pv = tmem + 128;
+  const uint32_t t_s = tmem, t_o = tmem + 128;
 
   if (warp == TMA_WARP) {
     if (lane == 0) {
@@ -174,18 +183,21 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = mbar_wait(q_full, 0, a.err, abort_flag) && issue_s(0);
       for (int j = 0; ok && j < nkb; ++j) {
         const int s = j & 1;
-        // P_j is in shared memory (and S_j has been read out of TMEM)
+        // S_{j+1} as soon as the row threads hold S_j in registers
+        if (j + 1 < nkb) {
+          if (!mbar_wait(s_free, j & 1, a.err, abort_flag) || !issue_s(j + 1)) break;
+        }
+        // P_j is in shared memory (and any rescale of O for block j is done)
         if (!mbar_wait(p_full, j & 1, a.err, abort_flag)) break;
         if (!mbar_wait(&v_full[s], (j >> 1) & 1, a.err, abort_flag)) break;
         tc_fence_after();
         const uint32_t va = smem_u32(Vs + s * C::TILE);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          tc_mma_bf16(t_pv, smem_desc(pa + (kk >> 2) * PANEL128 + (kk & 3) * 32, 16, 1024),
-                      smem_desc(va + kk * 2048, PANEL128, 1024), id_pv, kk > 0);
-        tc_commit(pv_full);
+          tc_mma_bf16(t_o, smem_desc(pa + (kk >> 2) * PANEL128 + (kk & 3) * 32, 16, 1024),
+                      smem_desc(va + kk * 2048, PANEL128, 1024), id_pv, (j | kk) != 0);
+        tc_commit(pv_done);
         tc_commit(&kv_empty[s]);
-        if (j + 1 < nkb) ok = issue_s(j + 1);
       }
       tc_commit(mma_done);
       volatile int no_abort = 0;
@@ -196,10 +208,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int r = threadIdx.x;
     const int row = qb * 128 + r;
     const uint32_t lq = (uint32_t)(warp * 32) << 16;
-    float o[D];
-#pragma unroll
-    for (int i = 0; i < D; ++i) o[i] = 0.f;
-    float m = -INFINITY, l = 0.f;
+    float ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nkb; ++j) {
       if (!warp_all(mbar_wait(s_full, j & 1, a.err, abort_flag))) {
@@ -207,74 +216,117 @@ __global__ void __launch_bounds__(THREADS, 1)
         break;
       }
       tc_fence_after();
+      uint32_t v0[32], v1[32], v2[32], v3[32];
+      __syncwarp();
+      tc_ld_32x32b_x32(t_s + lq, v0);
+      tc_ld_32x32b_x32(t_s + lq + 32, v1);
+      tc_ld_32x32b_x32(t_s + lq + 64, v2);
+      tc_ld_32x32b_x32(t_s + lq + 96, v3);
+      tc_wait_ld();
+      tc_fence_before();
+      mbar_arrive(s_free);  // S_j is in registers: the next block's scores may overwrite it
       // keys j*128 .. j*128 + lim are visible to this row (the causal mask; rows of the last
       // block past S are computed and dropped)
-      const int lim = (j == nkb - 1) ? r : 127;
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        __syncwarp();
-        tc_ld_32x32b_x32(t_s + lq + c * 32, v);
-        tc_wait_ld();
+      // keys after this row are masked to -inf; only the last (diagonal) block has any (rows of
+      // that block past S are computed and dropped)
+      if (j == nkb - 1) {
+        auto mask = [&](uint32_t(&v)[32], int c0) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (c * 32 + i <= lim) mx = fmaxf(mx, __uint_as_float(v[i]));
+          for (int i = 0; i < 32; ++i)
+            if (c0 + i > r) v[i] = 0xff800000u;
+        };
+        mask(v0, 0);
+        mask(v1, 32);
+        mask(v2, 64);
+        mask(v3, 96);
       }
-      const float mnew = fmaxf(m, mx * a.scale_log2);
-      const float mref = mnew == -INFINITY ? 0.f : mnew;
-      const float corr = exp2f(m - mref);
-      m = mnew;
-      l *= corr;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        __syncwarp();
-        tc_ld_32x32b_x32(t_s + lq + c * 32, v);
-        tc_wait_ld();
-        uint32_t pk[16];
+      // independent partial maxima and sums: the row is one thread's work, so the instruction
+      // stream needs the parallelism
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      auto rmax = [&](const uint32_t(&v)[32]) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(v[i]));
+      };
+      rmax(v0);
+      rmax(v1);
+      rmax(v2);
+      rmax(v3);
+      const float mnew = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * a.scale_log2;
+      const bool resc = mnew > ref + RESCALE_LOG2;  // always at the first block (ref = -inf)
+      const float nref = resc ? mnew : ref;
+      const float corr = resc ? ex2(ref - nref) : 1.f;  // 0 at the first block
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[4][16];
+      auto probs = [&](const uint32_t(&v)[32], int c) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int kc = c * 32 + 2 * i;
-          const float p0 = kc <= lim ? exp2f(__uint_as_float(v[2 * i]) * a.scale_log2 - mref) : 0.f;
-          const float p1 = kc + 1 <= lim ? exp2f(__uint_as_float(v[2 * i + 1]) * a.scale_log2 - mref) : 0.f;
-          l += p0 + p1;
-          pk[i] = pack_h2(p0, p1);
+          const float p0 = ex2(fmaf(__uint_as_float(v[2 * i]), a.scale_log2, -nref));
+          const float p1 = ex2(fmaf(__uint_as_float(v[2 * i + 1]), a.scale_log2, -nref));
+          s4[i & 3] += p0 + p1;
+          pk[c][i] = pack_h2(p0, p1);
         }
+      };
+      probs(v0, 0);
+      probs(v1, 1);
+      probs(v2, 2);
+      probs(v3, 3);
+      const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+      l = l * corr + sum;
+      if (j > 0) {
+        // P V of the previous block has finished with P's buffer and with O
+        if (!warp_all(mbar_wait(pv_done, (j - 1) & 1, a.err, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, resc)) {  // the warp rescales its 32 rows of O (corr 1: kept)
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tc_ld_32x32b_x32(t_o + lq + c * 32, o);
+            tc_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+            tc_st_32x32b_x32(t_o + lq + c * 32, o);
+          }
+          tc_wait_st();
+        }
+      }
+      ref = nref;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
         uint8_t *pp = Ps + (c >> 1) * PANEL128;
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          *reinterpret_cast<uint4 *>(pp + sw128(r, (c & 1) * 4 + q)) = u4(pk + 4 * q);
+          *reinterpret_cast<uint4 *>(pp + sw128(r, (c & 1) * 4 + q)) = u4(pk[c] + 4 * q);
       }
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(p_full);
-      if (!warp_all(mbar_wait(pv_full, j & 1, a.err, abort_flag))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        __syncwarp();
-        tc_ld_32x32b_x32(t_pv + lq + c * 32, v);
-        tc_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[c * 32 + i] = o[c * 32 + i] * corr + __uint_as_float(v[i]);
-      }
     }
-    if (ok && !*abort_flag && row < S) {
+    ok = warp_all(ok && mbar_wait(pv_done, (nkb - 1) & 1, a.err, abort_flag) && !*abort_flag);
+    tc_fence_after();
+    if (ok) {
       const float inv = l > 0.f ? 1.0f / l : 0.f;
       uint16_t *dst = a.o + ((size_t)b * S + row) * (size_t)(a.nh * D) + (size_t)h * D;
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        uint32_t w[4];
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        __syncwarp();
+        tc_ld_32x32b_x32(t_o + lq + c * 32, o);  // every lane of the warp; rows < S store
+        tc_wait_ld();
+        if (row < S) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) w[e] = pack_h2(o[8 * c + 2 * e] * inv, o[8 * c + 2 * e + 1] * inv);
-        *reinterpret_cast<uint4 *>(dst + 8 * c) = u4(w);
+          for (int q = 0; q < 4; ++q) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w[e] = pack_h2(__uint_as_float(o[8 * q + 2 * e]) * inv, __uint_as_float(o[8 * q + 2 * e + 1]) * inv);
+            *reinterpret_cast<uint4 *>(dst + c * 32 + 8 * q) = u4(w);
+          }
+        }
       }
-      a.lse[((size_t)b * a.nh + h) * S + row] = m + log2f(l);
+      if (row < S) a.lse[((size_t)b * a.nh + h) * S + row] = ref + log2f(l);
     }
     tc_fence_before();
   }
@@ -327,8 +379,8 @@ struct Dq {
   static constexpr int QT = 128 * D * 2;      // Q (half) or dO (bf16) tile, 128 rows
   static constexpr int KT = 64 * D * 2;       // K or V tile, 64 rows
   static constexpr int STAGE = 3 * KT;        // K half, K bf16, V bf16
-  static constexpr int DS_BYTES = 128 * 64 * 2;
-  static constexpr int SMEM = 2 * QT + 2 * STAGE + DS_BYTES + 1024 + 256;
+  static constexpr int DS_BYTES = 128 * 64 * 2;  // one dS buffer; two alternate
+  static constexpr int SMEM = 2 * QT + 2 * STAGE + 2 * DS_BYTES + 1024 + 256;
   static constexpr uint32_t TMEM_COLS = 512;  // S, dP double-buffered (4 x 64) + dQ (D)
 };
 
@@ -342,11 +394,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1k(smem_raw);
   uint8_t *Qs = smem, *dOs = smem + C::QT, *ring = smem + 2 * C::QT;
-  uint8_t *dSs = ring + 2 * C::STAGE;
-  uint64_t *bar = reinterpret_cast<uint64_t *>(dSs + C::DS_BYTES);
+  uint8_t *dSs = ring + 2 * C::STAGE;  // two buffers: block j writes buffer j & 1
+  uint64_t *bar = reinterpret_cast<uint64_t *>(dSs + 2 * C::DS_BYTES);
   uint64_t *qd_full = bar, *kv_full = bar + 1, *kv_empty = bar + 3, *sd_full = bar + 5;
-  uint64_t *ds_full = bar + 7, *ds_free = bar + 8, *mma_done = bar + 9;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 10);
+  uint64_t *ds_full = bar + 7, *ds_free = bar + 9, *mma_done = bar + 11;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 12);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -362,9 +414,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
       mbar_init(&sd_full[s], 1);
+      mbar_init(&ds_full[s], ROWS);
+      mbar_init(&ds_free[s], 1);
     }
-    mbar_init(ds_full, ROWS);
-    mbar_init(ds_free, 1);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -438,15 +490,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int s = j & 1;
         // the TMEM buffer of block j + 1 was last read by the row threads for block j - 1
         if (j + 1 < nkb && !issue_sd(j + 1)) break;
-        if (!mbar_wait(ds_full, j & 1, a.err, abort_flag)) break;
+        if (!mbar_wait(&ds_full[s], (j >> 1) & 1, a.err, abort_flag)) break;
         tc_fence_after();
         const uint32_t kb16 = smem_u32(ring + s * C::STAGE) + C::KT;
+        const uint32_t dsb = dsa + s * C::DS_BYTES;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          tc_mma_bf16(t_dq, smem_desc(dsa + kk * 32, 16, 1024),
+          tc_mma_bf16(t_dq, smem_desc(dsb + kk * 32, 16, 1024),
                       smem_desc(kb16 + kk * 2048, PANEL64, 1024), id_dq, (j | kk) != 0);
         tc_commit(&kv_empty[s]);
-        tc_commit(ds_free);
+        tc_commit(&ds_free[s]);
       }
       tc_commit(mma_done);
       volatile int no_abort = 0;
@@ -463,21 +516,20 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool ok = true;
     for (int j = 0; j < nkb; ++j) {
       const int s = j & 1;
-      bool w = mbar_wait(&sd_full[s], (j >> 1) & 1, a.err, abort_flag);
-      w = w && (j == 0 || mbar_wait(ds_free, (j - 1) & 1, a.err, abort_flag));
-      if (!warp_all(w)) {
+      if (!warp_all(mbar_wait(&sd_full[s], (j >> 1) & 1, a.err, abort_flag))) {
         ok = false;
         break;
       }
       tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t sv[32], dv[32];
-        __syncwarp();
-        tc_ld_32x32b_x32(tmem + lq + s * 128 + c * 32, sv);
-        tc_ld_32x32b_x32(tmem + lq + s * 128 + 64 + c * 32, dv);
-        tc_wait_ld();
-        uint32_t pk[16];
+      uint32_t s0[32], s1[32], d0[32], d1[32];  // S and dP of this row, one wait for all four
+      __syncwarp();
+      tc_ld_32x32b_x32(tmem + lq + s * 128, s0);
+      tc_ld_32x32b_x32(tmem + lq + s * 128 + 32, s1);
+      tc_ld_32x32b_x32(tmem + lq + s * 128 + 64, d0);
+      tc_ld_32x32b_x32(tmem + lq + s * 128 + 96, d1);
+      tc_wait_ld();
+      uint32_t pk[2][16];
+      auto dsrow = [&](const uint32_t(&sv)[32], const uint32_t(&dv)[32], int c) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int key = j * 64 + c * 32 + 2 * i;
@@ -485,17 +537,27 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const bool vis = key + e <= row && key + e < S && row < S;
-            const float p = vis ? exp2f(__uint_as_float(sv[2 * i + e]) * a.scale_log2 - lse_r) : 0.f;
+            const float p = vis ? ex2(__uint_as_float(sv[2 * i + e]) * a.scale_log2 - lse_r) : 0.f;
             d2[e] = p * (__uint_as_float(dv[2 * i + e]) - ds_r);
           }
-          pk[i] = pack_bf16x2(d2[0], d2[1]);
+          pk[c][i] = pack_bf16x2(d2[0], d2[1]);
         }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4 *>(dSs + sw128(r, c * 4 + q)) = u4(pk + 4 * q);
+      };
+      dsrow(s0, d0, 0);
+      dsrow(s1, d1, 1);
+      // buffer s was last read by the dQ product of block j - 2
+      if (j >= 2 && !warp_all(mbar_wait(&ds_free[s], ((j >> 1) - 1) & 1, a.err, abort_flag))) {
+        ok = false;
+        break;
       }
+      uint8_t *dsb = dSs + s * C::DS_BYTES;
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4 *>(dsb + sw128(r, c * 4 + q)) = u4(pk[c] + 4 * q);
       fence_async_smem();
       tc_fence_before();
-      mbar_arrive(ds_full);
+      mbar_arrive(&ds_full[s]);
     }
     volatile int no_abort = 0;
     ok = warp_all(ok && mbar_wait(mma_done, 0, a.err, &no_abort) && !*abort_flag);
@@ -680,13 +742,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int i = 0; i < nqb; ++i) {
       const int s = i & 1;
       const int q0 = (qfirst + i) * 64;
-      bool w = mbar_wait(&sd_full[s], (i >> 1) & 1, a.err, abort_flag);
-      w = w && (i == 0 || mbar_wait(pds_free, (i - 1) & 1, a.err, abort_flag));
-      if (!warp_all(w)) {
+      if (!warp_all(mbar_wait(&sd_full[s], (i >> 1) & 1, a.err, abort_flag))) {
         ok = false;
         break;
       }
       tc_fence_after();
+      uint32_t ppk[2][16], dpk[2][16];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         // the chunk's 32 query log-sum-exps and row sums: the same addresses across the warp
@@ -703,7 +764,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_ld_32x32b_x32(tmem + lq + s * 128 + c * 32, sv);
         tc_ld_32x32b_x32(tmem + lq + s * 128 + 64 + c * 32, dv);
         tc_wait_ld();
-        uint32_t ppk[16], dpk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           float p2[2], d2[2];
@@ -711,19 +771,26 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int u = 0; u < 2; ++u) {
             const int qi = c * 32 + 2 * e + u, q = q0 + qi;
             const bool vis = q >= key && q < S && key < S;
-            const float p = vis ? exp2f(__uint_as_float(sv[2 * e + u]) * a.scale_log2 - lsv[2 * e + u]) : 0.f;
+            const float p = vis ? ex2(__uint_as_float(sv[2 * e + u]) * a.scale_log2 - lsv[2 * e + u]) : 0.f;
             p2[u] = p;
             d2[u] = p * (__uint_as_float(dv[2 * e + u]) - dsv[2 * e + u]);
           }
-          ppk[e] = pack_bf16x2(p2[0], p2[1]);
-          dpk[e] = pack_bf16x2(d2[0], d2[1]);
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          *reinterpret_cast<uint4 *>(Pt + sw128(r, c * 4 + q)) = u4(ppk + 4 * q);
-          *reinterpret_cast<uint4 *>(dSt + sw128(r, c * 4 + q)) = u4(dpk + 4 * q);
+          ppk[c][e] = pack_bf16x2(p2[0], p2[1]);
+          dpk[c][e] = pack_bf16x2(d2[0], d2[1]);
         }
       }
+      // the dV / dK products of the previous query block have finished with P^T and dS^T
+      if (i >= 1 && !warp_all(mbar_wait(pds_free, (i - 1) & 1, a.err, abort_flag))) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          *reinterpret_cast<uint4 *>(Pt + sw128(r, c * 4 + q)) = u4(ppk[c] + 4 * q);
+          *reinterpret_cast<uint4 *>(dSt + sw128(r, c * 4 + q)) = u4(dpk[c] + 4 * q);
+        }
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(pds_full);
@@ -763,21 +830,30 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int per = (128 + grp - 1) / grp;
     const int r0 = rank * per, r1 = min(128, r0 + per);
     const float *pk[8], *pv[8];
-    for (int c = 0; c < grp; ++c) {
-      pk[c] = cluster.map_shared_rank(red_k, c);
-      pv[c] = cluster.map_shared_rank(red_v, c);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      pk[c] = cluster.map_shared_rank(red_k, c < grp ? c : 0);
+      pv[c] = cluster.map_shared_rank(red_v, c < grp ? c : 0);
     }
     constexpr int C4 = D / 4;
     for (int idx = threadIdx.x; idx < (r1 - r0) * C4; idx += THREADS) {
       const int rr = r0 + idx / C4, c4 = (idx % C4) * 4;
       const int t = k0 + rr;
       if (t >= S) continue;
+      // every remote load in flight before the first add; then the sum in head order
+      float4 xk[8], xv[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        xk[c] = c < grp ? *reinterpret_cast<const float4 *>(pk[c] + rr * C::LDR + c4) : z;
+        xv[c] = c < grp ? *reinterpret_cast<const float4 *>(pv[c] + rr * C::LDR + c4) : z;
+      }
       float4 sk = make_float4(0.f, 0.f, 0.f, 0.f), sv = sk;
-      for (int c = 0; c < grp; ++c) {
-        const float4 x = *reinterpret_cast<const float4 *>(pk[c] + rr * C::LDR + c4);
-        const float4 y = *reinterpret_cast<const float4 *>(pv[c] + rr * C::LDR + c4);
-        sk.x += x.x; sk.y += x.y; sk.z += x.z; sk.w += x.w;
-        sv.x += y.x; sv.y += y.y; sv.z += y.z; sv.w += y.w;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        if (c >= grp) break;
+        sk.x += xk[c].x; sk.y += xk[c].y; sk.z += xk[c].z; sk.w += xk[c].w;
+        sv.x += xv[c].x; sv.y += xv[c].y; sv.z += xv[c].z; sv.w += xv[c].w;
       }
       float *rowp = a.dqkv + ((size_t)b * S + t) * a.ld;
       *reinterpret_cast<float4 *>(rowp + (size_t)(a.nh + g) * D + c4) = sk;

@@ -47,6 +47,14 @@ SOUP_DEV uint32_t pack_h2(float lo, float hi) {
 SOUP_DEV float h16_to_f(uint16_t v) { return __half2float(__ushort_as_half(v)); }
 SOUP_DEV uint16_t f_to_h16(float f) { return __half_as_ushort(__float2half_rn(f)); }
 
+// 2^x on the special-function unit (PTX ex2.approx.ftz.f32): a relative error of a few ulp,
+// far below the 16-bit rounding of the probabilities it produces; 2^-inf = +0.
+SOUP_DEV float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // True when v does not survive a store as IEEE half: NaN, or |v| >= 65520 (which rounds to
 // infinity).  Kernels that store the forward's half operands OR SOUP_KERR_RANGE into their
 // error flag when any value fails; the compare is one instruction, the atomic runs only then.
@@ -196,6 +204,18 @@ SOUP_DEV void tc_ld_32x32b_x8(uint32_t taddr, uint32_t (&r)[8]) {
                : "memory");
 }
 SOUP_DEV void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// Store 32 consecutive f32 columns of this warp's 32 TMEM lanes (one lane per thread).
+SOUP_DEV void tc_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+      "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+      "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+SOUP_DEV void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Offset of 16-byte chunk c of row r inside a 128-byte-swizzled tile (rows of 128 bytes,
 // 8-row atoms of 1024 bytes): the layout a SWIZZLE_128B TMA copy writes into a 1024-byte

@@ -508,32 +508,46 @@ struct PackJobs {
   int n_out[4], n_in[4];
   uint16_t *vl[4], *ac[4];
 };
+// Eight consecutive elements per thread (one 16-byte store); 32-bit index arithmetic (a pack
+// holds well under 2^31 elements).  K % 8 == 0 (checked by the caller) keeps an Acat group in
+// one row; a vl group never leaves its row since Rpad is a multiple of 64.
 __global__ void pack_layer_kernel(const PackJobs J) {
   const int g = blockIdx.y >> 1;
   const LoraSeg &L = J.L[g];
-  const int Rp = L.Rpad();
+  const int Rp = L.Rpad(), nr = L.nseg * L.r;
+  const int stride = gridDim.x * blockDim.x;
   if ((blockIdx.y & 1) == 0) {
-    const int64_t total = (int64_t)J.n_out[g] * Rp;
+    const int per_row = Rp / 8;
+    const int total = J.n_out[g] * per_row;
     uint16_t *vl = J.vl[g];
-    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
-         idx += (int64_t)gridDim.x * blockDim.x) {
-      const int n = (int)(idx / Rp), c = (int)(idx % Rp);
-      float v = 0.f;
-      const int seg = c / L.r;
-      if (seg < L.nseg && n >= L.off[seg] && n < L.off[seg] + L.n[seg])
-        v = L.B[seg][(size_t)(n - L.off[seg]) * L.r + (c % L.r)];
-      vl[idx] = st16<true>(v);
+    for (int it = blockIdx.x * blockDim.x + threadIdx.x; it < total; it += stride) {
+      const int n = it / per_row, c0 = (it - n * per_row) * 8;
+      float v[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int c = c0 + e, seg = c / L.r;
+        v[e] = 0.f;
+        if (c < nr && n >= L.off[seg] && n < L.off[seg] + L.n[seg])
+          v[e] = L.B[seg][(size_t)(n - L.off[seg]) * L.r + (c - seg * L.r)];
+      }
+      *reinterpret_cast<uint4 *>(vl + (size_t)n * Rp + c0) =
+          make_uint4(pack_h2(v[0], v[1]), pack_h2(v[2], v[3]), pack_h2(v[4], v[5]), pack_h2(v[6], v[7]));
     }
   } else {
-    const int K = J.n_in[g];
-    const int64_t total = (int64_t)Rp * K;
+    const int K = J.n_in[g], per_row = K / 8;
+    const int total = Rp * per_row;
     uint16_t *acat = J.ac[g];
-    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
-         idx += (int64_t)gridDim.x * blockDim.x) {
-      const int row = (int)(idx / K), k = (int)(idx % K);
-      float v = 0.f;
-      if (row < L.nseg * L.r) v = L.A[row / L.r][(size_t)(row % L.r) * K + k];
-      acat[idx] = st16<false>(v);
+    for (int it = blockIdx.x * blockDim.x + threadIdx.x; it < total; it += stride) {
+      const int row = it / per_row, k0 = (it - row * per_row) * 8;
+      uint4 o = make_uint4(0, 0, 0, 0);
+      if (row < nr) {
+        const float *src = L.A[row / L.r] + (size_t)(row % L.r) * K + k0;
+        const float4 x0 = *reinterpret_cast<const float4 *>(src);
+        const float4 x1 = *reinterpret_cast<const float4 *>(src + 4);
+        o = make_uint4(pack_bf16x2(x0.x, x0.y), pack_bf16x2(x0.z, x0.w), pack_bf16x2(x1.x, x1.y),
+                       pack_bf16x2(x1.z, x1.w));
+      }
+      *reinterpret_cast<uint4 *>(acat + (size_t)row * K + k0) = o;
     }
   }
 }
@@ -723,6 +737,8 @@ template <bool DU>
 static void lora_proj(const uint16_t *X, int ldx, int M, int K, const LoraSeg &L, float *out_f32,
                       uint16_t *out16, bool x_f16, bool o_f16, float *part, int *err, cudaStream_t st) {
   if (M <= 0) return;
+  // one clustered launch (lora_proj.cu) for the shapes it takes; else partials + ordered reduce
+  if (lora_skinny(DU, X, ldx, M, K, L, out_f32, out16, x_f16, o_f16, err, st) <= 0) return;
   int KS;
   const int ns = lora_splits(M, K, &KS);
   dim3 grid(cdiv(M, 64), ns);
@@ -770,8 +786,21 @@ void k_pack_layer(const LoraSeg (&L)[4], const int n_out[4], const int n_in[4], 
     J.ac[g] = ac[g];
     most = std::max(most, (int64_t)L[g].Rpad() * std::max(n_out[g], n_in[g]));
   }
+  bool vec = true;  // the 8-wide kernel: K % 8, 16-byte aligned A rows and packs
+  for (int g = 0; g < 4; ++g) {
+    vec = vec && n_in[g] % 8 == 0 && (reinterpret_cast<uintptr_t>(vl[g]) & 15) == 0 &&
+          (reinterpret_cast<uintptr_t>(ac[g]) & 15) == 0;
+    for (int p = 0; p < L[g].nseg; ++p) vec = vec && (reinterpret_cast<uintptr_t>(L[g].A[p]) & 15) == 0;
+  }
+  if (!vec) {  // element by element, pack by pack
+    for (int g = 0; g < 4; ++g) {
+      k_pack_fwd(L[g], n_out[g], vl[g], true, st);
+      k_pack_bwd(L[g], n_in[g], ac[g], false, st);
+    }
+    return;
+  }
   // enough blocks for the largest pack, at most two waves per job
-  const int bx = std::min(grid_for(most, 256), 148 * 2);
+  const int bx = std::min(grid_for(most / 8, 256), 148 * 2);
   pack_layer_kernel<<<dim3(bx, 8), 256, 0, st>>>(J);
   count_launches(1);
 }

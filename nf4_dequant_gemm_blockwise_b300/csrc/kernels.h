@@ -56,6 +56,11 @@ void k_swiglu_bwd(const float *dact, const uint16_t *gu, int M, int I, uint16_t 
 int lora_splits(int M, int K, int *KS);
 size_t lora_scratch_floats(int M, int dim, int nout);
 // u = x A^T per segment -> u_f32 [M, nseg*r]; ul = 16-bit(s * u) [M, Rpad] (zero padded)
+// The clustered single-launch LoRA projection (lora_proj.cu): 0 when launched (or a negative
+// SOUP_E* code), 1 when the shape is not one it takes (16-byte alignment, rank a multiple of 8,
+// at most 64 fused outputs, segment boundaries on 8-element multiples).
+int lora_skinny(bool du, const uint16_t *X, int ldx, int M, int K, const LoraSeg &L, float *out_f32,
+                uint16_t *out16, bool x_f16, bool o_f16, int *err, cudaStream_t st);
 void k_lora_down(const uint16_t *x, int lda, int M, int K, const LoraSeg &L, float *u_f32,
                  uint16_t *ul, bool x_f16, bool ul_f16, float *part, int *err, cudaStream_t st);
 // du_p = s dY_p B_p -> du_f32 [M, nseg*r]; dul = 16-bit(du) [M, Rpad]

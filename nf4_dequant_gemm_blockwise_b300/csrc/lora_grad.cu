@@ -251,13 +251,19 @@ __global__ void __launch_bounds__(128) lora_grad_kernel(const GradJobs J) {
   if (is_db) {
     // rank c sums rows c * 64 / CL .. of the tile over the CL ranks, in rank order
     const float *part[CL_MAX];
-    for (int c = 0; c < CL; ++c) part[c] = cluster.map_shared_rank(&sm.b.red[0][0], c);
+#pragma unroll
+    for (int c = 0; c < CL_MAX; ++c) part[c] = cluster.map_shared_rank(&sm.b.red[0][0], c < CL ? c : 0);
     const int rows = 64 / CL;
     for (int i = threadIdx.x; i < rows * L.r; i += blockDim.x) {
       const int nl = rows * rank + i / L.r, j = i % L.r;
       const int n = local * 64 + nl;
-      float acc = part[0][nl * 24 + j];
-      for (int c = 1; c < CL; ++c) acc += part[c][nl * 24 + j];
+      float pv[CL_MAX];  // every remote load in flight before the first add
+#pragma unroll
+      for (int c = 0; c < CL_MAX; ++c) pv[c] = c < CL ? part[c][nl * 24 + j] : 0.f;
+      float acc = pv[0];
+#pragma unroll
+      for (int c = 1; c < CL_MAX; ++c)
+        if (c < CL) acc += pv[c];
       if (n < G.Ng) {
         const int sg = seg_of(L, n);
         if (n >= L.off[sg] && n < L.off[sg] + L.n[sg]) {
@@ -271,13 +277,19 @@ __global__ void __launch_bounds__(128) lora_grad_kernel(const GradJobs J) {
     // rank c sums outputs c * 64 / CL .. of the tile (x 64 features) over the CL ranks, in order
     const int nout = L.nseg * L.r;
     const float *part[CL_MAX];
-    for (int c = 0; c < CL; ++c) part[c] = cluster.map_shared_rank(&sm.a.red[0][0], c);
+#pragma unroll
+    for (int c = 0; c < CL_MAX; ++c) part[c] = cluster.map_shared_rank(&sm.a.red[0][0], c < CL ? c : 0);
     const int outs = 64 / CL;
     for (int i = threadIdx.x; i < outs * 64; i += blockDim.x) {
       const int ol = outs * rank + i / 64, kl = i % 64;
       const int k = local * 64 + kl;
-      float acc = part[0][ol * 68 + kl];
-      for (int c = 1; c < CL; ++c) acc += part[c][ol * 68 + kl];
+      float pv[CL_MAX];
+#pragma unroll
+      for (int c = 0; c < CL_MAX; ++c) pv[c] = c < CL ? part[c][ol * 68 + kl] : 0.f;
+      float acc = pv[0];
+#pragma unroll
+      for (int c = 1; c < CL_MAX; ++c)
+        if (c < CL) acc += pv[c];
       if (ol < nout && k < G.K) {
         float *dst = L.dA[ol / L.r] + (size_t)(ol % L.r) * G.K + k;
         *dst = L.accumulate ? *dst + acc : acc;
