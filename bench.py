@@ -41,11 +41,11 @@ def _train_step(sess, tok):
 
 
 # DRAM traffic of the NF4 GEMM launches of a step, from one ncu capture (dram__bytes_read.sum +
-# dram__bytes_write.sum over 11 consecutive launches of the timed step, M = 512).  Valid only
-# for the GEMM source it was taken on: reported while the hash of these files matches, null
-# otherwise.
-GEMM_TRAFFIC = {"sha256": "b2010d82c497c3bccd1e29c44c1bd8a7ba54e067ce34d9ae7c02a7bbda4371a4",
-                "bytes_per_launch": 42.09e6, "algorithmic_bytes_per_launch": 55.43e6}
+# dram__bytes_write.sum, a one-pass metric set, averaged over 388 consecutive NF4 GEMM launches
+# of the 8B step at B = 1, S = 512).  Valid only for the GEMM source it was taken on: reported
+# while the hash of these files matches, null otherwise.
+GEMM_TRAFFIC = {"sha256": "b0c2315ae0ce32a32f177dbe3545a1ea0ad4092d64289086bfed540af5324939",
+                "bytes_per_launch": 39.44e6, "algorithmic_bytes_per_launch": 55.43e6}
 GEMM_SOURCES = ("nf4_dequant_gemm_blockwise_b300/csrc/gemm.cu", "nf4_dequant_gemm_blockwise_b300/csrc/gemm.h",
                 "nf4_dequant_gemm_blockwise_b300/csrc/common.cuh")
 
@@ -603,6 +603,8 @@ def run_ours(args, rank, world, local_rank, dist):
         torch.cuda.synchronize()
         ms_res = g0.elapsed_time(g1) / args.steps
         sess_r.close()
+        del sess_r  # its device buffers (the whole store, resident) go before anything else is measured
+        torch.cuda.empty_cache()
 
     # ---- every kernel family of the step, event-timed per launch group over a few extra steps
     # (not the timed run: the events themselves cost a little)
@@ -691,6 +693,7 @@ def run_ours(args, rank, world, local_rank, dist):
             vcfg = cfg.with_(batch=vb)
             torch.cuda.synchronize()
             torch.cuda.reset_peak_memory_stats()
+            v_base = torch.cuda.memory_allocated()  # anything still held outside this variant
             vs = StreamedLoRA(vcfg, None, synth.embedding(cfg), synth.lm_head(cfg), synth.final_norm(cfg),
                               lora, vb, S, n_slots=vslots, store=store, keep_activations=keep,
                               stream_head=shead)
@@ -710,7 +713,7 @@ def run_ours(args, rank, world, local_rank, dist):
             torch.cuda.synchronize()
             vms = v0.elapsed_time(v1) / nsteps
             vst = vs.stream.stats(reset=True)
-            v_peak = torch.cuda.max_memory_allocated()
+            v_peak = torch.cuda.max_memory_allocated() - v_base
             variants.append({"batch": vb, "slots": vslots, "keep_activations": keep, "stream_head": shead,
                              "tokens_per_step": vb * S,
                              "value": world * vb * S / (vms * 1e-3), "ms_per_step": vms,
