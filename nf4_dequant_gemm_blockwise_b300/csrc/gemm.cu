@@ -564,11 +564,18 @@ __global__ void splitk_reduce_kernel(const RedParams p) {
     const size_t e = (size_t)m * p.Ng + n;
     float v[V];
     if constexpr (V == 4) {
-      float4 a = *reinterpret_cast<const float4 *>(p.part + e);
-      for (int z = 1; z < p.splits; ++z) {
-        const float4 b = *reinterpret_cast<const float4 *>(p.part + (size_t)z * plane + e);
-        a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
-      }
+      // every split's load in flight before the first add (splits <= 4); added in split order
+      float4 b[4];
+#pragma unroll
+      for (int z = 0; z < 4; ++z)
+        b[z] = z < p.splits ? *reinterpret_cast<const float4 *>(p.part + (size_t)z * plane + e)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 a = b[0];
+#pragma unroll
+      for (int z = 1; z < 4; ++z)
+        if (z < p.splits) {
+          a.x += b[z].x; a.y += b[z].y; a.z += b[z].z; a.w += b[z].w;
+        }
       v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
     } else {
       v[0] = p.part[e];
@@ -582,15 +589,27 @@ __global__ void splitk_reduce_kernel(const RedParams p) {
         for (int j = 0; j < V; ++j) bad |= half_out_of_range(v[j]);
         flag_range(bad, p.err);
       }
-#pragma unroll
-      for (int j = 0; j < V; ++j) o[j] = p.f16 ? f_to_h16(v[j]) : f_to_bf16(v[j]);
+      if constexpr (V == 4) {  // one 8-byte store (n, ldo multiples of 4, 16-byte aligned base)
+        *reinterpret_cast<uint2 *>(o) = p.f16 ? make_uint2(pack_h2(v[0], v[1]), pack_h2(v[2], v[3]))
+                                              : make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
+      } else {
+        o[0] = p.f16 ? f_to_h16(v[0]) : f_to_bf16(v[0]);
+      }
     } else {
       float *o = reinterpret_cast<float *>(p.out) + (size_t)m * p.ldo + n;
-#pragma unroll
-      for (int j = 0; j < V; ++j) {
-        if (p.epi == EPI_F32) o[j] = v[j];
-        else if (p.epi == EPI_F32_ADD) o[j] = p.add_src[(size_t)m * p.ld_add + n + j] + v[j];
-        else o[j] = o[j] + v[j];
+      if constexpr (V == 4) {
+        float4 r = make_float4(v[0], v[1], v[2], v[3]);
+        if (p.epi != EPI_F32) {
+          const float4 c = p.epi == EPI_F32_ADD
+                               ? *reinterpret_cast<const float4 *>(p.add_src + (size_t)m * p.ld_add + n)
+                               : *reinterpret_cast<const float4 *>(o);
+          r = make_float4(c.x + v[0], c.y + v[1], c.z + v[2], c.w + v[3]);
+        }
+        *reinterpret_cast<float4 *>(o) = r;
+      } else {
+        if (p.epi == EPI_F32) o[0] = v[0];
+        else if (p.epi == EPI_F32_ADD) o[0] = p.add_src[(size_t)m * p.ld_add + n] + v[0];
+        else o[0] = o[0] + v[0];
       }
     }
   }
@@ -669,7 +688,7 @@ int launch_tc(const GemmArgs &g, const CUtensorMap *maps, cudaStream_t st) {
     rp.f16 = g.op_f16; rp.ldo = g.ldo; rp.ld_add = g.ld_add; rp.out = g.out; rp.add_src = g.add_src;
     rp.err = g.err;
     const bool vec = p.Ng % 4 == 0 && g.ldo % 4 == 0 && (g.epi != EPI_F32_ADD || g.ld_add % 4 == 0) &&
-                     (reinterpret_cast<uintptr_t>(g.part) & 15) == 0;
+                     (reinterpret_cast<uintptr_t>(g.part) & 15) == 0 && p.splits <= 4;
     const int64_t n = (int64_t)g.M * p.Ng / (vec ? 4 : 1);
     const int blocks = (int)std::min<int64_t>((n + 255) / 256, 148 * 16);
     cudaError_t le = vec ? launch_pdl(splitk_reduce_kernel<4>, dim3(blocks), dim3(256), 0, st, rp)

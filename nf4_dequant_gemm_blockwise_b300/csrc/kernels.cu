@@ -149,26 +149,37 @@ __global__ void __launch_bounds__(RMS_T) rmsnorm_bwd_kernel(const float *dy, con
 }
 
 // ------------------------------------------------------------------ RoPE (rotate-half)
+// Four consecutive rotation pairs (i .. i+3, i+half .. i+half+3) per thread: 8-byte loads and
+// stores of the 16-bit halves and 16-byte loads of the tables (d % 8 == 0, 16-byte aligned
+// rows); 32-bit index arithmetic within a row.
 template <bool F16>
 __global__ void rope_fwd_kernel(uint16_t *qkv, int ld, const float *cs, const float *sn, int M,
                                 int S, int nheads_rot, int d, int *err) {
-  const int half = d >> 1;
+  const int half = d >> 1, q4 = half >> 2, per_row = nheads_rot * q4;
   bool bad = false;
-  const int64_t total = (int64_t)M * nheads_rot * half;
+  const int64_t total = (int64_t)M * per_row;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
        idx += (int64_t)gridDim.x * blockDim.x) {
-    const int i = (int)(idx % half);
-    const int64_t rest = idx / half;
-    const int head = (int)(rest % nheads_rot);
-    const int m = (int)(rest / nheads_rot);
+    const int m = (int)(idx / per_row), r = (int)(idx - (int64_t)m * per_row);
+    const int head = r / q4, i = (r - head * q4) * 4;
     const int pos = m % S;
     uint16_t *p = qkv + (size_t)m * ld + (size_t)head * d;
-    const float x1 = ld16<F16>(p[i]), x2 = ld16<F16>(p[i + half]);
-    const float c = cs[pos * half + i], s = sn[pos * half + i];
-    const float y1 = x1 * c - x2 * s, y2 = x2 * c + x1 * s;
-    if (F16) bad |= half_out_of_range(y1) | half_out_of_range(y2);
-    p[i] = st16<F16>(y1);
-    p[i + half] = st16<F16>(y2);
+    const uint2 a = *reinterpret_cast<const uint2 *>(p + i);
+    const uint2 b = *reinterpret_cast<const uint2 *>(p + i + half);
+    const float4 c = *reinterpret_cast<const float4 *>(cs + (size_t)pos * half + i);
+    const float4 sv = *reinterpret_cast<const float4 *>(sn + (size_t)pos * half + i);
+    const float x1[4] = {lo16<F16>(a.x), hi16<F16>(a.x), lo16<F16>(a.y), hi16<F16>(a.y)};
+    const float x2[4] = {lo16<F16>(b.x), hi16<F16>(b.x), lo16<F16>(b.y), hi16<F16>(b.y)};
+    const float cc[4] = {c.x, c.y, c.z, c.w}, ss[4] = {sv.x, sv.y, sv.z, sv.w};
+    float y1[4], y2[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      y1[e] = x1[e] * cc[e] - x2[e] * ss[e];
+      y2[e] = x2[e] * cc[e] + x1[e] * ss[e];
+      if (F16) bad |= half_out_of_range(y1[e]) | half_out_of_range(y2[e]);
+    }
+    *reinterpret_cast<uint2 *>(p + i) = make_uint2(pack16x2<F16>(y1[0], y1[1]), pack16x2<F16>(y1[2], y1[3]));
+    *reinterpret_cast<uint2 *>(p + i + half) = make_uint2(pack16x2<F16>(y2[0], y2[1]), pack16x2<F16>(y2[2], y2[3]));
   }
   flag_range(bad, err);
 }
@@ -176,26 +187,37 @@ __global__ void rope_fwd_kernel(uint16_t *qkv, int ld, const float *cs, const fl
 __global__ void rope_bwd_kernel(const float *dqkv, uint16_t *out, int ld, const float *cs,
                                 const float *sn, int M, int S, int nheads_rot, int nheads_all,
                                 int d) {
-  const int half = d >> 1;
-  const int64_t total = (int64_t)M * nheads_all * half;
+  const int half = d >> 1, q4 = half >> 2, per_row = nheads_all * q4;
+  const int64_t total = (int64_t)M * per_row;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
        idx += (int64_t)gridDim.x * blockDim.x) {
-    const int i = (int)(idx % half);
-    const int64_t rest = idx / half;
-    const int head = (int)(rest % nheads_all);
-    const int m = (int)(rest / nheads_all);
+    const int m = (int)(idx / per_row), r = (int)(idx - (int64_t)m * per_row);
+    const int head = r / q4, i = (r - head * q4) * 4;
     const float *g = dqkv + (size_t)m * ld + (size_t)head * d;
     uint16_t *o = out + (size_t)m * ld + (size_t)head * d;
-    const float d1 = g[i], d2 = g[i + half];
+    const float4 a = *reinterpret_cast<const float4 *>(g + i);
+    const float4 b = *reinterpret_cast<const float4 *>(g + i + half);
+    const float d1[4] = {a.x, a.y, a.z, a.w}, d2[4] = {b.x, b.y, b.z, b.w};
+    float r1[4], r2[4];
     if (head < nheads_rot) {
       const int pos = m % S;
-      const float c = cs[pos * half + i], s = sn[pos * half + i];
-      o[i] = f_to_bf16(d1 * c + d2 * s);
-      o[i + half] = f_to_bf16(d2 * c - d1 * s);
+      const float4 c = *reinterpret_cast<const float4 *>(cs + (size_t)pos * half + i);
+      const float4 sv = *reinterpret_cast<const float4 *>(sn + (size_t)pos * half + i);
+      const float cc[4] = {c.x, c.y, c.z, c.w}, ss[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        r1[e] = d1[e] * cc[e] + d2[e] * ss[e];
+        r2[e] = d2[e] * cc[e] - d1[e] * ss[e];
+      }
     } else {
-      o[i] = f_to_bf16(d1);
-      o[i + half] = f_to_bf16(d2);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        r1[e] = d1[e];
+        r2[e] = d2[e];
+      }
     }
+    *reinterpret_cast<uint2 *>(o + i) = make_uint2(pack_bf16x2(r1[0], r1[1]), pack_bf16x2(r1[2], r1[3]));
+    *reinterpret_cast<uint2 *>(o + i + half) = make_uint2(pack_bf16x2(r2[0], r2[1]), pack_bf16x2(r2[2], r2[3]));
   }
 }
 
@@ -681,7 +703,7 @@ void k_rmsnorm_bwd(const float *dy, const float *h, const uint16_t *w, float eps
 }
 void k_rope_fwd(uint16_t *qkv, int ld, const float *cos, const float *sin, int M, int S, int nh,
                 int nkv, int d, bool f16, int *err, cudaStream_t st) {
-  const int64_t n = (int64_t)M * (nh + nkv) * (d / 2);
+  const int64_t n = (int64_t)M * (nh + nkv) * (d / 8);  // d % 8 == 0 (checked with the configuration)
   if (n <= 0) return;
   if (f16) rope_fwd_kernel<true><<<grid_for(n, 256), 256, 0, st>>>(qkv, ld, cos, sin, M, S, nh + nkv, d, err);
   else rope_fwd_kernel<false><<<grid_for(n, 256), 256, 0, st>>>(qkv, ld, cos, sin, M, S, nh + nkv, d, err);
@@ -689,7 +711,7 @@ void k_rope_fwd(uint16_t *qkv, int ld, const float *cos, const float *sin, int M
 }
 void k_rope_bwd(const float *dqkv, uint16_t *out, int ld, const float *cos, const float *sin,
                 int M, int S, int nh, int nkv, int d, cudaStream_t st) {
-  const int64_t n = (int64_t)M * (nh + 2 * nkv) * (d / 2);
+  const int64_t n = (int64_t)M * (nh + 2 * nkv) * (d / 8);
   if (n <= 0) return;
   rope_bwd_kernel<<<grid_for(n, 256), 256, 0, st>>>(dqkv, out, ld, cos, sin, M, S, nh + nkv,
                                                     nh + 2 * nkv, d);
