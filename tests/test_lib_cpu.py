@@ -268,3 +268,39 @@ def test_host_packer_special_values_and_threads(n_threads):
     oc, oa = nf4.quantize(nf4.bf16_to_f32(bits))
     assert np.array_equal(absmax.view(np.uint32), oa.view(np.uint32))
     assert np.array_equal(codes, nf4.pack(oc[: x.size + (x.size % 2)]))
+
+
+def test_attention_entry_points_check_their_arguments_first():
+    """soup_attn_fwd / soup_attn_bwd reject bad shapes (kv heads not dividing the query heads,
+    head dims other than 64 / 128, negative sizes) and NULL buffers with SOUP_EINVAL before any
+    device work; an empty batch or sequence is a no-op that touches nothing."""
+    z = 16  # any non-NULL address: nothing is dereferenced on these paths
+    for B, S, nh, nkv, d in ((1, 8, 4, 3, 64), (1, 8, 4, 2, 96), (-1, 8, 4, 2, 64), (1, -2, 4, 2, 64),
+                             (1, 8, 0, 1, 64), (1, 8, 4, 0, 64)):
+        with pytest.raises(api.SoupError) as e:
+            api.attn_fwd(z, B, S, nh, nkv, d, z, z)
+        assert e.value.code == api.EINVAL
+        assert api.attn_bwd_scratch_bytes(B, S, nh, nkv, d) == 0
+    api.attn_fwd(z, 0, 64, 4, 2, 64, z, z)
+    api.attn_fwd(z, 2, 0, 4, 2, 64, z, z)
+    with pytest.raises(api.SoupError) as e:
+        api.attn_fwd(None, 1, 8, 4, 2, 64, z, z)
+    assert e.value.code == api.EINVAL
+    lib = api.lib
+    rc = lib.soup_attn_bwd(z, z, z, z, 1, 8, 4, 2, 64, z, 0, z, None, 0)  # scratch too small
+    assert rc == api.EINVAL
+    rc = lib.soup_attn_bwd(z, z, z, z, 1, 8, 4, 2, 64, 17, 1 << 30, z, None, 0)  # misaligned scratch
+    assert rc == api.EINVAL
+
+
+@pytest.mark.parametrize("nh,nkv,d", [(32, 8, 128), (4, 2, 64), (40, 8, 128), (16, 1, 64)])
+def test_attention_backward_scratch_covers_its_buffers(nh, nkv, d):
+    """The backward's scratch holds the row sums D [B, nh, S] (float) and a bf16 copy of the
+    fused q|k|v rows [B*S, (nh + 2 nkv) d] (or, on the warp-level path, per-head dK/dV partials);
+    it grows with B and S and never falls below the first two."""
+    prev = 0
+    for B, S in ((1, 1), (1, 63), (1, 512), (2, 512), (4, 1024)):
+        n = api.attn_bwd_scratch_bytes(B, S, nh, nkv, d)
+        assert n >= 4 * B * nh * S + 2 * B * S * (nh + 2 * nkv) * d
+        assert n >= prev
+        prev = n
