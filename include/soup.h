@@ -190,8 +190,10 @@ int soup_workspace_bytes(const soup_cfg *cfg, int max_batch, int max_seq, int n_
  * untied head — neither in SOUP_MODE_STREAM_HEAD, where the workspace holds the one vocabulary
  * buffer — final norm, float32 LoRA A/B, their gradients and the two AdamW moments).
  * The pages bound peak VRAM by a single layer plus the resident parts ("About Soup"); this
- * is that bound made exact.  Returns 0 for an invalid cfg or mode.  workspace_bytes
- * (optional) receives the workspace part. */
+ * is that bound made exact.  Not counted: the library's static 16 MiB array behind
+ * soup_proj_fwd_noalloc, module memory resident on every device that loads the library.
+ * Returns 0 for an invalid cfg or mode.  workspace_bytes (optional) receives the workspace
+ * part. */
 uint64_t soup_peak_bytes(const soup_cfg *cfg, int batch, int seq, int n_slots, int mode,
                          uint64_t *workspace_bytes);
 
