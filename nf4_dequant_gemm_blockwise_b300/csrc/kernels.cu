@@ -759,8 +759,9 @@ template <bool DU>
 static void lora_proj(const uint16_t *X, int ldx, int M, int K, const LoraSeg &L, float *out_f32,
                       uint16_t *out16, bool x_f16, bool o_f16, float *part, int *err, cudaStream_t st) {
   if (M <= 0) return;
-  // one clustered launch (lora_proj.cu) for the shapes it takes; else partials + ordered reduce
-  if (lora_skinny(DU, X, ldx, M, K, L, out_f32, out16, x_f16, o_f16, err, st) <= 0) return;
+  // one clustered launch (lora_proj.cu) for the shapes it takes; otherwise (or if its setup
+  // failed: a tensor map or attribute the driver refused) partials + an ordered reduce
+  if (lora_skinny(DU, X, ldx, M, K, L, out_f32, out16, x_f16, o_f16, err, st) == 0) return;
   int KS;
   const int ns = lora_splits(M, K, &KS);
   dim3 grid(cdiv(M, 64), ns);

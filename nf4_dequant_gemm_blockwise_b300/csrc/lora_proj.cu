@@ -304,7 +304,10 @@ int launch_skinny(const CUtensorMap *maps, const SkArgs &a, int mtiles, cudaStre
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, lora_skinny_kernel<DU, XF16, OF16>, maps[0], maps[1], maps[2],
                                      maps[3], a);
-  if (e != cudaSuccess) return set_error(SOUP_ECUDA, "LoRA projection launch: %s", cudaGetErrorString(e));
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // not sticky: the caller falls back to the two-kernel path
+    return set_error(SOUP_ECUDA, "LoRA projection launch: %s", cudaGetErrorString(e));
+  }
   count_launches(1);
   return 0;
 }
