@@ -210,7 +210,13 @@ uint64_t soup_peak_bytes(const soup_cfg *cfg, int batch, int seq, int n_slots, i
  *   (synchronously) and then runs the same kernels with no copies — the reference the
  *   streamed run must match bit for bit.  SOUP_MODE_KEEP_ACTIVATIONS skips the backward's
  *   recompute; results are bitwise those of the recomputing stream (same kernels, same
- *   inputs). */
+ *   inputs).
+ * Kernel paths follow from the shapes alone (so streamed and resident runs always take the
+ * same ones): a projection whose reduction length (hidden, inter, n_heads * head_dim) is a
+ * multiple of 256 runs on the tcgen05 GEMM, otherwise on a plain tiled CUDA-core kernel (the
+ * 2-layer test stack's inter = 688 does); batches of at most 16 tokens take the small-M path;
+ * attention runs on tcgen05 for head_dim 64 / 128 with at most 8 query heads per kv head,
+ * otherwise on the warp-level MMA kernels. */
 int soup_stream_init(soup_store *st, const soup_cfg *cfg, int max_batch, int max_seq,
                      void *dev_ws, uint64_t ws_bytes, const void *embed, const void *lm_head,
                      const void *final_norm, uintptr_t compute_stream, uintptr_t copy_stream,
