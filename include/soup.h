@@ -214,7 +214,8 @@ uint64_t soup_peak_bytes(const soup_cfg *cfg, int batch, int seq, int n_slots, i
  * Kernel paths follow from the shapes alone (so streamed and resident runs always take the
  * same ones): a projection whose reduction length (hidden, inter, n_heads * head_dim) is a
  * multiple of 256 runs on the tcgen05 GEMM, otherwise on a plain tiled CUDA-core kernel (the
- * 2-layer test stack's inter = 688 does); batches of at most 16 tokens take the small-M path;
+ * 2-layer test stack's inter = 688 does); NF4 projections over at most 16 tokens take the
+ * small-M path;
  * attention runs on tcgen05 for head_dim 64 / 128 with at most 8 query heads per kv head,
  * otherwise on the warp-level MMA kernels. */
 int soup_stream_init(soup_store *st, const soup_cfg *cfg, int max_batch, int max_seq,
